@@ -1,0 +1,173 @@
+// The extern "C" entry points of libfo.so (declared in include/fo.h):
+// argument checks, plan ownership and dispatch to the kernel launchers.
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "fo_internal.h"
+
+extern "C" {
+
+fo_status fo_wave_count(const fo_plan_desc* desc, int32_t* tiles, int32_t* waves) {
+  return fo::check_shape(desc, nullptr, tiles, waves);
+}
+
+fo_status fo_plan_groups(const fo_plan_desc* desc, fo_plan** out) {
+  if (!out) return FO_ERR_ARG;
+  *out = nullptr;
+  fo_plan* p = new (std::nothrow) fo_plan();
+  if (!p) return FO_ERR_ARG;
+  fo_status st = fo::build_plan(desc, p);
+  if (st == FO_OK && !desc->host_only) st = fo::upload_plan(p);
+  if (st != FO_OK) {
+    fo_plan_destroy(p);
+    return st;
+  }
+  *out = p;
+  return FO_OK;
+}
+
+fo_status fo_plan_info(const fo_plan* p, int32_t* tiles, int32_t* waves,
+                       int32_t* n_groups, int32_t* group_tiles,
+                       int32_t* tile_to_slot) {
+  if (!p) return FO_ERR_ARG;
+  if (tiles) *tiles = p->tiles;
+  if (waves) *waves = p->waves;
+  if (n_groups) *n_groups = p->P;
+  if (group_tiles) std::memcpy(group_tiles, p->group_tiles.data(), sizeof(int32_t) * p->P);
+  if (tile_to_slot)
+    std::memcpy(tile_to_slot, p->tile_slot.data(), sizeof(int32_t) * p->tiles);
+  return FO_OK;
+}
+
+fo_status fo_plan_table(const fo_plan* p, int32_t which, int32_t* out,
+                        int64_t capacity, int64_t* length) {
+  if (!p) return FO_ERR_ARG;
+  std::vector<int32_t> unit;
+  const std::vector<int32_t>* v = nullptr;
+  switch (which) {
+    case FO_TAB_SLOT_TILE: v = &p->slot_tile; break;
+    case FO_TAB_TILE_SLOT: v = &p->tile_slot; break;
+    case FO_TAB_SLOT_GROUP: v = &p->slot_group; break;
+    case FO_TAB_GROUP_TILES: v = &p->group_tiles; break;
+    case FO_TAB_PART_START: v = &p->part_start; break;
+    case FO_TAB_PART_LEN: v = &p->part_len; break;
+    case FO_TAB_PART_DST: v = &p->part_dst; break;
+    case FO_TAB_DEST_UNITS: v = &p->dest_units; break;
+    case FO_TAB_FINAL_ROWS: v = &p->final_rows; break;
+    case FO_TAB_UNIT:
+      unit.resize(size_t(p->tiles) * p->tile_m);
+      for (int32_t s = 0; s < p->tiles; ++s)
+        for (int32_t r = 0; r < p->tile_m; ++r)
+          unit[size_t(s) * p->tile_m + r] = fo::unit_of(p, s, r);
+      v = &unit;
+      break;
+    default: return FO_ERR_ARG;
+  }
+  if (length) *length = int64_t(v->size());
+  if (!out) return FO_OK;
+  if (capacity < int64_t(v->size())) return FO_ERR_ARG;
+  if (!v->empty()) std::memcpy(out, v->data(), v->size() * sizeof(int32_t));
+  return FO_OK;
+}
+
+fo_status fo_plan_set_ctas(fo_plan* p, int32_t consumer_ctas, int32_t reorder_ctas) {
+  if (!p) return FO_ERR_ARG;
+  p->consumer_ctas = consumer_ctas;
+  p->reorder_ctas = reorder_ctas;
+  return FO_OK;
+}
+
+fo_status fo_plan_device_status(const fo_plan* p, int32_t* gemm_status, int32_t clear) {
+  if (!p || !p->blob || !gemm_status) return FO_ERR_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FO_ERR_CUDA;
+  if (cudaMemcpy(gemm_status, p->dev.gemm_status, sizeof(int32_t), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return FO_ERR_CUDA;
+  if (clear && cudaMemset(p->dev.gemm_status, 0, sizeof(int32_t)) != cudaSuccess)
+    return FO_ERR_CUDA;
+  return FO_OK;
+}
+
+void fo_plan_destroy(fo_plan* p) {
+  if (!p) return;
+  if (p->blob) cudaFree(p->blob);
+  delete p;
+}
+
+fo_status fo_counting_table_init(const fo_plan* p, int32_t* count, void* stream) {
+  if (!p || !count) return FO_ERR_ARG;
+  return cudaMemsetAsync(count, 0, sizeof(int32_t) * p->P, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FO_OK
+             : FO_ERR_CUDA;
+}
+
+fo_status fo_signaled_gemm(const fo_plan* p, const void* A, const void* const* B,
+                           void* C_r, int32_t* count, uint32_t* flags,
+                           uint32_t epoch, void* stream) {
+  if (!p || !p->blob || !A || !B || !C_r) return FO_ERR_ARG;
+  if ((count == nullptr) != (flags == nullptr)) return FO_ERR_ARG;
+  return fo::launch_signaled_gemm(p, A, B, C_r, count, flags, epoch, stream);
+}
+
+fo_status fo_consume_group(const fo_plan* p, int32_t group, fo_consumer kind,
+                           const void* src, const void* const* partials,
+                           int32_t n_partials, void* const* dst,
+                           const uint32_t* flags, uint32_t epoch,
+                           uint64_t spin_limit_ns, int32_t* dev_status,
+                           void* stream) {
+  if (!p || !p->blob || !src || !dst || !flags || !dev_status) return FO_ERR_ARG;
+  if (group < -1 || group >= p->P) return FO_ERR_ARG;
+  const int32_t g0 = group < 0 ? 0 : group, g1 = group < 0 ? p->P : group + 1;
+  switch (kind) {
+    case FO_CONS_COPY:
+      if (n_partials != 0) return FO_ERR_ARG;
+      break;
+    case FO_CONS_SUM:
+      if (n_partials < 0 || n_partials > fo::kMaxPartials) return FO_ERR_ARG;
+      break;
+    case FO_CONS_RS:
+      if (n_partials < 0 || n_partials > fo::kMaxPartials) return FO_ERR_ARG;
+      if (p->layout != FO_LAYOUT_RS_SUBTILE && p->layout != FO_LAYOUT_RS_ROWBLOCK)
+        return FO_ERR_ARG;
+      break;
+    case FO_CONS_A2A:
+      if (n_partials != 0 || p->layout != FO_LAYOUT_A2A_SUBTOKEN) return FO_ERR_ARG;
+      break;
+    default: return FO_ERR_ARG;
+  }
+  if (n_partials > 0 && !partials) return FO_ERR_ARG;
+  for (int i = 0; i < n_partials; ++i)
+    if (!partials[i]) return FO_ERR_ARG;
+  const int n_dst = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
+  for (int k = 0; k < n_dst; ++k)
+    if (!dst[k]) return FO_ERR_ARG;
+  return fo::launch_consume(p, g0, g1, int(kind), src, partials, n_partials, dst,
+                            flags, epoch, spin_limit_ns, dev_status, stream);
+}
+
+fo_status fo_reorder_back(const fo_plan* p, int32_t group_begin, int32_t group_end,
+                          const void* const* src, void* const* dst, void* stream) {
+  if (!p || !p->blob || !src || !dst) return FO_ERR_ARG;
+  if (group_begin < 0 || group_end > p->P || group_begin > group_end) return FO_ERR_ARG;
+  const int n = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
+  for (int k = 0; k < n; ++k)
+    if (!src[k] || !dst[k]) return FO_ERR_ARG;
+  if (group_begin == group_end) return FO_OK;
+  return fo::launch_reorder_back(p, group_begin, group_end, src, dst, stream);
+}
+
+const char* fo_status_string(fo_status s) {
+  switch (s) {
+    case FO_OK: return "ok";
+    case FO_ERR_ARG: return "invalid argument";
+    case FO_ERR_CUDA: return "CUDA error";
+    case FO_ERR_TIMEOUT: return "device wait timed out";
+    case FO_ERR_UNSUPPORTED: return "unsupported shape or device";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

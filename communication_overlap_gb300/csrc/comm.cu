@@ -1,0 +1,323 @@
+// Consumer (communication stand-in) and post-communication reorder kernels.
+//
+// Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 核心设计 "通信侧" (the
+// communication runs as its own kernel on another stream), 五、CUTLASS 扩展实现
+// "专用监控内核" (a monitor kernel tracks progress through atomic counters),
+// 二、重排机制 (a group's data is contiguous so one collective call covers it;
+// the inverse mapping table restores the layout afterwards).
+//
+// Both kernels are HBM-bound streams of 16-byte vectors.  A unit (one tile
+// row, tile_n bf16) is tile_n / 8 vectors, so a warp moves one or two whole
+// units per instruction and every access is a full 512-byte (or 256-byte)
+// coalesced segment.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace fo {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+struct ConsumeArgs {
+  const uint4* src;
+  const uint4* partials[kMaxPartials];
+  uint4* dst[kMaxDest];
+  const uint32_t* flags;
+  int32_t* status;
+  const int32_t* group_unit_begin;
+  const int32_t* part_start;
+  const int32_t* part_len;
+  const int32_t* part_dst;
+  int32_t* work;
+  int32_t g0, g1, n_partials, R, vpu_shift, chunk_units;
+  uint32_t epoch;
+  uint64_t limit_ns;
+};
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = __fadd_rn(acc[2 * i], bf16lo(w[i]));
+    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], bf16hi(w[i]));
+  }
+}
+
+__device__ __forceinline__ void set_bf16x8(float (&acc)[8], const uint4& x) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = bf16lo(w[i]);
+    acc[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
+  return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+// Where vector v (unit v >> vpu_shift) of the group goes: destination k's
+// part (j, k) starts at unit part_dst there.
+__device__ __forceinline__ uint4* route(const int32_t* ps, const int32_t* pl,
+                                        const int32_t* pd, uint4* const* dst, int R,
+                                        int vpu_shift, int32_t v) {
+  const int32_t u = v >> vpu_shift;
+  int k = 0;
+  for (; k < R - 1; ++k)
+    if (uint32_t(u - ps[k]) < uint32_t(pl[k])) break;
+  const int32_t vu = (pd[k] + (u - ps[k])) << vpu_shift;
+  return dst[k] + vu + (v & ((1 << vpu_shift) - 1));
+}
+
+// One warp processes vectors [v0, v1) of the reordered buffer.
+template <int KIND, int U>
+__device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_t* ps,
+                                              const int32_t* pl, const int32_t* pd,
+                                              uint4* const* dst, int32_t v0, int32_t v1,
+                                              int lane) {
+  constexpr bool kSum = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS);
+  for (int32_t base = v0 + lane; base < v1; base += 32 * U) {
+    uint4 x[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+      if (base + 32 * i < v1) x[i] = ld_cg(a.src + base + 32 * i);
+    if constexpr (kSum) {
+      float acc[U][8];
+#pragma unroll
+      for (int i = 0; i < U; ++i) set_bf16x8(acc[i], x[i]);
+#pragma unroll
+      for (int q = 0; q < kMaxPartials; ++q) {
+        if (q >= a.n_partials) break;
+        uint4 y[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+          if (base + 32 * i < v1) y[i] = ld_cg(a.partials[q] + base + 32 * i);
+#pragma unroll
+        for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i) x[i] = pack8(acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int32_t v = base + 32 * i;
+      if (v >= v1) break;
+      if constexpr (KIND == FO_CONS_COPY || KIND == FO_CONS_SUM)
+        st_cs(dst[0] + v, x[i]);
+      else
+        st_cs(route(ps, pl, pd, dst, a.R, a.vpu_shift, v), x[i]);
+    }
+  }
+}
+
+// Persistent consumer: for each group in order, thread 0 waits on the
+// group's flag, then the CTA's warps take chunks of the group's unit range
+// from a per-group counter until none are left.  Dynamic chunks keep the
+// work balanced whichever CTAs are resident while the GEMM still runs.
+template <int KIND, int U>
+__global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant__ ConsumeArgs a) {
+  __shared__ int s_ok;
+  __shared__ int32_t s_ps[kMaxDest], s_pl[kMaxDest], s_pd[kMaxDest];
+  __shared__ uint4* s_dst[kMaxDest];
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid < kMaxDest) s_dst[tid] = a.dst[tid];
+  for (int j = a.g0; j < a.g1; ++j) {
+    if (tid == 0) s_ok = wait_flag(a.flags + j, a.epoch, a.limit_ns) ? 1 : 0;
+    if (tid < a.R) {
+      s_ps[tid] = a.part_start[j * a.R + tid];
+      s_pl[tid] = a.part_len[j * a.R + tid];
+      s_pd[tid] = a.part_dst[j * a.R + tid];
+    }
+    __syncthreads();
+    if (!s_ok) {
+      if (tid == 0) atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
+      return;
+    }
+    const int32_t ub = a.group_unit_begin[j], ue = a.group_unit_begin[j + 1];
+    const int32_t n_chunks = (ue - ub + a.chunk_units - 1) / a.chunk_units;
+    while (true) {
+      int32_t c = 0;
+      if (lane == 0) c = atomicAdd(a.work + j, 1);
+      c = __shfl_sync(0xffffffffu, c, 0);
+      if (c >= n_chunks) break;
+      const int32_t u0 = ub + c * a.chunk_units;
+      const int32_t u1 = min(u0 + a.chunk_units, ue);
+      consume_range<KIND, U>(a, s_ps, s_pl, s_pd, s_dst, u0 << a.vpu_shift,
+                             u1 << a.vpu_shift, lane);
+    }
+    __syncthreads();
+  }
+}
+
+struct ReorderArgs {
+  const uint4* src[kMaxDest];
+  uint4* dst[kMaxDest];
+  const TileInfo* tile;
+  const int32_t* part_start;
+  const int32_t* part_dst;
+  const int32_t* dest_base;
+  const int32_t* row_dest;
+  const int32_t* row_rank;
+  const int32_t* final_row;
+  int32_t layout, R, vpu_shift, row_vec, slot0, h, rows_per;
+  int64_t total;  // vectors over the slot range, ragged rows included
+};
+
+// Inverse mapping: vector `idx` of the slot range is lane (idx mod vpu) of
+// row r of the tile at slot s; find where the consumer left that unit and
+// where it belongs in the final layout.
+__device__ __forceinline__ bool reorder_addr(const ReorderArgs& a, const uint4* const* src,
+                                             uint4* const* dst, int64_t idx,
+                                             const uint4** from, uint4** to) {
+  const int32_t lane = int32_t(idx) & ((1 << a.vpu_shift) - 1);
+  const int64_t w = idx >> a.vpu_shift;
+  const int32_t s = a.slot0 + int32_t(w / kTileM);
+  const int32_t r = int32_t(w % kTileM);
+  const TileInfo ti = a.tile[s];
+  if (r >= ti.rows) return false;
+  int k = 0;
+  int32_t src_unit, dst_row;
+  if (a.layout == FO_LAYOUT_TILE) {
+    src_unit = ti.unit_base + r;
+    dst_row = ti.row0 + r;
+  } else {
+    int32_t u;
+    if (a.layout == FO_LAYOUT_RS_SUBTILE) {
+      k = r / a.h;
+      const int32_t i = r - k * a.h;
+      u = ti.unit_base + k * ti.sub_stride + i;
+      dst_row = (ti.row0 / kTileM) * a.h + i;
+    } else if (a.layout == FO_LAYOUT_RS_ROWBLOCK) {
+      k = ti.dest;
+      u = ti.unit_base + r;
+      dst_row = ti.row0 + r - k * a.rows_per;
+    } else {  // FO_LAYOUT_A2A_SUBTOKEN
+      const int32_t rho = ti.row0 + r;
+      k = a.row_dest[rho];
+      u = a.dest_base[s * a.R + k] + a.row_rank[rho];
+      dst_row = a.final_row[rho];
+    }
+    const int32_t jk = ti.group * a.R + k;
+    src_unit = a.part_dst[jk] + (u - a.part_start[jk]);
+  }
+  *from = src[k] + (int64_t(src_unit) << a.vpu_shift) + lane;
+  *to = dst[k] + int64_t(dst_row) * a.row_vec + (ti.col0 >> 3) + lane;
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads) reorder_kernel(const __grid_constant__ ReorderArgs a) {
+  constexpr int U = 4;
+  __shared__ const uint4* s_src[kMaxDest];
+  __shared__ uint4* s_dst[kMaxDest];
+  if (threadIdx.x < kMaxDest) {
+    s_src[threadIdx.x] = a.src[threadIdx.x];
+    s_dst[threadIdx.x] = a.dst[threadIdx.x];
+  }
+  __syncthreads();
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t base = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; base < a.total;
+       base += stride * U) {
+    const uint4* from[U];
+    uint4* to[U];
+    bool ok[U];
+    uint4 x[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int64_t idx = base + stride * i;
+      ok[i] = idx < a.total && reorder_addr(a, s_src, s_dst, idx, &from[i], &to[i]);
+      if (ok[i]) x[i] = ld_cg(from[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+      if (ok[i]) st_cs(to[i], x[i]);
+  }
+}
+
+int log2_exact(int v) {
+  int s = 0;
+  while ((1 << s) < v) ++s;
+  return s;
+}
+
+int default_ctas(const fo_plan* p, int requested) {
+  return requested > 0 ? requested : 2 * p->sm_count;
+}
+
+template <int KIND, int U>
+fo_status launch_consume_kind(const ConsumeArgs& a, int ctas, cudaStream_t st) {
+  consume_kernel<KIND, U><<<ctas, kThreads, 0, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
+}
+
+}  // namespace
+
+fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
+                         const void* src, const void* const* partials,
+                         int32_t n_partials, void* const* dst, const uint32_t* flags,
+                         uint32_t epoch, uint64_t spin_limit_ns, int32_t* dev_status,
+                         void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ConsumeArgs a{};
+  a.src = static_cast<const uint4*>(src);
+  for (int i = 0; i < n_partials; ++i) a.partials[i] = static_cast<const uint4*>(partials[i]);
+  const int n_dst = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
+  for (int k = 0; k < n_dst; ++k) a.dst[k] = static_cast<uint4*>(dst[k]);
+  a.flags = flags;
+  a.status = dev_status;
+  a.group_unit_begin = p->dev.group_unit_begin;
+  a.part_start = p->dev.part_start;
+  a.part_len = p->dev.part_len;
+  a.part_dst = p->dev.part_dst;
+  a.work = p->dev.work;
+  a.g0 = g0;
+  a.g1 = g1;
+  a.n_partials = n_partials;
+  a.R = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
+  a.vpu_shift = log2_exact(p->tile_n / 8);
+  a.chunk_units = (16 * 1024) / (p->tile_n * 2);  // 16 KB of the source per chunk
+  a.epoch = epoch;
+  a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
+  if (cudaMemsetAsync(p->dev.work + g0, 0, sizeof(int32_t) * (g1 - g0), st) != cudaSuccess)
+    return FO_ERR_CUDA;
+  const int ctas = default_ctas(p, p->consumer_ctas);
+  switch (kind) {
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, 4>(a, ctas, st);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, 2>(a, ctas, st);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, 2>(a, ctas, st);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, 4>(a, ctas, st);
+  }
+  return FO_ERR_ARG;
+}
+
+fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
+                              const void* const* src, void* const* dst, void* stream) {
+  ReorderArgs a{};
+  const int n = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
+  for (int k = 0; k < n; ++k) {
+    a.src[k] = static_cast<const uint4*>(src[k]);
+    a.dst[k] = static_cast<uint4*>(dst[k]);
+  }
+  a.tile = p->dev.tile;
+  a.part_start = p->dev.part_start;
+  a.part_dst = p->dev.part_dst;
+  a.dest_base = p->dev.dest_base;
+  a.row_dest = p->dev.row_dest;
+  a.row_rank = p->dev.row_rank;
+  a.final_row = p->dev.final_row;
+  a.layout = p->layout;
+  a.R = p->R;
+  a.vpu_shift = log2_exact(p->tile_n / 8);
+  a.row_vec = p->N / 8;
+  a.slot0 = p->group_slot_begin[g0];
+  a.h = kTileM / p->R;
+  a.rows_per = p->M / p->R;
+  a.total = int64_t(p->group_slot_begin[g1] - a.slot0) * kTileM * (p->tile_n / 8);
+  const int ctas = default_ctas(p, p->reorder_ctas);
+  reorder_kernel<<<ctas, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
+}
+
+}  // namespace fo

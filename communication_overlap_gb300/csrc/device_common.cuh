@@ -1,0 +1,65 @@
+// Device helpers shared by the kernels of libfo.so (sm_103a).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fo_internal.h"
+
+namespace fo {
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Wait until *flag == epoch: acquire loads with __nanosleep back-off, giving
+// up after limit_ns of globaltimer time.  Returns false on timeout.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch,
+                                          uint64_t limit_ns) {
+  if (ld_acquire_gpu(flag) == epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t backoff = 32;
+  while (true) {
+    __nanosleep(backoff);
+    if (ld_acquire_gpu(flag) == epoch) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (backoff < 1024) backoff <<= 1;
+  }
+}
+
+// bf16x2 <-> float2 (bf16 is the upper half of an fp32; the pack rounds to
+// nearest even through the CUDA intrinsic).
+__device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 ld_cg(const uint4* p) { return __ldcg(p); }
+__device__ __forceinline__ void st_cs(uint4* p, uint4 v) { __stcs(p, v); }
+
+}  // namespace fo

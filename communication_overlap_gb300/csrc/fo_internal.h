@@ -1,0 +1,98 @@
+// Internal declarations shared by the host planner, the C ABI and the
+// kernels of libfo.so.  Not installed; the public interface is include/fo.h.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "fo.h"
+
+namespace fo {
+
+constexpr int kTileM = 128;      // rows per tile (tcgen05 M = 128, one CTA)
+constexpr int kBlockK = 64;      // K per pipeline stage (one 128-byte swizzle atom)
+constexpr int kMaxDest = 16;     // ranks a layout may route to
+constexpr int kMaxPartials = 8;  // partial buffers a SUM / RS consumer adds
+constexpr int kMaxExperts = 16;  // B matrices of a grouped GEMM
+
+// One entry per launch slot (32 bytes, read by the GEMM producer and
+// epilogue and by the reorder kernel).
+struct TileInfo {
+  int32_t row0;        // first row of the tile in A and in the stacked C
+  int32_t col0;        // first column
+  int32_t rows;        // valid rows (an expert's last tile row may be ragged)
+  int32_t expert;      // which B
+  int32_t group;       // wave group j
+  int32_t unit_base;   // unit of row 0 (RS_SUBTILE: of row 0 of subtile 0)
+  int32_t sub_stride;  // RS_SUBTILE: units from subtile k to subtile k+1
+  int32_t dest;        // RS_ROWBLOCK: the rank all rows of the tile go to
+};
+static_assert(sizeof(TileInfo) == 32, "TileInfo is 32 bytes");
+
+// Device copies of the plan's tables: pointers into one allocation.
+struct DeviceTables {
+  TileInfo* tile = nullptr;            // [tiles]
+  int32_t* group_tiles = nullptr;      // [P]       |G_j|
+  int32_t* group_unit_begin = nullptr; // [P + 1]   unit range of each group
+  int32_t* group_slot_begin = nullptr; // [P + 1]   slot range of each group
+  int32_t* part_start = nullptr;       // [P * R]
+  int32_t* part_len = nullptr;         // [P * R]
+  int32_t* part_dst = nullptr;         // [P * R]
+  int32_t* dest_base = nullptr;        // [tiles * R]  A2A: unit of the tile's
+                                       //   first row bound for rank d
+  int32_t* row_dest = nullptr;         // [M] A2A: rank of each routed row
+  int32_t* row_rank = nullptr;         // [M] A2A: index among the rows of its
+                                       //   tile row that go to the same rank
+  int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
+  int32_t* work = nullptr;             // [P] scratch: consumer chunk counters
+  int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
+};
+
+}  // namespace fo
+
+struct fo_plan {
+  // description
+  int32_t M = 0, N = 0, K = 0, tile_m = 0, tile_n = 0, swizzle = 0, W = 0;
+  int32_t P = 0, R = 1, layout = 0, n_dest = 1, n_experts = 0, top_k = 1;
+  int32_t tiles = 0, tiles_n = 0, waves = 0, n_units = 0;
+  std::vector<int32_t> expert_rows, expert_row0, expert_tile0;
+  std::vector<int32_t> group_waves, group_tiles, group_slot_begin, group_unit_begin;
+  std::vector<int32_t> slot_tile, tile_slot, slot_group;
+  std::vector<fo::TileInfo> tile;
+  std::vector<int32_t> part_start, part_len, part_dst, dest_units, final_rows;
+  std::vector<int32_t> dest_base, row_dest, row_rank, final_row;
+  // device side
+  int device = -1;
+  int sm_count = 0;
+  int consumer_ctas = 0, reorder_ctas = 0;
+  void* blob = nullptr;
+  fo::DeviceTables dev;
+};
+
+namespace fo {
+
+// planner.cpp
+fo_status check_shape(const fo_plan_desc* d, int32_t* W, int32_t* tiles,
+                      int32_t* waves);
+fo_status build_plan(const fo_plan_desc* d, fo_plan* p);
+fo_status upload_plan(fo_plan* p);
+int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r);
+
+// gemm.cu
+fo_status launch_signaled_gemm(const fo_plan* p, const void* A,
+                               const void* const* B, void* C_r,
+                               int32_t* count, uint32_t* flags, uint32_t epoch,
+                               void* stream);
+
+// comm.cu
+fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
+                         const void* src, const void* const* partials,
+                         int32_t n_partials, void* const* dst,
+                         const uint32_t* flags, uint32_t epoch,
+                         uint64_t spin_limit_ns, int32_t* dev_status,
+                         void* stream);
+fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
+                              const void* const* src, void* const* dst,
+                              void* stream);
+
+}  // namespace fo

@@ -1,0 +1,539 @@
+// The signaled GEMM: one persistent, warp-specialised tcgen05 kernel for
+// sm_103a whose epilogue performs the pre-communication reorder and raises
+// the wave-group signal.
+//
+// Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 核心设计 "计算侧" (the GEMM
+// stays a single kernel, not split), 一、信号机制 "实现方法: 组级 Tile 计数" (each
+// finished tile adds 1 to its group's entry of the counting table; reaching
+// |G_j| starts G_j's communication), 二、重排机制 (finished tiles are written to
+// the contiguous range of their group), 五、CUTLASS 扩展实现 "Epilogue 集成"
+// (the signal and the reorder live in the epilogue).  "Efficient and
+// Adaptable Overlapping ...", Figure 5: reorder, then signal.
+//
+// Design for GB300 (the pages' CUTLASS kernel targets sm_80/sm_89):
+//  * W persistent CTAs, one per SM; CTA c computes launch slots c, c+W, ...
+//    so wave k is the k-th tile of every CTA (wave = slot / W exactly).
+//  * warp 0: TMA producer; A tile 128x64 (K-major) and B tile 64xBN
+//    (N-major) per stage, 128-byte swizzle, no multicast.
+//  * warp 1: allocates tensor memory and issues tcgen05.mma (M=128, N=BN,
+//    K=16, bf16 in, fp32 accumulate) from one thread; two accumulators of
+//    BN columns so tile i+1's main loop runs while tile i drains.
+//  * warps 2-5: epilogue; tcgen05.ld 32 lanes x 64 columns, round to bf16,
+//    transpose through a swizzled 4 KB staging buffer per warp, and store
+//    whole 128-byte row segments to the rows' units in C_r; then one
+//    acq_rel atomic on the group's counter and, for the group's last tile,
+//    a release store of the epoch into the group's flag.
+//  * Every mbarrier wait is bounded (globaltimer); a wait that runs out
+//    records FO_ERR_TIMEOUT in the plan's status word and the CTA winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+
+namespace fo {
+
+namespace {
+
+constexpr int kGemmThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kABytes = kTileM * kBlockK * 2;
+  static constexpr int kBBytes = kBlockK * BN * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;
+  static constexpr int kStagingBytes = 4 * 32 * 128;
+  static constexpr int kBarOffset = kStages * kStageBytes + kStagingBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
+  // instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits
+  // 7-9 = 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0), B MN-major
+  // (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+  static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                     (uint32_t(BN >> 3) << 17) |
+                                     (uint32_t(kTileM >> 4) << 24);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(2 * kStages + 7 + 1 <= 32, "barrier area");
+};
+
+struct GemmArgs {
+  CUtensorMap tmap_a;
+  CUtensorMap tmap_b[kMaxExperts];
+  const TileInfo* tile;
+  const int32_t* group_tiles;
+  const int32_t* dest_base;
+  const int32_t* row_dest;
+  const int32_t* row_rank;
+  uint16_t* c_r;
+  int32_t* count;
+  uint32_t* flags;
+  int32_t* status;
+  int32_t tiles, k_blocks, layout, R, h;
+  uint32_t epoch;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Gives up when another
+// role aborted (shared flag) or after kWaitLimitNs; then records the error.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(status, 0, int32_t(FO_ERR_TIMEOUT));
+      return false;
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used while winding down).
+__device__ __noinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address >> 4 at bits
+// 0-13, leading byte offset >> 4 at 16-29, stride byte offset >> 4 at
+// 32-45, version 1 at bits 46-47, layout 2 (128-byte swizzle) at 61-63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr >> 4) & 0x3FFF) | (uint64_t((lbo >> 4) & 0x3FFF) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFF) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- the kernel
+
+// Unit (row of the reordered buffer) of row r of a tile, or -1 past its rows.
+__device__ __forceinline__ int32_t row_unit(const GemmArgs& a, const TileInfo& ti, int32_t slot,
+                                            int32_t r) {
+  if (r >= ti.rows) return -1;
+  if (a.layout == FO_LAYOUT_RS_SUBTILE) {
+    const int32_t k = r / a.h;
+    return ti.unit_base + k * ti.sub_stride + (r - k * a.h);
+  }
+  if (a.layout == FO_LAYOUT_A2A_SUBTOKEN) {
+    const int32_t rho = ti.row0 + r;
+    return a.dest_base[slot * a.R + a.row_dest[rho]] + a.row_rank[rho];
+  }
+  return ti.unit_base + r;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    signaled_gemm_kernel(const __grid_constant__ GemmArgs a) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* staging = smem + C::kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::kStages;
+  uint64_t* acc_full = bars + 2 * C::kStages;
+  uint64_t* acc_empty = bars + 2 * C::kStages + 2;
+  uint64_t* epi_done = bars + 2 * C::kStages + 4;
+  uint64_t* drain = bars + 2 * C::kStages + 6;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 7);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&acc_full[b]), 1);
+      mbar_init(smem_u32(&acc_empty[b]), 4);
+      mbar_init(smem_u32(&epi_done[b]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    prefetch_tmap(&a.tmap_a);
+  }
+  if (warp == 1) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_u32(tmem_slot)),
+        "r"(uint32_t(C::kTmemCols))
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int64_t issued = 0;
+      for (int32_t slot = blockIdx.x; slot < a.tiles && ok; slot += gridDim.x) {
+        const TileInfo ti = a.tile[slot];
+        const CUtensorMap* mb = &a.tmap_b[ti.expert];
+        if (slot == int32_t(blockIdx.x))
+          for (int e = 0; e <= ti.expert; ++e) prefetch_tmap(&a.tmap_b[e]);
+        for (int kb = 0; kb < a.k_blocks; ++kb) {
+          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t sb = sa + C::kABytes;
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_expect_tx(fb, C::kStageBytes);
+          tma_load_2d(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c)
+            tma_load_2d(sb + c * (kBlockK * 128), mb, fb, ti.col0 + c * 64, kb * kBlockK);
+          ++issued;
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // wind-down: let copies already issued land before the CTA exits
+        for (int st = 0; st < C::kStages; ++st) {
+          const int64_t fills = issued / C::kStages + (st < issued % C::kStages ? 1 : 0);
+          if (fills > 0) mbar_wait_plain(smem_u32(&full[st]), uint32_t((fills - 1) & 1), 10000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int32_t slot = blockIdx.x; slot < a.tiles && ok; slot += gridDim.x) {
+        if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < a.k_blocks; ++kb) {
+          if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            // A: K-major, advance 16 elements (32 bytes) inside the swizzle
+            // atom; SBO = 8 rows x 128 B.  B: N-major, advance 16 K rows
+            // (two 1 KB atoms); LBO = 64 K rows x 128 B between 64-column
+            // blocks, SBO = 8 K rows x 128 B.
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc(sb + kk * 2048, kBlockK * 128, 1024);
+            mma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0);
+          }
+          mma_commit(smem_u32(&empty[stage]));
+          if (++stage == C::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&acc_full[acc]));
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* stage_buf = staging + (warp - 2) * (32 * 128);
+    const uint32_t stage_base = smem_u32(stage_buf);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int32_t slot = blockIdx.x; slot < a.tiles; slot += gridDim.x) {
+      const TileInfo ti = a.tile[slot];
+      const int32_t my_unit = row_unit(a, ti, slot, q * 32 + lane);
+      // one lane waits, the decision is warp-uniform (tcgen05.ld is .aligned)
+      int ok = 0;
+      if (lane == 0) ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 64; ++cc) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(t_row + cc * 64, v0);
+        tmem_ld32(t_row + cc * 64 + 32, v1);
+        tmem_wait_ld();
+        // round to bf16 and write this lane's row (128 B) into the staging
+        // buffer, 16-byte pieces rotated by row to spread the banks
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t* src = (c < 4) ? &v0[c * 8] : &v1[(c - 4) * 8];
+          uint32_t w0 = pack_bf16x2(__uint_as_float(src[0]), __uint_as_float(src[1]));
+          uint32_t w1 = pack_bf16x2(__uint_as_float(src[2]), __uint_as_float(src[3]));
+          uint32_t w2 = pack_bf16x2(__uint_as_float(src[4]), __uint_as_float(src[5]));
+          uint32_t w3 = pack_bf16x2(__uint_as_float(src[6]), __uint_as_float(src[7]));
+          const uint32_t off = lane * 128 + ((c ^ (lane & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage_base + off),
+                       "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                       : "memory");
+        }
+        __syncwarp();
+        // read back four rows per instruction (8 lanes x 16 B = 128 B each)
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int row = it * 4 + (lane >> 3);
+          const int piece = lane & 7;
+          const int32_t u = __shfl_sync(0xffffffffu, my_unit, row);
+          uint32_t w0, w1, w2, w3;
+          const uint32_t off = row * 128 + ((piece ^ (row & 7)) << 4);
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(stage_base + off)
+                       : "memory");
+          if (u >= 0) {
+            uint4* dst = reinterpret_cast<uint4*>(a.c_r + int64_t(u) * BN + cc * 64 + piece * 8);
+            *dst = make_uint4(w0, w1, w2, w3);
+          }
+        }
+        __syncwarp();
+      }
+      // This warp's rows are stored: report it, then hand the accumulator
+      // back to the MMA warp.  (The accumulator is released only after the
+      // report, so no warp can report a later tile on this barrier before
+      // every warp reported this one.)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&epi_done[acc]));
+        mbar_arrive(smem_u32(&acc_empty[acc]));
+      }
+      // Once all four warps have stored the tile, count it; the group's last
+      // tile raises the group's flag.
+      if (warp == 2 && lane == 0 && a.count != nullptr) {
+        if (mbar_wait(smem_u32(&epi_done[acc]), acc_phase, abort_flag, a.status)) {
+          __threadfence();
+          const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
+          if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
+        }
+      }
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  __syncthreads();
+  if (warp == 1) {
+    // every MMA this CTA issued has completed before the tensor memory is
+    // released (immediate on the normal path: the epilogue saw them all)
+    if (lane == 0) {
+      mma_commit(smem_u32(drain));
+      mbar_wait_plain(smem_u32(drain), 0, 10000000ull);
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(uint32_t(C::kTmemCols))
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+              uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN>
+fo_status launch_bn(const fo_plan* p, GemmArgs& a, cudaStream_t st) {
+  static std::once_flag attr_once[64];
+  static cudaError_t attr_err[64];
+  const int dev = p->device < 64 ? p->device : 63;
+  std::call_once(attr_once[dev], [&] {
+    attr_err[dev] = cudaFuncSetAttribute(signaled_gemm_kernel<BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<BN>::kSmemBytes);
+  });
+  if (attr_err[dev] != cudaSuccess) return FO_ERR_CUDA;
+  const int grid = p->W < p->tiles ? p->W : p->tiles;
+  signaled_gemm_kernel<BN><<<grid, kGemmThreads, Cfg<BN>::kSmemBytes, st>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
+}
+
+}  // namespace
+
+fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* const* B,
+                               void* C_r, int32_t* count, uint32_t* flags, uint32_t epoch,
+                               void* stream) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, p->device) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, p->device) !=
+          cudaSuccess)
+    return FO_ERR_CUDA;
+  if (major != 10 || minor != 3) return FO_ERR_UNSUPPORTED;
+  const uintptr_t align_bits = reinterpret_cast<uintptr_t>(A) |
+                               reinterpret_cast<uintptr_t>(C_r);
+  if (align_bits & 15) return FO_ERR_ARG;
+  GemmArgs a{};
+  if (!make_map(&a.tmap_a, A, uint64_t(p->K), uint64_t(p->M), kBlockK, kTileM))
+    return FO_ERR_CUDA;
+  const int E = p->n_experts > 0 ? p->n_experts : 1;
+  for (int e = 0; e < E; ++e) {
+    if (!B[e] || (reinterpret_cast<uintptr_t>(B[e]) & 15)) return FO_ERR_ARG;
+    if (!make_map(&a.tmap_b[e], B[e], uint64_t(p->N), uint64_t(p->K), 64, kBlockK))
+      return FO_ERR_CUDA;
+  }
+  a.tile = p->dev.tile;
+  a.group_tiles = p->dev.group_tiles;
+  a.dest_base = p->dev.dest_base;
+  a.row_dest = p->dev.row_dest;
+  a.row_rank = p->dev.row_rank;
+  a.c_r = static_cast<uint16_t*>(C_r);
+  a.count = count;
+  a.flags = flags;
+  a.status = p->dev.gemm_status;
+  a.tiles = p->tiles;
+  a.k_blocks = p->K / kBlockK;
+  a.layout = p->layout;
+  a.R = p->R;
+  a.h = kTileM / p->R;
+  a.epoch = epoch;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return p->tile_n == 256 ? launch_bn<256>(p, a, st) : launch_bn<128>(p, a, st);
+}
+
+}  // namespace fo

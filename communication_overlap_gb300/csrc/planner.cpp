@@ -1,0 +1,379 @@
+// Host planner: launch order, waves, wave groups, counting-table sizes,
+// mapping tables and the reordered layout of one GEMM shape.
+//
+// Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 一、信号机制 (waves are
+// tiles / SMs; block swizzling interleaves the tiles of a wave; a wave group
+// holds consecutive waves; the counting table has one entry per group and
+// the tile's index identifies its group), 二、重排机制 (the mapping table
+// makes a group's data contiguous; Figure 6's tile, subtile and sub-token
+// units), 四、实时调优 Algorithm 1 (T = tile_num / (sm_num - comm_sm_num)).
+//
+// Readings where the pages are silent: the launch order is banded (bands of
+// `swizzle` tile rows, each band walked column by column); wave = slot / W
+// with W persistent GEMM CTAs; |G_j| counts tiles; a unit is one tile row.
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+
+#include <cuda_runtime.h>
+
+#include "fo_internal.h"
+
+namespace fo {
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
+                      int32_t* waves_out) {
+  if (!d) return FO_ERR_ARG;
+  if (d->M <= 0 || d->N <= 0 || d->K <= 0) return FO_ERR_ARG;
+  if (d->tile_m != kTileM) return FO_ERR_UNSUPPORTED;
+  if (d->tile_n != 128 && d->tile_n != 256) return FO_ERR_UNSUPPORTED;
+  if (d->N % d->tile_n != 0 || d->K % kBlockK != 0) return FO_ERR_ARG;
+  if (d->swizzle < 1) return FO_ERR_ARG;
+  if (d->n_experts < 0 || d->n_experts > kMaxExperts) return FO_ERR_ARG;
+  int64_t tiles_m = 0;
+  if (d->n_experts > 0) {
+    if (!d->expert_rows) return FO_ERR_ARG;
+    int64_t sum = 0;
+    for (int e = 0; e < d->n_experts; ++e) {
+      if (d->expert_rows[e] < 0) return FO_ERR_ARG;
+      sum += d->expert_rows[e];
+      tiles_m += ceil_div(d->expert_rows[e], kTileM);
+    }
+    if (sum != d->M) return FO_ERR_ARG;
+  } else {
+    tiles_m = ceil_div(d->M, kTileM);
+  }
+  int64_t tiles = tiles_m * (d->N / d->tile_n);
+  if (tiles <= 0 || tiles > (int64_t(1) << 24)) return FO_ERR_ARG;
+  // units (tile rows) index the reordered buffer in int32
+  if (int64_t(d->M) * (d->N / d->tile_n) >= (int64_t(1) << 31)) return FO_ERR_ARG;
+  int32_t W = d->wave_width;
+  if (W <= 0) {
+    if (d->host_only) return FO_ERR_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FO_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&W, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FO_ERR_CUDA;
+  }
+  if (W_out) *W_out = W;
+  if (tiles_out) *tiles_out = int32_t(tiles);
+  if (waves_out) *waves_out = int32_t(ceil_div(tiles, W));
+  return FO_OK;
+}
+
+// Build every host table.  The layout is computed arithmetically from the
+// group and slot structure (prefix sums), not by walking units.
+fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
+  int32_t W = 0, tiles = 0, waves = 0;
+  fo_status st = check_shape(d, &W, &tiles, &waves);
+  if (st != FO_OK) return st;
+  if (d->n_groups < 1 || !d->group_waves) return FO_ERR_ARG;
+  int64_t wsum = 0;
+  for (int j = 0; j < d->n_groups; ++j) {
+    if (d->group_waves[j] < 1) return FO_ERR_ARG;
+    wsum += d->group_waves[j];
+  }
+  if (wsum != waves) return FO_ERR_ARG;
+
+  const int layout = d->layout;
+  if (layout < FO_LAYOUT_TILE || layout > FO_LAYOUT_A2A_SUBTOKEN) return FO_ERR_ARG;
+  int R = 1;
+  if (layout != FO_LAYOUT_TILE) {
+    R = d->n_dest;
+    if (R < 1 || R > kMaxDest) return FO_ERR_ARG;
+  }
+  if (layout == FO_LAYOUT_RS_SUBTILE || layout == FO_LAYOUT_RS_ROWBLOCK) {
+    if (d->n_experts > 1) return FO_ERR_ARG;
+    if (d->M % kTileM != 0) return FO_ERR_ARG;
+    if (layout == FO_LAYOUT_RS_SUBTILE && kTileM % R != 0) return FO_ERR_ARG;
+    if (layout == FO_LAYOUT_RS_ROWBLOCK && (d->M % R != 0 || (d->M / R) % kTileM != 0))
+      return FO_ERR_ARG;
+  }
+  if (layout == FO_LAYOUT_A2A_SUBTOKEN && (!d->row_token || !d->row_slot))
+    return FO_ERR_ARG;
+
+  p->M = d->M; p->N = d->N; p->K = d->K;
+  p->tile_m = d->tile_m; p->tile_n = d->tile_n; p->swizzle = d->swizzle;
+  p->W = W; p->P = d->n_groups; p->R = R; p->layout = layout;
+  p->n_dest = d->n_dest; p->n_experts = d->n_experts;
+  p->tiles = tiles; p->waves = waves; p->tiles_n = d->N / d->tile_n;
+  const int TN = p->tiles_n, P = p->P;
+
+  if (d->n_experts > 0)
+    p->expert_rows.assign(d->expert_rows, d->expert_rows + d->n_experts);
+  else
+    p->expert_rows.assign(1, d->M);
+  const int E = int(p->expert_rows.size());
+  p->expert_row0.assign(E, 0);
+  p->expert_tile0.assign(E, 0);
+  for (int e = 1; e < E; ++e) {
+    p->expert_row0[e] = p->expert_row0[e - 1] + p->expert_rows[e - 1];
+    p->expert_tile0[e] = p->expert_tile0[e - 1] +
+                         int32_t(ceil_div(p->expert_rows[e - 1], kTileM)) * TN;
+  }
+
+  // Launch order: experts in turn; inside an expert, band b covers tile rows
+  // [b*S, b*S + h) with h = min(S, rows left); position o inside the band is
+  // column o / h, row b*S + o % h.
+  p->slot_tile.assign(tiles, 0);
+  p->tile_slot.assign(tiles, 0);
+  p->tile.assign(tiles, TileInfo{});
+  {
+    int32_t s = 0;
+    for (int e = 0; e < E; ++e) {
+      const int32_t tm_count = int32_t(ceil_div(p->expert_rows[e], kTileM));
+      for (int32_t top = 0; top < tm_count; top += d->swizzle) {
+        const int32_t h = std::min<int32_t>(d->swizzle, tm_count - top);
+        for (int32_t o = 0; o < h * TN; ++o, ++s) {
+          const int32_t tm = top + o % h, tn = o / h;
+          const int32_t t = p->expert_tile0[e] + tm * TN + tn;
+          p->slot_tile[s] = t;
+          p->tile_slot[t] = s;
+          TileInfo& ti = p->tile[s];
+          ti.row0 = p->expert_row0[e] + tm * kTileM;
+          ti.col0 = tn * d->tile_n;
+          ti.rows = std::min<int32_t>(kTileM, p->expert_rows[e] - tm * kTileM);
+          ti.expert = e;
+        }
+      }
+    }
+  }
+
+  // Groups: consecutive wave ranges; slot ranges follow from W.
+  p->group_waves.assign(d->group_waves, d->group_waves + P);
+  p->group_slot_begin.assign(P + 1, 0);
+  p->group_tiles.assign(P, 0);
+  {
+    int64_t wave_end = 0;
+    for (int j = 0; j < P; ++j) {
+      wave_end += p->group_waves[j];
+      p->group_slot_begin[j + 1] = int32_t(std::min<int64_t>(tiles, wave_end * W));
+      p->group_tiles[j] = p->group_slot_begin[j + 1] - p->group_slot_begin[j];
+    }
+  }
+  p->slot_group.assign(tiles, 0);
+  for (int j = 0; j < P; ++j)
+    for (int32_t s = p->group_slot_begin[j]; s < p->group_slot_begin[j + 1]; ++s) {
+      p->slot_group[s] = j;
+      p->tile[s].group = j;
+    }
+
+  // Reordered layout.  A group's units start after all earlier groups'.
+  p->part_start.assign(size_t(P) * R, 0);
+  p->part_len.assign(size_t(P) * R, 0);
+  p->part_dst.assign(size_t(P) * R, 0);
+  p->group_unit_begin.assign(P + 1, 0);
+
+  if (layout == FO_LAYOUT_A2A_SUBTOKEN) {
+    // per routed row: destination rank, rank among the rows of its tile row
+    // going to the same destination, and its row in that rank's output
+    p->row_dest.assign(d->M, 0);
+    p->row_rank.assign(d->M, 0);
+    p->final_row.assign(d->M, 0);
+    int32_t top_k = 1;
+    for (int32_t r = 0; r < d->M; ++r) {
+      if (d->row_token[r] < 0 || d->row_slot[r] < 0) return FO_ERR_ARG;
+      top_k = std::max(top_k, d->row_slot[r] + 1);
+    }
+    p->top_k = top_k;
+    for (int32_t r = 0; r < d->M; ++r) {
+      p->row_dest[r] = d->row_token[r] % R;
+      p->final_row[r] = (d->row_token[r] / R) * top_k + d->row_slot[r];
+    }
+    // rows per (tile row, destination): tile rows are identified by row0
+    std::vector<int32_t> cnt(R);
+    for (int e = 0; e < E; ++e) {
+      for (int32_t b = p->expert_row0[e]; b < p->expert_row0[e] + p->expert_rows[e];
+           b += kTileM) {
+        std::fill(cnt.begin(), cnt.end(), 0);
+        const int32_t end = std::min(b + kTileM, p->expert_row0[e] + p->expert_rows[e]);
+        for (int32_t r = b; r < end; ++r) p->row_rank[r] = cnt[p->row_dest[r]]++;
+      }
+    }
+    // per slot and destination: rows of the tile bound there
+    auto rows_to = [&](int32_t s, int k) {
+      const TileInfo& ti = p->tile[s];
+      int32_t c = 0;
+      for (int32_t r = ti.row0; r < ti.row0 + ti.rows; ++r) c += (p->row_dest[r] == k);
+      return c;
+    };
+    std::vector<int32_t> tile_cnt(size_t(tiles) * R);
+    for (int32_t s = 0; s < tiles; ++s) {
+      // tiles of one tile row share their rows: count once per row0 would
+      // be enough, but the count is cheap
+      for (int k = 0; k < R; ++k) tile_cnt[size_t(s) * R + k] = rows_to(s, k);
+    }
+    p->dest_base.assign(size_t(tiles) * R, 0);
+    int32_t u = 0;
+    for (int j = 0; j < P; ++j) {
+      p->group_unit_begin[j] = u;
+      for (int k = 0; k < R; ++k) {
+        p->part_start[size_t(j) * R + k] = u;
+        for (int32_t s = p->group_slot_begin[j]; s < p->group_slot_begin[j + 1]; ++s) {
+          p->dest_base[size_t(s) * R + k] = u;
+          u += tile_cnt[size_t(s) * R + k];
+        }
+        p->part_len[size_t(j) * R + k] = u - p->part_start[size_t(j) * R + k];
+      }
+    }
+    p->group_unit_begin[P] = u;
+    p->n_units = u;
+  } else if (layout == FO_LAYOUT_RS_SUBTILE) {
+    const int32_t h = kTileM / R;
+    for (int j = 0; j < P; ++j) {
+      const int32_t n_j = p->group_tiles[j];
+      const int32_t gb = p->group_slot_begin[j] * kTileM;  // all tiles are full
+      p->group_unit_begin[j] = gb;
+      for (int k = 0; k < R; ++k) {
+        p->part_start[size_t(j) * R + k] = gb + k * n_j * h;
+        p->part_len[size_t(j) * R + k] = n_j * h;
+      }
+      for (int32_t i = 0; i < n_j; ++i) {
+        TileInfo& ti = p->tile[p->group_slot_begin[j] + i];
+        ti.unit_base = gb + i * h;
+        ti.sub_stride = n_j * h;
+      }
+    }
+    p->group_unit_begin[P] = tiles * kTileM;
+    p->n_units = tiles * kTileM;
+  } else if (layout == FO_LAYOUT_RS_ROWBLOCK) {
+    const int32_t rows_per = d->M / R;
+    for (int32_t s = 0; s < tiles; ++s) p->tile[s].dest = p->tile[s].row0 / rows_per;
+    int32_t u = 0;
+    for (int j = 0; j < P; ++j) {
+      p->group_unit_begin[j] = u;
+      for (int k = 0; k < R; ++k) {
+        p->part_start[size_t(j) * R + k] = u;
+        for (int32_t s = p->group_slot_begin[j]; s < p->group_slot_begin[j + 1]; ++s)
+          if (p->tile[s].dest == k) {
+            p->tile[s].unit_base = u;
+            u += kTileM;
+          }
+        p->part_len[size_t(j) * R + k] = u - p->part_start[size_t(j) * R + k];
+      }
+    }
+    p->group_unit_begin[P] = u;
+    p->n_units = u;
+  } else {  // FO_LAYOUT_TILE: prefix sum of valid rows in slot order
+    int32_t u = 0;
+    for (int j = 0; j < P; ++j) {
+      p->group_unit_begin[j] = u;
+      p->part_start[j] = u;
+      for (int32_t s = p->group_slot_begin[j]; s < p->group_slot_begin[j + 1]; ++s) {
+        p->tile[s].unit_base = u;
+        u += p->tile[s].rows;
+      }
+      p->part_len[j] = u - p->part_start[j];
+    }
+    p->group_unit_begin[P] = u;
+    p->n_units = u;
+  }
+
+  // parts are appended, group after group, to their destination buffer
+  p->dest_units.assign(R, 0);
+  for (int k = 0; k < R; ++k) {
+    int32_t off = 0;
+    for (int j = 0; j < P; ++j) {
+      p->part_dst[size_t(j) * R + k] = off;
+      off += p->part_len[size_t(j) * R + k];
+    }
+    p->dest_units[k] = off;
+  }
+  if (int64_t(p->n_units) != int64_t(d->M) * TN) return FO_ERR_ARG;  // every row once
+
+  // rows of each output of the post-communication reorder
+  if (layout == FO_LAYOUT_TILE) {
+    p->final_rows.assign(1, d->M);
+  } else if (layout == FO_LAYOUT_A2A_SUBTOKEN) {
+    p->final_rows.assign(R, 0);
+    for (int32_t r = 0; r < d->M; ++r)
+      p->final_rows[p->row_dest[r]] = std::max(p->final_rows[p->row_dest[r]], p->final_row[r] + 1);
+  } else {
+    p->final_rows.assign(R, d->M / R);
+  }
+  return FO_OK;
+}
+
+// Unit of row r of the tile at `slot`, from the same per-slot / per-row
+// fields the kernels read (-1 when the tile has no row r).
+int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r) {
+  const TileInfo& ti = p->tile[slot];
+  if (r >= ti.rows) return -1;
+  switch (p->layout) {
+    case FO_LAYOUT_RS_SUBTILE: {
+      const int32_t h = kTileM / p->R;
+      return ti.unit_base + (r / h) * ti.sub_stride + r % h;
+    }
+    case FO_LAYOUT_A2A_SUBTOKEN: {
+      const int32_t rho = ti.row0 + r;
+      return p->dest_base[size_t(slot) * p->R + p->row_dest[rho]] + p->row_rank[rho];
+    }
+    default:
+      return ti.unit_base + r;
+  }
+}
+
+namespace {
+
+template <typename T>
+size_t put(std::vector<char>& buf, const std::vector<T>& v) {
+  size_t off = (buf.size() + 255) & ~size_t(255);
+  buf.resize(off + std::max<size_t>(v.size() * sizeof(T), 16), 0);
+  if (!v.empty()) std::memcpy(buf.data() + off, v.data(), v.size() * sizeof(T));
+  return off;
+}
+
+}  // namespace
+
+// One device allocation holds every table plus the consumer's scratch
+// counters (zeroed by the consume call before each launch).
+fo_status upload_plan(fo_plan* p) {
+  if (cudaGetDevice(&p->device) != cudaSuccess) return FO_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) !=
+      cudaSuccess)
+    return FO_ERR_CUDA;
+  std::vector<char> buf;
+  const size_t o_tile = put(buf, p->tile);
+  const size_t o_gt = put(buf, p->group_tiles);
+  const size_t o_gub = put(buf, p->group_unit_begin);
+  const size_t o_gsb = put(buf, p->group_slot_begin);
+  const size_t o_ps = put(buf, p->part_start);
+  const size_t o_pl = put(buf, p->part_len);
+  const size_t o_pd = put(buf, p->part_dst);
+  const size_t o_db = put(buf, p->dest_base);
+  const size_t o_rd = put(buf, p->row_dest);
+  const size_t o_rr = put(buf, p->row_rank);
+  const size_t o_fr = put(buf, p->final_row);
+  const size_t o_work = put(buf, std::vector<int32_t>(p->P, 0));
+  const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
+  void* blob = nullptr;
+  if (cudaMalloc(&blob, buf.size()) != cudaSuccess) return FO_ERR_CUDA;
+  if (cudaMemcpy(blob, buf.data(), buf.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(blob);
+    return FO_ERR_CUDA;
+  }
+  char* b = static_cast<char*>(blob);
+  p->blob = blob;
+  p->dev.tile = reinterpret_cast<TileInfo*>(b + o_tile);
+  p->dev.group_tiles = reinterpret_cast<int32_t*>(b + o_gt);
+  p->dev.group_unit_begin = reinterpret_cast<int32_t*>(b + o_gub);
+  p->dev.group_slot_begin = reinterpret_cast<int32_t*>(b + o_gsb);
+  p->dev.part_start = reinterpret_cast<int32_t*>(b + o_ps);
+  p->dev.part_len = reinterpret_cast<int32_t*>(b + o_pl);
+  p->dev.part_dst = reinterpret_cast<int32_t*>(b + o_pd);
+  p->dev.dest_base = reinterpret_cast<int32_t*>(b + o_db);
+  p->dev.row_dest = reinterpret_cast<int32_t*>(b + o_rd);
+  p->dev.row_rank = reinterpret_cast<int32_t*>(b + o_rr);
+  p->dev.final_row = reinterpret_cast<int32_t*>(b + o_fr);
+  p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
+  p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
+  return FO_OK;
+}
+
+}  // namespace fo

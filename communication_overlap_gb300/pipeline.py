@@ -1,0 +1,148 @@
+"""Device buffers, streams and the per-iteration call sequence of the path.
+
+Plumbing only: torch provides device memory, streams and events; every
+step of the path is a libfo.so call (see ``fo.py``).  One iteration is
+
+  stream s0: fo_counting_table_init, fo_signaled_gemm(epoch)
+  stream s1: fo_consume_group(all groups, epoch), fo_reorder_back(all)
+  s0 waits for s1
+
+so the consumer processes each wave group as soon as the GEMM's epilogue
+raises that group's flag, while the GEMM keeps computing the rest.
+"""
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import fo
+from .workloads import Workload, Inputs, LAYOUT_TILE
+
+_CONSUMER_OF = {0: fo.FO_CONS_COPY, 1: fo.FO_CONS_SUM, 2: fo.FO_CONS_RS, 3: fo.FO_CONS_A2A}
+
+
+def _dev_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    """uint16 bit array -> device tensor of the same bits (int16 storage)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+
+
+def _bits(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().numpy().view(np.uint16)
+
+
+@dataclass
+class Buffers:
+    A: torch.Tensor
+    B: list
+    partials: list
+    C_r: torch.Tensor
+    count: torch.Tensor
+    flags: torch.Tensor
+    status: torch.Tensor
+    comm: list        # consumer outputs
+    final: list       # post-reorder outputs
+
+
+class Pipeline:
+    """One workload planned and resident on the device."""
+
+    def __init__(self, w: Workload, inp: Inputs, device="cuda", partition=None,
+                 wave_width=None, consumer_ctas=0, reorder_ctas=0, upload=True):
+        self.w = w
+        self.device = torch.device(device)
+        W = w.wave_width if wave_width is None else wave_width
+        self.desc_args = dict(
+            M=w.M, N=w.N, K=w.K, tile_m=w.tile_m, tile_n=w.tile_n, swizzle=w.swizzle,
+            wave_width=W, layout=w.layout, n_dest=w.n_dest,
+            expert_rows=inp.expert_rows if w.grouped else None,
+            row_token=inp.row_token, row_slot=inp.row_slot)
+        probe = fo.make_desc(**self.desc_args, host_only=True)
+        self.tiles, self.waves = fo.fo_wave_count(probe)
+        self.partition = list(partition) if partition else fo.partition_one_then_two(self.waves)
+        self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
+        self.plan = fo.fo_plan_groups(self.desc)
+        fo.fo_plan_set_ctas(self.plan, consumer_ctas, reorder_ctas)
+        _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
+        self.P = len(self.partition)
+        self.kind = _CONSUMER_OF[w.consumer]
+        self.dest_units = fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS)
+        self.final_rows = fo.fo_plan_table(self.plan, fo.FO_TAB_FINAL_ROWS)
+        self.s0 = torch.cuda.Stream(device=self.device)
+        self.s1 = torch.cuda.Stream(device=self.device)
+        self.epoch = 0
+        self.buf = self._alloc(inp) if upload else None
+
+    def _alloc(self, inp):
+        d, w = self.device, self.w
+        A = _dev_bf16(inp.A, d)
+        B = [_dev_bf16(b, d) for b in inp.B]
+        partials = [_dev_bf16(p, d) for p in inp.partials]
+        C_r = torch.empty((w.M * w.N,), dtype=torch.int16, device=d)
+        count = torch.zeros((self.P,), dtype=torch.int32, device=d)
+        flags = torch.zeros((self.P,), dtype=torch.int32, device=d)
+        status = torch.zeros((1,), dtype=torch.int32, device=d)
+        comm = [torch.empty((u * w.tile_n,), dtype=torch.int16, device=d)
+                for u in self.dest_units]
+        final = [torch.empty((r, w.N), dtype=torch.int16, device=d) for r in self.final_rows]
+        return Buffers(A, B, partials, C_r, count, flags, status, comm, final)
+
+    def close(self):
+        fo.fo_plan_destroy(self.plan)
+        self.plan = None
+
+    # ------------------------------------------------------------ calls
+    def gemm(self, stream, epoch, signal=True):
+        b = self.buf
+        if signal:
+            fo.fo_counting_table_init(self.plan, b.count.data_ptr(), stream.cuda_stream)
+        fo.fo_signaled_gemm(self.plan, b.A.data_ptr(), [x.data_ptr() for x in b.B],
+                            b.C_r.data_ptr(), b.count.data_ptr() if signal else 0,
+                            b.flags.data_ptr() if signal else 0, epoch, stream.cuda_stream)
+
+    def consume(self, stream, epoch, group=-1, spin_limit_ns=0):
+        b = self.buf
+        fo.fo_consume_group(self.plan, group, self.kind, b.C_r.data_ptr(),
+                            [p.data_ptr() for p in b.partials],
+                            [c.data_ptr() for c in b.comm], b.flags.data_ptr(), epoch,
+                            spin_limit_ns, b.status.data_ptr(), stream.cuda_stream)
+
+    def reorder(self, stream, g0=0, g1=None):
+        b = self.buf
+        fo.fo_reorder_back(self.plan, g0, self.P if g1 is None else g1,
+                           [c.data_ptr() for c in b.comm], [f.data_ptr() for f in b.final],
+                           stream.cuda_stream)
+
+    def step(self, overlap=True):
+        """One pass of the whole path with a fresh epoch.  With overlap the
+        consumer runs on s1 against the GEMM on s0; without, everything runs
+        on s0 one after the other (the serial baseline)."""
+        self.epoch = (self.epoch + 1) & 0xffffffff or 1
+        e = self.epoch
+        cur = torch.cuda.current_stream(self.device)
+        self.s0.wait_stream(cur)
+        if overlap:
+            self.s1.wait_stream(cur)
+            self.gemm(self.s0, e)
+            self.consume(self.s1, e)
+            self.reorder(self.s1)
+            self.s0.wait_stream(self.s1)
+        else:
+            self.gemm(self.s0, e)
+            self.consume(self.s0, e)
+            self.reorder(self.s0)
+        cur.wait_stream(self.s0)
+        return e
+
+    # ------------------------------------------------------------ results
+    def results(self):
+        torch.cuda.synchronize(self.device)
+        b = self.buf
+        w = self.w
+        return dict(
+            C_r=_bits(b.C_r).reshape(-1, w.tile_n),
+            count=b.count.cpu().numpy().tolist(),
+            flags=b.flags.cpu().numpy().view(np.uint32).tolist(),
+            status=int(b.status.item()),
+            comm=[_bits(c).reshape(-1, w.tile_n) for c in b.comm],
+            final=[_bits(f) for f in b.final],
+        )

@@ -1,0 +1,227 @@
+/*
+ * fo.h -- C ABI of libfo.so: FlashOverlap's signaled GEMM + reorder path on
+ * one GB300 (sm_103a).
+ *
+ * Pages followed (cited by title and section):
+ *  [P1] "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 核心设计 (system overview),
+ *       一、信号机制 (waves, wave groups, counting table), 二、重排机制 (mapping
+ *       table, pre-/post-communication reordering, Figure 6 patterns),
+ *       五、CUTLASS 扩展实现 (epilogue + monitor kernel on its own stream).
+ *  [P2] "Efficient and Adaptable Overlapping for Computation and
+ *       Communication via Signaling and Reordering" -- abstract, Figure 5.
+ *
+ * The pages describe no library interface.  These calls follow their
+ * statement of the problem: plan the wave groups, run one uninterrupted GEMM
+ * that reorders each finished tile into its group's contiguous range and
+ * signals when the group is complete, consume each group as soon as it is
+ * signalled, and reorder the results back.
+ *
+ * Conventions for every call:
+ *  - Matrices are bf16 (2-byte IEEE bfloat16), row-major.  A is M x K (for
+ *    the grouped workload: the routed rows stacked expert after expert), B
+ *    is K x N.  Accumulation is fp32; outputs are bf16 rounded to nearest
+ *    even.
+ *  - A "unit" is one tile row: tile_n consecutive bf16 values (512 bytes at
+ *    tile_n = 256).  The reordered buffer and every consumer buffer are
+ *    arrays of units.
+ *  - Ownership: the caller owns every device buffer it passes (A, B, C_r,
+ *    partials, destinations, counting table, flags, status word).  A plan
+ *    owns its host tables, its device copies of them and a small device
+ *    scratch area; fo_plan_destroy frees them.
+ *  - Streams are cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every launch is asynchronous on that stream.
+ *  - Argument errors return FO_ERR_ARG synchronously and launch nothing.
+ *    A failed CUDA call returns FO_ERR_CUDA.  Device-side waits are bounded:
+ *    a wait that runs out writes FO_ERR_TIMEOUT into the caller's status word
+ *    (read it after synchronising); no kernel traps or asserts.
+ *  - Device pointers must be 16-byte aligned.
+ */
+#ifndef FO_H
+#define FO_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FO_OK = 0,
+  FO_ERR_ARG = 1,          /* invalid argument; nothing launched */
+  FO_ERR_CUDA = 2,         /* a CUDA runtime call or launch failed */
+  FO_ERR_TIMEOUT = 3,      /* a bounded device wait ran out (status word) */
+  FO_ERR_UNSUPPORTED = 4   /* shape or device the kernels do not cover */
+} fo_status;
+
+/* How each wave group is laid out in the reordered buffer ([P1] 二,
+ * Figure 6).  In every layout a group is one contiguous unit range, and the
+ * group's part for destination k is one contiguous sub-range. */
+typedef enum {
+  FO_LAYOUT_TILE = 0,        /* AllReduce / copy: the group's tiles whole, in
+                                launch order, rows in order */
+  FO_LAYOUT_RS_SUBTILE = 1,  /* ReduceScatter: each tile cut along rows into
+                                n_dest subtiles; part k = the k-th subtile of
+                                each of the group's tiles, in launch order */
+  FO_LAYOUT_RS_ROWBLOCK = 2, /* ReduceScatter, literal reading: part k = the
+                                group's whole tiles whose rows lie in rank k's
+                                block of M / n_dest rows */
+  FO_LAYOUT_A2A_SUBTOKEN = 3 /* All-to-All: part d = the tile rows (sub-tokens)
+                                whose token t has t mod n_dest == d, over the
+                                group's tiles in launch order */
+} fo_layout;
+
+/* What stands in for the collective on one GPU ([P1] 二: the reordered
+ * group is what a ncclAllReduce / ReduceScatter / AlltoAll call would send). */
+typedef enum {
+  FO_CONS_COPY = 0,  /* dst[0][u] = src[u] over the group's range */
+  FO_CONS_SUM = 1,   /* dst[0][u] = bf16(((src[u] + P1[u]) + P2[u]) + ...),
+                        every addition in fp32, one rounding */
+  FO_CONS_RS = 2,    /* the same sum; part k of the group is appended to
+                        dst[k] (group after group) */
+  FO_CONS_A2A = 3    /* part d of the group is copied, appended to dst[d] */
+} fo_consumer;
+
+/* Plan description.  Host pointers are read during fo_plan_groups only. */
+typedef struct {
+  int32_t M, N, K;        /* C = A . B sizes; M = sum(expert_rows) if grouped */
+  int32_t tile_m;         /* 128 */
+  int32_t tile_n;         /* 128 or 256; N % tile_n == 0 */
+  int32_t swizzle;        /* band height, in tile rows, of the launch order */
+  int32_t wave_width;     /* W: persistent GEMM CTAs = tiles per wave;
+                             <= 0 means the device's SM count */
+  int32_t n_groups;       /* P */
+  const int32_t* group_waves; /* [P] waves per group, each >= 1, sum = T */
+  fo_layout layout;
+  int32_t n_dest;         /* ranks the layout routes to (RS: R, A2A: D) */
+  int32_t n_experts;      /* 0 = plain GEMM; >= 1 = grouped GEMM */
+  const int32_t* expert_rows; /* [n_experts] routed rows of each expert */
+  const int32_t* row_token;   /* [M] A2A: token id of each routed row */
+  const int32_t* row_slot;    /* [M] A2A: top-k slot of each routed row */
+  int32_t host_only;      /* 1: build host tables only (no device needed) */
+} fo_plan_desc;
+
+typedef struct fo_plan fo_plan;   /* opaque, library-owned */
+
+/* Tiles and waves of a description, T = ceil(tiles / W) ([P1] 一 "关键洞察",
+ * 四 Algorithm 1).  Checks the shape fields only (group_waves may be NULL),
+ * so a caller can choose a partition of T waves before planning. */
+fo_status fo_wave_count(const fo_plan_desc* desc, int32_t* tiles, int32_t* waves);
+
+/* Validate desc, build the launch order (banded swizzle), wave -> group map,
+ * |G_j| in tiles, mapping and inverse mapping tables and the reordered
+ * layout ([P1] 一 "组级 Tile 计数", 二 "映射表重排"), and upload the tables
+ * (unless host_only).  On success *out owns them. */
+fo_status fo_plan_groups(const fo_plan_desc* desc, fo_plan** out);
+
+/* Sizes of a plan.  Any output pointer may be NULL.  group_tiles: [P];
+ * tile_to_slot: [tiles], row-major tile id -> launch slot. */
+fo_status fo_plan_info(const fo_plan* plan, int32_t* tiles, int32_t* waves,
+                       int32_t* n_groups, int32_t* group_tiles,
+                       int32_t* tile_to_slot);
+
+/* Host copies of a plan's tables, for inspection and tests. */
+typedef enum {
+  FO_TAB_SLOT_TILE = 0,   /* [tiles] inverse mapping: slot -> tile id */
+  FO_TAB_TILE_SLOT = 1,   /* [tiles] mapping: tile id -> slot */
+  FO_TAB_SLOT_GROUP = 2,  /* [tiles] group of each slot */
+  FO_TAB_GROUP_TILES = 3, /* [P] |G_j| */
+  FO_TAB_UNIT = 4,        /* [tiles * tile_m] unit of row r of the tile at
+                             slot s (index s * tile_m + r); -1 = no row */
+  FO_TAB_PART_START = 5,  /* [P * R] first unit of part (j, k) in C_r */
+  FO_TAB_PART_LEN = 6,    /* [P * R] units of part (j, k) */
+  FO_TAB_PART_DST = 7,    /* [P * R] offset (units) of part (j, k) in dst[k] */
+  FO_TAB_DEST_UNITS = 8,  /* [R] units each destination buffer receives */
+  FO_TAB_FINAL_ROWS = 9   /* [R] rows of each output of fo_reorder_back
+                             (each row has N values) */
+} fo_table;               /* R = 1 for FO_LAYOUT_TILE, else n_dest */
+
+/* Copy table `which` into out[0 .. capacity); *length = its full length.
+ * FO_ERR_ARG if capacity is too small (length is still set). */
+fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
+                        int64_t capacity, int64_t* length);
+
+/* CTAs the consumer and reorder kernels launch (<= 0: 2 per SM, default). */
+fo_status fo_plan_set_ctas(fo_plan* plan, int32_t consumer_ctas,
+                           int32_t reorder_ctas);
+
+/* Sticky status word of the plan's GEMM launches (the GEMM call has no
+ * status argument): FO_OK, or FO_ERR_TIMEOUT if one of its bounded
+ * pipeline waits ran out.  Synchronises the device; clears the word when
+ * `clear` is non-zero. */
+fo_status fo_plan_device_status(const fo_plan* plan, int32_t* gemm_status,
+                                int32_t clear);
+
+void fo_plan_destroy(fo_plan* plan);
+
+/* Counting table initialisation ([P1] 一 "实现方法: 组级 Tile 计数": the table
+ * starts at [0, ..., 0]): cudaMemsetAsync of count_table[0 .. P) on the
+ * stream the GEMM will run on.  count_table: device int32[P]. */
+fo_status fo_counting_table_init(const fo_plan* plan, int32_t* count_table,
+                                 void* cuda_stream);
+
+/* The signaled GEMM ([P1] 五 "扩展主循环"/"Epilogue 集成", [P2] Figure 5):
+ * one persistent kernel of W CTAs computes every tile of C = A . B
+ * (tcgen05 tensor cores, fp32 accumulation in tensor memory); as each tile
+ * finishes, its epilogue writes the tile's rows, rounded to bf16, to their
+ * units in C_reordered (the pre-communication reorder), then adds 1 to
+ * count_table[j] of the tile's group j, and the tile that makes it reach
+ * |G_j| stores `epoch` into flags[j] (release at GPU scope, after every
+ * store of the group is visible).
+ *  A:  device, M x K bf16 row-major.
+ *  B:  host array of n_experts (1 for a plain GEMM) device pointers, each
+ *      K x N bf16 row-major.
+ *  C_reordered: device, M * N bf16 (M * N / tile_n units).
+ *  count_table: device int32[P], zeroed by the caller before the launch
+ *      (cudaMemsetAsync on the same stream); ends equal to |G_j|.
+ *  flags: device uint32[P].  count_table and flags may both be NULL: the
+ *      GEMM then signals nothing.
+ *  epoch: the value this iteration's flags take; use a new one per
+ *      iteration so flags never need resetting.
+ * Requires K % 64 == 0 and a device with compute capability 10.3. */
+fo_status fo_signaled_gemm(const fo_plan* plan, const void* A,
+                           const void* const* B, void* C_reordered,
+                           int32_t* count_table, uint32_t* flags,
+                           uint32_t epoch, void* cuda_stream);
+
+/* The communication stand-in ([P1] 五 "专用监控内核": a monitor kernel on its
+ * own stream).  For group = j, or every group in order when group = -1, the
+ * kernel waits until flags[j] == epoch (acquire at GPU scope, __nanosleep
+ * back-off, at most spin_limit_ns per group, 0 = 2 s), then processes the
+ * group's contiguous range of src_reordered as `kind` says.
+ *  partials: host array of n_partials device pointers, same layout as
+ *      src_reordered (SUM and RS; n_partials <= 8).
+ *  dst: host array of device pointers: 1 buffer for COPY/SUM (same size as
+ *      src), R buffers for RS/A2A sized by FO_TAB_DEST_UNITS.
+ *  dev_status: device int32, 0 before the call; a wait that runs out sets it
+ *      to FO_ERR_TIMEOUT and the kernel returns without that group's work.
+ * Concurrent consume calls on one plan race on the plan's scratch. */
+fo_status fo_consume_group(const fo_plan* plan, int32_t group,
+                           fo_consumer kind, const void* src_reordered,
+                           const void* const* partials, int32_t n_partials,
+                           void* const* dst, const uint32_t* flags,
+                           uint32_t epoch, uint64_t spin_limit_ns,
+                           int32_t* dev_status, void* cuda_stream);
+
+/* Post-communication reorder ([P1] 二 "通信后重排"): for the groups
+ * [group_begin, group_end), move every unit from where the consumer left it
+ * to its place in the final row-major layout, by the inverse mapping table.
+ *  TILE:        src[0] (consumer output) -> dst[0], M x N.
+ *  RS_SUBTILE:  src[k] = slice k -> dst[k], (M / R) x N; slice row
+ *               h * tm + i holds global row tile_m * tm + h * k + i
+ *               (h = tile_m / R).
+ *  RS_ROWBLOCK: src[k] -> dst[k], (M / R) x N, rows k M/R .. (k+1) M/R - 1.
+ *  A2A:         src[d] -> dst[d]: the sub-token of routed row (token t,
+ *               slot q) lands in row (t / D) * top_k + q of dst[d]
+ *               (top_k = 1 + the largest row_slot).
+ * Stream-ordered after the consumer; no flags. */
+fo_status fo_reorder_back(const fo_plan* plan, int32_t group_begin,
+                          int32_t group_end, const void* const* src,
+                          void* const* dst, void* cuda_stream);
+
+const char* fo_status_string(fo_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FO_H */

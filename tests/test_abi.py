@@ -1,0 +1,76 @@
+"""The C ABI: libfo.so loads on a machine without a GPU and exports every
+function include/fo.h declares; argument errors come back synchronously."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from communication_overlap_gb300 import fo
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "fo.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fo_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("fo_plan_groups", "fo_signaled_gemm", "fo_consume_group",
+                     "fo_reorder_back"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(fo.LIB_PATH)
+    missing = [n for n in _declared() if not hasattr(L, n)]
+    assert not missing, missing
+    # the binding exposes the same names
+    for n in _declared():
+        assert hasattr(fo, n), n
+
+
+def test_status_strings():
+    assert fo.fo_status_string(fo.FO_OK) == "ok"
+    assert "timed out" in fo.fo_status_string(fo.FO_ERR_TIMEOUT)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(N=500),                       # N not a multiple of tile_n
+    dict(K=100),                       # K not a multiple of 64
+    dict(tile_n=64),                   # unsupported tile
+    dict(swizzle=0),
+    dict(group_waves=(1, 2)),          # does not sum to T = 4
+    dict(group_waves=(0, 4)),          # empty group
+    dict(layout=fo.FO_LAYOUT_RS_SUBTILE, n_dest=3),   # R does not divide 128
+    dict(layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=8), # no routing given
+    dict(wave_width=0),                # host-only plan needs an explicit W
+])
+def test_bad_descriptions_are_rejected(bad):
+    args = dict(M=256, N=512, K=256, tile_n=128, swizzle=2, wave_width=2,
+                group_waves=(1, 2, 1), host_only=True)
+    args.update(bad)
+    d = fo.make_desc(**args)
+    with pytest.raises(fo.FoError) as e:
+        fo.fo_plan_groups(d)
+    assert e.value.status in (fo.FO_ERR_ARG, fo.FO_ERR_UNSUPPORTED)
+
+
+def test_host_only_plan_refuses_launches():
+    d = fo.make_desc(M=256, N=512, K=256, tile_n=128, swizzle=2, wave_width=2,
+                     group_waves=(1, 2, 1), host_only=True)
+    plan = fo.fo_plan_groups(d)
+    try:
+        with pytest.raises(fo.FoError) as e:
+            fo.fo_signaled_gemm(plan, 16, [16], 16, 16, 16, 1, 0)
+        assert e.value.status == fo.FO_ERR_ARG
+        with pytest.raises(fo.FoError):
+            fo.fo_reorder_back(plan, 0, 3, [16], [16], 0)
+        with pytest.raises(fo.FoError):
+            fo.fo_consume_group(plan, -1, fo.FO_CONS_COPY, 16, [], [16], 16, 1, 0, 16, 0)
+    finally:
+        fo.fo_plan_destroy(plan)

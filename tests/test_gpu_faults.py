@@ -1,0 +1,75 @@
+"""Failure handling on the GPU without faulting it (-m gpu).
+
+A consumer whose flags are never raised must give up after its bounded
+wait, report FO_ERR_TIMEOUT in the status word and leave the context usable.
+No trap, no bad address, no endless loop: the wait is a flag nothing sets.
+"""
+import numpy as np
+import pytest
+import torch
+
+from communication_overlap_gb300 import fo
+from communication_overlap_gb300 import workloads as W
+from communication_overlap_gb300.pipeline import Pipeline
+
+pytestmark = pytest.mark.gpu
+
+
+def _pipe():
+    w = W.scaled(W.WORKLOADS["wave_pattern"], M=256, N=512, K=128, wave_width=2)
+    return Pipeline(w, W.make_inputs(w))
+
+
+def test_consumer_times_out_without_gemm():
+    pipe = _pipe()
+    try:
+        pipe.buf.flags.zero_()
+        pipe.buf.status.zero_()
+        torch.cuda.synchronize()
+        pipe.consume(pipe.s1, epoch=12345, spin_limit_ns=2_000_000)   # 2 ms
+        torch.cuda.synchronize()
+        assert int(pipe.buf.status.item()) == fo.FO_ERR_TIMEOUT
+        # the context still works: a normal iteration afterwards is clean
+        pipe.buf.status.zero_()
+        torch.cuda.synchronize()
+        pipe.step()
+        res = pipe.results()
+        assert res["status"] == 0
+        assert res["count"] == pipe.group_tiles
+    finally:
+        pipe.close()
+
+
+def test_stale_epoch_times_out():
+    """Flags left at an older epoch do not satisfy a newer wait."""
+    pipe = _pipe()
+    try:
+        pipe.step()
+        torch.cuda.synchronize()
+        pipe.buf.status.zero_()
+        torch.cuda.synchronize()
+        pipe.consume(pipe.s1, epoch=pipe.epoch + 1, spin_limit_ns=1_000_000)
+        torch.cuda.synchronize()
+        assert int(pipe.buf.status.item()) == fo.FO_ERR_TIMEOUT
+        assert fo.fo_plan_device_status(pipe.plan) == 0   # the GEMM never timed out
+    finally:
+        pipe.close()
+
+
+def test_bad_arguments_launch_nothing():
+    pipe = _pipe()
+    try:
+        with pytest.raises(fo.FoError) as e:
+            fo.fo_consume_group(pipe.plan, 7, fo.FO_CONS_COPY, pipe.buf.C_r.data_ptr(), [],
+                                [pipe.buf.comm[0].data_ptr()], pipe.buf.flags.data_ptr(), 1,
+                                0, pipe.buf.status.data_ptr(), 0)
+        assert e.value.status == fo.FO_ERR_ARG
+        with pytest.raises(fo.FoError):
+            fo.fo_reorder_back(pipe.plan, 1, 0, [pipe.buf.comm[0].data_ptr()],
+                               [pipe.buf.final[0].data_ptr()], 0)
+        with pytest.raises(fo.FoError):   # misaligned A
+            fo.fo_signaled_gemm(pipe.plan, pipe.buf.A.data_ptr() + 2,
+                                [pipe.buf.B[0].data_ptr()], pipe.buf.C_r.data_ptr(), 0, 0,
+                                1, 0)
+    finally:
+        pipe.close()

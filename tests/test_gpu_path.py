@@ -1,0 +1,162 @@
+"""GPU parity of the whole path against the CPU oracle (-m gpu).
+
+Tables, reorders, consumer outputs and the counting table are compared
+bit-exact (the reorders and consumers on the GPU's own GEMM output); the
+GEMM within relative Frobenius 5e-3 and |d| <= 2e-2 (1 + |ref|) per element
+against the fp64 oracle, and bit-exact where the result is exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from communication_overlap_gb300 import fo
+from communication_overlap_gb300 import workloads as W
+from communication_overlap_gb300.pipeline import Pipeline
+from oracle import bf16 as OB
+from oracle import gemm as OG
+
+from gpu_checks import check_run, run_workload, gpu_gemm_output, oracle_plan
+
+pytestmark = pytest.mark.gpu
+
+
+def _small(name, **kw):
+    return W.scaled(W.WORKLOADS[name], **kw)
+
+
+def test_worked_example_end_to_end():
+    pipe, inp, res = run_workload(W.WORKLOADS["worked_example"])
+    try:
+        assert res["count"] == [2, 4, 2]   # the page's final counting table
+        check_run(pipe, inp, res)
+    finally:
+        pipe.close()
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+@pytest.mark.parametrize("case", [
+    dict(name="wave_pattern", M=512, N=1024, K=512, wave_width=6),          # 16 tiles
+    dict(name="wave_pattern", M=300, N=768, K=192, wave_width=4, swizzle=3),  # ragged M
+    dict(name="worked_example", M=640, N=384, K=320, wave_width=5),          # BN=128
+    dict(name="allreduce", M=512, N=1024, K=448, wave_width=5),
+    dict(name="reducescatter", M=1024, N=512, K=384, wave_width=7),
+])
+def test_small_cases(case, overlap):
+    case = dict(case)
+    w = _small(case.pop("name"), **case)
+    pipe, inp, res = run_workload(w, overlap=overlap)
+    try:
+        check_run(pipe, inp, res)
+    finally:
+        pipe.close()
+
+
+def test_rowblock_layout():
+    w = _small("reducescatter", M=1024, N=512, K=192, wave_width=3,
+               layout=W.LAYOUT_RS_ROWBLOCK)
+    pipe, inp, res = run_workload(w)
+    try:
+        check_run(pipe, inp, res)
+    finally:
+        pipe.close()
+
+
+def test_small_alltoall_ragged_experts():
+    w = _small("alltoall", M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5,
+               wave_width=9)
+    pipe, inp, res = run_workload(w)
+    try:
+        assert any(m % 128 for m in inp.expert_rows)
+        check_run(pipe, inp, res)
+    finally:
+        pipe.close()
+
+
+def test_gemm_exact_unit_entries_and_identity():
+    """Entries in {-1, 0, 1} with K <= 256 give exact integer sums: the GPU
+    result must equal the oracle bit for bit; an identity A returns B."""
+    w = _small("wave_pattern", M=384, N=512, K=256, wave_width=4)
+    rng = np.random.default_rng(5)
+    inp = W.make_inputs(w)
+    inp.A = OB.round_to_bf16(rng.integers(-1, 2, (w.M, w.K)).astype(np.float64))
+    inp.B = [OB.round_to_bf16(rng.integers(-1, 2, (w.K, w.N)).astype(np.float64))]
+    pipe, inp, res = run_workload(w, inp)
+    try:
+        op = oracle_plan(w, inp, pipe.partition)
+        C = gpu_gemm_output(pipe, res, op)
+        assert np.array_equal(C, OG.gemm_bf16(inp.A, inp.B[0]))
+    finally:
+        pipe.close()
+    w2 = _small("wave_pattern", M=256, N=512, K=256, wave_width=4)
+    inp2 = W.make_inputs(w2)
+    inp2.A = OB.round_to_bf16(np.eye(256))
+    pipe, inp2, res = run_workload(w2, inp2)
+    try:
+        op = oracle_plan(w2, inp2, pipe.partition)
+        assert np.array_equal(gpu_gemm_output(pipe, res, op), inp2.B[0])
+    finally:
+        pipe.close()
+
+
+def test_signals_off_and_repeat_epochs():
+    """With count/flags NULL the GEMM writes the same C_r and signals
+    nothing; repeated epochs keep flags monotone without resets."""
+    w = _small("wave_pattern", M=512, N=1024, K=256, wave_width=6)
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp)
+    try:
+        for _ in range(3):
+            pipe.step()
+        ref = pipe.results()
+        assert ref["flags"] == [3] * pipe.P
+        pipe.buf.C_r.zero_()
+        torch.cuda.synchronize()
+        pipe.gemm(pipe.s0, 99, signal=False)
+        torch.cuda.synchronize()
+        res = pipe.results()
+        assert np.array_equal(res["C_r"], ref["C_r"])
+        assert res["flags"] == [3] * pipe.P
+    finally:
+        pipe.close()
+
+
+def test_per_group_calls_match_whole_call():
+    """Consuming and reordering group by group gives the same bytes as the
+    single all-groups call."""
+    w = _small("allreduce", M=512, N=1024, K=256, wave_width=3)
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp)
+    try:
+        pipe.step()
+        whole = pipe.results()
+        for c in pipe.buf.comm + pipe.buf.final:
+            c.zero_()
+        torch.cuda.synchronize()
+        e = pipe.epoch
+        for j in range(pipe.P):
+            pipe.consume(pipe.s1, e, group=j)
+            pipe.reorder(pipe.s1, j, j + 1)
+        torch.cuda.synchronize()
+        parts = pipe.results()
+        for a, b in zip(whole["comm"] + whole["final"], parts["comm"] + parts["final"]):
+            assert np.array_equal(a, b)
+    finally:
+        pipe.close()
+
+
+FULL = ["wave_pattern", "allreduce", "reducescatter", "alltoall"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    """Each workload at full size, overlapped as the benchmark runs it:
+    every table, reorder and consumer output bit-exact; the GEMM on 512
+    sampled rows against the fp64 oracle."""
+    w = W.WORKLOADS[name]
+    pipe, inp, res = run_workload(w, steps=3)
+    try:
+        rng = np.random.default_rng(123)
+        rows = np.sort(rng.choice(w.M, size=512, replace=False))
+        check_run(pipe, inp, res, gemm_rows=rows, full_gemm=False)
+    finally:
+        pipe.close()

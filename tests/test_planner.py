@@ -1,0 +1,91 @@
+"""The CUDA path's host planner against the oracle, table by table,
+bit-exact (no GPU: host-only plans)."""
+import numpy as np
+import pytest
+
+from communication_overlap_gb300 import fo
+from communication_overlap_gb300 import workloads as W
+from oracle import plan as OP
+
+_LAYOUT_NAME = {fo.FO_LAYOUT_TILE: OP.LAYOUT_TILE, fo.FO_LAYOUT_RS_SUBTILE: OP.LAYOUT_RS_SUBTILE,
+                fo.FO_LAYOUT_RS_ROWBLOCK: OP.LAYOUT_RS_ROWBLOCK,
+                fo.FO_LAYOUT_A2A_SUBTOKEN: OP.LAYOUT_A2A}
+
+
+def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
+             partition=None):
+    M = int(sum(expert_rows))
+    grouped = tok is not None or len(expert_rows) > 1
+    args = dict(M=M, N=N, K=K, tile_n=tile_n, swizzle=S, wave_width=Wd, layout=layout,
+                n_dest=R, expert_rows=list(expert_rows) if grouped else None,
+                row_token=tok, row_slot=sl, host_only=True)
+    tiles, T = fo.fo_wave_count(fo.make_desc(**args))
+    if partition is None:
+        partition = OP.one_then_two(OP.wave_count(tiles, Wd))
+    plan = fo.fo_plan_groups(fo.make_desc(**args, group_waves=partition))
+    try:
+        op = OP.build_plan(list(expert_rows), N, K, 128, tile_n, S, Wd, partition,
+                           _LAYOUT_NAME[layout], R, tok, sl)
+        assert (tiles, T) == (op.tiles, op.waves)
+        t, waves, gt, t2s = fo.fo_plan_info(plan)
+        assert (t, waves) == (op.tiles, op.waves)
+        assert gt == op.group_tiles.tolist()
+        assert t2s == op.tile_to_slot.tolist()
+        assert fo.fo_plan_table(plan, fo.FO_TAB_SLOT_TILE) == op.slot_to_tile.tolist()
+        assert fo.fo_plan_table(plan, fo.FO_TAB_SLOT_GROUP) == op.slot_group.tolist()
+        unit = np.array(fo.fo_plan_table(plan, fo.FO_TAB_UNIT)).reshape(op.tiles, 128)
+        assert np.array_equal(unit, op.unit)
+        for which, ref in ((fo.FO_TAB_PART_START, op.part_start),
+                           (fo.FO_TAB_PART_LEN, op.part_len),
+                           (fo.FO_TAB_PART_DST, op.part_dst)):
+            assert fo.fo_plan_table(plan, which) == ref.reshape(-1).tolist()
+        assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_UNITS) == \
+            [OP.dest_rows(op, k) for k in range(op.part_start.shape[1])]
+    finally:
+        fo.fo_plan_destroy(plan)
+
+
+def test_worked_example_tables():
+    _compare([256], 512, 256, 128, 2, 2, fo.FO_LAYOUT_TILE, partition=(1, 2, 1))
+
+
+@pytest.mark.parametrize("name", ["wave_pattern", "allreduce", "reducescatter"])
+def test_workload_tables(name):
+    w = W.WORKLOADS[name]
+    _compare([w.M], w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest)
+
+
+def test_alltoall_workload_tables():
+    w = W.WORKLOADS["alltoall"]
+    er, tok, sl = W.routing(w)
+    _compare(er, w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest, tok, sl)
+
+
+def test_rowblock_tables():
+    _compare([1024], 1024, 64, 256, 3, 5, fo.FO_LAYOUT_RS_ROWBLOCK, R=4)
+
+
+@pytest.mark.parametrize("rows", [[300], [128, 5, 0, 260], [1]])
+def test_ragged_tile_tables(rows):
+    _compare(rows, 768, 64, 256, 2, 3, fo.FO_LAYOUT_TILE)
+
+
+def test_ragged_a2a_tables():
+    rng = np.random.default_rng(0)
+    n_tok, E, k, D = 300, 5, 2, 8
+    picks = np.argsort(rng.random((n_tok, E)), axis=1)[:, :k]
+    tok = np.repeat(np.arange(n_tok), k)
+    sl = np.tile(np.arange(k), n_tok)
+    ex = picks.reshape(-1)
+    order = np.lexsort((sl, tok, ex))
+    er = np.bincount(ex, minlength=E).tolist()
+    _compare(er, 512, 64, 128, 3, 7, fo.FO_LAYOUT_A2A_SUBTOKEN, D, tok[order], sl[order])
+
+
+@pytest.mark.parametrize("tm,tn,S,Wd", [(3, 5, 2, 4), (4, 4, 8, 3), (5, 3, 3, 7)])
+def test_every_partition_tables(tm, tn, S, Wd):
+    T = OP.wave_count(tm * tn, Wd)
+    for part in OP.design_space(T):
+        _compare([tm * 128], tn * 128, 64, 128, S, Wd, fo.FO_LAYOUT_TILE, partition=part)
+        _compare([tm * 128], tn * 128, 64, 128, S, Wd, fo.FO_LAYOUT_RS_SUBTILE, R=4,
+                 partition=part)
