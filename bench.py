@@ -1,0 +1,477 @@
+"""Benchmark of the signaled-GEMM + reorder path (one JSON line on rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+A step is one pass of the whole path on the workload (default: the
+wave-pattern GEMM M=2048, N=8192, K=8192, 128x256 tiles, 148-CTA waves,
+groups of 1 then 2 waves, copy consumer + reorder back), inputs resident in
+HBM: counting-table reset, signaled GEMM, consumer (a programmatic
+dependent launch running alongside the GEMM) and post-communication
+reorder.  ``value`` is the GEMM's FLOPs per step divided by the step time
+(TFLOPS of the whole overlapped step).  L2 is flushed (a 256 MiB write)
+before every timed step, outside the timed events.
+
+Extra keys: the GEMM alone (signals on and off), the consumer+reorder alone
+(flags already raised), the serial step (consumer after the GEMM), the
+overlap ratio serial/overlapped, the GEMM's in-kernel duration inside the
+overlapped step (per-tile globaltimer stamps) and its slowdown against the
+GEMM alone, ``roofline`` of the dominant kernel (the GEMM), ``e2e`` through
+the C ABI with host buffers, and ``cpu_baseline`` (the CPU oracle on a
+bounded sample).
+
+For N > 1 (torchrun) every rank runs its own replica of the workload (the
+path has no data exchange on one node: "replicas only"); value sums the
+ranks' FLOPs over the slowest rank's time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wave_pattern")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace-out", default="", help="write per-tile stamps (json)")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+# ----------------------------------------------------------------- peaks / clocks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], d["bf16_tflops"], d["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- timing helpers
+
+def timed(torch, stream, fn, steps, flush=None):
+    """Run fn() `steps` times on `stream`; CUDA events around each call,
+    L2 flushed before each (outside the events).  Returns per-call ms."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def traffic_from_profile(kernel_src):
+    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if
+    it was taken on the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "signaled_gemm_wave_pattern_ncu.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    src, traffic = None, None
+    for line in txt.splitlines():
+        if line.startswith("source_sha256_16:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            try:
+                traffic = float(line.split(":", 1)[1].strip())
+            except ValueError:
+                traffic = None
+    return traffic if src == h else None
+
+
+# ----------------------------------------------------------------- CPU oracle leg
+
+def calibrate_rows(w, inp, cpu_seconds):
+    """Output rows of the oracle's GEMM sample: grown by 4x until one GEMM
+    on them takes about a quarter of the CPU budget."""
+    from oracle import gemm as OG
+    rows = 128
+    while rows < w.M:
+        t0 = time.perf_counter()
+        OG.gemm_rows_bf16(inp.A, inp.B, inp.expert_rows, np.arange(rows))
+        if time.perf_counter() - t0 > cpu_seconds / 16:
+            break
+        rows = min(w.M, rows * 4)
+    return rows
+
+
+_LAYOUT_NAMES = {0: "tile", 1: "rs_subtile", 2: "rs_rowblock", 3: "a2a"}
+
+
+def oracle_sample(w, inp, partition, rows):
+    """Time the CPU oracle on a bounded sample of the workload: the fp64 GEMM
+    on the first `rows` output rows, plus pre-reorder, consumer and
+    post-reorder on the full output (the plan is built once per shape and
+    not counted).  Returns (seconds per full step estimate, description,
+    cores)."""
+    from oracle import gemm as OG
+    from oracle import pipeline as OPL
+
+    t0 = time.perf_counter()
+    OG.gemm_rows_bf16(inp.A, inp.B, inp.expert_rows, np.arange(rows))
+    t_rows = time.perf_counter() - t0
+    gemm_full = t_rows * (w.M / rows)
+    # the rest of the path on the full output (values do not matter for time)
+    C = np.zeros((w.M, w.N), dtype=np.uint16)
+    cons = {0: "copy", 1: "sum", 2: "rs", 3: "a2a"}[w.consumer]
+    res = OPL.run(inp.expert_rows, w.N, w.K, w.tile_m, w.tile_n, w.swizzle, w.wave_width,
+                  partition, _LAYOUT_NAMES[w.layout], cons, inp.A, inp.B, inp.partials,
+                  w.n_dest, inp.row_token, inp.row_slot, w.top_k or 2, C_given=C)
+    rest = sum(v for k, v in res.seconds.items() if k not in ("gemm", "plan"))
+    desc = (f"fp64 GEMM on {rows} of {w.M} output rows ({t_rows:.2f} s, scaled x"
+            f"{w.M / rows:.1f}) + pre-reorder, consumer and post-reorder on the full "
+            f"output ({rest:.2f} s); plan ({res.seconds['plan']:.2f} s) excluded")
+    return gemm_full + rest, desc, os.cpu_count()
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, as it stands, on this host's cores."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from communication_overlap_gb300 import workloads as W
+    from oracle import plan as OPN
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    tiles = sum(-(-m // w.tile_m) for m in inp.expert_rows) * (w.N // w.tile_n)
+    partition = OPN.one_then_two(OPN.wave_count(tiles, w.wave_width))
+    per = []
+    budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
+    rows = calibrate_rows(w, inp, budget)
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        secs, desc, cores = oracle_sample(w, inp, partition, rows)
+        if i >= args.warmup:
+            per.append(secs)
+    step_s = statistics.mean(per)
+    value = w.gemm_flops() / step_s / 1e12
+    line = {
+        "impl": "reference", "metric": "signaled GEMM TFLOPS (% of bf16 peak); "
+        "overlap time vs serial GEMM+consumer", "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(w)},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_name(w):
+    if w.grouped:
+        return (f"{w.name}: grouped bf16 GEMM {w.n_tokens} tokens x top-{w.top_k} over "
+                f"{w.n_experts} experts, N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
+                f"W={w.wave_width}, swizzle {w.swizzle}")
+    return (f"{w.name}: bf16 GEMM M={w.M} N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
+            f"W={w.wave_width}, swizzle {w.swizzle}")
+
+
+# ----------------------------------------------------------------- our path
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from communication_overlap_gb300 import fo
+    from communication_overlap_gb300 import workloads as W
+    from communication_overlap_gb300.pipeline import Pipeline
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp, device=dev)
+    s = pipe.s0
+    flops = w.gemm_flops()
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    trace = torch.zeros(pipe.tiles + w.wave_width, dtype=torch.int64, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up (also the first correctness evidence: status and counting table)
+    for _ in range(max(3, args.warmup)):
+        pipe.step(overlap=True)
+    torch.cuda.synchronize()
+    assert int(pipe.buf.status.item()) == 0, "consumer wait timed out"
+    assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
+
+    # the headline: overlapped steps
+    barrier()
+    with Clocks(local) as clk:
+        t_ov = timed(torch, s, lambda: pipe.step(overlap=True, sync_current=False),
+                     args.steps, flush)
+    barrier()
+    ms_ov = statistics.mean(t_ov)
+    status_ok = int(pipe.buf.status.item()) == 0
+
+    # serial baseline: consumer after the GEMM
+    t_ser = timed(torch, s, lambda: pipe.step(overlap=False, sync_current=False),
+                  args.steps, flush)
+    # GEMM alone (signals on, as in the step; and off)
+    t_gemm = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch), args.steps, flush)
+    t_gemm_nosig = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch, signal=False),
+                         args.steps, flush)
+    # consumer + reorder alone: the flags of the last epoch are already raised;
+    # ordinary launches so nothing overlaps the flush before them
+    pipe.step(overlap=True)
+    torch.cuda.synchronize()
+    pipe.set_overlap(False)
+
+    def cons_alone():
+        pipe.consume(s, pipe.epoch)
+        pipe.reorder(s)
+    t_cons = timed(torch, s, cons_alone, args.steps, flush)
+
+    def cons_only():
+        pipe.consume(s, pipe.epoch)
+    t_cons_only = timed(torch, s, cons_only, args.steps, flush)
+    t_reo = timed(torch, s, lambda: pipe.reorder(s), args.steps, flush)
+    pipe.set_overlap(True)
+
+    # in-kernel GEMM duration (per-tile stamps) alone and inside the step
+    fo.fo_plan_set_trace(pipe.plan, trace.data_ptr())
+
+    def gemm_span():
+        t = trace.cpu().numpy().astype(np.int64)
+        starts = t[pipe.tiles:pipe.tiles + min(w.wave_width, pipe.tiles)]
+        return (t[:pipe.tiles].max() - starts.min()) / 1e6, t
+
+    span_alone, span_step = [], []
+    for _ in range(args.steps):
+        with torch.cuda.stream(s):
+            flush()
+        pipe.gemm(s, pipe.epoch)
+        torch.cuda.synchronize()
+        span_alone.append(gemm_span()[0])
+        with torch.cuda.stream(s):
+            flush()
+        pipe.step(overlap=True)
+        torch.cuda.synchronize()
+        sp, stamps = gemm_span()
+        span_step.append(sp)
+    fo.fo_plan_set_trace(pipe.plan, 0)
+    if args.trace_out:
+        t0 = stamps[pipe.tiles:].min()
+        with open(args.trace_out, "w") as f:
+            json.dump({"tile_done_us": ((stamps[:pipe.tiles] - t0) / 1e3).tolist(),
+                       "wave_width": w.wave_width, "partition": pipe.partition}, f)
+
+    # end to end through the C ABI with host buffers
+    hA = torch.from_numpy(inp.A.view(np.int16)).pin_memory()
+    hB = [torch.from_numpy(b.view(np.int16)).pin_memory() for b in inp.B]
+    hP = [torch.from_numpy(p.view(np.int16)).pin_memory() for p in inp.partials]
+    hOut = [torch.empty(f.shape, dtype=torch.int16).pin_memory() for f in pipe.buf.final]
+    h2d = hA.numel() * 2 + sum(b.numel() * 2 for b in hB) + sum(p.numel() * 2 for p in hP)
+    d2h = sum(o.numel() * 2 for o in hOut)
+
+    def e2e_step():
+        with torch.cuda.stream(s):
+            pipe.buf.A.copy_(hA, non_blocking=True)
+            for d_, h_ in zip(pipe.buf.B, hB):
+                d_.copy_(h_, non_blocking=True)
+            for d_, h_ in zip(pipe.buf.partials, hP):
+                d_.copy_(h_, non_blocking=True)
+        pipe.step(overlap=True, sync_current=False)
+        with torch.cuda.stream(s):
+            for h_, d_ in zip(hOut, pipe.buf.final):
+                h_.copy_(d_, non_blocking=True)
+    t_e2e = timed(torch, s, e2e_step, args.steps, flush)
+
+    # max over ranks
+    def rmax(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms_ov = rmax(ms_ov)
+    ms_ser = rmax(statistics.mean(t_ser))
+    ms_gemm = rmax(statistics.mean(t_gemm))
+    ms_e2e = rmax(statistics.mean(t_e2e))
+
+    hbm, peak_burst, peak_sust, peak_kind = measured_peaks()
+    gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
+    traffic = traffic_from_profile(os.path.join(ROOT, "communication_overlap_gb300",
+                                                "csrc", "gemm.cu"))
+    cons_bytes = consumer_bytes(w, pipe)
+    reo_bytes = 2 * w.M * w.N * 2
+    out = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            rows = calibrate_rows(w, inp, args.cpu_seconds)
+            secs, desc, cores = oracle_sample(w, inp, pipe.partition, rows)
+            cpu = {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": cores,
+                   "kind": "oracle", "sample": desc}
+        out = {
+            "metric": "signaled GEMM TFLOPS (% of bf16 peak); overlap time vs serial "
+                      "GEMM+consumer",
+            "value": world * flops / (ms_ov * 1e-3) / 1e12,
+            "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_ov, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(w), "partition": pipe.partition,
+                       "groups_tiles": pipe.group_tiles, "consumer": consumer_name(w),
+                       "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_burst,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,
+                         "traffic": traffic,
+                         "kernel": "signaled_gemm_kernel<256> (alone, signals on)",
+                         "peak_source": f"{peak_kind} bf16 burst"},
+            "clocks": clk.summary(),
+            "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": ms_e2e},
+            "gpu_launches": 3 * args.steps,
+            "cpu_baseline": cpu,
+            "detail": {
+                "ms_overlapped_step": ms_ov,
+                "ms_serial_step": ms_ser,
+                "overlap_speedup": ms_ser / ms_ov,
+                "ms_gemm_alone": ms_gemm,
+                "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
+                "gemm_tflops_alone": gemm_tflops,
+                "gemm_frac_of_sustained": gemm_tflops / peak_sust,
+                "ms_consumer_plus_reorder_alone": statistics.mean(t_cons),
+                "ms_consumer_alone": statistics.mean(t_cons_only),
+                "ms_reorder_alone": statistics.mean(t_reo),
+                "consumer_gbs": cons_bytes / (statistics.mean(t_cons_only) * 1e-3) / 1e9,
+                "reorder_gbs": reo_bytes / (statistics.mean(t_reo) * 1e-3) / 1e9,
+                "hbm_peak_gbs": hbm,
+                "gemm_in_kernel_ms_alone": statistics.median(span_alone),
+                "gemm_in_kernel_ms_in_step": statistics.median(span_step),
+                "gemm_slowdown": statistics.median(span_step) / statistics.median(span_alone),
+                "status_ok": status_ok,
+            },
+        }
+        print(json.dumps(out))
+    pipe.close()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def consumer_name(w):
+    return {0: "copy", 1: f"sum with {w.n_partials} partials",
+            2: f"sum with {w.n_partials} partials + scatter to {w.n_dest} slices",
+            3: f"bucket by token mod {w.n_dest}"}[w.consumer]
+
+
+def consumer_bytes(w, pipe):
+    """Algorithmic bytes of the consumer: every source read once, every
+    output written once."""
+    c = w.M * w.N * 2
+    if w.consumer in (1, 2):
+        return c * (1 + w.n_partials) + c
+    return 2 * c
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

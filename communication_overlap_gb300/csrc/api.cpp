@@ -72,10 +72,18 @@ fo_status fo_plan_table(const fo_plan* p, int32_t which, int32_t* out,
   return FO_OK;
 }
 
-fo_status fo_plan_set_ctas(fo_plan* p, int32_t consumer_ctas, int32_t reorder_ctas) {
+fo_status fo_plan_set_launch(fo_plan* p, int32_t consumer_ctas, int32_t reorder_ctas,
+                             int32_t overlap) {
   if (!p) return FO_ERR_ARG;
   p->consumer_ctas = consumer_ctas;
   p->reorder_ctas = reorder_ctas;
+  p->overlap = overlap ? 1 : 0;
+  return FO_OK;
+}
+
+fo_status fo_plan_set_trace(fo_plan* p, uint64_t* stamps) {
+  if (!p) return FO_ERR_ARG;
+  p->trace = stamps;
   return FO_OK;
 }
 

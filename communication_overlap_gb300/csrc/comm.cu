@@ -12,6 +12,8 @@
 // coalesced segment.
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 
 namespace fo {
@@ -30,8 +32,8 @@ struct ConsumeArgs {
   const int32_t* part_start;
   const int32_t* part_len;
   const int32_t* part_dst;
-  int32_t* work;
-  int32_t g0, g1, n_partials, R, vpu_shift, chunk_units;
+  int32_t* work;   // [P] chunk counters, then one "CTAs done" counter
+  int32_t g0, g1, n_partials, R, P, vpu_shift, chunk_units;
   uint32_t epoch;
   uint64_t limit_ns;
 };
@@ -117,6 +119,10 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
 // group's flag, then the CTA's warps take chunks of the group's unit range
 // from a per-group counter until none are left.  Dynamic chunks keep the
 // work balanced whichever CTAs are resident while the GEMM still runs.
+//
+// The chunk counters clean up after themselves: the last CTA to finish
+// (counted on work[P]) zeroes them, so the next launch needs no memset and
+// can follow the GEMM directly as a programmatic dependent launch.
 template <int KIND, int U>
 __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant__ ConsumeArgs a) {
   __shared__ int s_ok;
@@ -134,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
     __syncthreads();
     if (!s_ok) {
       if (tid == 0) atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
-      return;
+      break;
     }
     const int32_t ub = a.group_unit_begin[j], ue = a.group_unit_begin[j + 1];
     const int32_t n_chunks = (ue - ub + a.chunk_units - 1) / a.chunk_units;
@@ -149,6 +155,16 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
                              u1 << a.vpu_shift, lane);
     }
     __syncthreads();
+  }
+  // every CTA, finished or timed out, reports; the last one resets the
+  // counters of this launch's groups and the report counter
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.work + a.P, 1) == int32_t(gridDim.x) - 1) {
+      for (int j = a.g0; j < a.g1; ++j) atomicExch(a.work + j, 0);
+      atomicExch(a.work + a.P, 0);
+    }
   }
 }
 
@@ -246,9 +262,33 @@ int default_ctas(const fo_plan* p, int requested) {
   return requested > 0 ? requested : 2 * p->sm_count;
 }
 
+// The consumer is launched as a programmatic dependent (when `overlap`):
+// after fo_signaled_gemm on the same stream it starts once every GEMM CTA
+// is resident and runs alongside it.  Its shared-memory carveout matches the
+// GEMM's so its CTAs can share SMs with GEMM CTAs.
 template <int KIND, int U>
-fo_status launch_consume_kind(const ConsumeArgs& a, int ctas, cudaStream_t st) {
-  consume_kernel<KIND, U><<<ctas, kThreads, 0, st>>>(a);
+fo_status launch_consume_kind(const ConsumeArgs& a, int ctas, bool overlap, int device,
+                              cudaStream_t st) {
+  static std::once_flag once[64];
+  static cudaError_t err[64];
+  const int d = device < 64 ? device : 63;
+  std::call_once(once[d], [&] {
+    err[d] = cudaFuncSetAttribute(consume_kernel<KIND, U>,
+                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  int(cudaSharedmemCarveoutMaxShared));
+  });
+  if (err[d] != cudaSuccess) return FO_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, consume_kernel<KIND, U>, a) != cudaSuccess) return FO_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
@@ -274,20 +314,21 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.work = p->dev.work;
   a.g0 = g0;
   a.g1 = g1;
+  a.P = p->P;
   a.n_partials = n_partials;
   a.R = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
   a.vpu_shift = log2_exact(p->tile_n / 8);
   a.chunk_units = (16 * 1024) / (p->tile_n * 2);  // 16 KB of the source per chunk
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
-  if (cudaMemsetAsync(p->dev.work + g0, 0, sizeof(int32_t) * (g1 - g0), st) != cudaSuccess)
-    return FO_ERR_CUDA;
   const int ctas = default_ctas(p, p->consumer_ctas);
+  const bool ov = p->overlap != 0;
+  const int dv = p->device;
   switch (kind) {
-    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, 4>(a, ctas, st);
-    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, 2>(a, ctas, st);
-    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, 2>(a, ctas, st);
-    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, 4>(a, ctas, st);
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, 4>(a, ctas, ov, dv, st);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, 2>(a, ctas, ov, dv, st);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, 2>(a, ctas, ov, dv, st);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, 4>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
 }

@@ -44,7 +44,7 @@ struct DeviceTables {
   int32_t* row_rank = nullptr;         // [M] A2A: index among the rows of its
                                        //   tile row that go to the same rank
   int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
-  int32_t* work = nullptr;             // [P] scratch: consumer chunk counters
+  int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
 };
 
@@ -64,7 +64,8 @@ struct fo_plan {
   // device side
   int device = -1;
   int sm_count = 0;
-  int consumer_ctas = 0, reorder_ctas = 0;
+  int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
+  uint64_t* trace = nullptr;   // caller's device buffer, see fo_plan_set_trace
   void* blob = nullptr;
   fo::DeviceTables dev;
 };

@@ -72,6 +72,7 @@ struct GemmArgs {
   int32_t* count;
   uint32_t* flags;
   int32_t* status;
+  uint64_t* trace;  // optional: [tiles] tile done times, then [grid] CTA starts
   int32_t tiles, k_blocks, layout, R, h;
   uint32_t epoch;
 };
@@ -261,6 +262,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // This CTA is resident: a consumer launched as a programmatic dependent of
+  // this grid may start once every CTA got here, so it can never hold an SM
+  // that a GEMM CTA still needs while it waits for that CTA's tiles.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (a.trace != nullptr && threadIdx.x == 0) a.trace[a.tiles + blockIdx.x] = globaltimer_ns();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -415,11 +421,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // Once all four warps have stored the tile, count it; the group's last
       // tile raises the group's flag.
-      if (warp == 2 && lane == 0 && a.count != nullptr) {
+      if (warp == 2 && lane == 0 && (a.count != nullptr || a.trace != nullptr)) {
         if (mbar_wait(smem_u32(&epi_done[acc]), acc_phase, abort_flag, a.status)) {
-          __threadfence();
-          const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
-          if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
+          if (a.count != nullptr) {
+            __threadfence();
+            const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
+            if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
+          }
+          if (a.trace != nullptr) a.trace[slot] = globaltimer_ns();
         }
       }
       __syncwarp();
@@ -526,6 +535,7 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.count = count;
   a.flags = flags;
   a.status = p->dev.gemm_status;
+  a.trace = p->trace;
   a.tiles = p->tiles;
   a.k_blocks = p->K / kBlockK;
   a.layout = p->layout;

@@ -350,7 +350,7 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_rd = put(buf, p->row_dest);
   const size_t o_rr = put(buf, p->row_rank);
   const size_t o_fr = put(buf, p->final_row);
-  const size_t o_work = put(buf, std::vector<int32_t>(p->P, 0));
+  const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
   void* blob = nullptr;
   if (cudaMalloc(&blob, buf.size()) != cudaSuccess) return FO_ERR_CUDA;

@@ -61,7 +61,9 @@ def lib():
             "fo_plan_info": (ctypes.c_int, [_vp, _i32p, _i32p, _i32p, _i32p, _i32p]),
             "fo_plan_table": (ctypes.c_int, [_vp, ctypes.c_int32, _i32p, ctypes.c_int64,
                                              ctypes.POINTER(ctypes.c_int64)]),
-            "fo_plan_set_ctas": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32]),
+            "fo_plan_set_launch": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32,
+                                                  ctypes.c_int32]),
+            "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
             "fo_plan_destroy": (None, [_vp]),
             "fo_counting_table_init": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -160,8 +162,14 @@ def fo_plan_table(plan, which):
     return list(out)[:n.value]
 
 
-def fo_plan_set_ctas(plan, consumer_ctas=0, reorder_ctas=0):
-    _check("fo_plan_set_ctas", lib().fo_plan_set_ctas(plan, consumer_ctas, reorder_ctas))
+def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):
+    _check("fo_plan_set_launch",
+           lib().fo_plan_set_launch(plan, consumer_ctas, reorder_ctas, 1 if overlap else 0))
+
+
+def fo_plan_set_trace(plan, stamps):
+    """stamps: device address of uint64[tiles + W], or 0 to stop tracing."""
+    _check("fo_plan_set_trace", lib().fo_plan_set_trace(plan, int(stamps) or None))
 
 
 def fo_plan_device_status(plan, clear=False):

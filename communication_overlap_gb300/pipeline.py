@@ -1,14 +1,18 @@
 """Device buffers, streams and the per-iteration call sequence of the path.
 
 Plumbing only: torch provides device memory, streams and events; every
-step of the path is a libfo.so call (see ``fo.py``).  One iteration is
+step of the path is a libfo.so call (see ``fo.py``).  One iteration is, on
+one stream:
 
-  stream s0: fo_counting_table_init, fo_signaled_gemm(epoch)
-  stream s1: fo_consume_group(all groups, epoch), fo_reorder_back(all)
-  s0 waits for s1
+  fo_counting_table_init, fo_signaled_gemm(epoch),
+  fo_consume_group(all groups, epoch)   -- a programmatic dependent launch:
+                                           runs alongside the GEMM
+  fo_reorder_back(all groups)
 
 so the consumer processes each wave group as soon as the GEMM's epilogue
-raises that group's flag, while the GEMM keeps computing the rest.
+raises that group's flag, while the GEMM keeps computing the rest.  With
+overlap off the consumer is an ordinary launch and starts after the GEMM
+(the serial baseline).
 """
 from dataclasses import dataclass
 
@@ -61,14 +65,15 @@ class Pipeline:
         self.partition = list(partition) if partition else fo.partition_one_then_two(self.waves)
         self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
         self.plan = fo.fo_plan_groups(self.desc)
-        fo.fo_plan_set_ctas(self.plan, consumer_ctas, reorder_ctas)
+        self.consumer_ctas, self.reorder_ctas = consumer_ctas, reorder_ctas
+        self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
         self.P = len(self.partition)
         self.kind = _CONSUMER_OF[w.consumer]
         self.dest_units = fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS)
         self.final_rows = fo.fo_plan_table(self.plan, fo.FO_TAB_FINAL_ROWS)
         self.s0 = torch.cuda.Stream(device=self.device)
-        self.s1 = torch.cuda.Stream(device=self.device)
+        self.s1 = self.s0   # the consumer follows the GEMM on its stream
         self.epoch = 0
         self.buf = self._alloc(inp) if upload else None
 
@@ -112,25 +117,26 @@ class Pipeline:
                            [c.data_ptr() for c in b.comm], [f.data_ptr() for f in b.final],
                            stream.cuda_stream)
 
-    def step(self, overlap=True):
-        """One pass of the whole path with a fresh epoch.  With overlap the
-        consumer runs on s1 against the GEMM on s0; without, everything runs
-        on s0 one after the other (the serial baseline)."""
+    def set_overlap(self, overlap):
+        if overlap != self._overlap:
+            fo.fo_plan_set_launch(self.plan, self.consumer_ctas, self.reorder_ctas, overlap)
+            self._overlap = overlap
+
+    def step(self, overlap=True, sync_current=True):
+        """One pass of the whole path with a fresh epoch, on stream s0.  With
+        overlap the consumer runs alongside the GEMM (dependent launch);
+        without, it starts after the GEMM (the serial baseline)."""
+        self.set_overlap(overlap)
         self.epoch = (self.epoch + 1) & 0xffffffff or 1
         e = self.epoch
         cur = torch.cuda.current_stream(self.device)
-        self.s0.wait_stream(cur)
-        if overlap:
-            self.s1.wait_stream(cur)
-            self.gemm(self.s0, e)
-            self.consume(self.s1, e)
-            self.reorder(self.s1)
-            self.s0.wait_stream(self.s1)
-        else:
-            self.gemm(self.s0, e)
-            self.consume(self.s0, e)
-            self.reorder(self.s0)
-        cur.wait_stream(self.s0)
+        if sync_current:
+            self.s0.wait_stream(cur)
+        self.gemm(self.s0, e)
+        self.consume(self.s0, e)
+        self.reorder(self.s0)
+        if sync_current:
+            cur.wait_stream(self.s0)
         return e
 
     # ------------------------------------------------------------ results

@@ -140,9 +140,23 @@ typedef enum {
 fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length);
 
-/* CTAs the consumer and reorder kernels launch (<= 0: 2 per SM, default). */
-fo_status fo_plan_set_ctas(fo_plan* plan, int32_t consumer_ctas,
-                           int32_t reorder_ctas);
+/* Launch settings of the consumer and reorder kernels.
+ *  consumer_ctas, reorder_ctas: grid sizes (<= 0: 2 per SM, the default).
+ *  overlap: non-zero (default) launches the consumer as a programmatic
+ *      dependent launch: issued on the GEMM's stream right after
+ *      fo_signaled_gemm, it starts as soon as every GEMM CTA is resident and
+ *      runs alongside the GEMM.  Zero launches it as an ordinary kernel
+ *      (it then starts after the GEMM has finished: the serial baseline). */
+fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
+                             int32_t reorder_ctas, int32_t overlap);
+
+/* Per-tile completion times ([P2] Figure 3 records each tile's completion
+ * time with globaltimer to show the wave pattern).  stamps: device uint64
+ * [tiles + W], or NULL to stop tracing.  While set, every GEMM launch writes
+ * stamps[slot] = %globaltimer (ns) when the tile at that launch slot has
+ * been stored and counted, and stamps[tiles + c] = the start time of CTA c.
+ * The caller owns the buffer and keeps it alive while tracing. */
+fo_status fo_plan_set_trace(fo_plan* plan, uint64_t* stamps);
 
 /* Sticky status word of the plan's GEMM launches (the GEMM call has no
  * status argument): FO_OK, or FO_ERR_TIMEOUT if one of its bounded
@@ -183,18 +197,26 @@ fo_status fo_signaled_gemm(const fo_plan* plan, const void* A,
                            int32_t* count_table, uint32_t* flags,
                            uint32_t epoch, void* cuda_stream);
 
-/* The communication stand-in ([P1] 五 "专用监控内核": a monitor kernel on its
- * own stream).  For group = j, or every group in order when group = -1, the
- * kernel waits until flags[j] == epoch (acquire at GPU scope, __nanosleep
- * back-off, at most spin_limit_ns per group, 0 = 2 s), then processes the
- * group's contiguous range of src_reordered as `kind` says.
+/* The communication stand-in ([P1] 五 "专用监控内核": a monitor kernel
+ * tracking progress through atomic counters).  For group = j, or every group
+ * in order when group = -1, the kernel waits until flags[j] == epoch
+ * (acquire at GPU scope, __nanosleep back-off, at most spin_limit_ns per
+ * group, 0 = 2 s), then processes the group's contiguous range of
+ * src_reordered as `kind` says.
+ *  Launch: pass the GEMM's stream to overlap (see fo_plan_set_launch).  On
+ *  another stream the kernel can be scheduled before the GEMM's CTAs and
+ *  hold the SMs they need; its waits then run out (FO_ERR_TIMEOUT) rather
+ *  than hang, but the GEMM is delayed -- the pages' separate-stream design
+ *  has this hazard, which the dependent launch removes.
  *  partials: host array of n_partials device pointers, same layout as
  *      src_reordered (SUM and RS; n_partials <= 8).
  *  dst: host array of device pointers: 1 buffer for COPY/SUM (same size as
  *      src), R buffers for RS/A2A sized by FO_TAB_DEST_UNITS.
  *  dev_status: device int32, 0 before the call; a wait that runs out sets it
  *      to FO_ERR_TIMEOUT and the kernel returns without that group's work.
- * Concurrent consume calls on one plan race on the plan's scratch. */
+ * The kernel hands work out through chunk counters in the plan's device
+ * scratch; the last CTA resets them.  Consume calls on one plan that overlap
+ * in time race on that scratch. */
 fo_status fo_consume_group(const fo_plan* plan, int32_t group,
                            fo_consumer kind, const void* src_reordered,
                            const void* const* partials, int32_t n_partials,
