@@ -362,3 +362,122 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
 }
 
 }  // namespace fo
+
+// ---------------------------------------------------------------------------
+// Allocation-free consumer entry point.
+//
+// Some callers may not allocate device memory at the moment they run the
+// overlap: code being captured into a CUDA graph (cudaMalloc is not allowed
+// inside a capture), serving runtimes that hand all device memory to their
+// own pool and forbid allocations on the request path, and latency-critical
+// loops that cannot afford the synchronisation an allocation may cause.
+// fo_consume_group keeps its chunk counters in scratch memory that
+// fo_plan_groups allocated; this variant keeps them instead in a fixed
+// array that lives in the library's own device image, so the call itself
+// allocates nothing.  The plan's tables and every buffer are still the
+// caller's, created beforehand.
+
+// The shared scratch: chunk counters of up to FO_NOALLOC_MAX_GROUPS groups
+// plus the "CTAs done" counter.  Every GPU that loads the library holds it
+// (16 KB) until the process exits.
+static __device__ __align__(256) int32_t fo_noalloc_scratch[FO_NOALLOC_MAX_GROUPS + 1];
+
+namespace fo {
+namespace {
+
+std::mutex g_noalloc_mutex;
+int32_t* g_noalloc_addr[64] = {};
+
+// Device address of fo_noalloc_scratch on the current device.  In host code
+// the array's name only stands for it; its address on a device comes from
+// cudaGetSymbolAddress, taken once per device with that device current.  The
+// first call on a device also clears the array (synchronous cudaMemset);
+// every consumer launch leaves the counters at zero again.
+fo_status noalloc_scratch(int device, int32_t** out) {
+  if (device < 0 || device >= 64) return FO_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_addr[device] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, fo_noalloc_scratch) != cudaSuccess) return FO_ERR_CUDA;
+    if (cudaMemset(ptr, 0, sizeof(fo_noalloc_scratch)) != cudaSuccess) return FO_ERR_CUDA;
+    g_noalloc_addr[device] = static_cast<int32_t*>(ptr);
+  }
+  *out = g_noalloc_addr[device];
+  return FO_OK;
+}
+
+}  // namespace
+}  // namespace fo
+
+extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
+                                              fo_consumer kind, const void* src,
+                                              const void* const* partials,
+                                              int32_t n_partials, void* const* dst,
+                                              const uint32_t* flags, uint32_t epoch,
+                                              uint64_t spin_limit_ns, int32_t* dev_status,
+                                              void* stream) {
+  using namespace fo;
+  if (!p || !p->blob || !src || !dst || !flags || !dev_status) return FO_ERR_ARG;
+  if (p->P > FO_NOALLOC_MAX_GROUPS) return FO_ERR_ARG;  // scratch too small for this plan
+  if (group < -1 || group >= p->P) return FO_ERR_ARG;
+  switch (kind) {
+    case FO_CONS_COPY:
+      if (n_partials != 0) return FO_ERR_ARG;
+      break;
+    case FO_CONS_SUM:
+      if (n_partials < 0 || n_partials > kMaxPartials) return FO_ERR_ARG;
+      break;
+    case FO_CONS_RS:
+      if (n_partials < 0 || n_partials > kMaxPartials) return FO_ERR_ARG;
+      if (p->layout != FO_LAYOUT_RS_SUBTILE && p->layout != FO_LAYOUT_RS_ROWBLOCK)
+        return FO_ERR_ARG;
+      break;
+    case FO_CONS_A2A:
+      if (n_partials != 0 || p->layout != FO_LAYOUT_A2A_SUBTOKEN) return FO_ERR_ARG;
+      break;
+    default: return FO_ERR_ARG;
+  }
+  if (n_partials > 0 && !partials) return FO_ERR_ARG;
+  for (int i = 0; i < n_partials; ++i)
+    if (!partials[i]) return FO_ERR_ARG;
+  const int n_dst = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
+  for (int k = 0; k < n_dst; ++k)
+    if (!dst[k]) return FO_ERR_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) return FO_ERR_CUDA;
+  if (device != p->device) return FO_ERR_ARG;  // the plan's device must be current
+  int32_t* scratch = nullptr;
+  const fo_status st = noalloc_scratch(device, &scratch);
+  if (st != FO_OK) return st;
+
+  ConsumeArgs a{};
+  a.src = static_cast<const uint4*>(src);
+  for (int i = 0; i < n_partials; ++i) a.partials[i] = static_cast<const uint4*>(partials[i]);
+  for (int k = 0; k < n_dst; ++k) a.dst[k] = static_cast<uint4*>(dst[k]);
+  a.flags = flags;
+  a.status = dev_status;
+  a.group_unit_begin = p->dev.group_unit_begin;
+  a.part_start = p->dev.part_start;
+  a.part_len = p->dev.part_len;
+  a.part_dst = p->dev.part_dst;
+  a.work = scratch;
+  a.g0 = group < 0 ? 0 : group;
+  a.g1 = group < 0 ? p->P : group + 1;
+  a.P = p->P;
+  a.n_partials = n_partials;
+  a.R = n_dst;
+  a.vpu_shift = log2_exact(p->tile_n / 8);
+  a.chunk_units = (16 * 1024) / (p->tile_n * 2);
+  a.epoch = epoch;
+  a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
+  const int ctas = default_ctas(p, p->consumer_ctas);
+  const bool ov = p->overlap != 0;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  switch (kind) {
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, 4>(a, ctas, ov, device, cs);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, 2>(a, ctas, ov, device, cs);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, 2>(a, ctas, ov, device, cs);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, 4>(a, ctas, ov, device, cs);
+  }
+  return FO_ERR_ARG;
+}

@@ -13,6 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libfo.so")
 
 FO_OK, FO_ERR_ARG, FO_ERR_CUDA, FO_ERR_TIMEOUT, FO_ERR_UNSUPPORTED = range(5)
+FO_NOALLOC_MAX_GROUPS = 4096   # include/fo.h
 FO_LAYOUT_TILE, FO_LAYOUT_RS_SUBTILE, FO_LAYOUT_RS_ROWBLOCK, FO_LAYOUT_A2A_SUBTOKEN = range(4)
 FO_CONS_COPY, FO_CONS_SUM, FO_CONS_RS, FO_CONS_A2A = range(4)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
@@ -72,6 +73,10 @@ def lib():
             "fo_consume_group": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int, _vp, _vpp,
                                                 ctypes.c_int32, _vpp, _vp, ctypes.c_uint32,
                                                 ctypes.c_uint64, _vp, _vp]),
+            "fo_consume_group_noalloc": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int, _vp,
+                                                        _vpp, ctypes.c_int32, _vpp, _vp,
+                                                        ctypes.c_uint32, ctypes.c_uint64, _vp,
+                                                        _vp]),
             "fo_reorder_back": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, _vpp,
                                                _vpp, _vp]),
             "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -203,6 +208,17 @@ def fo_consume_group(plan, group, kind, src, partials, dst, flags, epoch,
                                   len(partials), _ptrs(dst), int(flags),
                                   epoch & 0xffffffff, spin_limit_ns, int(dev_status),
                                   stream or None))
+
+
+def fo_consume_group_noalloc(plan, group, kind, src, partials, dst, flags, epoch,
+                             spin_limit_ns, dev_status, stream):
+    """fo_consume_group without any device allocation (fixed scratch inside
+    the library; see include/fo.h)."""
+    _check("fo_consume_group_noalloc",
+           lib().fo_consume_group_noalloc(plan, group, kind, int(src), _ptrs(partials),
+                                          len(partials), _ptrs(dst), int(flags),
+                                          epoch & 0xffffffff, spin_limit_ns, int(dev_status),
+                                          stream or None))
 
 
 def fo_reorder_back(plan, group_begin, group_end, src, dst, stream):

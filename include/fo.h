@@ -224,6 +224,34 @@ fo_status fo_consume_group(const fo_plan* plan, int32_t group,
                            uint32_t epoch, uint64_t spin_limit_ns,
                            int32_t* dev_status, void* cuda_stream);
 
+/* Allocation-free variant of fo_consume_group.  The pages have no
+ * counterpart to this entry point: it exists for callers that may not
+ * allocate device memory when they run the overlap -- code captured into a
+ * CUDA graph (no cudaMalloc during capture), serving runtimes whose memory
+ * pool owns all device memory and forbids allocations on the request path,
+ * and latency-critical loops that cannot wait for the allocator.
+ *
+ * Same arguments, results and launch behaviour as fo_consume_group.  It
+ * allocates nothing: instead of the plan's scratch it keeps its chunk
+ * counters in a fixed array inside the library's device image, room for
+ * FO_NOALLOC_MAX_GROUPS groups (16 KB on every GPU that loads the library,
+ * held until the process exits).  A plan with more groups gets FO_ERR_ARG
+ * and nothing is launched.  The plan's device must be the current device.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and clears it with a synchronous cudaMemset;
+ *    make that first call before any stream capture.  Every launch leaves
+ *    the counters at zero for the next one.
+ *  - All calls share the one array: calls whose kernels overlap on the GPU
+ *    (other streams, other plans) race on it.  Issue them one after
+ *    another, e.g. on one stream. */
+#define FO_NOALLOC_MAX_GROUPS 4096
+fo_status fo_consume_group_noalloc(const fo_plan* plan, int32_t group,
+                                   fo_consumer kind, const void* src_reordered,
+                                   const void* const* partials, int32_t n_partials,
+                                   void* const* dst, const uint32_t* flags,
+                                   uint32_t epoch, uint64_t spin_limit_ns,
+                                   int32_t* dev_status, void* cuda_stream);
+
 /* Post-communication reorder ([P1] 二 "通信后重排"): for the groups
  * [group_begin, group_end), move every unit from where the consumer left it
  * to its place in the final row-major layout, by the inverse mapping table.
