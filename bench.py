@@ -29,7 +29,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -42,7 +41,7 @@ import numpy as np
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="wave_pattern")
@@ -71,55 +70,91 @@ def measured_peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled DURING the timed region.
 
-    def __init__(self, index):
-        self.index = index
-        self.proc = None
+    Polls NVML (libnvidia-ml, read-only queries) from a thread every ~2 ms,
+    so even a timed region of a few milliseconds gets samples.  Changes no
+    setting of the GPU."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index):
+        import ctypes
+        import threading
+        self.ctypes, self.threading = ctypes, threading
+        self.samples, self.max_mhz, self.handle, self.nvml = [], None, None, None
+        try:
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            count = ctypes.c_uint()
+            nvml.nvmlDeviceGetCount_v2(ctypes.byref(count))
+            handle = ctypes.c_void_p()
+            index = self._nvml_index(nvml, count.value, cuda_index)
+            if nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            try:
+                self.reasons_fn = nvml.nvmlDeviceGetCurrentClocksEventReasons
+            except AttributeError:
+                self.reasons_fn = nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nvml, self.handle = nvml, handle
+        except (OSError, AttributeError):
+            pass
+
+    def _nvml_index(self, nvml, count, cuda_index):
+        """Match the CUDA device to an NVML device by UUID when possible."""
+        ct = self.ctypes
+        try:
+            import torch
+            want = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            for i in range(count):
+                h = ct.c_void_p()
+                buf = ct.create_string_buffer(96)
+                if nvml.nvmlDeviceGetHandleByIndex_v2(i, ct.byref(h)) == 0 and \
+                        nvml.nvmlDeviceGetUUID(h, buf, 96) == 0 and \
+                        want.replace("GPU-", "") in buf.value.decode():
+                    return i
+        except Exception:
+            pass
+        return cuda_index if cuda_index < count else 0
+
+    def _poll(self):
+        ct = self.ctypes
+        clk, reasons = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(clk)) == 0:
+                r = 0
+                if self.reasons_fn(self.handle, ct.byref(reasons)) == 0:
+                    r = reasons.value
+                self.samples.append((float(clk.value), r))
+            self._stop.wait(0.002)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        if self.nvml is not None:
+            self._stop = self.threading.Event()
+            self._thread = self.threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        if self.nvml is not None:
+            self._stop.set()
+            self._thread.join()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unsampled"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"]}
+        reasons = set()
+        for _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples), "source": "NVML, every ~2 ms"}
 
 
 # ----------------------------------------------------------------- timing helpers

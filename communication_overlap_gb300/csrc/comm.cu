@@ -22,6 +22,13 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// 16-byte vectors each lane keeps in flight per source (per iteration).
+template <int KIND>
+constexpr int kUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 2 : 8;
+// Units of the group a warp takes per chunk counter increment (32 KB at
+// tile_n = 256).
+constexpr int kChunkBytes = 32 * 1024;
+
 struct ConsumeArgs {
   const uint4* src;
   const uint4* partials[kMaxPartials];
@@ -107,10 +114,12 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
     for (int i = 0; i < U; ++i) {
       const int32_t v = base + 32 * i;
       if (v >= v1) break;
+      // ordinary write-back stores: the post-communication reorder reads
+      // these buffers next, so they may stay in L2
       if constexpr (KIND == FO_CONS_COPY || KIND == FO_CONS_SUM)
-        st_cs(dst[0] + v, x[i]);
+        dst[0][v] = x[i];
       else
-        st_cs(route(ps, pl, pd, dst, a.R, a.vpu_shift, v), x[i]);
+        *route(ps, pl, pd, dst, a.R, a.vpu_shift, v) = x[i];
     }
   }
 }
@@ -178,54 +187,52 @@ struct ReorderArgs {
   const int32_t* row_dest;
   const int32_t* row_rank;
   const int32_t* final_row;
-  int32_t layout, R, vpu_shift, row_vec, slot0, h, rows_per;
-  int64_t total;  // vectors over the slot range, ragged rows included
+  int32_t layout, R, row_vec, slot0, n_slots, h, rows_per;
 };
 
-// Inverse mapping: vector `idx` of the slot range is lane (idx mod vpu) of
-// row r of the tile at slot s; find where the consumer left that unit and
-// where it belongs in the final layout.
-__device__ __forceinline__ bool reorder_addr(const ReorderArgs& a, const uint4* const* src,
-                                             uint4* const* dst, int64_t idx,
-                                             const uint4** from, uint4** to) {
-  const int32_t lane = int32_t(idx) & ((1 << a.vpu_shift) - 1);
-  const int64_t w = idx >> a.vpu_shift;
-  const int32_t s = a.slot0 + int32_t(w / kTileM);
-  const int32_t r = int32_t(w % kTileM);
-  const TileInfo ti = a.tile[s];
-  if (r >= ti.rows) return false;
+// Inverse mapping of row r of the tile at slot s: the unit's place in the
+// consumer's buffer k and the row it belongs to in output k.
+__device__ __forceinline__ void reorder_row(const ReorderArgs& a, const TileInfo& ti, int32_t s,
+                                            int32_t r, int* k_out, int32_t* src_unit,
+                                            int32_t* dst_row) {
   int k = 0;
-  int32_t src_unit, dst_row;
   if (a.layout == FO_LAYOUT_TILE) {
-    src_unit = ti.unit_base + r;
-    dst_row = ti.row0 + r;
+    *src_unit = ti.unit_base + r;
+    *dst_row = ti.row0 + r;
   } else {
     int32_t u;
     if (a.layout == FO_LAYOUT_RS_SUBTILE) {
       k = r / a.h;
       const int32_t i = r - k * a.h;
       u = ti.unit_base + k * ti.sub_stride + i;
-      dst_row = (ti.row0 / kTileM) * a.h + i;
+      *dst_row = (ti.row0 / kTileM) * a.h + i;
     } else if (a.layout == FO_LAYOUT_RS_ROWBLOCK) {
       k = ti.dest;
       u = ti.unit_base + r;
-      dst_row = ti.row0 + r - k * a.rows_per;
+      *dst_row = ti.row0 + r - k * a.rows_per;
     } else {  // FO_LAYOUT_A2A_SUBTOKEN
       const int32_t rho = ti.row0 + r;
-      k = a.row_dest[rho];
-      u = a.dest_base[s * a.R + k] + a.row_rank[rho];
-      dst_row = a.final_row[rho];
+      k = __ldg(a.row_dest + rho);
+      u = __ldg(a.dest_base + s * a.R + k) + __ldg(a.row_rank + rho);
+      *dst_row = __ldg(a.final_row + rho);
     }
     const int32_t jk = ti.group * a.R + k;
-    src_unit = a.part_dst[jk] + (u - a.part_start[jk]);
+    *src_unit = __ldg(a.part_dst + jk) + (u - __ldg(a.part_start + jk));
   }
-  *from = src[k] + (int64_t(src_unit) << a.vpu_shift) + lane;
-  *to = dst[k] + int64_t(dst_row) * a.row_vec + (ti.col0 >> 3) + lane;
-  return true;
+  *k_out = k;
 }
 
+// Tile-major post-communication reorder: a CTA moves one tile at a time
+// (its TileInfo read once, the next one prefetched); each warp takes every
+// 8th row group and each lane issues kBatch independent 16-byte loads
+// before its stores, so enough bytes are in flight to keep HBM busy.
+template <int VPU>  // 16-byte vectors per unit: 32 (tile_n 256) or 16 (128)
 __global__ void __launch_bounds__(kThreads) reorder_kernel(const __grid_constant__ ReorderArgs a) {
-  constexpr int U = 4;
+  constexpr int kRowsPerInstr = 32 / VPU;            // rows one warp instruction covers
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kRowsPerWarp = kTileM / kWarps;      // 16
+  constexpr int kBatch = 8;                           // loads per lane per round
+  constexpr int kRounds = kRowsPerWarp / kRowsPerInstr / kBatch;
   __shared__ const uint4* s_src[kMaxDest];
   __shared__ uint4* s_dst[kMaxDest];
   if (threadIdx.x < kMaxDest) {
@@ -233,22 +240,35 @@ __global__ void __launch_bounds__(kThreads) reorder_kernel(const __grid_constant
     s_dst[threadIdx.x] = a.dst[threadIdx.x];
   }
   __syncthreads();
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t base = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; base < a.total;
-       base += stride * U) {
-    const uint4* from[U];
-    uint4* to[U];
-    bool ok[U];
-    uint4 x[U];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int sub = lane / VPU, vl = lane % VPU;
+  int32_t t = blockIdx.x;
+  TileInfo next{};
+  if (t < a.n_slots) next = a.tile[a.slot0 + t];
+  for (; t < a.n_slots; t += gridDim.x) {
+    const int32_t s = a.slot0 + t;
+    const TileInfo ti = next;
+    if (t + int32_t(gridDim.x) < a.n_slots) next = a.tile[s + gridDim.x];
+#pragma unroll 1
+    for (int round = 0; round < kRounds; ++round) {
+      uint4 x[kBatch];
+      int64_t to[kBatch];   // element offsets (vector units) into output k
+      int kk[kBatch];
 #pragma unroll
-    for (int i = 0; i < U; ++i) {
-      const int64_t idx = base + stride * i;
-      ok[i] = idx < a.total && reorder_addr(a, s_src, s_dst, idx, &from[i], &to[i]);
-      if (ok[i]) x[i] = ld_cg(from[i]);
+      for (int i = 0; i < kBatch; ++i) {
+        const int32_t r = ((round * kBatch + i) * kWarps + warp) * kRowsPerInstr + sub;
+        kk[i] = -1;
+        if (r < ti.rows) {
+          int32_t su, dr;
+          reorder_row(a, ti, s, r, &kk[i], &su, &dr);
+          x[i] = ld_cg(s_src[kk[i]] + int64_t(su) * VPU + vl);
+          to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (kk[i] >= 0) st_cs(s_dst[kk[i]] + to[i], x[i]);
     }
-#pragma unroll
-    for (int i = 0; i < U; ++i)
-      if (ok[i]) st_cs(to[i], x[i]);
   }
 }
 
@@ -259,7 +279,7 @@ int log2_exact(int v) {
 }
 
 int default_ctas(const fo_plan* p, int requested) {
-  return requested > 0 ? requested : 2 * p->sm_count;
+  return requested > 0 ? requested : 4 * p->sm_count;
 }
 
 // The consumer is launched as a programmatic dependent (when `overlap`):
@@ -318,17 +338,17 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.n_partials = n_partials;
   a.R = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
   a.vpu_shift = log2_exact(p->tile_n / 8);
-  a.chunk_units = (16 * 1024) / (p->tile_n * 2);  // 16 KB of the source per chunk
+  a.chunk_units = kChunkBytes / (p->tile_n * 2);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
   const int ctas = default_ctas(p, p->consumer_ctas);
   const bool ov = p->overlap != 0;
   const int dv = p->device;
   switch (kind) {
-    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, 4>(a, ctas, ov, dv, st);
-    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, 2>(a, ctas, ov, dv, st);
-    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, 2>(a, ctas, ov, dv, st);
-    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, 4>(a, ctas, ov, dv, st);
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, dv, st);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, dv, st);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>>(a, ctas, ov, dv, st);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
 }
@@ -350,14 +370,18 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   a.final_row = p->dev.final_row;
   a.layout = p->layout;
   a.R = p->R;
-  a.vpu_shift = log2_exact(p->tile_n / 8);
   a.row_vec = p->N / 8;
   a.slot0 = p->group_slot_begin[g0];
+  a.n_slots = p->group_slot_begin[g1] - a.slot0;
   a.h = kTileM / p->R;
   a.rows_per = p->M / p->R;
-  a.total = int64_t(p->group_slot_begin[g1] - a.slot0) * kTileM * (p->tile_n / 8);
-  const int ctas = default_ctas(p, p->reorder_ctas);
-  reorder_kernel<<<ctas, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  int ctas = default_ctas(p, p->reorder_ctas);
+  if (ctas > a.n_slots) ctas = a.n_slots;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p->tile_n == 256)
+    reorder_kernel<32><<<ctas, kThreads, 0, st>>>(a);
+  else
+    reorder_kernel<16><<<ctas, kThreads, 0, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
@@ -467,17 +491,17 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.n_partials = n_partials;
   a.R = n_dst;
   a.vpu_shift = log2_exact(p->tile_n / 8);
-  a.chunk_units = (16 * 1024) / (p->tile_n * 2);
+  a.chunk_units = kChunkBytes / (p->tile_n * 2);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
   const int ctas = default_ctas(p, p->consumer_ctas);
   const bool ov = p->overlap != 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   switch (kind) {
-    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, 4>(a, ctas, ov, device, cs);
-    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, 2>(a, ctas, ov, device, cs);
-    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, 2>(a, ctas, ov, device, cs);
-    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, 4>(a, ctas, ov, device, cs);
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, device, cs);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, device, cs);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>>(a, ctas, ov, device, cs);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, device, cs);
   }
   return FO_ERR_ARG;
 }

@@ -141,7 +141,7 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length);
 
 /* Launch settings of the consumer and reorder kernels.
- *  consumer_ctas, reorder_ctas: grid sizes (<= 0: 2 per SM, the default).
+ *  consumer_ctas, reorder_ctas: grid sizes (<= 0: 4 per SM, the default).
  *  overlap: non-zero (default) launches the consumer as a programmatic
  *      dependent launch: issued on the GEMM's stream right after
  *      fo_signaled_gemm, it starts as soon as every GEMM CTA is resident and
