@@ -81,9 +81,10 @@ fo_status fo_plan_set_launch(fo_plan* p, int32_t consumer_ctas, int32_t reorder_
   return FO_OK;
 }
 
-fo_status fo_plan_set_trace(fo_plan* p, uint64_t* stamps) {
+fo_status fo_plan_set_trace(fo_plan* p, uint64_t* stamps, uint64_t* consumer_stamps) {
   if (!p) return FO_ERR_ARG;
   p->trace = stamps;
+  p->consumer_trace = consumer_stamps;
   return FO_OK;
 }
 

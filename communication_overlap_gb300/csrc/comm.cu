@@ -25,9 +25,10 @@ constexpr int kThreads = 256;
 // 16-byte vectors each lane keeps in flight per source (per iteration).
 template <int KIND>
 constexpr int kUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 2 : 8;
-// Units of the group a warp takes per chunk counter increment (32 KB at
-// tile_n = 256).
-constexpr int kChunkBytes = 32 * 1024;
+// Bytes of the source a CTA takes per chunk: one pass of U vectors per
+// thread for the copies (32 KB), two passes for the sums (16 KB).
+template <int KIND>
+constexpr int kChunkBytes = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 16 * 1024 : 32 * 1024;
 
 struct ConsumeArgs {
   const uint4* src;
@@ -43,6 +44,7 @@ struct ConsumeArgs {
   int32_t g0, g1, n_partials, R, P, vpu_shift, chunk_units;
   uint32_t epoch;
   uint64_t limit_ns;
+  uint64_t* trace;  // optional: [P] group fully consumed, then [grid][4] CTA records
 };
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& x) {
@@ -81,18 +83,21 @@ __device__ __forceinline__ uint4* route(const int32_t* ps, const int32_t* pl,
   return dst[k] + vu + (v & ((1 << vpu_shift) - 1));
 }
 
-// One warp processes vectors [v0, v1) of the reordered buffer.
+// The CTA processes vectors [v0, v1) of the reordered buffer: thread t
+// takes v0 + t + kThreads * i, so each warp instruction covers 512
+// contiguous bytes and every thread keeps U loads (per source) in flight.
 template <int KIND, int U>
 __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_t* ps,
                                               const int32_t* pl, const int32_t* pd,
                                               uint4* const* dst, int32_t v0, int32_t v1,
-                                              int lane) {
+                                              int tid) {
   constexpr bool kSum = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS);
-  for (int32_t base = v0 + lane; base < v1; base += 32 * U) {
+  constexpr int S = kThreads;
+  for (int32_t base = v0 + tid; base < v1; base += S * U) {
     uint4 x[U];
 #pragma unroll
     for (int i = 0; i < U; ++i)
-      if (base + 32 * i < v1) x[i] = ld_cg(a.src + base + 32 * i);
+      if (base + S * i < v1) x[i] = ld_cg(a.src + base + S * i);
     if constexpr (kSum) {
       float acc[U][8];
 #pragma unroll
@@ -103,7 +108,7 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
         uint4 y[U];
 #pragma unroll
         for (int i = 0; i < U; ++i)
-          if (base + 32 * i < v1) y[i] = ld_cg(a.partials[q] + base + 32 * i);
+          if (base + S * i < v1) y[i] = ld_cg(a.partials[q] + base + S * i);
 #pragma unroll
         for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[i]);
       }
@@ -112,7 +117,7 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
     }
 #pragma unroll
     for (int i = 0; i < U; ++i) {
-      const int32_t v = base + 32 * i;
+      const int32_t v = base + S * i;
       if (v >= v1) break;
       // ordinary write-back stores: the post-communication reorder reads
       // these buffers next, so they may stay in L2
@@ -125,9 +130,11 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
 }
 
 // Persistent consumer: for each group in order, thread 0 waits on the
-// group's flag, then the CTA's warps take chunks of the group's unit range
-// from a per-group counter until none are left.  Dynamic chunks keep the
-// work balanced whichever CTAs are resident while the GEMM still runs.
+// group's flag, then the CTA takes chunks of the group's unit range from a
+// per-group counter until none are left (thread 0 fetches the next chunk
+// index while the CTA works on the current one).  Chunks are small enough
+// that every CTA gets work in every group, and dynamic so the work stays
+// balanced whichever CTAs are resident while the GEMM still runs.
 //
 // The chunk counters clean up after themselves: the last CTA to finish
 // (counted on work[P]) zeroes them, so the next launch needs no memset and
@@ -135,10 +142,14 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
 template <int KIND, int U>
 __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant__ ConsumeArgs a) {
   __shared__ int s_ok;
+  __shared__ int32_t s_chunk[2];
   __shared__ int32_t s_ps[kMaxDest], s_pl[kMaxDest], s_pd[kMaxDest];
   __shared__ uint4* s_dst[kMaxDest];
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   if (tid < kMaxDest) s_dst[tid] = a.dst[tid];
+  uint64_t t_start = 0;
+  int32_t chunks_done = 0;
+  if (a.trace != nullptr && tid == 0) t_start = globaltimer_ns();
   for (int j = a.g0; j < a.g1; ++j) {
     if (tid == 0) s_ok = wait_flag(a.flags + j, a.epoch, a.limit_ns) ? 1 : 0;
     if (tid < a.R) {
@@ -153,17 +164,36 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
     }
     const int32_t ub = a.group_unit_begin[j], ue = a.group_unit_begin[j + 1];
     const int32_t n_chunks = (ue - ub + a.chunk_units - 1) / a.chunk_units;
-    while (true) {
-      int32_t c = 0;
-      if (lane == 0) c = atomicAdd(a.work + j, 1);
-      c = __shfl_sync(0xffffffffu, c, 0);
+    if (tid == 0) s_chunk[0] = atomicAdd(a.work + j, 1);
+    __syncthreads();
+    for (int buf = 0;; buf ^= 1) {
+      const int32_t c = s_chunk[buf];
       if (c >= n_chunks) break;
+      if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(a.work + j, 1);
       const int32_t u0 = ub + c * a.chunk_units;
       const int32_t u1 = min(u0 + a.chunk_units, ue);
       consume_range<KIND, U>(a, s_ps, s_pl, s_pd, s_dst, u0 << a.vpu_shift,
-                             u1 << a.vpu_shift, lane);
+                             u1 << a.vpu_shift, tid);
+      __syncthreads();
+      if (a.trace != nullptr && tid == 0) {
+        // the latest chunk end of the group is when it is fully consumed
+        atomicMax(reinterpret_cast<unsigned long long*>(a.trace + j),
+                  static_cast<unsigned long long>(globaltimer_ns()));
+        ++chunks_done;
+      }
     }
     __syncthreads();
+  }
+  if (a.trace != nullptr) {
+    if (tid == 0) {
+      a.trace[a.P + 4 * blockIdx.x + 3] = uint64_t(chunks_done);
+      uint32_t smid;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+      uint64_t* rec = a.trace + a.P + 4 * blockIdx.x;
+      rec[0] = smid;
+      rec[1] = t_start;
+      rec[2] = globaltimer_ns();
+    }
   }
   // every CTA, finished or timed out, reports; the last one resets the
   // counters of this launch's groups and the report counter
@@ -272,6 +302,12 @@ __global__ void __launch_bounds__(kThreads) reorder_kernel(const __grid_constant
   }
 }
 
+int chunk_units_of(int kind, int tile_n) {
+  const int bytes = (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? kChunkBytes<FO_CONS_SUM>
+                                                                 : kChunkBytes<FO_CONS_COPY>;
+  return bytes / (tile_n * 2);
+}
+
 int log2_exact(int v) {
   int s = 0;
   while ((1 << s) < v) ++s;
@@ -338,9 +374,10 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.n_partials = n_partials;
   a.R = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
   a.vpu_shift = log2_exact(p->tile_n / 8);
-  a.chunk_units = kChunkBytes / (p->tile_n * 2);
+  a.chunk_units = chunk_units_of(kind, p->tile_n);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
+  a.trace = p->consumer_trace;
   const int ctas = default_ctas(p, p->consumer_ctas);
   const bool ov = p->overlap != 0;
   const int dv = p->device;
@@ -491,7 +528,7 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.n_partials = n_partials;
   a.R = n_dst;
   a.vpu_shift = log2_exact(p->tile_n / 8);
-  a.chunk_units = kChunkBytes / (p->tile_n * 2);
+  a.chunk_units = chunk_units_of(kind, p->tile_n);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
   const int ctas = default_ctas(p, p->consumer_ctas);

@@ -65,7 +65,8 @@ struct fo_plan {
   int device = -1;
   int sm_count = 0;
   int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
-  uint64_t* trace = nullptr;   // caller's device buffer, see fo_plan_set_trace
+  uint64_t* trace = nullptr;           // caller's device buffers, see fo_plan_set_trace
+  uint64_t* consumer_trace = nullptr;
   void* blob = nullptr;
   fo::DeviceTables dev;
 };

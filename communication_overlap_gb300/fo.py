@@ -64,7 +64,7 @@ def lib():
                                              ctypes.POINTER(ctypes.c_int64)]),
             "fo_plan_set_launch": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32,
                                                   ctypes.c_int32]),
-            "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp]),
+            "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp, _vp]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
             "fo_plan_destroy": (None, [_vp]),
             "fo_counting_table_init": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -172,9 +172,11 @@ def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):
            lib().fo_plan_set_launch(plan, consumer_ctas, reorder_ctas, 1 if overlap else 0))
 
 
-def fo_plan_set_trace(plan, stamps):
-    """stamps: device address of uint64[tiles + W], or 0 to stop tracing."""
-    _check("fo_plan_set_trace", lib().fo_plan_set_trace(plan, int(stamps) or None))
+def fo_plan_set_trace(plan, stamps, consumer_stamps=0):
+    """stamps: device uint64[tiles + W]; consumer_stamps: device
+    uint64[P + 4 * consumer CTAs]; 0 stops that trace."""
+    _check("fo_plan_set_trace", lib().fo_plan_set_trace(plan, int(stamps) or None,
+                                                        int(consumer_stamps) or None))
 
 
 def fo_plan_device_status(plan, clear=False):

@@ -150,13 +150,16 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
 fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
                              int32_t reorder_ctas, int32_t overlap);
 
-/* Per-tile completion times ([P2] Figure 3 records each tile's completion
- * time with globaltimer to show the wave pattern).  stamps: device uint64
- * [tiles + W], or NULL to stop tracing.  While set, every GEMM launch writes
- * stamps[slot] = %globaltimer (ns) when the tile at that launch slot has
- * been stored and counted, and stamps[tiles + c] = the start time of CTA c.
- * The caller owns the buffer and keeps it alive while tracing. */
-fo_status fo_plan_set_trace(fo_plan* plan, uint64_t* stamps);
+/* Timelines ([P2] Figure 3 records each tile's completion time with
+ * globaltimer to show the wave pattern).  Device uint64 buffers owned by the
+ * caller, kept alive while tracing; NULL stops that trace.
+ *  stamps [tiles + W]: every GEMM launch writes stamps[slot] = %globaltimer
+ *      (ns) when the tile at that launch slot has been stored and counted,
+ *      and stamps[tiles + c] = the start time of CTA c.
+ *  consumer_stamps [P + 4 * consumer CTAs], zeroed by the caller before the
+ *      consume call: [j] = when group j's last chunk was processed; then per
+ *      CTA c, [P + 4c ..]: SM id, start time, end time, chunks processed. */
+fo_status fo_plan_set_trace(fo_plan* plan, uint64_t* stamps, uint64_t* consumer_stamps);
 
 /* Sticky status word of the plan's GEMM launches (the GEMM call has no
  * status argument): FO_OK, or FO_ERR_TIMEOUT if one of its bounded
