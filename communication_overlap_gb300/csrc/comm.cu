@@ -1,15 +1,12 @@
-// Consumer (communication stand-in) and post-communication reorder kernels.
+// Consumer kernel: the communication stand-in.
 //
 // Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 核心设计 "通信侧" (the
 // communication runs as its own kernel on another stream), 五、CUTLASS 扩展实现
 // "专用监控内核" (a monitor kernel tracks progress through atomic counters),
-// 二、重排机制 (a group's data is contiguous so one collective call covers it;
-// the inverse mapping table restores the layout afterwards).
+// 二、重排机制 (a group's data is contiguous so one collective call covers it).
 //
-// Both kernels are HBM-bound streams of 16-byte vectors.  A unit (one tile
-// row, tile_n bf16) is tile_n / 8 vectors, so a warp moves one or two whole
-// units per instruction and every access is a full 512-byte (or 256-byte)
-// coalesced segment.
+// The kernel is an HBM-bound stream of 16-byte vectors over each group's
+// contiguous unit range: every warp instruction moves 512 contiguous bytes.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -207,101 +204,6 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
   }
 }
 
-struct ReorderArgs {
-  const uint4* src[kMaxDest];
-  uint4* dst[kMaxDest];
-  const TileInfo* tile;
-  const int32_t* part_start;
-  const int32_t* part_dst;
-  const int32_t* dest_base;
-  const int32_t* row_dest;
-  const int32_t* row_rank;
-  const int32_t* final_row;
-  int32_t layout, R, row_vec, slot0, n_slots, h, rows_per;
-};
-
-// Inverse mapping of row r of the tile at slot s: the unit's place in the
-// consumer's buffer k and the row it belongs to in output k.
-__device__ __forceinline__ void reorder_row(const ReorderArgs& a, const TileInfo& ti, int32_t s,
-                                            int32_t r, int* k_out, int32_t* src_unit,
-                                            int32_t* dst_row) {
-  int k = 0;
-  if (a.layout == FO_LAYOUT_TILE) {
-    *src_unit = ti.unit_base + r;
-    *dst_row = ti.row0 + r;
-  } else {
-    int32_t u;
-    if (a.layout == FO_LAYOUT_RS_SUBTILE) {
-      k = r / a.h;
-      const int32_t i = r - k * a.h;
-      u = ti.unit_base + k * ti.sub_stride + i;
-      *dst_row = (ti.row0 / kTileM) * a.h + i;
-    } else if (a.layout == FO_LAYOUT_RS_ROWBLOCK) {
-      k = ti.dest;
-      u = ti.unit_base + r;
-      *dst_row = ti.row0 + r - k * a.rows_per;
-    } else {  // FO_LAYOUT_A2A_SUBTOKEN
-      const int32_t rho = ti.row0 + r;
-      k = __ldg(a.row_dest + rho);
-      u = __ldg(a.dest_base + s * a.R + k) + __ldg(a.row_rank + rho);
-      *dst_row = __ldg(a.final_row + rho);
-    }
-    const int32_t jk = ti.group * a.R + k;
-    *src_unit = __ldg(a.part_dst + jk) + (u - __ldg(a.part_start + jk));
-  }
-  *k_out = k;
-}
-
-// Tile-major post-communication reorder: a CTA moves one tile at a time
-// (its TileInfo read once, the next one prefetched); each warp takes every
-// 8th row group and each lane issues kBatch independent 16-byte loads
-// before its stores, so enough bytes are in flight to keep HBM busy.
-template <int VPU>  // 16-byte vectors per unit: 32 (tile_n 256) or 16 (128)
-__global__ void __launch_bounds__(kThreads) reorder_kernel(const __grid_constant__ ReorderArgs a) {
-  constexpr int kRowsPerInstr = 32 / VPU;            // rows one warp instruction covers
-  constexpr int kWarps = kThreads / 32;
-  constexpr int kRowsPerWarp = kTileM / kWarps;      // 16
-  constexpr int kBatch = 8;                           // loads per lane per round
-  constexpr int kRounds = kRowsPerWarp / kRowsPerInstr / kBatch;
-  __shared__ const uint4* s_src[kMaxDest];
-  __shared__ uint4* s_dst[kMaxDest];
-  if (threadIdx.x < kMaxDest) {
-    s_src[threadIdx.x] = a.src[threadIdx.x];
-    s_dst[threadIdx.x] = a.dst[threadIdx.x];
-  }
-  __syncthreads();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int sub = lane / VPU, vl = lane % VPU;
-  int32_t t = blockIdx.x;
-  TileInfo next{};
-  if (t < a.n_slots) next = a.tile[a.slot0 + t];
-  for (; t < a.n_slots; t += gridDim.x) {
-    const int32_t s = a.slot0 + t;
-    const TileInfo ti = next;
-    if (t + int32_t(gridDim.x) < a.n_slots) next = a.tile[s + gridDim.x];
-#pragma unroll 1
-    for (int round = 0; round < kRounds; ++round) {
-      uint4 x[kBatch];
-      int64_t to[kBatch];   // element offsets (vector units) into output k
-      int kk[kBatch];
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int32_t r = ((round * kBatch + i) * kWarps + warp) * kRowsPerInstr + sub;
-        kk[i] = -1;
-        if (r < ti.rows) {
-          int32_t su, dr;
-          reorder_row(a, ti, s, r, &kk[i], &su, &dr);
-          x[i] = ld_cg(s_src[kk[i]] + int64_t(su) * VPU + vl);
-          to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i)
-        if (kk[i] >= 0) st_cs(s_dst[kk[i]] + to[i], x[i]);
-    }
-  }
-}
-
 int chunk_units_of(int kind, int tile_n) {
   const int bytes = (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? kChunkBytes<FO_CONS_SUM>
                                                                  : kChunkBytes<FO_CONS_COPY>;
@@ -388,38 +290,6 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
     case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
-}
-
-fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
-                              const void* const* src, void* const* dst, void* stream) {
-  ReorderArgs a{};
-  const int n = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
-  for (int k = 0; k < n; ++k) {
-    a.src[k] = static_cast<const uint4*>(src[k]);
-    a.dst[k] = static_cast<uint4*>(dst[k]);
-  }
-  a.tile = p->dev.tile;
-  a.part_start = p->dev.part_start;
-  a.part_dst = p->dev.part_dst;
-  a.dest_base = p->dev.dest_base;
-  a.row_dest = p->dev.row_dest;
-  a.row_rank = p->dev.row_rank;
-  a.final_row = p->dev.final_row;
-  a.layout = p->layout;
-  a.R = p->R;
-  a.row_vec = p->N / 8;
-  a.slot0 = p->group_slot_begin[g0];
-  a.n_slots = p->group_slot_begin[g1] - a.slot0;
-  a.h = kTileM / p->R;
-  a.rows_per = p->M / p->R;
-  int ctas = default_ctas(p, p->reorder_ctas);
-  if (ctas > a.n_slots) ctas = a.n_slots;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (p->tile_n == 256)
-    reorder_kernel<32><<<ctas, kThreads, 0, st>>>(a);
-  else
-    reorder_kernel<16><<<ctas, kThreads, 0, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
 }  // namespace fo

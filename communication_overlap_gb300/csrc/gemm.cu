@@ -32,6 +32,7 @@
 #include <mutex>
 
 #include "device_common.cuh"
+#include "tensor_map.h"
 
 namespace fo {
 
@@ -78,35 +79,6 @@ struct GemmArgs {
 };
 
 // ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
 
 // Bounded wait for the phase with the given parity.  Gives up when another
 // role aborted (shared flag) or after kWaitLimitNs; then records the error.
@@ -458,34 +430,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-              uint32_t box_inner, uint32_t box_outer) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int BN>
 fo_status launch_bn(const fo_plan* p, GemmArgs& a, cudaStream_t st) {
   static std::once_flag attr_once[64];
@@ -518,12 +462,12 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
                                reinterpret_cast<uintptr_t>(C_r);
   if (align_bits & 15) return FO_ERR_ARG;
   GemmArgs a{};
-  if (!make_map(&a.tmap_a, A, uint64_t(p->K), uint64_t(p->M), kBlockK, kTileM))
+  if (!encode_tensor_map_2d(&a.tmap_a, A, uint64_t(p->K), uint64_t(p->M), kBlockK, kTileM, true))
     return FO_ERR_CUDA;
   const int E = p->n_experts > 0 ? p->n_experts : 1;
   for (int e = 0; e < E; ++e) {
     if (!B[e] || (reinterpret_cast<uintptr_t>(B[e]) & 15)) return FO_ERR_ARG;
-    if (!make_map(&a.tmap_b[e], B[e], uint64_t(p->N), uint64_t(p->K), 64, kBlockK))
+    if (!encode_tensor_map_2d(&a.tmap_b[e], B[e], uint64_t(p->N), uint64_t(p->K), 64, kBlockK, true))
       return FO_ERR_CUDA;
   }
   a.tile = p->dev.tile;

@@ -1,0 +1,224 @@
+// Post-communication reorder kernel (TMA bulk copies).
+//
+// Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 二、重排机制 "解决方案:
+// 映射表重排" (after communication the inverse mapping table restores the
+// original layout) and Figure 6's per-primitive patterns; "Efficient and
+// Adaptable Overlapping ...", Figure 5 ("the tiles are reordered back when
+// communication finishes").
+//
+// A CTA moves one tile at a time through 64 KB of shared memory using the
+// Tensor Memory Accelerator, so almost no thread time goes into moving
+// bytes:
+//  * the tile's rows are contiguous in the communication buffer (one run
+//    per destination part), so they arrive with one 1-D bulk copy per run
+//    (a per-row copy for the All-to-All layout, whose rows are spread over
+//    the receive buffers by rank);
+//  * a full tile leaves with one 2-D tensor store of a 128 x tile_n box (a
+//    32-row box per subtile for the ReduceScatter layout) into the
+//    row-major output; ragged tiles and All-to-All rows leave as per-row
+//    512-byte bulk stores.
+// Three CTAs per SM keep ~192 KB per SM in flight.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "tensor_map.h"
+
+namespace fo {
+
+namespace {
+
+constexpr int kRThreads = kTileM;                  // one thread per tile row
+constexpr int kRTileBytes = kTileM * 256 * 2;      // a full 128 x 256 bf16 tile
+constexpr int kRSmem = 1024 + kRTileBytes + 64;    // alignment slack, tile, barrier
+constexpr uint64_t kRWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+struct ReorderArgs {
+  CUtensorMap dst_map[kMaxDest];  // outputs, boxes of box_rows x tile_n
+  const uint8_t* src[kMaxDest];
+  uint8_t* dst[kMaxDest];
+  const TileInfo* tile;
+  const int32_t* part_start;
+  const int32_t* part_dst;
+  const int32_t* dest_base;
+  const int32_t* row_dest;
+  const int32_t* row_rank;
+  const int32_t* final_row;
+  int32_t* status;
+  int32_t layout, R, unit_bytes, row_bytes, slot0, n_slots, h, rows_per;
+};
+
+// Inverse mapping of row r of the tile at slot s: the unit's place in the
+// consumer's buffer k and the row it belongs to in output k.
+__device__ __forceinline__ void reorder_row(const ReorderArgs& a, const TileInfo& ti, int32_t s,
+                                            int32_t r, int* k_out, int32_t* src_unit,
+                                            int32_t* dst_row) {
+  int k = 0;
+  if (a.layout == FO_LAYOUT_TILE) {
+    *src_unit = ti.unit_base + r;
+    *dst_row = ti.row0 + r;
+  } else {
+    int32_t u;
+    if (a.layout == FO_LAYOUT_RS_SUBTILE) {
+      k = r / a.h;
+      const int32_t i = r - k * a.h;
+      u = ti.unit_base + k * ti.sub_stride + i;
+      *dst_row = (ti.row0 / kTileM) * a.h + i;
+    } else if (a.layout == FO_LAYOUT_RS_ROWBLOCK) {
+      k = ti.dest;
+      u = ti.unit_base + r;
+      *dst_row = ti.row0 + r - k * a.rows_per;
+    } else {  // FO_LAYOUT_A2A_SUBTOKEN
+      const int32_t rho = ti.row0 + r;
+      k = a.row_dest[rho];
+      u = a.dest_base[s * a.R + k] + a.row_rank[rho];
+      *dst_row = a.final_row[rho];
+    }
+    const int32_t jk = ti.group * a.R + k;
+    *src_unit = a.part_dst[jk] + (u - a.part_start[jk]);
+  }
+  *k_out = k;
+}
+
+__global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constant__ ReorderArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* buf = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(buf + kRTileBytes);
+  __shared__ int s_ok;
+  const int tid = threadIdx.x;
+  const uint32_t sbuf = smem_u32(buf), sfull = smem_u32(full);
+  if (tid == 0) {
+    mbar_init(sfull, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int32_t ub = a.unit_bytes;
+  uint32_t phase = 0;
+  for (int32_t t = blockIdx.x; t < a.n_slots; t += gridDim.x, phase ^= 1) {
+    const int32_t s = a.slot0 + t;
+    const TileInfo ti = a.tile[s];
+    // the previous tile's stores have finished reading the buffer
+    bulk_wait_read_all();
+    __syncthreads();
+    if (tid == 0) mbar_expect_tx(sfull, uint32_t(ti.rows * ub));
+    __syncthreads();
+    const bool whole = (a.layout == FO_LAYOUT_TILE || a.layout == FO_LAYOUT_RS_ROWBLOCK);
+    if (whole) {
+      if (tid == 0) {
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, 0, &k, &su, &dr);   // rows are contiguous from row 0
+        bulk_load(sbuf, a.src[k] + int64_t(su) * ub, uint32_t(ti.rows * ub), sfull);
+      }
+    } else if (a.layout == FO_LAYOUT_RS_SUBTILE) {
+      if (tid < a.R) {   // subtile tid: rows tid*h .. +h, contiguous in slice tid
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, tid * a.h, &k, &su, &dr);
+        bulk_load(sbuf + tid * a.h * ub, a.src[k] + int64_t(su) * ub, uint32_t(a.h * ub), sfull);
+      }
+    } else if (tid < ti.rows) {  // All-to-All: row by row
+      int k;
+      int32_t su, dr;
+      reorder_row(a, ti, s, tid, &k, &su, &dr);
+      bulk_load(sbuf + tid * ub, a.src[k] + int64_t(su) * ub, uint32_t(ub), sfull);
+    }
+    // wait for the tile to land (bounded)
+    if (tid == 0) {
+      int ok = 1;
+      if (!mbar_try_wait(sfull, phase)) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(sfull, phase))
+          if (globaltimer_ns() - t0 > kRWaitLimitNs) {
+            ok = 0;
+            atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
+            break;
+          }
+      }
+      s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) break;
+    if (whole && ti.rows == kTileM) {
+      if (tid == 0) {
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, 0, &k, &su, &dr);
+        tensor_store_2d(&a.dst_map[k], sbuf, ti.col0, dr);
+        bulk_commit();
+      }
+    } else if (a.layout == FO_LAYOUT_RS_SUBTILE) {
+      if (tid < a.R) {
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, tid * a.h, &k, &su, &dr);
+        tensor_store_2d(&a.dst_map[k], sbuf + tid * a.h * ub, ti.col0, dr);
+        bulk_commit();
+      }
+    } else if (tid < ti.rows) {  // ragged tiles and All-to-All rows: per row
+      int k;
+      int32_t su, dr;
+      reorder_row(a, ti, s, tid, &k, &su, &dr);
+      bulk_store(a.dst[k] + int64_t(dr) * a.row_bytes + int64_t(ti.col0) * 2, sbuf + tid * ub,
+                 uint32_t(ub));
+      bulk_commit();
+    }
+  }
+  // every store has completed before the CTA (and its shared memory) ends
+  bulk_wait_all();
+}
+
+}  // namespace
+
+fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
+                              const void* const* src, void* const* dst, void* stream) {
+  static std::once_flag once[64];
+  static cudaError_t attr_err[64];
+  const int dv = p->device < 64 ? p->device : 63;
+  std::call_once(once[dv], [&] {
+    attr_err[dv] = cudaFuncSetAttribute(reorder_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmem);
+  });
+  if (attr_err[dv] != cudaSuccess) return FO_ERR_CUDA;
+
+  ReorderArgs a{};
+  const int n = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
+  for (int k = 0; k < n; ++k) {
+    if ((reinterpret_cast<uintptr_t>(src[k]) | reinterpret_cast<uintptr_t>(dst[k])) & 15)
+      return FO_ERR_ARG;
+    a.src[k] = static_cast<const uint8_t*>(src[k]);
+    a.dst[k] = static_cast<uint8_t*>(dst[k]);
+    if (p->layout != FO_LAYOUT_A2A_SUBTOKEN) {
+      const int box_rows = p->layout == FO_LAYOUT_RS_SUBTILE ? kTileM / p->R : kTileM;
+      if (!encode_tensor_map_2d(&a.dst_map[k], dst[k], uint64_t(p->N),
+                                uint64_t(p->final_rows[k]), uint32_t(p->tile_n),
+                                uint32_t(box_rows), false))
+        return FO_ERR_CUDA;
+    }
+  }
+  a.tile = p->dev.tile;
+  a.part_start = p->dev.part_start;
+  a.part_dst = p->dev.part_dst;
+  a.dest_base = p->dev.dest_base;
+  a.row_dest = p->dev.row_dest;
+  a.row_rank = p->dev.row_rank;
+  a.final_row = p->dev.final_row;
+  a.status = p->dev.gemm_status;
+  a.layout = p->layout;
+  a.R = p->R;
+  a.unit_bytes = p->tile_n * 2;
+  a.row_bytes = p->N * 2;
+  a.slot0 = p->group_slot_begin[g0];
+  a.n_slots = p->group_slot_begin[g1] - a.slot0;
+  a.h = kTileM / p->R;
+  a.rows_per = p->M / p->R;
+  int ctas = p->reorder_ctas > 0 ? p->reorder_ctas : 3 * p->sm_count;
+  if (ctas > a.n_slots) ctas = a.n_slots;
+  reorder_kernel<<<ctas, kRThreads, kRSmem, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
+}
+
+}  // namespace fo

@@ -141,7 +141,8 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length);
 
 /* Launch settings of the consumer and reorder kernels.
- *  consumer_ctas, reorder_ctas: grid sizes (<= 0: 4 per SM, the default).
+ *  consumer_ctas, reorder_ctas: grid sizes (<= 0: the defaults, 4 consumer
+ *      and 3 reorder CTAs per SM).
  *  overlap: non-zero (default) launches the consumer as a programmatic
  *      dependent launch: issued on the GEMM's stream right after
  *      fo_signaled_gemm, it starts as soon as every GEMM CTA is resident and
@@ -161,11 +162,11 @@ fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
  *      CTA c, [P + 4c ..]: SM id, start time, end time, chunks processed. */
 fo_status fo_plan_set_trace(fo_plan* plan, uint64_t* stamps, uint64_t* consumer_stamps);
 
-/* Sticky status word of the plan's GEMM launches (the GEMM call has no
- * status argument): FO_OK, or FO_ERR_TIMEOUT if one of its bounded
- * pipeline waits ran out.  Synchronises the device; clears the word when
- * `clear` is non-zero. */
-fo_status fo_plan_device_status(const fo_plan* plan, int32_t* gemm_status,
+/* Sticky status word of the plan's GEMM and reorder launches (calls with
+ * no status argument): FO_OK, or FO_ERR_TIMEOUT if one of their bounded
+ * waits on their own copies ran out.  Synchronises the device; clears the
+ * word when `clear` is non-zero. */
+fo_status fo_plan_device_status(const fo_plan* plan, int32_t* kernel_status,
                                 int32_t clear);
 
 void fo_plan_destroy(fo_plan* plan);
