@@ -410,11 +410,7 @@ def run_ours(args):
 
     # max over ranks
     def rmax(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, dist if world > 1 else None, dev)
 
     ms_ov = rmax(ms_ov)
     ms_ser = rmax(statistics.mean(t_ser))
@@ -438,7 +434,7 @@ def run_ours(args):
         out = {
             "metric": "signaled GEMM TFLOPS (% of bf16 peak); overlap time vs serial "
                       "GEMM+consumer",
-            "value": world * flops / (ms_ov * 1e-3) / 1e12,
+            "value": whole_job_tflops(world, flops, ms_ov),
             "unit": "TFLOPS",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_ov, "higher_is_better": True, "scaling": "weak",
@@ -453,7 +449,7 @@ def run_ours(args):
                          "kernel": "signaled_gemm_kernel<256> (alone, signals on)",
                          "peak_source": f"{peak_kind} bf16 burst"},
             "clocks": clk.summary(),
-            "e2e": {"value": world * flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS",
+            "e2e": {"value": whole_job_tflops(world, flops, ms_e2e), "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ms_e2e},
             "gpu_launches": 3 * args.steps,
@@ -484,6 +480,22 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def max_over_ranks(x, dist=None, device=None):
+    """The slowest rank's value (every rank gets it); identity on one rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_rank, ms_slowest):
+    """Every rank runs its own replica: the job's FLOPs over the slowest
+    rank's time per step."""
+    return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
 
 
 def consumer_name(w):
