@@ -49,6 +49,10 @@ def parse():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--trace-out", default="", help="write per-tile stamps (json)")
+    ap.add_argument("--consumer-ctas", type=int, default=0,
+                    help="consumer grid (0: library default, 4 per SM)")
+    ap.add_argument("--reorder-ctas", type=int, default=0,
+                    help="reorder grid (0: library default, 3 per SM)")
     return ap.parse_args()
 
 
@@ -304,7 +308,8 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     w = W.WORKLOADS[args.workload]
     inp = W.make_inputs(w)
-    pipe = Pipeline(w, inp, device=dev)
+    pipe = Pipeline(w, inp, device=dev, consumer_ctas=args.consumer_ctas,
+                    reorder_ctas=args.reorder_ctas)
     s = pipe.s0
     flops = w.gemm_flops()
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -442,6 +447,7 @@ def run_ours(args):
             "config": {"workload": workload_name(w), "partition": pipe.partition,
                        "groups_tiles": pipe.group_tiles, "consumer": consumer_name(w),
                        "l2": "flushed before every timed step (256 MiB write)",
+                       "consumer_ctas": args.consumer_ctas or "4 per SM",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_burst,
                          "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,

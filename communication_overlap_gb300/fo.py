@@ -23,6 +23,7 @@ FO_CONS_COPY, FO_CONS_SUM, FO_CONS_RS, FO_CONS_A2A = range(4)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p
 _vpp = ctypes.POINTER(ctypes.c_void_p)
+_dp = ctypes.POINTER(ctypes.c_double)
 
 
 class fo_plan_desc(ctypes.Structure):
@@ -79,6 +80,12 @@ def lib():
                                                         _vp]),
             "fo_reorder_back": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, _vpp,
                                                _vpp, _vp]),
+            "fo_predict_partition": (ctypes.c_int, [ctypes.POINTER(fo_plan_desc),
+                                                    ctypes.c_double, _dp, _dp, ctypes.c_int32,
+                                                    _dp]),
+            "fo_tune_partition": (ctypes.c_int, [ctypes.POINTER(fo_plan_desc), ctypes.c_double,
+                                                 _dp, _dp, ctypes.c_int32, _i32p,
+                                                 ctypes.c_int32, _i32p, _dp]),
             "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -227,6 +234,35 @@ def fo_reorder_back(plan, group_begin, group_end, src, dst, stream):
     _check("fo_reorder_back",
            lib().fo_reorder_back(plan, group_begin, group_end, _ptrs(src), _ptrs(dst),
                                  stream or None))
+
+
+def _curve(curve):
+    pts = list(curve)
+    b = (ctypes.c_double * len(pts))(*[float(x) for x, _ in pts])
+    t = (ctypes.c_double * len(pts))(*[float(y) for _, y in pts])
+    return b, t, len(pts)
+
+
+def fo_predict_partition(desc, gemm_us, curve):
+    """curve: [(bytes, us), ...]; desc carries the partition."""
+    b, t, n = _curve(curve)
+    out = ctypes.c_double()
+    _check("fo_predict_partition",
+           lib().fo_predict_partition(ctypes.byref(desc), gemm_us, b, t, n, ctypes.byref(out)))
+    return out.value
+
+
+def fo_tune_partition(desc, gemm_us, curve):
+    """Returns (waves per group, predicted us)."""
+    b, t, n = _curve(curve)
+    _, T = fo_wave_count(desc)
+    parts = (ctypes.c_int32 * max(1, T))()
+    ng = ctypes.c_int32()
+    out = ctypes.c_double()
+    _check("fo_tune_partition",
+           lib().fo_tune_partition(ctypes.byref(desc), gemm_us, b, t, n, parts, T,
+                                   ctypes.byref(ng), ctypes.byref(out)))
+    return list(parts)[:ng.value], out.value
 
 
 def partition_one_then_two(T):

@@ -95,6 +95,23 @@ class Pipeline:
         fo.fo_plan_destroy(self.plan)
         self.plan = None
 
+    def replan(self, partition):
+        """Switch to another wave-group partition, keeping the data buffers
+        (their sizes do not depend on the partition)."""
+        torch.cuda.synchronize(self.device)
+        fo.fo_plan_destroy(self.plan)
+        self.partition = list(partition)
+        self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
+        self.plan = fo.fo_plan_groups(self.desc)
+        self._overlap = None
+        _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
+        self.P = len(self.partition)
+        assert fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS) == self.dest_units
+        d = self.device
+        self.buf.count = torch.zeros((self.P,), dtype=torch.int32, device=d)
+        self.buf.flags = torch.zeros((self.P,), dtype=torch.int32, device=d)
+        self.buf.status.zero_()
+
     # ------------------------------------------------------------ calls
     def gemm(self, stream, epoch, signal=True):
         b = self.buf

@@ -1,0 +1,164 @@
+"""Algorithm 1 on one GB300: offline measurements, the predictive search,
+and a check of the prediction against measured step times.
+
+  python -m communication_overlap_gb300.tuning --workload allreduce [--validate]
+
+Offline ([P1] "FlashOverlap: 信号驱动计算通信重叠论文详解", 四、实时调优, 离线阶段):
+  * GEMM configuration: our own signaled GEMM, its duration timed alone;
+  * "bandwidth curve": on one GPU the communication is the consumer
+    stand-in, so the curve is the consumer's latency against group bytes,
+    sampled by timing fo_consume_group on a first group of k waves
+    (k = 1 .. T), its flag already raised;
+  * SM contention: W = the GEMM's persistent CTAs, fixed by the workload.
+Online: fo_tune_partition (exact over all 2^(T-1) candidates).
+
+--validate runs the overlapped step for every candidate partition (T <= 8)
+and reports how the predicted best compares with the measured best.
+"""
+import argparse
+import json
+import statistics
+import sys
+
+import torch
+
+from . import fo
+from . import workloads as W
+from .pipeline import Pipeline
+
+
+def _design_space(T):
+    """All partitions of T waves into consecutive groups (2^(T-1))."""
+    out = []
+    for mask in range(1 << (T - 1)):
+        parts, run = [], 0
+        for k in range(T):
+            run += 1
+            if k == T - 1 or (mask >> (T - 2 - k)) & 1:
+                parts.append(run)
+                run = 0
+        out.append(parts)
+    return out
+
+
+def _time(fn, stream, reps, flush):
+    ms = []
+    for _ in range(reps):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    return statistics.median(ms) * 1e3   # us
+
+
+class Tuner:
+    def __init__(self, w, inp=None, reps=20):
+        self.w = w
+        self.inp = inp or W.make_inputs(w)
+        self.reps = reps
+        self.pipe = Pipeline(w, self.inp)
+        self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.tile_bytes = w.tile_m * w.tile_n * 2
+
+    def flush(self):
+        with torch.cuda.stream(self.pipe.s0):
+            self.flush_buf.fill_(1)
+
+    def close(self):
+        self.pipe.close()
+
+    def gemm_us(self):
+        p = self.pipe
+        for _ in range(3):
+            p.gemm(p.s0, p.epoch)
+        return _time(lambda: p.gemm(p.s0, p.epoch), p.s0, self.reps, self.flush)
+
+    def curve(self):
+        """[(bytes, us)] for first groups of 1 .. T waves."""
+        p = self.pipe
+        T = p.waves
+        pts = []
+        for k in range(1, T + 1):
+            p.replan([k, T - k] if k < T else [T])
+            p.step(overlap=False)
+            torch.cuda.synchronize()
+            p.set_overlap(False)
+            us = _time(lambda: p.consume(p.s0, p.epoch, group=0), p.s0, self.reps, self.flush)
+            nbytes = p.group_tiles[0] * self.tile_bytes
+            pts.append((float(nbytes), us))
+        return pts
+
+    def step_us(self, partition):
+        p = self.pipe
+        p.replan(partition)
+        for _ in range(3):
+            p.step(overlap=True)
+        torch.cuda.synchronize()
+        assert int(p.buf.status.item()) == 0
+        return _time(lambda: p.step(overlap=True, sync_current=False), p.s0, self.reps,
+                     self.flush)
+
+    def desc(self, partition=()):
+        return fo.make_desc(**self.pipe.desc_args, group_waves=partition, host_only=True)
+
+
+def run(name, validate=False, reps=20):
+    w = W.WORKLOADS[name]
+    t = Tuner(w, reps=reps)
+    try:
+        gemm = t.gemm_us()
+        curve = t.curve()
+        best, pred = fo.fo_tune_partition(t.desc(), gemm, curve)
+        out = {"workload": name, "waves": t.pipe.waves, "gemm_us": gemm,
+               "curve": curve, "tuned": best, "tuned_predicted_us": pred}
+        base = fo.partition_one_then_two(t.pipe.waves)
+        out["one_then_two_predicted_us"] = fo.fo_predict_partition(t.desc(base), gemm, curve)
+        if validate:
+            rows = []
+            for cand in _design_space(t.pipe.waves):
+                rows.append({"partition": cand,
+                             "predicted_us": fo.fo_predict_partition(t.desc(cand), gemm, curve),
+                             "measured_us": t.step_us(cand)})
+            meas_best = min(rows, key=lambda r: r["measured_us"])
+            tuned_meas = next(r for r in rows if r["partition"] == best)["measured_us"]
+            finest = next(r for r in rows if r["partition"] == [1] * t.pipe.waves)
+            coarsest = next(r for r in rows if r["partition"] == [t.pipe.waves])
+            out.update({
+                "candidates": len(rows),
+                "measured_best": meas_best,
+                "tuned_measured_us": tuned_meas,
+                "tuned_regret": tuned_meas / meas_best["measured_us"] - 1.0,
+                "finest_measured_us": finest["measured_us"],
+                "finest_loss": finest["measured_us"] / meas_best["measured_us"] - 1.0,
+                "coarsest_measured_us": coarsest["measured_us"],
+                "rank_of_tuned": 1 + sorted(r["measured_us"] for r in rows).index(tuned_meas),
+                "all": rows,
+            })
+        return out
+    finally:
+        t.close()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="allreduce")
+    ap.add_argument("--validate", action="store_true")
+    ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--out", default="")
+    a = ap.parse_args(argv)
+    res = run(a.workload, a.validate, a.reps)
+    text = json.dumps(res)
+    if a.out:
+        with open(a.out, "w") as f:
+            f.write(text)
+    summary = {k: v for k, v in res.items() if k not in ("all", "curve")}
+    print(json.dumps(summary))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -272,6 +272,34 @@ fo_status fo_reorder_back(const fo_plan* plan, int32_t group_begin,
                           int32_t group_end, const void* const* src,
                           void* const* dst, void* cuda_stream);
 
+/* Wave-group tuning ([P1] 四、实时调优, Algorithm 1).  The offline inputs are
+ * the GEMM's duration (gemm_us, e.g. measured with fo_signaled_gemm) and the
+ * communication latency curve: n_points >= 2 samples (curve_bytes[i],
+ * curve_us[i]) of latency against message size, distinct sizes, any order;
+ * between samples the curve is linear, below the smallest sample it is that
+ * sample's latency, above the largest it follows the last segment's slope.
+ * A group's data size is its tile count (the last wave may be partial)
+ * times tile_m * tile_n * 2 bytes; its compute time is gemm_us / T per
+ * wave.  The predicted latency of a partition is E_P, with
+ *   E_i = max(compute end of groups 1..i, E_{i-1}) + curve(bytes of G_i).
+ * desc: the shape fields as for fo_plan_groups (host_only may be set). */
+
+/* Predicted latency (us) of the partition in desc->group_waves. */
+fo_status fo_predict_partition(const fo_plan_desc* desc, double gemm_us,
+                               const double* curve_bytes, const double* curve_us,
+                               int32_t n_points, double* predicted_us);
+
+/* The partition with the smallest predicted latency over all 2^(T-1)
+ * candidates, found exactly by a dynamic program over group boundaries in
+ * O(T^2) (the pages enumerate the candidates).  Writes the waves per group
+ * to group_waves[0 .. *n_groups) (capacity >= T always suffices; FO_ERR_ARG
+ * if capacity is too small, *n_groups still set) and the prediction to
+ * *predicted_us (may be NULL). */
+fo_status fo_tune_partition(const fo_plan_desc* desc, double gemm_us,
+                            const double* curve_bytes, const double* curve_us,
+                            int32_t n_points, int32_t* group_waves, int32_t capacity,
+                            int32_t* n_groups, double* predicted_us);
+
 const char* fo_status_string(fo_status status);
 
 #ifdef __cplusplus

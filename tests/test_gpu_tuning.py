@@ -1,0 +1,32 @@
+"""Offline measurements and the predictive search on the GPU (-m gpu):
+the sampled latency curve is positive and grows with the group size, the
+tuned partition is valid, and re-planning keeps the path bit-exact."""
+import pytest
+import torch
+
+from communication_overlap_gb300 import fo
+from communication_overlap_gb300 import workloads as W
+from communication_overlap_gb300.tuning import Tuner
+
+from gpu_checks import check_run
+
+pytestmark = pytest.mark.gpu
+
+
+def test_tuner_small_allreduce():
+    w = W.scaled(W.WORKLOADS["allreduce"], M=1024, N=2048, K=256, wave_width=8)
+    t = Tuner(w, reps=3)
+    try:
+        gemm = t.gemm_us()
+        curve = t.curve()
+        assert gemm > 0 and len(curve) == t.pipe.waves
+        assert all(us > 0 for _, us in curve)
+        assert curve[-1][1] > curve[0][1]          # more bytes take longer
+        parts, pred = fo.fo_tune_partition(t.desc(), gemm, curve)
+        assert sum(parts) == t.pipe.waves and pred >= gemm
+        t.pipe.replan(parts)
+        t.pipe.step()
+        res = t.pipe.results()
+        check_run(t.pipe, t.inp, res)
+    finally:
+        t.close()

@@ -1,0 +1,63 @@
+"""The library's partition tuner (exact dynamic program) against the
+oracle's Algorithm 1 brute force.  No GPU."""
+import numpy as np
+import pytest
+
+from communication_overlap_gb300 import fo
+from oracle import plan as OP
+from oracle import tune as OT
+
+
+def _desc(M, N, W, tn=256, parts=()):
+    return fo.make_desc(M=M, N=N, K=64, tile_n=tn, swizzle=8, wave_width=W,
+                        group_waves=parts, host_only=True)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_dp_finds_the_brute_force_minimum(seed):
+    rng = np.random.default_rng(seed)
+    W = int(rng.integers(2, 9))
+    tm, tn = int(rng.integers(2, 7)), int(rng.integers(2, 6))
+    tiles = tm * tn
+    T = OP.wave_count(tiles, W)
+    if T > 11:
+        T = 11
+        W = -(-tiles // T)
+        T = OP.wave_count(tiles, W)
+    tile_bytes = 128 * 256 * 2
+    dur = float(rng.uniform(50, 500))
+    xs = np.sort(rng.choice(np.arange(1, 4 * tiles + 1), 5, replace=False)) * tile_bytes / 2
+    ys = np.sort(rng.uniform(1, 80, 5)) if seed % 2 else rng.uniform(1, 80, 5)
+    curve = list(zip(xs.tolist(), ys.tolist()))
+    best, t_min = OT.best_partition(T, dur, curve, W, tiles, tile_bytes)
+    parts, pred = fo.fo_tune_partition(_desc(tm * 128, tn * 256, W), dur, curve)
+    assert sum(parts) == T and min(parts) >= 1
+    assert pred == pytest.approx(t_min, rel=1e-12, abs=1e-9)
+    # the returned partition really has that prediction
+    assert OT.predict(tuple(parts), dur, curve, W, tiles, tile_bytes) == pytest.approx(t_min)
+    # and the predictor agrees with the oracle on every candidate
+    for cand in OP.design_space(T)[:64]:
+        p = fo.fo_predict_partition(_desc(tm * 128, tn * 256, W, parts=cand), dur, curve)
+        assert p == pytest.approx(OT.predict(cand, dur, curve, W, tiles, tile_bytes))
+
+
+def test_large_T_is_fast_and_no_worse_than_one_then_two():
+    # the grouped workload has about 98 waves: 2^97 candidates
+    W, tiles_m, tiles_n = 148, 259, 56
+    d = _desc(tiles_m * 128, tiles_n * 256, W)
+    _, T = fo.fo_wave_count(d)
+    curve = [(65536 * 16, 4.0), (65536 * 148, 20.0), (65536 * 2960, 300.0)]
+    parts, pred = fo.fo_tune_partition(d, 2700.0, curve)
+    assert sum(parts) == T
+    base = OP.one_then_two(T)
+    p_base = fo.fo_predict_partition(_desc(tiles_m * 128, tiles_n * 256, W, parts=base),
+                                     2700.0, curve)
+    assert pred <= p_base + 1e-9
+    assert pred >= 2700.0   # never below the GEMM itself
+
+
+def test_bad_curves_rejected():
+    d = _desc(512, 1024, 4)
+    for curve in ([(1, 2.0)], [(1, 2.0), (1, 3.0)], [(1, float("nan")), (2, 1.0)]):
+        with pytest.raises(fo.FoError):
+            fo.fo_tune_partition(d, 10.0, curve)
