@@ -7,8 +7,10 @@ Offline ([P1] "FlashOverlap: 信号驱动计算通信重叠论文详解", 四、
   * GEMM configuration: our own signaled GEMM, its duration timed alone;
   * "bandwidth curve": on one GPU the communication is the consumer
     stand-in, so the curve is the consumer's latency against group bytes,
-    sampled by timing fo_consume_group on a first group of k waves
-    (k = 1 .. T), its flag already raised;
+    sampled on a first group of k waves (k = 1 .. T), its flag already
+    raised.  The latency is taken inside the kernel (first CTA start to last
+    CTA end, from the consumer's globaltimer trace): in the overlapped step
+    one consumer launch serves every group, so no group pays a launch;
   * SM contention: W = the GEMM's persistent CTAs, fixed by the workload.
 Online: fo_tune_partition (exact over all 2^(T-1) candidates).
 
@@ -78,18 +80,29 @@ class Tuner:
         return _time(lambda: p.gemm(p.s0, p.epoch), p.s0, self.reps, self.flush)
 
     def curve(self):
-        """[(bytes, us)] for first groups of 1 .. T waves."""
+        """[(bytes, us)] for first groups of 1 .. T waves (in-kernel time)."""
         p = self.pipe
         T = p.waves
+        ctas = 4 * torch.cuda.get_device_properties(p.device).multi_processor_count
         pts = []
         for k in range(1, T + 1):
             p.replan([k, T - k] if k < T else [T])
             p.step(overlap=False)
             torch.cuda.synchronize()
             p.set_overlap(False)
-            us = _time(lambda: p.consume(p.s0, p.epoch, group=0), p.s0, self.reps, self.flush)
-            nbytes = p.group_tiles[0] * self.tile_bytes
-            pts.append((float(nbytes), us))
+            trace = torch.zeros(p.P + 4 * ctas, dtype=torch.int64, device=p.device)
+            fo.fo_plan_set_trace(p.plan, 0, trace.data_ptr())
+            spans = []
+            for _ in range(self.reps):
+                self.flush()
+                trace.zero_()
+                p.consume(p.s0, p.epoch, group=0)
+                torch.cuda.synchronize()
+                rec = trace[p.P:].view(-1, 4).cpu()
+                ran = rec[rec[:, 1] > 0]
+                spans.append(float(ran[:, 2].max() - ran[:, 1].min()) / 1e3)
+            fo.fo_plan_set_trace(p.plan, 0, 0)
+            pts.append((float(p.group_tiles[0] * self.tile_bytes), statistics.median(spans)))
         return pts
 
     def step_us(self, partition):
