@@ -81,6 +81,15 @@ fo_status fo_plan_set_launch(fo_plan* p, int32_t consumer_ctas, int32_t reorder_
   return FO_OK;
 }
 
+fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairable) {
+  if (!p) return FO_ERR_ARG;
+  if (pairable) *pairable = p->pairable ? 1 : 0;
+  if (variant < FO_GEMM_AUTO || variant > FO_GEMM_PAIRS) return FO_ERR_ARG;
+  if (variant == FO_GEMM_PAIRS && !p->pairable) return FO_ERR_UNSUPPORTED;
+  p->gemm_variant = variant;
+  return FO_OK;
+}
+
 fo_status fo_plan_set_trace(fo_plan* p, uint64_t* stamps, uint64_t* consumer_stamps) {
   if (!p) return FO_ERR_ARG;
   p->trace = stamps;

@@ -65,6 +65,8 @@ struct fo_plan {
   int device = -1;
   int sm_count = 0;
   int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
+  int gemm_variant = 0;   // fo_gemm_variant
+  bool pairable = false;  // launch slots (2i, 2i+1) are vertically adjacent tiles
   uint64_t* trace = nullptr;           // caller's device buffers, see fo_plan_set_trace
   uint64_t* consumer_trace = nullptr;
   void* blob = nullptr;

@@ -41,22 +41,29 @@ namespace {
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
-template <int BN>
+// PAIR: two CTAs of a cluster compute vertically adjacent 128 x BN tiles with
+// one tcgen05.mma.cta_group::2 (M = 256): each CTA stages its own A rows
+// and half of B's columns, so a CTA loads 32 KB per 64-deep k-block instead
+// of 48 KB (BN = 256).
+template <int BN, bool PAIR>
 struct Cfg {
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kBCols = PAIR ? BN / 2 : BN;       // B columns this CTA stages
   static constexpr int kABytes = kTileM * kBlockK * 2;
-  static constexpr int kBBytes = kBlockK * BN * 2;
+  static constexpr int kBBytes = kBlockK * kBCols * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
+  // as many stages as fit in 192 KB (4 of 48 KB, 6 of 32 KB, 8 of 24 KB)
+  static constexpr int kStages = (196608 / kStageBytes) < 8 ? (196608 / kStageBytes) : 8;
   static constexpr int kTmemCols = 2 * BN;
   static constexpr int kStagingBytes = 4 * 32 * 128;
   static constexpr int kBarOffset = kStages * kStageBytes + kStagingBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 256;
+  static constexpr int kMmaM = PAIR ? 2 * kTileM : kTileM;
   // instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (bits
   // 7-9 = 1), B bf16 (bits 10-12 = 1), A K-major (bit 15 = 0), B MN-major
   // (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
   static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
                                      (uint32_t(BN >> 3) << 17) |
-                                     (uint32_t(kTileM >> 4) << 24);
+                                     (uint32_t(kMmaM >> 4) << 24);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(2 * kStages + 7 + 1 <= 32, "barrier area");
 };
@@ -168,6 +175,68 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                   addr),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on the
+// pair leader's mbarrier (`bar` is a cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Commit the pair's MMAs to the mbarrier at `bar` in both CTAs.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(uint16_t(3))
+      : "memory");
+}
+
 // ---------------------------------------------------------------- the kernel
 
 // Unit (row of the reordered buffer) of row r of a tile, or -1 past its rows.
@@ -185,35 +254,37 @@ __device__ __forceinline__ int32_t row_unit(const GemmArgs& a, const TileInfo& t
   return ti.unit_base + r;
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     signaled_gemm_kernel(const __grid_constant__ GemmArgs a) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the 128-byte swizzle atoms
+  // 1024-byte alignment for the 128-byte swizzle atoms (the same offsets in
+  // both CTAs of a pair: the pair's MMA reads both at the leader's offsets)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* staging = smem + C::kStages * C::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
-  uint64_t* full = bars;
+  uint64_t* full = bars;                         // PAIR: used in the leader only
   uint64_t* empty = bars + C::kStages;
   uint64_t* acc_full = bars + 2 * C::kStages;
-  uint64_t* acc_empty = bars + 2 * C::kStages + 2;
+  uint64_t* acc_empty = bars + 2 * C::kStages + 2;   // PAIR: leader's counts both CTAs
   uint64_t* epi_done = bars + 2 * C::kStages + 4;
   uint64_t* drain = bars + 2 * C::kStages + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 7);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? cluster_rank() : 0;   // 0 = the pair's leader
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&full[s]), PAIR ? 2 : 1);   // one producer per CTA
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&acc_full[b]), 1);
-      mbar_init(smem_u32(&acc_empty[b]), 4);
+      mbar_init(smem_u32(&acc_empty[b]), PAIR ? 8 : 4);   // epilogue warps
       mbar_init(smem_u32(&epi_done[b]), 4);
     }
     mbar_init(smem_u32(drain), 1);
@@ -223,15 +294,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tmap(&a.tmap_a);
   }
   if (warp == 1) {
-    asm volatile(
-        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-            smem_u32(tmem_slot)),
-        "r"(uint32_t(C::kTmemCols))
-        : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    // PAIR: one warp in each CTA of the pair allocates collectively; both
+    // get the same columns in their own tensor memory
+    if constexpr (PAIR) {
+      asm volatile(
+          "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+              smem_u32(tmem_slot)),
+          "r"(uint32_t(C::kTmemCols))
+          : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile(
+          "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+              smem_u32(tmem_slot)),
+          "r"(uint32_t(C::kTmemCols))
+          : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // This CTA is resident: a consumer launched as a programmatic dependent of
@@ -259,12 +342,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
           const uint32_t sb = sa + C::kABytes;
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_expect_tx(fb, C::kStageBytes);
-          tma_load_2d(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
+          if constexpr (PAIR) {
+            // this CTA's A rows and its half of B land in its own shared
+            // memory; the leader's full barrier counts both CTAs' bytes
+            const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
+            mbar_expect_tx_cluster(fb, C::kStageBytes);
+            tma_load_2d_pair(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
 #pragma unroll
-          for (int c = 0; c < BN / 64; ++c)
-            tma_load_2d(sb + c * (kBlockK * 128), mb, fb, ti.col0 + c * 64, kb * kBlockK);
+            for (int c = 0; c < C::kBCols / 64; ++c)
+              tma_load_2d_pair(sb + c * (kBlockK * 128), mb, fb,
+                               ti.col0 + int32_t(rank) * C::kBCols + c * 64, kb * kBlockK);
+          } else {
+            const uint32_t fb = smem_u32(&full[stage]);
+            mbar_expect_tx(fb, C::kStageBytes);
+            tma_load_2d(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
+#pragma unroll
+            for (int c = 0; c < C::kBCols / 64; ++c)
+              tma_load_2d(sb + c * (kBlockK * 128), mb, fb, ti.col0 + c * 64, kb * kBlockK);
+          }
           ++issued;
           if (++stage == C::kStages) {
             stage = 0;
@@ -272,17 +367,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      if (!ok) {
+      if (!ok && !PAIR) {
         // wind-down: let copies already issued land before the CTA exits
         for (int st = 0; st < C::kStages; ++st) {
           const int64_t fills = issued / C::kStages + (st < issued % C::kStages ? 1 : 0);
-          if (fills > 0) mbar_wait_plain(smem_u32(&full[st]), uint32_t((fills - 1) & 1), 10000000ull);
+          if (fills > 0)
+            mbar_wait_plain(smem_u32(&full[st]), uint32_t((fills - 1) & 1), 10000000ull);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // (PAIR: the leader's thread issues the pair's MMAs)
+    if (lane == 0 && rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -308,16 +405,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // blocks, SBO = 8 K rows x 128 B.
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc(sb + kk * 2048, kBlockK * 128, 1024);
-            mma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0);
+            if constexpr (PAIR)
+              mma_bf16_pair(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0);
+            else
+              mma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0);
           }
-          mma_commit(smem_u32(&empty[stage]));
+          if constexpr (PAIR)
+            mma_commit_pair(smem_u32(&empty[stage]));
+          else
+            mma_commit(smem_u32(&empty[stage]));
           if (++stage == C::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit(smem_u32(&acc_full[acc]));
+        if constexpr (PAIR)
+          mma_commit_pair(smem_u32(&acc_full[acc]));
+        else
+          mma_commit(smem_u32(&acc_full[acc]));
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
@@ -389,7 +495,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&epi_done[acc]));
-        mbar_arrive(smem_u32(&acc_empty[acc]));
+        if constexpr (PAIR)
+          mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[acc]), 0));
+        else
+          mbar_arrive(smem_u32(&acc_empty[acc]));
       }
       // Once all four warps have stored the tile, count it; the group's last
       // tile raises the group's flag.
@@ -414,35 +523,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // ------------------------------------------------------------ teardown
   __syncthreads();
   if (warp == 1) {
-    // every MMA this CTA issued has completed before the tensor memory is
-    // released (immediate on the normal path: the epilogue saw them all)
+    // every MMA has completed before the tensor memory is released
+    // (immediate on the normal path: the epilogue saw them all)
     if (lane == 0) {
-      mma_commit(smem_u32(drain));
+      if constexpr (PAIR) {
+        if (rank == 0) mma_commit_pair(smem_u32(drain));
+      } else {
+        mma_commit(smem_u32(drain));
+      }
       mbar_wait_plain(smem_u32(drain), 0, 10000000ull);
     }
     __syncwarp();
+  }
+  tc_fence_before();
+  if constexpr (PAIR) cluster_sync();   // neither CTA leaves while the pair still works
+  if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(uint32_t(C::kTmemCols))
-                 : "memory");
+    if constexpr (PAIR)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(uint32_t(C::kTmemCols))
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(uint32_t(C::kTmemCols))
+                   : "memory");
   }
 }
 
 // ---------------------------------------------------------------- host side
 
-template <int BN>
+template <int BN, bool PAIR>
 fo_status launch_bn(const fo_plan* p, GemmArgs& a, cudaStream_t st) {
   static std::once_flag attr_once[64];
   static cudaError_t attr_err[64];
   const int dev = p->device < 64 ? p->device : 63;
   std::call_once(attr_once[dev], [&] {
-    attr_err[dev] = cudaFuncSetAttribute(signaled_gemm_kernel<BN>,
+    attr_err[dev] = cudaFuncSetAttribute(signaled_gemm_kernel<BN, PAIR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<BN>::kSmemBytes);
+                                         Cfg<BN, PAIR>::kSmemBytes);
   });
   if (attr_err[dev] != cudaSuccess) return FO_ERR_CUDA;
   const int grid = p->W < p->tiles ? p->W : p->tiles;
-  signaled_gemm_kernel<BN><<<grid, kGemmThreads, Cfg<BN>::kSmemBytes, st>>>(a);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = Cfg<BN, PAIR>::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, signaled_gemm_kernel<BN, PAIR>, a) != cudaSuccess)
+    return FO_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
@@ -487,7 +622,16 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.h = kTileM / p->R;
   a.epoch = epoch;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return p->tile_n == 256 ? launch_bn<256>(p, a, st) : launch_bn<128>(p, a, st);
+  bool pair = false;
+  if (p->gemm_variant == FO_GEMM_PAIRS) {
+    if (!p->pairable) return FO_ERR_UNSUPPORTED;
+    pair = true;
+  } else if (p->gemm_variant == FO_GEMM_AUTO) {
+    pair = p->pairable;
+  }
+  if (p->tile_n == 256)
+    return pair ? launch_bn<256, true>(p, a, st) : launch_bn<256, false>(p, a, st);
+  return pair ? launch_bn<128, true>(p, a, st) : launch_bn<128, false>(p, a, st);
 }
 
 }  // namespace fo

@@ -145,6 +145,16 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
     }
   }
 
+  // CTA pairs: with W even, CTAs 2p and 2p+1 take slots 2i and 2i+1 of every
+  // wave; they can share one M = 256 MMA when those are vertically adjacent
+  // tiles of the same expert and column.
+  p->pairable = (W % 2 == 0) && (tiles % 2 == 0);
+  for (int32_t s = 0; p->pairable && s < tiles; s += 2) {
+    const TileInfo& t0 = p->tile[s];
+    const TileInfo& t1 = p->tile[s + 1];
+    p->pairable = t0.expert == t1.expert && t0.col0 == t1.col0 && t1.row0 == t0.row0 + kTileM;
+  }
+
   // Groups: consecutive wave ranges; slot ranges follow from W.
   p->group_waves.assign(d->group_waves, d->group_waves + P);
   p->group_slot_begin.assign(P + 1, 0);

@@ -16,6 +16,7 @@ FO_OK, FO_ERR_ARG, FO_ERR_CUDA, FO_ERR_TIMEOUT, FO_ERR_UNSUPPORTED = range(5)
 FO_NOALLOC_MAX_GROUPS = 4096   # include/fo.h
 FO_LAYOUT_TILE, FO_LAYOUT_RS_SUBTILE, FO_LAYOUT_RS_ROWBLOCK, FO_LAYOUT_A2A_SUBTOKEN = range(4)
 FO_CONS_COPY, FO_CONS_SUM, FO_CONS_RS, FO_CONS_A2A = range(4)
+FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
  FO_TAB_FINAL_ROWS) = range(10)
@@ -66,6 +67,7 @@ def lib():
             "fo_plan_set_launch": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32,
                                                   ctypes.c_int32]),
             "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp, _vp]),
+            "fo_plan_set_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _i32p]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
             "fo_plan_destroy": (None, [_vp]),
             "fo_counting_table_init": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -177,6 +179,13 @@ def fo_plan_table(plan, which):
 def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):
     _check("fo_plan_set_launch",
            lib().fo_plan_set_launch(plan, consumer_ctas, reorder_ctas, 1 if overlap else 0))
+
+
+def fo_plan_set_gemm(plan, variant=FO_GEMM_AUTO):
+    """Select the GEMM variant; returns whether the plan allows CTA pairs."""
+    pairable = ctypes.c_int32()
+    _check("fo_plan_set_gemm", lib().fo_plan_set_gemm(plan, variant, ctypes.byref(pairable)))
+    return bool(pairable.value)
 
 
 def fo_plan_set_trace(plan, stamps, consumer_stamps=0):

@@ -51,7 +51,8 @@ class Pipeline:
     """One workload planned and resident on the device."""
 
     def __init__(self, w: Workload, inp: Inputs, device="cuda", partition=None,
-                 wave_width=None, consumer_ctas=0, reorder_ctas=0, upload=True):
+                 wave_width=None, consumer_ctas=0, reorder_ctas=0, upload=True,
+                 gemm_variant=None):
         self.w = w
         self.device = torch.device(device)
         W = w.wave_width if wave_width is None else wave_width
@@ -65,6 +66,8 @@ class Pipeline:
         self.partition = list(partition) if partition else fo.partition_one_then_two(self.waves)
         self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
         self.plan = fo.fo_plan_groups(self.desc)
+        self.gemm_variant = fo.FO_GEMM_AUTO if gemm_variant is None else gemm_variant
+        self.pairable = fo.fo_plan_set_gemm(self.plan, self.gemm_variant)
         self.consumer_ctas, self.reorder_ctas = consumer_ctas, reorder_ctas
         self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
@@ -103,6 +106,7 @@ class Pipeline:
         self.partition = list(partition)
         self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
         self.plan = fo.fo_plan_groups(self.desc)
+        fo.fo_plan_set_gemm(self.plan, self.gemm_variant)
         self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
         self.P = len(self.partition)

@@ -151,6 +151,23 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
 fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
                              int32_t reorder_ctas, int32_t overlap);
 
+/* How fo_signaled_gemm maps tiles onto CTAs.  Either way W CTAs take the
+ * launch slots c, c + W, ... (wave = slot / W) and every tile gets the same
+ * epilogue; only the MMA differs.
+ *  FO_GEMM_SINGLE: one CTA per tile, tcgen05.mma with M = 128.
+ *  FO_GEMM_PAIRS:  CTAs 2p and 2p+1 form a cluster; their tiles at slots
+ *      2i and 2i+1 must be vertically adjacent (same expert and columns,
+ *      rows 128 apart: W even, an even tile count and even band heights),
+ *      and one tcgen05.mma.cta_group::2 (M = 256) computes both, each CTA
+ *      staging its own A rows and half of B.
+ *  FO_GEMM_AUTO (default): pairs when the plan allows them. */
+typedef enum { FO_GEMM_AUTO = 0, FO_GEMM_SINGLE = 1, FO_GEMM_PAIRS = 2 } fo_gemm_variant;
+
+/* Select the variant; *pairable (may be NULL) tells whether the plan's
+ * launch order allows pairs.  FO_ERR_UNSUPPORTED if FO_GEMM_PAIRS is asked
+ * of a plan that does not. */
+fo_status fo_plan_set_gemm(fo_plan* plan, fo_gemm_variant variant, int32_t* pairable);
+
 /* Timelines ([P2] Figure 3 records each tile's completion time with
  * globaltimer to show the wave pattern).  Device uint64 buffers owned by the
  * caller, kept alive while tracing; NULL stops that trace.
