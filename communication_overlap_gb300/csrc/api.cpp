@@ -81,11 +81,16 @@ fo_status fo_plan_set_launch(fo_plan* p, int32_t consumer_ctas, int32_t reorder_
   return FO_OK;
 }
 
-fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairable) {
+fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairable,
+                           int32_t* pair_capacity) {
   if (!p) return FO_ERR_ARG;
-  if (pairable) *pairable = p->pairable ? 1 : 0;
+  const int cap = p->blob ? fo::gemm_pair_capacity(p) : 0;
+  const int grid = p->W < p->tiles ? p->W : p->tiles;
+  const bool ok = p->pairable && cap >= grid;
+  if (pairable) *pairable = ok ? 1 : 0;
+  if (pair_capacity) *pair_capacity = cap;
   if (variant < FO_GEMM_AUTO || variant > FO_GEMM_PAIRS) return FO_ERR_ARG;
-  if (variant == FO_GEMM_PAIRS && !p->pairable) return FO_ERR_UNSUPPORTED;
+  if (variant == FO_GEMM_PAIRS && !ok) return FO_ERR_UNSUPPORTED;
   p->gemm_variant = variant;
   return FO_OK;
 }

@@ -83,6 +83,7 @@ fo_status upload_plan(fo_plan* p);
 int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r);
 
 // gemm.cu
+int gemm_pair_capacity(const fo_plan* p);
 fo_status launch_signaled_gemm(const fo_plan* p, const void* A,
                                const void* const* B, void* C_r,
                                int32_t* count, uint32_t* flags, uint32_t epoch,

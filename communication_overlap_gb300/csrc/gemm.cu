@@ -195,8 +195,11 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t addr, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+// Arrive on the leader's full barrier announcing this CTA's TMA bytes.  No
+// release ordering is needed (the data is tracked by the transaction count),
+// and a release at cluster scope would fence the producer on every stage.
+__device__ __forceinline__ void mbar_expect_tx_cluster_relaxed(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
                    addr),
                "r"(bytes)
                : "memory");
@@ -346,7 +349,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // this CTA's A rows and its half of B land in its own shared
             // memory; the leader's full barrier counts both CTAs' bytes
             const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
-            mbar_expect_tx_cluster(fb, C::kStageBytes);
+            if (rank == 0)
+              mbar_expect_tx(smem_u32(&full[stage]), C::kStageBytes);
+            else
+              mbar_expect_tx_cluster_relaxed(fb, C::kStageBytes);
             tma_load_2d_pair(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
 #pragma unroll
             for (int c = 0; c < C::kBCols / 64; ++c)
@@ -495,7 +501,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&epi_done[acc]));
-        if constexpr (PAIR)
+        if (PAIR && rank != 0)
           mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[acc]), 0));
         else
           mbar_arrive(smem_u32(&acc_empty[acc]));
@@ -581,7 +587,44 @@ fo_status launch_bn(const fo_plan* p, GemmArgs& a, cudaStream_t st) {
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
+template <int BN>
+int pair_capacity_bn(int device) {
+  static std::once_flag once[64];
+  static int cap[64];
+  const int dev = device < 64 ? device : 63;
+  std::call_once(once[dev], [&] {
+    cap[dev] = 0;
+    if (cudaFuncSetAttribute(signaled_gemm_kernel<BN, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<BN, true>::kSmemBytes) != cudaSuccess)
+      return;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = Cfg<BN, true>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, signaled_gemm_kernel<BN, true>, &cfg) ==
+        cudaSuccess)
+      cap[dev] = 2 * clusters;
+  });
+  return cap[dev];
+}
+
 }  // namespace
+
+// CTAs the device can hold at once as CTA pairs of the pair kernel (pairs
+// need both SMs of a TPC; a device with partly disabled TPCs holds fewer
+// pairs than half its SMs).
+int gemm_pair_capacity(const fo_plan* p) {
+  return p->tile_n == 256 ? pair_capacity_bn<256>(p->device) : pair_capacity_bn<128>(p->device);
+}
 
 fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* const* B,
                                void* C_r, int32_t* count, uint32_t* flags, uint32_t epoch,
@@ -622,12 +665,15 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.h = kTileM / p->R;
   a.epoch = epoch;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // pairs only when every pair of the W CTAs can be resident at once:
+  // otherwise the waves would not run side by side
+  const bool fits = p->pairable && gemm_pair_capacity(p) >= (p->W < p->tiles ? p->W : p->tiles);
   bool pair = false;
   if (p->gemm_variant == FO_GEMM_PAIRS) {
-    if (!p->pairable) return FO_ERR_UNSUPPORTED;
+    if (!fits) return FO_ERR_UNSUPPORTED;
     pair = true;
   } else if (p->gemm_variant == FO_GEMM_AUTO) {
-    pair = p->pairable;
+    pair = fits;
   }
   if (p->tile_n == 256)
     return pair ? launch_bn<256, true>(p, a, st) : launch_bn<256, false>(p, a, st);

@@ -67,7 +67,7 @@ def lib():
             "fo_plan_set_launch": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32,
                                                   ctypes.c_int32]),
             "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp, _vp]),
-            "fo_plan_set_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _i32p]),
+            "fo_plan_set_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _i32p]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
             "fo_plan_destroy": (None, [_vp]),
             "fo_counting_table_init": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -182,10 +182,11 @@ def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):
 
 
 def fo_plan_set_gemm(plan, variant=FO_GEMM_AUTO):
-    """Select the GEMM variant; returns whether the plan allows CTA pairs."""
-    pairable = ctypes.c_int32()
-    _check("fo_plan_set_gemm", lib().fo_plan_set_gemm(plan, variant, ctypes.byref(pairable)))
-    return bool(pairable.value)
+    """Select the GEMM variant; returns (pairs possible, pair capacity in CTAs)."""
+    pairable, cap = ctypes.c_int32(), ctypes.c_int32()
+    _check("fo_plan_set_gemm", lib().fo_plan_set_gemm(plan, variant, ctypes.byref(pairable),
+                                                      ctypes.byref(cap)))
+    return bool(pairable.value), cap.value
 
 
 def fo_plan_set_trace(plan, stamps, consumer_stamps=0):

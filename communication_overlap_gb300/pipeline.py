@@ -67,7 +67,7 @@ class Pipeline:
         self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
         self.plan = fo.fo_plan_groups(self.desc)
         self.gemm_variant = fo.FO_GEMM_AUTO if gemm_variant is None else gemm_variant
-        self.pairable = fo.fo_plan_set_gemm(self.plan, self.gemm_variant)
+        self.pairable, self.pair_capacity = fo.fo_plan_set_gemm(self.plan, self.gemm_variant)
         self.consumer_ctas, self.reorder_ctas = consumer_ctas, reorder_ctas
         self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)

@@ -160,13 +160,18 @@ fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
  *      rows 128 apart: W even, an even tile count and even band heights),
  *      and one tcgen05.mma.cta_group::2 (M = 256) computes both, each CTA
  *      staging its own A rows and half of B.
- *  FO_GEMM_AUTO (default): pairs when the plan allows them. */
+ *      The device must also hold all W CTAs as pairs at once (a pair needs
+ *      both SMs of a TPC; with partly disabled TPCs that can be fewer than
+ *      the SM count), or the waves would not run side by side.
+ *  FO_GEMM_AUTO (default): pairs when the plan and the device allow them. */
 typedef enum { FO_GEMM_AUTO = 0, FO_GEMM_SINGLE = 1, FO_GEMM_PAIRS = 2 } fo_gemm_variant;
 
-/* Select the variant; *pairable (may be NULL) tells whether the plan's
- * launch order allows pairs.  FO_ERR_UNSUPPORTED if FO_GEMM_PAIRS is asked
- * of a plan that does not. */
-fo_status fo_plan_set_gemm(fo_plan* plan, fo_gemm_variant variant, int32_t* pairable);
+/* Select the variant.  *pairable (may be NULL): whether pairs are possible
+ * for this plan on this device; *pair_capacity (may be NULL): how many CTAs
+ * the device holds at once as pairs of the pair kernel.  FO_ERR_UNSUPPORTED
+ * if FO_GEMM_PAIRS is asked when pairs are not possible. */
+fo_status fo_plan_set_gemm(fo_plan* plan, fo_gemm_variant variant, int32_t* pairable,
+                           int32_t* pair_capacity);
 
 /* Timelines ([P2] Figure 3 records each tile's completion time with
  * globaltimer to show the wave pattern).  Device uint64 buffers owned by the
