@@ -171,15 +171,38 @@ fo_status fo_consume_group(const fo_plan* p, int32_t group, fo_consumer kind,
                             flags, epoch, spin_limit_ns, dev_status, stream);
 }
 
-fo_status fo_reorder_back(const fo_plan* p, int32_t group_begin, int32_t group_end,
-                          const void* const* src, void* const* dst, void* stream) {
+fo_status fo_reorder_back_fused(const fo_plan* p, int32_t group_begin, int32_t group_end,
+                                const void* const* src, void* const* dst, const void* bias,
+                                fo_activation act, void* stream) {
   if (!p || !p->blob || !src || !dst) return FO_ERR_ARG;
   if (group_begin < 0 || group_end > p->P || group_begin > group_end) return FO_ERR_ARG;
+  if (act < FO_ACT_NONE || act > FO_ACT_SILU) return FO_ERR_ARG;
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & 15)) return FO_ERR_ARG;
   const int n = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
   for (int k = 0; k < n; ++k)
     if (!src[k] || !dst[k]) return FO_ERR_ARG;
   if (group_begin == group_end) return FO_OK;
-  return fo::launch_reorder_back(p, group_begin, group_end, src, dst, stream);
+  return fo::launch_reorder_back(p, group_begin, group_end, src, dst, bias, int(act), stream);
+}
+
+fo_status fo_reorder_back(const fo_plan* p, int32_t group_begin, int32_t group_end,
+                          const void* const* src, void* const* dst, void* stream) {
+  return fo_reorder_back_fused(p, group_begin, group_end, src, dst, nullptr, FO_ACT_NONE,
+                               stream);
+}
+
+fo_status fo_allgather_rows(const fo_plan* p, const void* const* slices, void* out,
+                            const void* bias, fo_activation act, void* stream) {
+  if (!p || !p->blob || !slices || !out) return FO_ERR_ARG;
+  if (p->layout != FO_LAYOUT_RS_SUBTILE && p->layout != FO_LAYOUT_RS_ROWBLOCK) return FO_ERR_ARG;
+  if (act < FO_ACT_NONE || act > FO_ACT_SILU) return FO_ERR_ARG;
+  uintptr_t bits = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(bias);
+  for (int k = 0; k < p->R; ++k) {
+    if (!slices[k]) return FO_ERR_ARG;
+    bits |= reinterpret_cast<uintptr_t>(slices[k]);
+  }
+  if (bits & 15) return FO_ERR_ARG;
+  return fo::launch_allgather_rows(p, slices, out, bias, int(act), stream);
 }
 
 const char* fo_status_string(fo_status s) {

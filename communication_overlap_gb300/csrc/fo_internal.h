@@ -98,6 +98,8 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
                          void* stream);
 fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
                               const void* const* src, void* const* dst,
-                              void* stream);
+                              const void* bias, int act, void* stream);
+fo_status launch_allgather_rows(const fo_plan* p, const void* const* slices, void* out,
+                                const void* bias, int act, void* stream);
 
 }  // namespace fo

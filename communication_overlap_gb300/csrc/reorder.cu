@@ -47,8 +47,35 @@ struct ReorderArgs {
   const int32_t* row_rank;
   const int32_t* final_row;
   int32_t* status;
+  const uint16_t* bias;   // optional bf16[N] added before the activation
+  int32_t act;            // fo_activation
   int32_t layout, R, unit_bytes, row_bytes, slot0, n_slots, h, rows_per;
 };
+
+// The fused element-wise epilogue: act(x + bias) in fp32, rounded once to
+// bf16 (nearest even).  ReLU keeps v only when v > 0; SiLU is v / (1 + e^-v).
+__device__ __forceinline__ float epilogue_op(float v, float b, int act) {
+  v = __fadd_rn(v, b);
+  if (act == FO_ACT_RELU) v = v > 0.0f ? v : 0.0f;
+  else if (act == FO_ACT_SILU) v = v / (1.0f + expf(-v));
+  return v;
+}
+
+// Eight bf16 values of columns col .. col+7 through the epilogue.
+__device__ __forceinline__ uint4 epilogue8(uint4 x, const uint16_t* bias, int32_t col, int act) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float b0 = 0.0f, b1 = 0.0f;
+    if (bias != nullptr) {
+      b0 = __uint_as_float(uint32_t(bias[col + 2 * i]) << 16);
+      b1 = __uint_as_float(uint32_t(bias[col + 2 * i + 1]) << 16);
+    }
+    o[i] = pack_bf16x2(epilogue_op(bf16lo(w[i]), b0, act), epilogue_op(bf16hi(w[i]), b1, act));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 // Inverse mapping of row r of the tile at slot s: the unit's place in the
 // consumer's buffer k and the row it belongs to in output k.
@@ -142,6 +169,19 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
     }
     __syncthreads();
     if (!s_ok) break;
+    if (a.act != FO_ACT_NONE || a.bias != nullptr) {
+      // element-wise epilogue in place ([P1] 五: fused with the reorder):
+      // row r of the tile is at r * ub in every layout
+      const int vpr = ub / 16;
+      for (int v = tid; v < ti.rows * vpr; v += kRThreads) {
+        const int r = v / vpr, cv = v - r * vpr;
+        uint4* pv = reinterpret_cast<uint4*>(buf + r * ub + cv * 16);
+        *pv = epilogue8(*pv, a.bias, ti.col0 + cv * 8, a.act);
+      }
+      // generic writes to shared memory, read next by the TMA engine
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+    }
     if (whole && ti.rows == kTileM) {
       if (tid == 0) {
         int k;
@@ -174,7 +214,8 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
 }  // namespace
 
 fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
-                              const void* const* src, void* const* dst, void* stream) {
+                              const void* const* src, void* const* dst, const void* bias,
+                              int act, void* stream) {
   static std::once_flag once[64];
   static cudaError_t attr_err[64];
   const int dv = p->device < 64 ? p->device : 63;
@@ -207,6 +248,8 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   a.row_rank = p->dev.row_rank;
   a.final_row = p->dev.final_row;
   a.status = p->dev.gemm_status;
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.act = act;
   a.layout = p->layout;
   a.R = p->R;
   a.unit_bytes = p->tile_n * 2;
@@ -218,6 +261,81 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   int ctas = p->reorder_ctas > 0 ? p->reorder_ctas : 3 * p->sm_count;
   if (ctas > a.n_slots) ctas = a.n_slots;
   reorder_kernel<<<ctas, kRThreads, kRSmem, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
+}
+
+namespace {
+
+struct GatherArgs {
+  const uint4* src[kMaxDest];
+  uint4* out;
+  const uint16_t* bias;
+  int32_t act, layout, h, rows_per, row_vec;
+  int64_t total;  // 16-byte vectors of the M x N output
+};
+
+// The AllGather stand-in and the local row exchange in one pass ([P1] 二 (2):
+// after ReduceScatter + AllGather the rows are fixed by a block-cyclic
+// permutation that needs no mapping table and fuses with element-wise
+// operations).  Output row g takes row rho of slice k:
+//   subtile layout: g = tile_m * tm + h * k + i  <-  rho = h * tm + i
+//   row-block layout: g = k * M/R + rho
+// Both sides are read and written as contiguous rows (16-byte vectors,
+// four in flight per thread).
+__global__ void __launch_bounds__(256) allgather_kernel(const __grid_constant__ GatherArgs a) {
+  constexpr int U = 4;
+  __shared__ const uint4* s_src[kMaxDest];
+  if (threadIdx.x < kMaxDest) s_src[threadIdx.x] = a.src[threadIdx.x];
+  __syncthreads();
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t base = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; base < a.total;
+       base += stride * U) {
+    uint4 x[U];
+    int32_t col[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = base + stride * u;
+      if (v >= a.total) break;
+      const int32_t g = int32_t(v / a.row_vec), cv = int32_t(v - int64_t(g) * a.row_vec);
+      int32_t k, rho;
+      if (a.layout == FO_LAYOUT_RS_SUBTILE) {
+        const int32_t tm = g / kTileM, w = g - tm * kTileM;
+        k = w / a.h;
+        rho = tm * a.h + (w - k * a.h);
+      } else {
+        k = g / a.rows_per;
+        rho = g - k * a.rows_per;
+      }
+      x[u] = ld_cg(s_src[k] + int64_t(rho) * a.row_vec + cv);
+      col[u] = cv * 8;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t v = base + stride * u;
+      if (v >= a.total) break;
+      uint4 y = x[u];
+      if (a.act != FO_ACT_NONE || a.bias != nullptr) y = epilogue8(y, a.bias, col[u], a.act);
+      st_cs(a.out + v, y);
+    }
+  }
+}
+
+}  // namespace
+
+fo_status launch_allgather_rows(const fo_plan* p, const void* const* slices, void* out,
+                                const void* bias, int act, void* stream) {
+  GatherArgs a{};
+  for (int k = 0; k < p->R; ++k) a.src[k] = static_cast<const uint4*>(slices[k]);
+  a.out = static_cast<uint4*>(out);
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.act = act;
+  a.layout = p->layout;
+  a.h = kTileM / p->R;
+  a.rows_per = p->M / p->R;
+  a.row_vec = p->N / 8;
+  a.total = int64_t(p->M) * a.row_vec;
+  const int ctas = 4 * p->sm_count;
+  allgather_kernel<<<ctas, 256, 0, static_cast<cudaStream_t>(stream)>>>(a);
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 

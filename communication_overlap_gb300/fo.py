@@ -17,6 +17,7 @@ FO_NOALLOC_MAX_GROUPS = 4096   # include/fo.h
 FO_LAYOUT_TILE, FO_LAYOUT_RS_SUBTILE, FO_LAYOUT_RS_ROWBLOCK, FO_LAYOUT_A2A_SUBTOKEN = range(4)
 FO_CONS_COPY, FO_CONS_SUM, FO_CONS_RS, FO_CONS_A2A = range(4)
 FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
+FO_ACT_NONE, FO_ACT_RELU, FO_ACT_SILU = range(3)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
  FO_TAB_FINAL_ROWS) = range(10)
@@ -88,6 +89,9 @@ def lib():
             "fo_tune_partition": (ctypes.c_int, [ctypes.POINTER(fo_plan_desc), ctypes.c_double,
                                                  _dp, _dp, ctypes.c_int32, _i32p,
                                                  ctypes.c_int32, _i32p, _dp]),
+            "fo_reorder_back_fused": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, _vpp,
+                                                     _vpp, _vp, ctypes.c_int, _vp]),
+            "fo_allgather_rows": (ctypes.c_int, [_vp, _vpp, _vp, _vp, ctypes.c_int, _vp]),
             "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -244,6 +248,19 @@ def fo_reorder_back(plan, group_begin, group_end, src, dst, stream):
     _check("fo_reorder_back",
            lib().fo_reorder_back(plan, group_begin, group_end, _ptrs(src), _ptrs(dst),
                                  stream or None))
+
+
+def fo_reorder_back_fused(plan, group_begin, group_end, src, dst, bias, act, stream):
+    """bias: device address of bf16[N] or 0."""
+    _check("fo_reorder_back_fused",
+           lib().fo_reorder_back_fused(plan, group_begin, group_end, _ptrs(src), _ptrs(dst),
+                                       int(bias) or None, act, stream or None))
+
+
+def fo_allgather_rows(plan, slices, out, bias, act, stream):
+    _check("fo_allgather_rows",
+           lib().fo_allgather_rows(plan, _ptrs(slices), int(out), int(bias) or None, act,
+                                   stream or None))
 
 
 def _curve(curve):

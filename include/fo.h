@@ -322,6 +322,34 @@ fo_status fo_tune_partition(const fo_plan_desc* desc, double gemm_us,
                             int32_t n_points, int32_t* group_waves, int32_t capacity,
                             int32_t* n_groups, double* predicted_us);
 
+/* Element-wise epilogue fused into the post-communication pass ([P1] 五
+ * "Epilogue 集成": ReLU, SiLU and bias addition usually run in the GEMM's
+ * epilogue; FlashOverlap fuses the post-communication reorder with them).
+ * y = act(x + bias[col]): x and bias are bf16, the addition and the
+ * activation fp32, one rounding to bf16 (nearest even); RELU keeps v when
+ * v > 0 (else 0), SILU is v / (1 + exp(-v)).  bias: device bf16[N] or NULL
+ * (16-byte aligned), indexed by the output column. */
+typedef enum { FO_ACT_NONE = 0, FO_ACT_RELU = 1, FO_ACT_SILU = 2 } fo_activation;
+
+/* fo_reorder_back with the element-wise epilogue applied to every moved
+ * value (fo_reorder_back is this call with bias = NULL, act = NONE). */
+fo_status fo_reorder_back_fused(const fo_plan* plan, int32_t group_begin, int32_t group_end,
+                                const void* const* src, void* const* dst, const void* bias,
+                                fo_activation act, void* cuda_stream);
+
+/* The AllGather after a ReduceScatter, with the row exchange and the
+ * element-wise epilogue in one pass ([P1] 二 (2): the gathered rows are put
+ * in order by a block-cyclic permutation that needs no mapping table and
+ * fuses with element-wise operations).  RS layouts only.
+ *  slices: host array of R device pointers, slice k as fo_reorder_back
+ *      leaves it ((M / R) x N, row-major).
+ *  out: device M x N row-major.  RS_SUBTILE: out row tile_m * tm + h * k + i
+ *      = slice k row h * tm + i (h = tile_m / R); RS_ROWBLOCK: out row
+ *      k * M/R + rho = slice k row rho.  On one GPU every slice is local, so
+ *      the gather is this copy. */
+fo_status fo_allgather_rows(const fo_plan* plan, const void* const* slices, void* out,
+                            const void* bias, fo_activation act, void* cuda_stream);
+
 const char* fo_status_string(fo_status status);
 
 #ifdef __cplusplus
