@@ -171,6 +171,46 @@ fo_status fo_consume_group(const fo_plan* p, int32_t group, fo_consumer kind,
                             flags, epoch, spin_limit_ns, dev_status, stream);
 }
 
+fo_status fo_consume_reorder(const fo_plan* p, int32_t group, fo_consumer kind,
+                             const void* src, const void* const* partials, int32_t n_partials,
+                             void* const* comm_dst, void* const* final_dst, const void* bias,
+                             fo_activation act, const uint32_t* flags, uint32_t epoch,
+                             uint64_t spin_limit_ns, int32_t* dev_status, void* stream) {
+  if (!p || !p->blob || !src || !comm_dst || !final_dst || !flags || !dev_status)
+    return FO_ERR_ARG;
+  if (group < -1 || group >= p->P) return FO_ERR_ARG;
+  if (act < FO_ACT_NONE || act > FO_ACT_SILU) return FO_ERR_ARG;
+  if (bias && (reinterpret_cast<uintptr_t>(bias) & 15)) return FO_ERR_ARG;
+  switch (kind) {
+    case FO_CONS_COPY:
+      if (n_partials != 0 || p->layout != FO_LAYOUT_TILE) return FO_ERR_ARG;
+      break;
+    case FO_CONS_SUM:
+      if (n_partials < 0 || n_partials > fo::kMaxPartials || p->layout != FO_LAYOUT_TILE)
+        return FO_ERR_ARG;
+      break;
+    case FO_CONS_RS:
+      if (n_partials < 0 || n_partials > fo::kMaxPartials) return FO_ERR_ARG;
+      if (p->layout != FO_LAYOUT_RS_SUBTILE && p->layout != FO_LAYOUT_RS_ROWBLOCK)
+        return FO_ERR_ARG;
+      break;
+    case FO_CONS_A2A:
+      if (n_partials != 0 || p->layout != FO_LAYOUT_A2A_SUBTOKEN) return FO_ERR_ARG;
+      break;
+    default: return FO_ERR_ARG;
+  }
+  if (n_partials > 0 && !partials) return FO_ERR_ARG;
+  for (int i = 0; i < n_partials; ++i)
+    if (!partials[i]) return FO_ERR_ARG;
+  const int n = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
+  for (int k = 0; k < n; ++k)
+    if (!comm_dst[k] || !final_dst[k]) return FO_ERR_ARG;
+  const int32_t g0 = group < 0 ? 0 : group, g1 = group < 0 ? p->P : group + 1;
+  return fo::launch_consume_reorder(p, g0, g1, int(kind), src, partials, n_partials, comm_dst,
+                                    final_dst, bias, int(act), flags, epoch, spin_limit_ns,
+                                    dev_status, stream);
+}
+
 fo_status fo_reorder_back_fused(const fo_plan* p, int32_t group_begin, int32_t group_end,
                                 const void* const* src, void* const* dst, const void* bias,
                                 fo_activation act, void* stream) {

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "device_common.cuh"
+#include "row_map.cuh"
 
 namespace fo {
 
@@ -204,6 +205,210 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
   }
 }
 
+// ---------------------------------------------------------------------------
+// Consumer with the post-communication reorder (and the element-wise
+// epilogue) fused in: one persistent kernel in which a CTA, once it has
+// taken its share of group j's communication, reorders group j-1 back to
+// the final layout -- while the GEMM is still computing later groups.  Only
+// the last group's reorder is left when the GEMM ends.
+
+struct FusedArgs {
+  ConsumeArgs c;                  // the communication part (c.dst: its outputs)
+  uint4* fin[kMaxDest];           // final outputs of the reorder
+  RowMap map;
+  const uint16_t* bias;
+  const int32_t* group_slot_begin;
+  int32_t* rwork;  // [P] reorder chunk counters, [P] units consumed, [1] CTAs done
+  int32_t act, row_vec;
+};
+
+// Wait until *p >= target (acquire loads, __nanosleep back-off, bounded).
+__device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, uint64_t limit_ns) {
+  if (int32_t(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p))) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t backoff = 32;
+  while (true) {
+    __nanosleep(backoff);
+    if (int32_t(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p))) >= target) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+    if (backoff < 1024) backoff <<= 1;
+  }
+}
+
+// One tile's rows from the communication buffers to the final layout: warp
+// w takes every 8th row group; each lane keeps 8 independent 16-byte loads
+// in flight before its stores.
+template <int VPU>
+__device__ __forceinline__ void reorder_tile_regs(const FusedArgs& a, uint4* const* src,
+                                                  uint4* const* fin, int32_t s, int tid) {
+  constexpr int kRowsPerInstr = 32 / VPU;
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kRounds = kTileM / kWarps / kRowsPerInstr / 8;
+  const int warp = tid / 32, lane = tid % 32, sub = lane / VPU, vl = lane % VPU;
+  const TileInfo ti = a.map.tile[s];
+#pragma unroll 1
+  for (int round = 0; round < kRounds; ++round) {
+    uint4 x[8];
+    int64_t to[8];
+    int kk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int32_t r = ((round * 8 + i) * kWarps + warp) * kRowsPerInstr + sub;
+      kk[i] = -1;
+      if (r < ti.rows) {
+        int32_t su, dr;
+        map_row(a.map, ti, s, r, &kk[i], &su, &dr);
+        x[i] = ld_cg(src[kk[i]] + int64_t(su) * VPU + vl);
+        to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (kk[i] < 0) continue;
+      uint4 y = x[i];
+      if (a.act != FO_ACT_NONE || a.bias != nullptr)
+        y = epilogue8(y, a.bias, ti.col0 + vl * 8, a.act);
+      st_cs(fin[kk[i]] + to[i], y);
+    }
+  }
+}
+
+template <int KIND, int U, int VPU>
+__global__ void __launch_bounds__(kThreads)
+    consume_reorder_kernel(const __grid_constant__ FusedArgs a) {
+  const ConsumeArgs& c = a.c;
+  __shared__ int s_ok;
+  __shared__ int32_t s_chunk[2];
+  __shared__ int32_t s_ps[kMaxDest], s_pl[kMaxDest], s_pd[kMaxDest];
+  __shared__ uint4* s_dst[kMaxDest];
+  __shared__ uint4* s_fin[kMaxDest];
+  const int tid = threadIdx.x;
+  if (tid < kMaxDest) {
+    s_dst[tid] = c.dst[tid];
+    s_fin[tid] = a.fin[tid];
+  }
+  int32_t* done = a.rwork + c.P;
+  bool ok = true;
+
+  // reorder every tile of group j once its communication is complete
+  auto reorder_group = [&](int j) {
+    if (tid == 0) {
+      const int32_t units = c.group_unit_begin[j + 1] - c.group_unit_begin[j];
+      s_ok = wait_count(done + j, units, c.limit_ns) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_ok) {
+      if (tid == 0) atomicCAS(c.status, 0, int32_t(FO_ERR_TIMEOUT));
+      ok = false;
+      return;
+    }
+    const int32_t s0 = a.group_slot_begin[j], n = a.group_slot_begin[j + 1] - s0;
+    if (tid == 0) s_chunk[0] = atomicAdd(a.rwork + j, 1);
+    __syncthreads();
+    for (int buf = 0;; buf ^= 1) {
+      const int32_t t = s_chunk[buf];
+      if (t >= n) break;
+      if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(a.rwork + j, 1);
+      reorder_tile_regs<VPU>(a, s_dst, s_fin, s0 + t, tid);
+      __syncthreads();
+    }
+    __syncthreads();
+  };
+
+  for (int j = c.g0; j < c.g1 && ok; ++j) {
+    if (j > c.g0) {
+      reorder_group(j - 1);
+      if (!ok) break;
+    }
+    if (tid == 0) s_ok = wait_flag(c.flags + j, c.epoch, c.limit_ns) ? 1 : 0;
+    if (tid < c.R) {
+      s_ps[tid] = c.part_start[j * c.R + tid];
+      s_pl[tid] = c.part_len[j * c.R + tid];
+      s_pd[tid] = c.part_dst[j * c.R + tid];
+    }
+    __syncthreads();
+    if (!s_ok) {
+      if (tid == 0) atomicCAS(c.status, 0, int32_t(FO_ERR_TIMEOUT));
+      ok = false;
+      break;
+    }
+    const int32_t ub = c.group_unit_begin[j], ue = c.group_unit_begin[j + 1];
+    const int32_t n_chunks = (ue - ub + c.chunk_units - 1) / c.chunk_units;
+    if (tid == 0) s_chunk[0] = atomicAdd(c.work + j, 1);
+    __syncthreads();
+    for (int buf = 0;; buf ^= 1) {
+      const int32_t ch = s_chunk[buf];
+      if (ch >= n_chunks) break;
+      if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(c.work + j, 1);
+      const int32_t u0 = ub + ch * c.chunk_units;
+      const int32_t u1 = min(u0 + c.chunk_units, ue);
+      consume_range<KIND, U>(c, s_ps, s_pl, s_pd, s_dst, u0 << c.vpu_shift, u1 << c.vpu_shift,
+                             tid);
+      __syncthreads();
+      if (tid == 0) {
+        // this chunk's outputs are visible before it is counted as consumed
+        __threadfence();
+        atomicAdd(done + j, u1 - u0);
+      }
+    }
+    __syncthreads();
+  }
+  if (ok && c.g1 > c.g0) reorder_group(c.g1 - 1);
+
+  // every CTA reports; the last one resets this launch's counters
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    int32_t* exit_count = a.rwork + 2 * c.P;
+    if (atomicAdd(exit_count, 1) == int32_t(gridDim.x) - 1) {
+      for (int j = c.g0; j < c.g1; ++j) {
+        atomicExch(c.work + j, 0);
+        atomicExch(a.rwork + j, 0);
+        atomicExch(done + j, 0);
+      }
+      atomicExch(exit_count, 0);
+    }
+  }
+}
+
+template <int KIND, int U, int VPU>
+fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int device,
+                            cudaStream_t st) {
+  static std::once_flag once[64];
+  static cudaError_t err[64];
+  const int d = device < 64 ? device : 63;
+  std::call_once(once[d], [&] {
+    err[d] = cudaFuncSetAttribute(consume_reorder_kernel<KIND, U, VPU>,
+                                  cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  int(cudaSharedmemCarveoutMaxShared));
+  });
+  if (err[d] != cudaSuccess) return FO_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, consume_reorder_kernel<KIND, U, VPU>, a) != cudaSuccess)
+    return FO_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
+}
+
+template <int VPU>
+fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int dv,
+                           cudaStream_t st) {
+  switch (kind) {
+    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_SUM: return launch_fused_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_RS: return launch_fused_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_A2A: return launch_fused_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>, VPU>(a, ctas, ov, dv, st);
+  }
+  return FO_ERR_ARG;
+}
+
 int chunk_units_of(int kind, int tile_n) {
   const int bytes = (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? kChunkBytes<FO_CONS_SUM>
                                                                  : kChunkBytes<FO_CONS_COPY>;
@@ -290,6 +495,49 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
     case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
+}
+
+fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int kind,
+                                 const void* src, const void* const* partials,
+                                 int32_t n_partials, void* const* comm_dst,
+                                 void* const* final_dst, const void* bias, int act,
+                                 const uint32_t* flags, uint32_t epoch, uint64_t spin_limit_ns,
+                                 int32_t* dev_status, void* stream) {
+  FusedArgs a{};
+  ConsumeArgs& c = a.c;
+  c.src = static_cast<const uint4*>(src);
+  for (int i = 0; i < n_partials; ++i) c.partials[i] = static_cast<const uint4*>(partials[i]);
+  const int n_comm = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
+  for (int k = 0; k < n_comm; ++k) c.dst[k] = static_cast<uint4*>(comm_dst[k]);
+  const int n_fin = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
+  for (int k = 0; k < n_fin; ++k) a.fin[k] = static_cast<uint4*>(final_dst[k]);
+  c.flags = flags;
+  c.status = dev_status;
+  c.group_unit_begin = p->dev.group_unit_begin;
+  c.part_start = p->dev.part_start;
+  c.part_len = p->dev.part_len;
+  c.part_dst = p->dev.part_dst;
+  c.work = p->dev.work;
+  c.g0 = g0;
+  c.g1 = g1;
+  c.P = p->P;
+  c.n_partials = n_partials;
+  c.R = n_comm;
+  c.vpu_shift = log2_exact(p->tile_n / 8);
+  c.chunk_units = chunk_units_of(kind, p->tile_n);
+  c.epoch = epoch;
+  c.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
+  a.map = make_row_map(p);
+  a.bias = static_cast<const uint16_t*>(bias);
+  a.group_slot_begin = p->dev.group_slot_begin;
+  a.rwork = p->dev.rwork;
+  a.act = act;
+  a.row_vec = p->N / 8;
+  const int ctas = default_ctas(p, p->consumer_ctas);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool ov = p->overlap != 0;
+  return p->tile_n == 256 ? launch_fused_vpu<32>(kind, a, ctas, ov, p->device, st)
+                          : launch_fused_vpu<16>(kind, a, ctas, ov, p->device, st);
 }
 
 }  // namespace fo

@@ -45,6 +45,7 @@ struct DeviceTables {
                                        //   tile row that go to the same rank
   int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
+  int32_t* rwork = nullptr;            // [2P + 1] scratch of the fused consumer+reorder
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
 };
 
@@ -96,6 +97,12 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
                          const uint32_t* flags, uint32_t epoch,
                          uint64_t spin_limit_ns, int32_t* dev_status,
                          void* stream);
+fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int kind,
+                                 const void* src, const void* const* partials,
+                                 int32_t n_partials, void* const* comm_dst,
+                                 void* const* final_dst, const void* bias, int act,
+                                 const uint32_t* flags, uint32_t epoch, uint64_t spin_limit_ns,
+                                 int32_t* dev_status, void* stream);
 fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
                               const void* const* src, void* const* dst,
                               const void* bias, int act, void* stream);

@@ -361,6 +361,7 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_rr = put(buf, p->row_rank);
   const size_t o_fr = put(buf, p->final_row);
   const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
+  const size_t o_rwork = put(buf, std::vector<int32_t>(2 * p->P + 1, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
   void* blob = nullptr;
   if (cudaMalloc(&blob, buf.size()) != cudaSuccess) return FO_ERR_CUDA;
@@ -382,6 +383,7 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.row_rank = reinterpret_cast<int32_t*>(b + o_rr);
   p->dev.final_row = reinterpret_cast<int32_t*>(b + o_fr);
   p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
+  p->dev.rwork = reinterpret_cast<int32_t*>(b + o_rwork);
   p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
   return FO_OK;
 }

@@ -24,6 +24,7 @@
 #include <mutex>
 
 #include "device_common.cuh"
+#include "row_map.cuh"
 #include "tensor_map.h"
 
 namespace fo {
@@ -39,74 +40,17 @@ struct ReorderArgs {
   CUtensorMap dst_map[kMaxDest];  // outputs, boxes of box_rows x tile_n
   const uint8_t* src[kMaxDest];
   uint8_t* dst[kMaxDest];
-  const TileInfo* tile;
-  const int32_t* part_start;
-  const int32_t* part_dst;
-  const int32_t* dest_base;
-  const int32_t* row_dest;
-  const int32_t* row_rank;
-  const int32_t* final_row;
+  RowMap map;
   int32_t* status;
   const uint16_t* bias;   // optional bf16[N] added before the activation
   int32_t act;            // fo_activation
-  int32_t layout, R, unit_bytes, row_bytes, slot0, n_slots, h, rows_per;
+  int32_t unit_bytes, row_bytes, slot0, n_slots;
 };
 
-// The fused element-wise epilogue: act(x + bias) in fp32, rounded once to
-// bf16 (nearest even).  ReLU keeps v only when v > 0; SiLU is v / (1 + e^-v).
-__device__ __forceinline__ float epilogue_op(float v, float b, int act) {
-  v = __fadd_rn(v, b);
-  if (act == FO_ACT_RELU) v = v > 0.0f ? v : 0.0f;
-  else if (act == FO_ACT_SILU) v = v / (1.0f + expf(-v));
-  return v;
-}
-
-// Eight bf16 values of columns col .. col+7 through the epilogue.
-__device__ __forceinline__ uint4 epilogue8(uint4 x, const uint16_t* bias, int32_t col, int act) {
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float b0 = 0.0f, b1 = 0.0f;
-    if (bias != nullptr) {
-      b0 = __uint_as_float(uint32_t(bias[col + 2 * i]) << 16);
-      b1 = __uint_as_float(uint32_t(bias[col + 2 * i + 1]) << 16);
-    }
-    o[i] = pack_bf16x2(epilogue_op(bf16lo(w[i]), b0, act), epilogue_op(bf16hi(w[i]), b1, act));
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// Inverse mapping of row r of the tile at slot s: the unit's place in the
-// consumer's buffer k and the row it belongs to in output k.
 __device__ __forceinline__ void reorder_row(const ReorderArgs& a, const TileInfo& ti, int32_t s,
-                                            int32_t r, int* k_out, int32_t* src_unit,
+                                            int32_t r, int* k, int32_t* src_unit,
                                             int32_t* dst_row) {
-  int k = 0;
-  if (a.layout == FO_LAYOUT_TILE) {
-    *src_unit = ti.unit_base + r;
-    *dst_row = ti.row0 + r;
-  } else {
-    int32_t u;
-    if (a.layout == FO_LAYOUT_RS_SUBTILE) {
-      k = r / a.h;
-      const int32_t i = r - k * a.h;
-      u = ti.unit_base + k * ti.sub_stride + i;
-      *dst_row = (ti.row0 / kTileM) * a.h + i;
-    } else if (a.layout == FO_LAYOUT_RS_ROWBLOCK) {
-      k = ti.dest;
-      u = ti.unit_base + r;
-      *dst_row = ti.row0 + r - k * a.rows_per;
-    } else {  // FO_LAYOUT_A2A_SUBTOKEN
-      const int32_t rho = ti.row0 + r;
-      k = a.row_dest[rho];
-      u = a.dest_base[s * a.R + k] + a.row_rank[rho];
-      *dst_row = a.final_row[rho];
-    }
-    const int32_t jk = ti.group * a.R + k;
-    *src_unit = a.part_dst[jk] + (u - a.part_start[jk]);
-  }
-  *k_out = k;
+  map_row(a.map, ti, s, r, k, src_unit, dst_row);
 }
 
 __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constant__ ReorderArgs a) {
@@ -126,13 +70,13 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   uint32_t phase = 0;
   for (int32_t t = blockIdx.x; t < a.n_slots; t += gridDim.x, phase ^= 1) {
     const int32_t s = a.slot0 + t;
-    const TileInfo ti = a.tile[s];
+    const TileInfo ti = a.map.tile[s];
     // the previous tile's stores have finished reading the buffer
     bulk_wait_read_all();
     __syncthreads();
     if (tid == 0) mbar_expect_tx(sfull, uint32_t(ti.rows * ub));
     __syncthreads();
-    const bool whole = (a.layout == FO_LAYOUT_TILE || a.layout == FO_LAYOUT_RS_ROWBLOCK);
+    const bool whole = (a.map.layout == FO_LAYOUT_TILE || a.map.layout == FO_LAYOUT_RS_ROWBLOCK);
     if (whole) {
       if (tid == 0) {
         int k;
@@ -140,12 +84,13 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
         reorder_row(a, ti, s, 0, &k, &su, &dr);   // rows are contiguous from row 0
         bulk_load(sbuf, a.src[k] + int64_t(su) * ub, uint32_t(ti.rows * ub), sfull);
       }
-    } else if (a.layout == FO_LAYOUT_RS_SUBTILE) {
-      if (tid < a.R) {   // subtile tid: rows tid*h .. +h, contiguous in slice tid
+    } else if (a.map.layout == FO_LAYOUT_RS_SUBTILE) {
+      if (tid < a.map.R) {   // subtile tid: rows tid*h .. +h, contiguous in slice tid
         int k;
         int32_t su, dr;
-        reorder_row(a, ti, s, tid * a.h, &k, &su, &dr);
-        bulk_load(sbuf + tid * a.h * ub, a.src[k] + int64_t(su) * ub, uint32_t(a.h * ub), sfull);
+        reorder_row(a, ti, s, tid * a.map.h, &k, &su, &dr);
+        bulk_load(sbuf + tid * a.map.h * ub, a.src[k] + int64_t(su) * ub, uint32_t(a.map.h * ub),
+                  sfull);
       }
     } else if (tid < ti.rows) {  // All-to-All: row by row
       int k;
@@ -190,12 +135,12 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
         tensor_store_2d(&a.dst_map[k], sbuf, ti.col0, dr);
         bulk_commit();
       }
-    } else if (a.layout == FO_LAYOUT_RS_SUBTILE) {
-      if (tid < a.R) {
+    } else if (a.map.layout == FO_LAYOUT_RS_SUBTILE) {
+      if (tid < a.map.R) {
         int k;
         int32_t su, dr;
-        reorder_row(a, ti, s, tid * a.h, &k, &su, &dr);
-        tensor_store_2d(&a.dst_map[k], sbuf + tid * a.h * ub, ti.col0, dr);
+        reorder_row(a, ti, s, tid * a.map.h, &k, &su, &dr);
+        tensor_store_2d(&a.dst_map[k], sbuf + tid * a.map.h * ub, ti.col0, dr);
         bulk_commit();
       }
     } else if (tid < ti.rows) {  // ragged tiles and All-to-All rows: per row
@@ -240,24 +185,14 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
         return FO_ERR_CUDA;
     }
   }
-  a.tile = p->dev.tile;
-  a.part_start = p->dev.part_start;
-  a.part_dst = p->dev.part_dst;
-  a.dest_base = p->dev.dest_base;
-  a.row_dest = p->dev.row_dest;
-  a.row_rank = p->dev.row_rank;
-  a.final_row = p->dev.final_row;
+  a.map = make_row_map(p);
   a.status = p->dev.gemm_status;
   a.bias = static_cast<const uint16_t*>(bias);
   a.act = act;
-  a.layout = p->layout;
-  a.R = p->R;
   a.unit_bytes = p->tile_n * 2;
   a.row_bytes = p->N * 2;
   a.slot0 = p->group_slot_begin[g0];
   a.n_slots = p->group_slot_begin[g1] - a.slot0;
-  a.h = kTileM / p->R;
-  a.rows_per = p->M / p->R;
   int ctas = p->reorder_ctas > 0 ? p->reorder_ctas : 3 * p->sm_count;
   if (ctas > a.n_slots) ctas = a.n_slots;
   reorder_kernel<<<ctas, kRThreads, kRSmem, static_cast<cudaStream_t>(stream)>>>(a);

@@ -91,6 +91,10 @@ def lib():
                                                  ctypes.c_int32, _i32p, _dp]),
             "fo_reorder_back_fused": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, _vpp,
                                                      _vpp, _vp, ctypes.c_int, _vp]),
+            "fo_consume_reorder": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int, _vp, _vpp,
+                                                  ctypes.c_int32, _vpp, _vpp, _vp, ctypes.c_int,
+                                                  _vp, ctypes.c_uint32, ctypes.c_uint64, _vp,
+                                                  _vp]),
             "fo_allgather_rows": (ctypes.c_int, [_vp, _vpp, _vp, _vp, ctypes.c_int, _vp]),
             "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
@@ -255,6 +259,15 @@ def fo_reorder_back_fused(plan, group_begin, group_end, src, dst, bias, act, str
     _check("fo_reorder_back_fused",
            lib().fo_reorder_back_fused(plan, group_begin, group_end, _ptrs(src), _ptrs(dst),
                                        int(bias) or None, act, stream or None))
+
+
+def fo_consume_reorder(plan, group, kind, src, partials, comm_dst, final_dst, bias, act,
+                       flags, epoch, spin_limit_ns, dev_status, stream):
+    _check("fo_consume_reorder",
+           lib().fo_consume_reorder(plan, group, kind, int(src), _ptrs(partials), len(partials),
+                                    _ptrs(comm_dst), _ptrs(final_dst), int(bias) or None, act,
+                                    int(flags), epoch & 0xffffffff, spin_limit_ns,
+                                    int(dev_status), stream or None))
 
 
 def fo_allgather_rows(plan, slices, out, bias, act, stream):

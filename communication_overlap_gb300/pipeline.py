@@ -138,15 +138,25 @@ class Pipeline:
                            [c.data_ptr() for c in b.comm], [f.data_ptr() for f in b.final],
                            stream.cuda_stream)
 
+    def consume_reorder(self, stream, epoch, group=-1, spin_limit_ns=0, bias=0,
+                        act=fo.FO_ACT_NONE):
+        b = self.buf
+        fo.fo_consume_reorder(self.plan, group, self.kind, b.C_r.data_ptr(),
+                              [p.data_ptr() for p in b.partials],
+                              [c.data_ptr() for c in b.comm], [f.data_ptr() for f in b.final],
+                              bias, act, b.flags.data_ptr(), epoch, spin_limit_ns,
+                              b.status.data_ptr(), stream.cuda_stream)
+
     def set_overlap(self, overlap):
         if overlap != self._overlap:
             fo.fo_plan_set_launch(self.plan, self.consumer_ctas, self.reorder_ctas, overlap)
             self._overlap = overlap
 
-    def step(self, overlap=True, sync_current=True):
+    def step(self, overlap=True, sync_current=True, fused=False):
         """One pass of the whole path with a fresh epoch, on stream s0.  With
         overlap the consumer runs alongside the GEMM (dependent launch);
-        without, it starts after the GEMM (the serial baseline)."""
+        without, it starts after the GEMM (the serial baseline).  fused: the
+        consumer and the post-communication reorder in one kernel."""
         self.set_overlap(overlap)
         self.epoch = (self.epoch + 1) & 0xffffffff or 1
         e = self.epoch
@@ -154,8 +164,11 @@ class Pipeline:
         if sync_current:
             self.s0.wait_stream(cur)
         self.gemm(self.s0, e)
-        self.consume(self.s0, e)
-        self.reorder(self.s0)
+        if fused:
+            self.consume_reorder(self.s0, e)
+        else:
+            self.consume(self.s0, e)
+            self.reorder(self.s0)
         if sync_current:
             cur.wait_stream(self.s0)
         return e

@@ -337,6 +337,23 @@ fo_status fo_reorder_back_fused(const fo_plan* plan, int32_t group_begin, int32_
                                 const void* const* src, void* const* dst, const void* bias,
                                 fo_activation act, void* cuda_stream);
 
+/* fo_consume_group and fo_reorder_back_fused in one persistent kernel, for
+ * the same results in both sets of buffers: comm_dst receives what
+ * fo_consume_group writes to dst, final_dst what fo_reorder_back_fused
+ * writes to dst.  A CTA that has taken its share of group j's
+ * communication reorders group j-1 (waiting, bounded, until every chunk of
+ * j-1 is counted as consumed), so on the GEMM's stream every group but the
+ * last is reordered while the GEMM still runs ([P1] 五: the post-
+ * communication reorder fused with the element-wise epilogue to save a
+ * launch).  Layouts: TILE (COPY, SUM), RS (RS), A2A (A2A).  Uses the plan's
+ * scratch; calls that overlap in time on one plan race on it. */
+fo_status fo_consume_reorder(const fo_plan* plan, int32_t group, fo_consumer kind,
+                             const void* src_reordered, const void* const* partials,
+                             int32_t n_partials, void* const* comm_dst, void* const* final_dst,
+                             const void* bias, fo_activation act, const uint32_t* flags,
+                             uint32_t epoch, uint64_t spin_limit_ns, int32_t* dev_status,
+                             void* cuda_stream);
+
 /* The AllGather after a ReduceScatter, with the row exchange and the
  * element-wise epilogue in one pass ([P1] 二 (2): the gathered rows are put
  * in order by a block-cyclic permutation that needs no mapping table and

@@ -92,12 +92,12 @@ def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
     return out
 
 
-def run_workload(w, inp=None, overlap=True, steps=2, **kw):
+def run_workload(w, inp=None, overlap=True, steps=2, fused=False, **kw):
     inp = inp or W.make_inputs(w)
     pipe = Pipeline(w, inp, **kw)
     try:
         for _ in range(steps):
-            pipe.step(overlap=overlap)
+            pipe.step(overlap=overlap, fused=fused)
         res = pipe.results()
     except Exception:
         pipe.close()

@@ -100,3 +100,35 @@ def test_allgather_row_exchange(case):
             assert _close(out.cpu().numpy().view(np.uint16), want, act)
     finally:
         pipe.close()
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_fused_consume_reorder(case):
+    """One kernel for the consumer and the reorder: the same bytes in the
+    communication and the final buffers as the two separate calls, with the
+    GEMM running alongside; with an epilogue, the oracle's result."""
+    w = _workload(case)
+    pipe, inp, res = run_workload(w, steps=2)           # separate calls
+    try:
+        check_run(pipe, inp, res)
+        for c in pipe.buf.comm + pipe.buf.final:
+            c.zero_()
+        torch.cuda.synchronize()
+        for _ in range(2):                               # fused, overlapped, twice
+            pipe.step(fused=True)
+        fused = pipe.results()
+        assert fused["status"] == 0
+        for a, b in zip(res["comm"] + res["final"], fused["comm"] + fused["final"]):
+            assert np.array_equal(a, b)
+        op = oracle_plan(w, inp, pipe.partition)
+        bias = _bias(w.N, 5)
+        dbias = torch.from_numpy(bias.view(np.int16)).cuda()
+        pipe.epoch += 1
+        pipe.gemm(pipe.s0, pipe.epoch)
+        pipe.consume_reorder(pipe.s0, pipe.epoch, bias=dbias.data_ptr(), act=fo.FO_ACT_SILU)
+        got = pipe.results()
+        assert got["status"] == 0
+        for g, r in zip(got["final"], res["final"]):
+            assert _close(g, OE.elementwise(r, bias, fo.FO_ACT_SILU), fo.FO_ACT_SILU)
+    finally:
+        pipe.close()
