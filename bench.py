@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--trace-out", default="", help="write per-tile stamps (json)")
     ap.add_argument("--consumer-ctas", type=int, default=0,
                     help="consumer grid (0: library default, 4 per SM)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="headline with separate consumer and reorder kernels")
     ap.add_argument("--reorder-ctas", type=int, default=0,
                     help="reorder grid (0: library default, 3 per SM)")
     return ap.parse_args()
@@ -325,8 +327,9 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     # warm-up (also the first correctness evidence: status and counting table)
+    fused = not args.unfused
     for _ in range(max(3, args.warmup)):
-        pipe.step(overlap=True)
+        pipe.step(overlap=True, fused=fused)
     torch.cuda.synchronize()
     assert int(pipe.buf.status.item()) == 0, "consumer wait timed out"
     assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
@@ -334,13 +337,16 @@ def run_ours(args):
     # the headline: overlapped steps
     barrier()
     with Clocks(local) as clk:
-        t_ov = timed(torch, s, lambda: pipe.step(overlap=True, sync_current=False),
+        t_ov = timed(torch, s, lambda: pipe.step(overlap=True, sync_current=False, fused=fused),
                      args.steps, flush)
     barrier()
     ms_ov = statistics.mean(t_ov)
     status_ok = int(pipe.buf.status.item()) == 0
 
     # serial baseline: consumer after the GEMM
+    # the other overlapped variant (separate kernels, or fused)
+    t_alt = timed(torch, s, lambda: pipe.step(overlap=True, sync_current=False, fused=not fused),
+                  args.steps, flush)
     t_ser = timed(torch, s, lambda: pipe.step(overlap=False, sync_current=False),
                   args.steps, flush)
     # GEMM alone (signals on, as in the step; and off)
@@ -381,7 +387,7 @@ def run_ours(args):
         span_alone.append(gemm_span()[0])
         with torch.cuda.stream(s):
             flush()
-        pipe.step(overlap=True)
+        pipe.step(overlap=True, fused=fused)
         torch.cuda.synchronize()
         sp, stamps = gemm_span()
         span_step.append(sp)
@@ -407,7 +413,7 @@ def run_ours(args):
                 d_.copy_(h_, non_blocking=True)
             for d_, h_ in zip(pipe.buf.partials, hP):
                 d_.copy_(h_, non_blocking=True)
-        pipe.step(overlap=True, sync_current=False)
+        pipe.step(overlap=True, sync_current=False, fused=fused)
         with torch.cuda.stream(s):
             for h_, d_ in zip(hOut, pipe.buf.final):
                 h_.copy_(d_, non_blocking=True)
@@ -458,10 +464,12 @@ def run_ours(args):
             "e2e": {"value": whole_job_tflops(world, flops, ms_e2e), "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ms_e2e},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": (2 if fused else 3) * args.steps,
             "cpu_baseline": cpu,
             "detail": {
                 "ms_overlapped_step": ms_ov,
+                "overlapped_step_kernels": "consumer+reorder fused" if fused else "separate",
+                "ms_overlapped_step_other_variant": statistics.mean(t_alt),
                 "ms_serial_step": ms_ser,
                 "overlap_speedup": ms_ser / ms_ov,
                 "ms_gemm_alone": ms_gemm,
