@@ -51,8 +51,9 @@ def parse():
     ap.add_argument("--trace-out", default="", help="write per-tile stamps (json)")
     ap.add_argument("--consumer-ctas", type=int, default=0,
                     help="consumer grid (0: library default, 4 per SM)")
-    ap.add_argument("--unfused", action="store_true",
-                    help="headline with separate consumer and reorder kernels")
+    ap.add_argument("--step-kernels", default="auto", choices=["auto", "fused", "separate"],
+                    help="consumer and reorder as one kernel (fo_consume_reorder) or two; "
+                         "auto: fused for the copy and bucket consumers, separate for sums")
     ap.add_argument("--reorder-ctas", type=int, default=0,
                     help="reorder grid (0: library default, 3 per SM)")
     return ap.parse_args()
@@ -327,7 +328,13 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     # warm-up (also the first correctness evidence: status and counting table)
-    fused = not args.unfused
+    # measured: the fused kernel saves the reorder's launch and overlaps it
+    # for the copy and bucket consumers, but its register budget halves the
+    # sums' occupancy next to the GEMM, so sums keep two kernels
+    if args.step_kernels == "auto":
+        fused = w.consumer in (W.CONS_COPY, W.CONS_A2A)
+    else:
+        fused = args.step_kernels == "fused"
     for _ in range(max(3, args.warmup)):
         pipe.step(overlap=True, fused=fused)
     torch.cuda.synchronize()

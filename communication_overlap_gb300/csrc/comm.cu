@@ -236,24 +236,26 @@ __device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, uin
 }
 
 // One tile's rows from the communication buffers to the final layout: warp
-// w takes every 8th row group; each lane keeps 8 independent 16-byte loads
-// in flight before its stores.
+// w takes every 8th row group; each lane keeps kBatch independent 16-byte
+// loads in flight before its stores.
 template <int VPU>
 __device__ __forceinline__ void reorder_tile_regs(const FusedArgs& a, uint4* const* src,
                                                   uint4* const* fin, int32_t s, int tid) {
   constexpr int kRowsPerInstr = 32 / VPU;
   constexpr int kWarps = kThreads / 32;
-  constexpr int kRounds = kTileM / kWarps / kRowsPerInstr / 8;
+  constexpr int kBatch = 4;   // loads per lane per round (kept small: this kernel
+                              // shares its register budget with the consumer)
+  constexpr int kRounds = kTileM / kWarps / kRowsPerInstr / kBatch;
   const int warp = tid / 32, lane = tid % 32, sub = lane / VPU, vl = lane % VPU;
   const TileInfo ti = a.map.tile[s];
 #pragma unroll 1
   for (int round = 0; round < kRounds; ++round) {
-    uint4 x[8];
-    int64_t to[8];
-    int kk[8];
+    uint4 x[kBatch];
+    int64_t to[kBatch];
+    int kk[kBatch];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int32_t r = ((round * 8 + i) * kWarps + warp) * kRowsPerInstr + sub;
+    for (int i = 0; i < kBatch; ++i) {
+      const int32_t r = ((round * kBatch + i) * kWarps + warp) * kRowsPerInstr + sub;
       kk[i] = -1;
       if (r < ti.rows) {
         int32_t su, dr;
@@ -263,7 +265,7 @@ __device__ __forceinline__ void reorder_tile_regs(const FusedArgs& a, uint4* con
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kBatch; ++i) {
       if (kk[i] < 0) continue;
       uint4 y = x[i];
       if (a.act != FO_ACT_NONE || a.bias != nullptr)
@@ -274,7 +276,7 @@ __device__ __forceinline__ void reorder_tile_regs(const FusedArgs& a, uint4* con
 }
 
 template <int KIND, int U, int VPU>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
     consume_reorder_kernel(const __grid_constant__ FusedArgs a) {
   const ConsumeArgs& c = a.c;
   __shared__ int s_ok;
