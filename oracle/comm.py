@@ -34,7 +34,9 @@ def pre_reorder(p, C_bits):
     for s in range(p.tiles):
         rows = p.tile_rows(s)
         r0, c0 = p.tile_row0(s), p.tile_col0(s)
-        C_r[p.unit[s, :rows]] = C_bits[r0:r0 + rows, c0:c0 + p.tile_n]
+        u = p.unit[s, :rows]
+        keep = u >= 0                 # rows that hold no token are not sent
+        C_r[u[keep]] = C_bits[r0:r0 + rows, c0:c0 + p.tile_n][keep]
     return C_r
 
 
@@ -138,7 +140,7 @@ def _positions_in_dest(p, s):
         inside = (u >= st) & (u < st + n)
         k[inside] = d
         idx[inside] = int(p.part_dst[j, d]) + (u[inside] - st)
-    assert (k >= 0).all(), "unit outside its group's parts"
+    assert ((k >= 0) | (u < 0)).all(), "unit outside its group's parts"
     return k, idx
 
 
@@ -171,13 +173,13 @@ def reorder_back_rs(p, slices, groups=None, out=None):
     return outs
 
 
-def reorder_back_a2a(p, recv, top_k, groups=None, out=None):
+def reorder_back_a2a(p, recv, top_k, groups=None, out=None, n_tokens=None):
     """Inverse mapping after the All-to-All: on rank d, the sub-token of
     routed row rho (token t, top-k slot q), column block c0, goes to row
     (t // D) * top_k + q, columns c0.. of rank d's output.  Each rank
     receives the tokens t with t mod D == d, all their top-k rows."""
     D = p.n_dest
-    n_tok = int(p.row_token.max()) + 1
+    n_tok = int(p.row_token.max()) + 1 if n_tokens is None else n_tokens
     outs = out if out is not None else [
         np.zeros((len(range(d, n_tok, D)) * top_k, p.N), dtype=np.uint16)
         for d in range(D)]
@@ -189,7 +191,7 @@ def reorder_back_a2a(p, recv, top_k, groups=None, out=None):
         t = p.row_token[r0:r0 + rows].astype(np.int64)
         q = p.row_slot[r0:r0 + rows].astype(np.int64)
         final_row = (t // D) * top_k + q
-        for d in range(D):
+        for d in range(D):           # rows without a token (k = -1) match no d
             sel = k == d
             outs[d][final_row[sel], c0:c0 + p.tile_n] = recv[d][idx[sel]]
     return outs

@@ -166,11 +166,17 @@ class Plan:
 def _row_dests(plan, slot):
     """Destination rank of every valid row of the tile at ``slot``, for the
     layouts that route rows: a2a sends row rho to rank token(rho) mod n_dest;
-    rs_rowblock sends global row g to rank g // (M / n_dest)."""
+    rs_rowblock sends global row g to rank g // (M / n_dest).
+
+    A2A rows whose token is negative hold no token (an expert's capacity left
+    unfilled by the routing) and go nowhere: destination -1.  Reading of
+    [P1] 二 (3) "映射表需要考虑动态路由模式": the mapping follows the routing,
+    and a row the routing leaves empty has nothing to send."""
     rows = plan.tile_rows(slot)
     g = plan.tile_row0(slot) + np.arange(rows)
     if plan.layout == LAYOUT_A2A:
-        return plan.row_token[g] % plan.n_dest
+        t = plan.row_token[g].astype(np.int64)
+        return np.where(t >= 0, t % plan.n_dest, -1)
     if plan.layout == LAYOUT_RS_ROWBLOCK:
         return g // (plan.M // plan.n_dest)
     raise ValueError(plan.layout)

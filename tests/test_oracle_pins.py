@@ -280,6 +280,55 @@ def test_a2a_every_routed_row_lands_once():
     assert sum(o.shape[0] for o in outs) == p.M
 
 
+def _padded_routing(capacity, n_tok=40, E=3, k=2, D=4, seed=0):
+    """The routing of ``_tiny_routing`` with every expert's rows padded to a
+    fixed capacity by rows that hold no token (token -1): the static layout a
+    dynamic router fills at run time."""
+    er, tok, sl = _tiny_routing(n_tok, E, k, D, seed)
+    T, S = [], []
+    r = 0
+    for m in er:
+        assert m <= capacity
+        T += tok[r:r + m].tolist() + [-1] * (capacity - m)
+        S += sl[r:r + m].tolist() + [0] * (capacity - m)
+        r += m
+    return [capacity] * E, np.array(T), np.array(S), n_tok
+
+
+def test_a2a_padding_rows_go_nowhere():
+    """Rows the routing leaves empty (token -1) are sent to no rank: C_r holds
+    exactly the routed rows, each lands once at its token's place, and the
+    sentinel written into every empty row appears in no received buffer."""
+    D, k = 4, 2
+    er, tok, sl, n_tok = _padded_routing(capacity=40, D=D)
+    p = _tiny_plan(P.LAYOUT_A2A, R=D, N=3 * 64, tokens=(er, tok, sl))
+    valid = tok >= 0
+    assert p.n_units == int(valid.sum()) * p.tiles_n < p.M * p.tiles_n
+    pad_rows = np.nonzero(~valid)[0]
+    for s in range(p.tiles):
+        g = p.tile_row0(s) + np.arange(p.tile_rows(s))
+        assert (p.unit[s, :p.tile_rows(s)][~valid[g]] == -1).all()
+    assert sorted(p.unit[p.unit >= 0].tolist()) == list(range(p.n_units))
+    rng = np.random.default_rng(6)
+    C = rng.integers(0, 0x7F00, (p.M, p.N)).astype(np.uint16)
+    C[pad_rows] = 0xFFFF                         # a NaN nothing else carries
+    recv = cm.consume_a2a(p, cm.pre_reorder(p, C))
+    assert sum(r.shape[0] for r in recv) == p.n_units
+    assert not any((r == 0xFFFF).any() for r in recv)
+    outs = cm.reorder_back_a2a(p, recv, k, n_tokens=n_tok)
+    assert sum(o.shape[0] for o in outs) == n_tok * k
+    for rho in np.nonzero(valid)[0]:
+        t, q = int(tok[rho]), int(sl[rho])
+        assert np.array_equal(outs[t % D][(t // D) * k + q], C[rho])
+    # the same tokens routed without padding give the same received rows
+    er0, tok0, sl0 = _tiny_routing(D=D)
+    p0 = _tiny_plan(P.LAYOUT_A2A, R=D, N=3 * 64, tokens=(er0, tok0, sl0))
+    C0 = C[valid]
+    outs0 = cm.reorder_back_a2a(p0, cm.consume_a2a(p0, cm.pre_reorder(p0, C0)), k)
+    for a, b in zip(outs, outs0):
+        assert np.array_equal(a, b)
+
+
 # ---------------------------------------------------------------- GEMM pins
 
 def _exact_gemm(A, Bm):
@@ -409,6 +458,15 @@ def test_planted_subtile_index_is_caught(monkeypatch):
     monkeypatch.setattr(P, "_assign_units", wrong)
     with pytest.raises((AssertionError, IndexError)):
         test_rs_subtile_kth_subtiles_form_whole_rows()
+
+
+def test_planted_padding_routed_by_modulo_is_caught(monkeypatch):
+    def wrong(plan, slot):   # token -1 taken modulo D like a real token
+        g = plan.tile_row0(slot) + np.arange(plan.tile_rows(slot))
+        return plan.row_token[g] % plan.n_dest
+    monkeypatch.setattr(P, "_row_dests", wrong)
+    with pytest.raises((AssertionError, IndexError)):
+        test_a2a_padding_rows_go_nowhere()
 
 
 def test_planted_swapped_group_order_is_caught(monkeypatch):
