@@ -242,10 +242,15 @@ def oracle_sample(w, inp, partition, rows):
     res = OPL.run(inp.expert_rows, w.N, w.K, w.tile_m, w.tile_n, w.swizzle, w.wave_width,
                   partition, _LAYOUT_NAMES[w.layout], cons, inp.A, inp.B, inp.partials,
                   w.n_dest, inp.row_token, inp.row_slot, w.top_k or 2, C_given=C)
-    rest = sum(v for k, v in res.seconds.items() if k not in ("gemm", "plan"))
+    # with dynamic routing the routing tables are rebuilt every step: the
+    # plan is part of the step
+    skip = ("gemm",) if w.capacity else ("gemm", "plan")
+    rest = sum(v for k, v in res.seconds.items() if k not in skip)
+    plan_note = (f"plan ({res.seconds['plan']:.2f} s) included: the routing changes every step"
+                 if w.capacity else f"plan ({res.seconds['plan']:.2f} s) excluded")
     desc = (f"fp64 GEMM on {rows} of {w.M} output rows ({t_rows:.2f} s, scaled x"
             f"{w.M / rows:.1f}) + pre-reorder, consumer and post-reorder on the full "
-            f"output ({rest:.2f} s); plan ({res.seconds['plan']:.2f} s) excluded")
+            f"output ({rest:.2f} s); {plan_note}")
     return gemm_full + rest, desc, os.cpu_count()
 
 
@@ -288,9 +293,11 @@ def run_reference(args):
 
 def workload_name(w):
     if w.grouped:
+        cap = (f", capacity {w.capacity} rows per expert (M={w.M}), a new routing built on "
+               f"the device every step" if w.capacity else "")
         return (f"{w.name}: grouped bf16 GEMM {w.n_tokens} tokens x top-{w.top_k} over "
                 f"{w.n_experts} experts, N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
-                f"W={w.wave_width}, swizzle {w.swizzle}")
+                f"W={w.wave_width}, swizzle {w.swizzle}{cap}")
     return (f"{w.name}: bf16 GEMM M={w.M} N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
             f"W={w.wave_width}, swizzle {w.swizzle}")
 
@@ -322,6 +329,29 @@ def run_ours(args):
 
     trace = torch.zeros(pipe.tiles + w.wave_width, dtype=torch.int64, device=dev)
 
+    # Dynamic routing (expert capacities fixed): every step takes the next of
+    # a few routings resident in HBM, with its routed A (the dispatch gather,
+    # outside the path), and rebuilds the routing tables on the device
+    # (fo_plan_route) before its GEMM.
+    dyn = w.capacity > 0
+    routes = []
+    if dyn:
+        X = W.token_matrix(w)
+        for k in range(1, 5):
+            _, tok, sl = W.routing(w, k)
+            routes.append((torch.from_numpy(tok).to(dev), torch.from_numpy(sl).to(dev),
+                           torch.from_numpy(W.gather_rows(X, tok).view(np.int16)).to(dev)))
+        del X
+    turn = [0]
+
+    def step(**kw):
+        if dyn:
+            tok, sl, A = routes[turn[0] % len(routes)]
+            turn[0] += 1
+            pipe.buf.A = A
+            pipe.route(tok, sl)
+        return pipe.step(**kw)
+
     def barrier():
         if world > 1:
             dist.barrier()
@@ -336,7 +366,7 @@ def run_ours(args):
     else:
         fused = args.step_kernels == "fused"
     for _ in range(max(3, args.warmup)):
-        pipe.step(overlap=True, fused=fused)
+        step(overlap=True, fused=fused)
     torch.cuda.synchronize()
     assert int(pipe.buf.status.item()) == 0, "consumer wait timed out"
     assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
@@ -344,7 +374,7 @@ def run_ours(args):
     # the headline: overlapped steps
     barrier()
     with Clocks(local) as clk:
-        t_ov = timed(torch, s, lambda: pipe.step(overlap=True, sync_current=False, fused=fused),
+        t_ov = timed(torch, s, lambda: step(overlap=True, sync_current=False, fused=fused),
                      args.steps, flush)
     barrier()
     ms_ov = statistics.mean(t_ov)
@@ -352,10 +382,13 @@ def run_ours(args):
 
     # serial baseline: consumer after the GEMM
     # the other overlapped variant (separate kernels, or fused)
-    t_alt = timed(torch, s, lambda: pipe.step(overlap=True, sync_current=False, fused=not fused),
+    t_alt = timed(torch, s, lambda: step(overlap=True, sync_current=False, fused=not fused),
                   args.steps, flush)
-    t_ser = timed(torch, s, lambda: pipe.step(overlap=False, sync_current=False),
+    t_ser = timed(torch, s, lambda: step(overlap=False, sync_current=False),
                   args.steps, flush)
+    t_route = []
+    if dyn:   # the two routing kernels alone
+        t_route = timed(torch, s, lambda: pipe.route(*routes[0][:2]), args.steps, flush)
     # GEMM alone (signals on, as in the step; and off)
     t_gemm = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch), args.steps, flush)
     t_gemm_nosig = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch, signal=False),
@@ -407,19 +440,35 @@ def run_ours(args):
 
     # end to end through the C ABI with host buffers
     hA = torch.from_numpy(inp.A.view(np.int16)).pin_memory()
+    h_route = []
+    if dyn:   # each step's routing and routed A come from the host
+        h_route = [(t.cpu().pin_memory(), q.cpu().pin_memory(), a.cpu().pin_memory())
+                   for t, q, a in routes]
+        d_tok, d_sl = torch.empty_like(routes[0][0]), torch.empty_like(routes[0][1])
+        pipe.buf.A = torch.empty_like(routes[0][2])
     hB = [torch.from_numpy(b.view(np.int16)).pin_memory() for b in inp.B]
     hP = [torch.from_numpy(p.view(np.int16)).pin_memory() for p in inp.partials]
     hOut = [torch.empty(f.shape, dtype=torch.int16).pin_memory() for f in pipe.buf.final]
     h2d = hA.numel() * 2 + sum(b.numel() * 2 for b in hB) + sum(p.numel() * 2 for p in hP)
+    h2d += 2 * w.M * 4 if dyn else 0
     d2h = sum(o.numel() * 2 for o in hOut)
 
     def e2e_step():
         with torch.cuda.stream(s):
-            pipe.buf.A.copy_(hA, non_blocking=True)
+            if dyn:
+                t_, q_, a_ = h_route[turn[0] % len(h_route)]
+                turn[0] += 1
+                pipe.buf.A.copy_(a_, non_blocking=True)
+                d_tok.copy_(t_, non_blocking=True)
+                d_sl.copy_(q_, non_blocking=True)
+            else:
+                pipe.buf.A.copy_(hA, non_blocking=True)
             for d_, h_ in zip(pipe.buf.B, hB):
                 d_.copy_(h_, non_blocking=True)
             for d_, h_ in zip(pipe.buf.partials, hP):
                 d_.copy_(h_, non_blocking=True)
+        if dyn:
+            pipe.route(d_tok, d_sl)
         pipe.step(overlap=True, sync_current=False, fused=fused)
         with torch.cuda.stream(s):
             for h_, d_ in zip(hOut, pipe.buf.final):
@@ -439,8 +488,8 @@ def run_ours(args):
     gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
     traffic = traffic_from_profile(os.path.join(ROOT, "communication_overlap_gb300",
                                                 "csrc", "gemm.cu"))
-    cons_bytes = consumer_bytes(w, pipe)
-    reo_bytes = 2 * w.M * w.N * 2
+    cons_bytes = consumer_bytes(w, inp)
+    reo_bytes = 2 * moved_rows(w, inp) * w.N * 2
     out = None
     if rank == 0:
         cpu = None
@@ -471,7 +520,7 @@ def run_ours(args):
             "e2e": {"value": whole_job_tflops(world, flops, ms_e2e), "unit": "TFLOPS",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ms_e2e},
-            "gpu_launches": (2 if fused else 3) * args.steps,
+            "gpu_launches": ((2 if fused else 3) + (2 if dyn else 0)) * args.steps,
             "cpu_baseline": cpu,
             "detail": {
                 "ms_overlapped_step": ms_ov,
@@ -493,6 +542,9 @@ def run_ours(args):
                 "gemm_in_kernel_ms_in_step": statistics.median(span_step),
                 "gemm_slowdown": statistics.median(span_step) / statistics.median(span_alone),
                 "status_ok": status_ok,
+                **({"ms_route_alone": statistics.mean(t_route),
+                    "routings": "4 routings resident in HBM, taken in turn, one per step"}
+                   if dyn else {}),
             },
         }
         print(json.dumps(out))
@@ -525,10 +577,18 @@ def consumer_name(w):
             3: f"bucket by token mod {w.n_dest}"}[w.consumer]
 
 
-def consumer_bytes(w, pipe):
+def moved_rows(w, inp):
+    """Rows the consumer and the reorder move: all of them, except the empty
+    rows of an expert capacity that the routing left unfilled."""
+    if inp.row_token is None:
+        return w.M
+    return int((np.asarray(inp.row_token) >= 0).sum())
+
+
+def consumer_bytes(w, inp):
     """Algorithmic bytes of the consumer: every source read once, every
     output written once."""
-    c = w.M * w.N * 2
+    c = moved_rows(w, inp) * w.N * 2
     if w.consumer in (1, 2):
         return c * (1 + w.n_partials) + c
     return 2 * c

@@ -44,6 +44,12 @@ fo_status fo_plan_info(const fo_plan* p, int32_t* tiles, int32_t* waves,
 fo_status fo_plan_table(const fo_plan* p, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length) {
   if (!p) return FO_ERR_ARG;
+  if (p->routing_on_device) {
+    // the routing tables were last built on the device: bring the host
+    // copies up to date (the plan's contents do not change, only its cache)
+    const fo_status st = fo::refresh_routing(const_cast<fo_plan*>(p));
+    if (st != FO_OK) return st;
+  }
   std::vector<int32_t> unit;
   const std::vector<int32_t>* v = nullptr;
   switch (which) {
@@ -56,6 +62,7 @@ fo_status fo_plan_table(const fo_plan* p, int32_t which, int32_t* out,
     case FO_TAB_PART_DST: v = &p->part_dst; break;
     case FO_TAB_DEST_UNITS: v = &p->dest_units; break;
     case FO_TAB_FINAL_ROWS: v = &p->final_rows; break;
+    case FO_TAB_DEST_CAPACITY: v = &p->dest_capacity; break;
     case FO_TAB_UNIT:
       unit.resize(size_t(p->tiles) * p->tile_m);
       for (int32_t s = 0; s < p->tiles; ++s)
@@ -223,6 +230,30 @@ fo_status fo_reorder_back_fused(const fo_plan* p, int32_t group_begin, int32_t g
     if (!src[k] || !dst[k]) return FO_ERR_ARG;
   if (group_begin == group_end) return FO_OK;
   return fo::launch_reorder_back(p, group_begin, group_end, src, dst, bias, int(act), stream);
+}
+
+fo_status fo_plan_route(fo_plan* p, const int32_t* row_token, const int32_t* row_slot,
+                        int32_t n_tokens, int32_t top_k, int32_t* dev_status, void* stream) {
+  if (!p || !p->blob || p->layout != FO_LAYOUT_A2A_SUBTOKEN) return FO_ERR_ARG;
+  if (!row_token || !row_slot || !dev_status) return FO_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(row_token) | reinterpret_cast<uintptr_t>(row_slot) |
+       reinterpret_cast<uintptr_t>(dev_status)) & 3)
+    return FO_ERR_ARG;
+  if (n_tokens < 0 || top_k < 1) return FO_ERR_ARG;
+  // every output row and receive-buffer unit must stay addressable in int32
+  const int64_t toks = (int64_t(n_tokens) + p->R - 1) / p->R;
+  if (toks * top_k * p->tiles_n >= (int64_t(1) << 31)) return FO_ERR_ARG;
+  // the kernels read the new output sizes from the plan; a failed launch
+  // leaves the plan as it was
+  const int32_t old_tokens = p->n_tokens, old_top_k = p->top_k;
+  fo::set_a2a_outputs(p, n_tokens, top_k);
+  const fo_status st = fo::launch_plan_route(p, row_token, row_slot, dev_status, stream);
+  if (st != FO_OK) {
+    fo::set_a2a_outputs(p, old_tokens, old_top_k);
+    return st;
+  }
+  p->routing_on_device = true;
+  return FO_OK;
 }
 
 fo_status fo_reorder_back(const fo_plan* p, int32_t group_begin, int32_t group_end,

@@ -260,8 +260,10 @@ __device__ __forceinline__ void reorder_tile_regs(const FusedArgs& a, uint4* con
       if (r < ti.rows) {
         int32_t su, dr;
         map_row(a.map, ti, s, r, &kk[i], &su, &dr);
-        x[i] = ld_cg(src[kk[i]] + int64_t(su) * VPU + vl);
-        to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
+        if (kk[i] >= 0) {   // not an empty All-to-All row
+          x[i] = ld_cg(src[kk[i]] + int64_t(su) * VPU + vl);
+          to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
+        }
       }
     }
 #pragma unroll

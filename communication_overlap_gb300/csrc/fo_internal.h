@@ -47,6 +47,10 @@ struct DeviceTables {
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
   int32_t* rwork = nullptr;            // [2P + 1] scratch of the fused consumer+reorder
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
+  int32_t* route_cnt = nullptr;        // [blocks * (R + 1)] A2A scratch of
+                                       //   fo_plan_route: rows per (tile-row
+                                       //   block, rank), then a flag per block
+                                       //   that saw an invalid row
 };
 
 }  // namespace fo
@@ -54,14 +58,18 @@ struct DeviceTables {
 struct fo_plan {
   // description
   int32_t M = 0, N = 0, K = 0, tile_m = 0, tile_n = 0, swizzle = 0, W = 0;
-  int32_t P = 0, R = 1, layout = 0, n_dest = 1, n_experts = 0, top_k = 1;
+  int32_t P = 0, R = 1, layout = 0, n_dest = 1, n_experts = 0, top_k = 1, n_tokens = 0;
   int32_t tiles = 0, tiles_n = 0, waves = 0, n_units = 0;
   std::vector<int32_t> expert_rows, expert_row0, expert_tile0;
   std::vector<int32_t> group_waves, group_tiles, group_slot_begin, group_unit_begin;
   std::vector<int32_t> slot_tile, tile_slot, slot_group;
   std::vector<fo::TileInfo> tile;
-  std::vector<int32_t> part_start, part_len, part_dst, dest_units, final_rows;
+  std::vector<int32_t> part_start, part_len, part_dst, dest_units, final_rows, dest_capacity;
   std::vector<int32_t> dest_base, row_dest, row_rank, final_row;
+  int32_t route_blocks = 0;       // A2A: tile-row blocks (ceil(rows / 128) per expert)
+  // fo_plan_route rebuilt the routing tables on the device: the host copies
+  // above are stale until refresh_routing() downloads them
+  bool routing_on_device = false;
   // device side
   int device = -1;
   int sm_count = 0;
@@ -82,6 +90,12 @@ fo_status check_shape(const fo_plan_desc* d, int32_t* W, int32_t* tiles,
 fo_status build_plan(const fo_plan_desc* d, fo_plan* p);
 fo_status upload_plan(fo_plan* p);
 int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r);
+void set_a2a_outputs(fo_plan* p, int32_t n_tokens, int32_t top_k);
+fo_status refresh_routing(fo_plan* p);
+
+// route.cu
+fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const int32_t* row_slot,
+                            int32_t* dev_status, void* stream);
 
 // gemm.cu
 int gemm_pair_capacity(const fo_plan* p);

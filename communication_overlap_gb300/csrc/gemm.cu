@@ -242,7 +242,8 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
 
 // ---------------------------------------------------------------- the kernel
 
-// Unit (row of the reordered buffer) of row r of a tile, or -1 past its rows.
+// Unit (row of the reordered buffer) of row r of a tile, or -1 past its rows
+// (and, in the All-to-All layout, for a row that holds no token).
 __device__ __forceinline__ int32_t row_unit(const GemmArgs& a, const TileInfo& ti, int32_t slot,
                                             int32_t r) {
   if (r >= ti.rows) return -1;
@@ -252,7 +253,9 @@ __device__ __forceinline__ int32_t row_unit(const GemmArgs& a, const TileInfo& t
   }
   if (a.layout == FO_LAYOUT_A2A_SUBTOKEN) {
     const int32_t rho = ti.row0 + r;
-    return a.dest_base[slot * a.R + a.row_dest[rho]] + a.row_rank[rho];
+    const int32_t d = a.row_dest[rho];
+    if (d < 0) return -1;   // the row holds no token: it is sent nowhere
+    return a.dest_base[slot * a.R + d] + a.row_rank[rho];
   }
   return ti.unit_base + r;
 }

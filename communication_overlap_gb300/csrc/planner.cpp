@@ -95,8 +95,8 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
     if (layout == FO_LAYOUT_RS_ROWBLOCK && (d->M % R != 0 || (d->M / R) % kTileM != 0))
       return FO_ERR_ARG;
   }
-  if (layout == FO_LAYOUT_A2A_SUBTOKEN && (!d->row_token || !d->row_slot))
-    return FO_ERR_ARG;
+  if (layout == FO_LAYOUT_A2A_SUBTOKEN && (!d->row_token != !d->row_slot))
+    return FO_ERR_ARG;   // both routing arrays or neither (every row empty)
 
   p->M = d->M; p->N = d->N; p->K = d->K;
   p->tile_m = d->tile_m; p->tile_n = d->tile_n; p->swizzle = d->swizzle;
@@ -180,19 +180,28 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   p->part_dst.assign(size_t(P) * R, 0);
   p->group_unit_begin.assign(P + 1, 0);
 
+  int64_t routed_rows = d->M;
   if (layout == FO_LAYOUT_A2A_SUBTOKEN) {
     // per routed row: destination rank, rank among the rows of its tile row
-    // going to the same destination, and its row in that rank's output
-    p->row_dest.assign(d->M, 0);
-    p->row_rank.assign(d->M, 0);
-    p->final_row.assign(d->M, 0);
-    int32_t top_k = 1;
-    for (int32_t r = 0; r < d->M; ++r) {
-      if (d->row_token[r] < 0 || d->row_slot[r] < 0) return FO_ERR_ARG;
+    // going to the same destination, and its row in that rank's output.  A
+    // row with a negative token holds none (an expert's capacity left
+    // unfilled by the routing): it goes nowhere and all three are -1.
+    p->row_dest.assign(d->M, -1);
+    p->row_rank.assign(d->M, -1);
+    p->final_row.assign(d->M, -1);
+    int32_t top_k = 1, n_tokens = 0;
+    routed_rows = 0;
+    for (int32_t r = 0; d->row_token && r < d->M; ++r) {
+      if (d->row_token[r] < 0) continue;
+      if (d->row_slot[r] < 0) return FO_ERR_ARG;
       top_k = std::max(top_k, d->row_slot[r] + 1);
+      n_tokens = std::max(n_tokens, d->row_token[r] + 1);
+      ++routed_rows;
     }
     p->top_k = top_k;
-    for (int32_t r = 0; r < d->M; ++r) {
+    p->n_tokens = n_tokens;
+    for (int32_t r = 0; d->row_token && r < d->M; ++r) {
+      if (d->row_token[r] < 0) continue;
       p->row_dest[r] = d->row_token[r] % R;
       p->final_row[r] = (d->row_token[r] / R) * top_k + d->row_slot[r];
     }
@@ -203,7 +212,8 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
            b += kTileM) {
         std::fill(cnt.begin(), cnt.end(), 0);
         const int32_t end = std::min(b + kTileM, p->expert_row0[e] + p->expert_rows[e]);
-        for (int32_t r = b; r < end; ++r) p->row_rank[r] = cnt[p->row_dest[r]]++;
+        for (int32_t r = b; r < end; ++r)
+          if (p->row_dest[r] >= 0) p->row_rank[r] = cnt[p->row_dest[r]]++;
       }
     }
     // per slot and destination: rows of the tile bound there
@@ -295,19 +305,37 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
     }
     p->dest_units[k] = off;
   }
-  if (int64_t(p->n_units) != int64_t(d->M) * TN) return FO_ERR_ARG;  // every row once
+  if (int64_t(p->n_units) != routed_rows * TN) return FO_ERR_ARG;  // every row once
 
   // rows of each output of the post-communication reorder
   if (layout == FO_LAYOUT_TILE) {
     p->final_rows.assign(1, d->M);
   } else if (layout == FO_LAYOUT_A2A_SUBTOKEN) {
-    p->final_rows.assign(R, 0);
-    for (int32_t r = 0; r < d->M; ++r)
-      p->final_rows[p->row_dest[r]] = std::max(p->final_rows[p->row_dest[r]], p->final_row[r] + 1);
+    set_a2a_outputs(p, p->n_tokens, p->top_k);
+    // a routing with a (token, slot) pair twice could outgrow the buffers
+    for (int k = 0; k < R; ++k)
+      if (p->dest_units[k] > p->dest_capacity[k]) return FO_ERR_ARG;
   } else {
     p->final_rows.assign(R, d->M / R);
   }
+  if (layout != FO_LAYOUT_A2A_SUBTOKEN) p->dest_capacity = p->dest_units;
   return FO_OK;
+}
+
+// All-to-All outputs for routings of n_tokens tokens with top_k slots each:
+// rank d receives the tokens t = d, d + R, ... and all their slots, so its
+// output has ceil((n_tokens - d) / R) * top_k rows and its receive buffer
+// at most that many rows of every column block.
+void set_a2a_outputs(fo_plan* p, int32_t n_tokens, int32_t top_k) {
+  p->n_tokens = n_tokens;
+  p->top_k = top_k;
+  p->final_rows.assign(p->R, 0);
+  p->dest_capacity.assign(p->R, 0);
+  for (int k = 0; k < p->R; ++k) {
+    const int64_t toks = n_tokens > k ? (int64_t(n_tokens) - k + p->R - 1) / p->R : 0;
+    p->final_rows[k] = int32_t(toks * top_k);
+    p->dest_capacity[k] = int32_t(toks * top_k * p->tiles_n);
+  }
 }
 
 // Unit of row r of the tile at `slot`, from the same per-slot / per-row
@@ -322,6 +350,7 @@ int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r) {
     }
     case FO_LAYOUT_A2A_SUBTOKEN: {
       const int32_t rho = ti.row0 + r;
+      if (p->row_dest[rho] < 0) return -1;   // the row holds no token
       return p->dest_base[size_t(slot) * p->R + p->row_dest[rho]] + p->row_rank[rho];
     }
     default:
@@ -363,6 +392,13 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
   const size_t o_rwork = put(buf, std::vector<int32_t>(2 * p->P + 1, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
+  const bool a2a = p->layout == FO_LAYOUT_A2A_SUBTOKEN;
+  if (a2a) {
+    p->route_blocks = 0;
+    for (int32_t rows : p->expert_rows) p->route_blocks += (rows + kTileM - 1) / kTileM;
+  }
+  const size_t o_rc =
+      put(buf, std::vector<int32_t>(a2a ? size_t(p->route_blocks) * (p->R + 1) : 1, 0));
   void* blob = nullptr;
   if (cudaMalloc(&blob, buf.size()) != cudaSuccess) return FO_ERR_CUDA;
   if (cudaMemcpy(blob, buf.data(), buf.size(), cudaMemcpyHostToDevice) != cudaSuccess) {
@@ -385,6 +421,32 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
   p->dev.rwork = reinterpret_cast<int32_t*>(b + o_rwork);
   p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
+  p->dev.route_cnt = reinterpret_cast<int32_t*>(b + o_rc);
+  return FO_OK;
+}
+
+// Download the routing tables fo_plan_route built on the device (waits for
+// the device first), so that the host copies and every table derived from
+// them describe the routing the kernels now use.
+fo_status refresh_routing(fo_plan* p) {
+  if (!p->routing_on_device) return FO_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) return FO_ERR_CUDA;
+  auto get = [](std::vector<int32_t>& v, const int32_t* src) {
+    return cudaMemcpy(v.data(), src, v.size() * sizeof(int32_t), cudaMemcpyDeviceToHost) ==
+           cudaSuccess;
+  };
+  if (!get(p->part_start, p->dev.part_start) || !get(p->part_len, p->dev.part_len) ||
+      !get(p->part_dst, p->dev.part_dst) || !get(p->group_unit_begin, p->dev.group_unit_begin) ||
+      !get(p->dest_base, p->dev.dest_base) || !get(p->row_dest, p->dev.row_dest) ||
+      !get(p->row_rank, p->dev.row_rank) || !get(p->final_row, p->dev.final_row))
+    return FO_ERR_CUDA;
+  for (int k = 0; k < p->R; ++k) {
+    int32_t off = 0;
+    for (int j = 0; j < p->P; ++j) off += p->part_len[size_t(j) * p->R + k];
+    p->dest_units[k] = off;
+  }
+  p->n_units = p->group_unit_begin[p->P];
+  p->routing_on_device = false;
   return FO_OK;
 }
 

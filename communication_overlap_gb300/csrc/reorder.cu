@@ -71,12 +71,18 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   for (int32_t t = blockIdx.x; t < a.n_slots; t += gridDim.x, phase ^= 1) {
     const int32_t s = a.slot0 + t;
     const TileInfo ti = a.map.tile[s];
+    const bool whole = (a.map.layout == FO_LAYOUT_TILE || a.map.layout == FO_LAYOUT_RS_ROWBLOCK);
+    const bool a2a = a.map.layout == FO_LAYOUT_A2A_SUBTOKEN;
+    // All-to-All: this thread's row (k = -1: it holds no token, moves nowhere)
+    int rk = -1;
+    int32_t rsu = 0, rdr = 0;
+    if (a2a && tid < ti.rows) reorder_row(a, ti, s, tid, &rk, &rsu, &rdr);
+    const int32_t in_rows = a2a ? __syncthreads_count(rk >= 0) : ti.rows;
     // the previous tile's stores have finished reading the buffer
     bulk_wait_read_all();
     __syncthreads();
-    if (tid == 0) mbar_expect_tx(sfull, uint32_t(ti.rows * ub));
+    if (tid == 0) mbar_expect_tx(sfull, uint32_t(in_rows * ub));
     __syncthreads();
-    const bool whole = (a.map.layout == FO_LAYOUT_TILE || a.map.layout == FO_LAYOUT_RS_ROWBLOCK);
     if (whole) {
       if (tid == 0) {
         int k;
@@ -92,11 +98,8 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
         bulk_load(sbuf + tid * a.map.h * ub, a.src[k] + int64_t(su) * ub, uint32_t(a.map.h * ub),
                   sfull);
       }
-    } else if (tid < ti.rows) {  // All-to-All: row by row
-      int k;
-      int32_t su, dr;
-      reorder_row(a, ti, s, tid, &k, &su, &dr);
-      bulk_load(sbuf + tid * ub, a.src[k] + int64_t(su) * ub, uint32_t(ub), sfull);
+    } else if (rk >= 0) {  // All-to-All: row by row
+      bulk_load(sbuf + tid * ub, a.src[rk] + int64_t(rsu) * ub, uint32_t(ub), sfull);
     }
     // wait for the tile to land (bounded)
     if (tid == 0) {
@@ -143,7 +146,13 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
         tensor_store_2d(&a.dst_map[k], sbuf + tid * a.map.h * ub, ti.col0, dr);
         bulk_commit();
       }
-    } else if (tid < ti.rows) {  // ragged tiles and All-to-All rows: per row
+    } else if (a2a) {  // All-to-All rows: per row
+      if (rk >= 0) {
+        bulk_store(a.dst[rk] + int64_t(rdr) * a.row_bytes + int64_t(ti.col0) * 2,
+                   sbuf + tid * ub, uint32_t(ub));
+        bulk_commit();
+      }
+    } else if (tid < ti.rows) {  // ragged tiles: per row
       int k;
       int32_t su, dr;
       reorder_row(a, ti, s, tid, &k, &su, &dr);

@@ -40,7 +40,8 @@ inline RowMap make_row_map(const fo_plan* p) {
 }
 
 // Row r of the tile at slot s: the unit's place in the consumer's buffer k
-// (src_unit) and the row it belongs to in output k (dst_row).
+// (src_unit) and the row it belongs to in output k (dst_row).  k = -1 (and
+// nothing else set) for an All-to-All row that holds no token.
 __device__ __forceinline__ void map_row(const RowMap& a, const TileInfo& ti, int32_t s, int32_t r,
                                         int* k_out, int32_t* src_unit, int32_t* dst_row) {
   int k = 0;
@@ -61,6 +62,10 @@ __device__ __forceinline__ void map_row(const RowMap& a, const TileInfo& ti, int
     } else {  // FO_LAYOUT_A2A_SUBTOKEN
       const int32_t rho = ti.row0 + r;
       k = a.row_dest[rho];
+      if (k < 0) {
+        *k_out = -1;
+        return;
+      }
       u = a.dest_base[s * a.R + k] + a.row_rank[rho];
       *dst_row = a.final_row[rho];
     }

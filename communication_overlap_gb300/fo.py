@@ -20,7 +20,7 @@ FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
 FO_ACT_NONE, FO_ACT_RELU, FO_ACT_SILU = range(3)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
- FO_TAB_FINAL_ROWS) = range(10)
+ FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY) = range(11)
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p
@@ -96,6 +96,8 @@ def lib():
                                                   _vp, ctypes.c_uint32, ctypes.c_uint64, _vp,
                                                   _vp]),
             "fo_allgather_rows": (ctypes.c_int, [_vp, _vpp, _vp, _vp, ctypes.c_int, _vp]),
+            "fo_plan_route": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
+                                             _vp, _vp]),
             "fo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         }
         for name, (res, args) in sig.items():
@@ -182,6 +184,13 @@ def fo_plan_table(plan, which):
     out = (ctypes.c_int32 * max(1, n.value))()
     _check("fo_plan_table", lib().fo_plan_table(plan, which, out, n.value, ctypes.byref(n)))
     return list(out)[:n.value]
+
+
+def fo_plan_route(plan, row_token, row_slot, n_tokens, top_k, dev_status, stream):
+    """Rebuild the All-to-All routing tables on the device from device int32
+    arrays row_token[M], row_slot[M] (addresses), stream-ordered on `stream`."""
+    _check("fo_plan_route", lib().fo_plan_route(plan, row_token, row_slot, n_tokens, top_k,
+                                                dev_status, stream))
 
 
 def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):

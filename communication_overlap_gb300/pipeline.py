@@ -75,6 +75,14 @@ class Pipeline:
         self.kind = _CONSUMER_OF[w.consumer]
         self.dest_units = fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS)
         self.final_rows = fo.fo_plan_table(self.plan, fo.FO_TAB_FINAL_ROWS)
+        self.dest_capacity = fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_CAPACITY)
+        if w.grouped:
+            # buffers for any routing of the workload's tokens (fo_plan_route)
+            R, TN = w.n_dest, w.N // w.tile_n
+            self.final_rows = [max(f, len(range(d, w.n_tokens, R)) * w.top_k)
+                               for d, f in enumerate(self.final_rows)]
+            self.dest_capacity = [max(c, f * TN)
+                                  for c, f in zip(self.dest_capacity, self.final_rows)]
         self.s0 = torch.cuda.Stream(device=self.device)
         self.s1 = self.s0   # the consumer follows the GEMM on its stream
         self.epoch = 0
@@ -90,8 +98,9 @@ class Pipeline:
         flags = torch.zeros((self.P,), dtype=torch.int32, device=d)
         status = torch.zeros((1,), dtype=torch.int32, device=d)
         comm = [torch.empty((u * w.tile_n,), dtype=torch.int16, device=d)
-                for u in self.dest_units]
-        final = [torch.empty((r, w.N), dtype=torch.int16, device=d) for r in self.final_rows]
+                for u in self.dest_capacity]
+        # (zeroed: a routing need not fill every row of an All-to-All output)
+        final = [torch.zeros((r, w.N), dtype=torch.int16, device=d) for r in self.final_rows]
         return Buffers(A, B, partials, C_r, count, flags, status, comm, final)
 
     def close(self):
@@ -100,7 +109,8 @@ class Pipeline:
 
     def replan(self, partition):
         """Switch to another wave-group partition, keeping the data buffers
-        (their sizes do not depend on the partition)."""
+        (their sizes do not depend on the partition).  The new plan starts
+        from the routing the pipeline was built with."""
         torch.cuda.synchronize(self.device)
         fo.fo_plan_destroy(self.plan)
         self.partition = list(partition)
@@ -110,11 +120,27 @@ class Pipeline:
         self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
         self.P = len(self.partition)
-        assert fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS) == self.dest_units
+        assert all(u <= c for u, c in zip(fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS),
+                                          self.dest_capacity))
         d = self.device
         self.buf.count = torch.zeros((self.P,), dtype=torch.int32, device=d)
         self.buf.flags = torch.zeros((self.P,), dtype=torch.int32, device=d)
         self.buf.status.zero_()
+
+    def route(self, row_token, row_slot, stream=None):
+        """A new routing (device int32 tensors [M]) for the grouped workload:
+        fo_plan_route rebuilds the plan's routing tables on the device, in
+        stream order before the next step's GEMM."""
+        w, st = self.w, stream or self.s0
+        assert row_token.dtype == torch.int32 and row_token.numel() == w.M
+        assert row_slot.dtype == torch.int32 and row_slot.numel() == w.M
+        fo.fo_plan_route(self.plan, row_token.data_ptr(), row_slot.data_ptr(), w.n_tokens,
+                         w.top_k, self.buf.status.data_ptr(), st.cuda_stream)
+        self._routed = (row_token, row_slot)   # alive until the kernels have read them
+
+    def set_A(self, bits):
+        """Replace the routed activations A (uint16 bf16 bits, M x K)."""
+        self.buf.A.copy_(_dev_bf16(bits, self.device))
 
     # ------------------------------------------------------------ calls
     def gemm(self, stream, epoch, signal=True):
@@ -178,11 +204,14 @@ class Pipeline:
         torch.cuda.synchronize(self.device)
         b = self.buf
         w = self.w
+        # the units each destination holds now (after fo_plan_route: as the
+        # device tables say)
+        self.dest_units = fo.fo_plan_table(self.plan, fo.FO_TAB_DEST_UNITS)
         return dict(
             C_r=_bits(b.C_r).reshape(-1, w.tile_n),
             count=b.count.cpu().numpy().tolist(),
             flags=b.flags.cpu().numpy().view(np.uint32).tolist(),
             status=int(b.status.item()),
-            comm=[_bits(c).reshape(-1, w.tile_n) for c in b.comm],
+            comm=[_bits(c).reshape(-1, w.tile_n)[:u] for c, u in zip(b.comm, self.dest_units)],
             final=[_bits(f) for f in b.final],
         )

@@ -17,10 +17,14 @@ Workloads (the shapes of the pages' workloads; synthetic data, no weights):
   alltoall        16384 tokens x top-2 = 32768 routed rows over 8 experts,
                   N=14336 K=4096 (Mixtral-8x7B-shaped expert up-projection);
                   consumer: bucket rows by token mod 8 into 8 buffers
+  alltoall_dynamic  the same layer with a fixed capacity of 5120 rows per
+                  expert (1.25 x the mean load, a multiple of 128): the GEMM
+                  shape never changes, each step draws a new routing, and the
+                  rows an expert does not fill hold no token (token -1)
 
 Seeds: ``numpy.random.default_rng(1000 * index + stream)`` with stream 0 for
 A (or the token matrix X), 1 for B, 2 for the partial buffers and 9 for the
-routing.  Values are drawn in fp32 and rounded once to bf16 (round to
+routing (9 + step for the routing of step ``step`` of the dynamic workload).  Values are drawn in fp32 and rounded once to bf16 (round to
 nearest even, by torch's conversion).  Distributions: the worked example
 U[-1,1]; the others N(0,1)/sqrt(K) for A and B and N(0,1) for partials.
 """
@@ -54,6 +58,7 @@ class Workload:
     n_tokens: int = 0
     n_experts: int = 0
     top_k: int = 0
+    capacity: int = 0     # rows per expert (0: exactly the routed rows)
 
     @property
     def grouped(self):
@@ -75,6 +80,9 @@ WORKLOADS = {
     "alltoall": Workload("alltoall", 5, 32768, 14336, 4096,
                          layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
                          n_tokens=16384, n_experts=8, top_k=2),
+    "alltoall_dynamic": Workload("alltoall_dynamic", 6, 8 * 5120, 14336, 4096,
+                                 layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
+                                 n_tokens=16384, n_experts=8, top_k=2, capacity=5120),
 }
 
 
@@ -113,12 +121,28 @@ class Inputs:
     row_slot: np.ndarray = None   # grouped: top-k slot of each routed row
 
 
-def routing(w: Workload):
+def routing(w: Workload, step=0):
     """Top-k routing: every token draws n_experts i.i.d. U(0,1) keys and
     picks the experts with the k smallest keys (distinct), in key order; the
     first pick is slot 0.  Routed rows are sorted by (expert, token, slot).
-    Returns (expert_rows, row_token, row_slot)."""
-    rng = _rng(w, 9)
+    Returns (expert_rows, row_token, row_slot).
+
+    With a capacity, every expert has exactly ``capacity`` rows: its routed
+    rows in that order, those past the capacity dropped (the router's
+    capacity limit), then empty rows (token -1, slot 0)."""
+    if w.capacity:
+        er, tok, sl = routing(scaled(w, capacity=0), step)
+        T, S, r = [], [], 0
+        for m in er:
+            keep = min(m, w.capacity)
+            T.append(tok[r:r + keep])
+            S.append(sl[r:r + keep])
+            T.append(np.full(w.capacity - keep, -1, np.int32))
+            S.append(np.zeros(w.capacity - keep, np.int32))
+            r += m
+        return ([w.capacity] * w.n_experts, np.concatenate(T).astype(np.int32),
+                np.concatenate(S).astype(np.int32))
+    rng = _rng(w, 9 + step)
     keys = rng.random((w.n_tokens, w.n_experts))
     picks = np.argsort(keys, axis=1, kind="stable")[:, :w.top_k]
     tok = np.repeat(np.arange(w.n_tokens), w.top_k)
@@ -134,7 +158,7 @@ def make_inputs(w: Workload, with_partials=True) -> Inputs:
     if w.grouped:
         expert_rows, row_token, row_slot = routing(w)
         X = _draw(w, _rng(w, 0), (w.n_tokens, w.K), scale)
-        A = X[row_token]
+        A = gather_rows(X, row_token)
         rb = _rng(w, 1)
         B = [_draw(w, rb, (w.K, w.N), scale) for _ in range(w.n_experts)]
     else:
@@ -149,3 +173,17 @@ def make_inputs(w: Workload, with_partials=True) -> Inputs:
             x = rp.standard_normal(size=(units, w.tile_n), dtype=np.float32)
             partials.append(to_bf16_bits(x))
     return Inputs(A, B, partials, expert_rows, row_token, row_slot)
+
+
+def gather_rows(X, row_token):
+    """The dispatch gather that forms the routed A: row r is X[token(r)], an
+    empty row (token < 0) is zero."""
+    A = np.zeros((len(row_token), X.shape[1]), dtype=X.dtype)
+    valid = row_token >= 0
+    A[valid] = X[row_token[valid]]
+    return A
+
+
+def token_matrix(w: Workload):
+    """The grouped workload's token matrix X (n_tokens x K bf16 bits)."""
+    return _draw(w, _rng(w, 0), (w.n_tokens, w.K), 1.0 / math.sqrt(w.K))

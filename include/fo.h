@@ -95,7 +95,12 @@ typedef struct {
   int32_t n_dest;         /* ranks the layout routes to (RS: R, A2A: D) */
   int32_t n_experts;      /* 0 = plain GEMM; >= 1 = grouped GEMM */
   const int32_t* expert_rows; /* [n_experts] routed rows of each expert */
-  const int32_t* row_token;   /* [M] A2A: token id of each routed row */
+  const int32_t* row_token;   /* [M] A2A: token id of each routed row; a
+                                 negative id marks a row that holds no token
+                                 (expert capacity the routing left unfilled:
+                                 it is sent nowhere).  row_token and row_slot
+                                 may both be NULL: every row starts empty,
+                                 for a routing given by fo_plan_route */
   const int32_t* row_slot;    /* [M] A2A: top-k slot of each routed row */
   int32_t host_only;      /* 1: build host tables only (no device needed) */
 } fo_plan_desc;
@@ -131,12 +136,19 @@ typedef enum {
   FO_TAB_PART_LEN = 6,    /* [P * R] units of part (j, k) */
   FO_TAB_PART_DST = 7,    /* [P * R] offset (units) of part (j, k) in dst[k] */
   FO_TAB_DEST_UNITS = 8,  /* [R] units each destination buffer receives */
-  FO_TAB_FINAL_ROWS = 9   /* [R] rows of each output of fo_reorder_back
+  FO_TAB_FINAL_ROWS = 9,  /* [R] rows of each output of fo_reorder_back
                              (each row has N values) */
+  FO_TAB_DEST_CAPACITY = 10 /* [R] units a destination buffer must hold: A2A
+                             final_rows[k] * (N / tile_n), enough for any
+                             routing of the plan's tokens (see
+                             fo_plan_route); other layouts DEST_UNITS */
 } fo_table;               /* R = 1 for FO_LAYOUT_TILE, else n_dest */
 
 /* Copy table `which` into out[0 .. capacity); *length = its full length.
- * FO_ERR_ARG if capacity is too small (length is still set). */
+ * FO_ERR_ARG if capacity is too small (length is still set).  After
+ * fo_plan_route the routing-dependent tables (UNIT, PART_*, DEST_UNITS) live
+ * on the device: the first call afterwards synchronises the device and
+ * downloads them (FO_ERR_CUDA if that fails). */
 fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length);
 
@@ -278,6 +290,32 @@ fo_status fo_consume_group_noalloc(const fo_plan* plan, int32_t group,
                                    uint32_t epoch, uint64_t spin_limit_ns,
                                    int32_t* dev_status, void* cuda_stream);
 
+/* Dynamic routing ([P1] 二 (3): in an MoE layer tokens are routed to their
+ * experts at run time, and the mapping table has to follow that routing).
+ * The plan fixes the shape: n_experts experts of expert_rows[e] rows each
+ * (each expert's capacity), so the GEMM, its tiles, waves and groups never
+ * change.  This call takes a new assignment of tokens to those rows, in
+ * device memory, and rebuilds every routing-dependent table on the device
+ * (per-row destination, rank and output row; per-(tile, rank) bases; per-
+ * (group, rank) parts) with two kernels on `stream`, so the routing never
+ * goes through the host.  Later launches on the same stream use it.
+ *  row_token, row_slot: device int32[M] (4-byte aligned).  Row r of the
+ *      stacked expert rows holds token row_token[r], top-k slot row_slot[r];
+ *      row_token[r] < 0 marks an empty row (sent nowhere).
+ *  n_tokens, top_k: token ids lie in [0, n_tokens), slots in [0, top_k).
+ *      They size the outputs: rank d's output of fo_reorder_back has
+ *      ceil((n_tokens - d) / n_dest) * top_k rows (FO_TAB_FINAL_ROWS) and its
+ *      receive buffer FO_TAB_DEST_CAPACITY units; both tables follow at once.
+ *  dev_status: device int32.  A routing with a token or slot out of range,
+ *      or more rows for one rank than its capacity (a (token, slot) pair
+ *      given twice), sets it to FO_ERR_ARG and yields a plan that routes no
+ *      row: nothing is written out of bounds.
+ * Only for FO_LAYOUT_A2A_SUBTOKEN plans; FO_ERR_ARG otherwise.  Must not
+ * overlap in time with a launch that reads the plan's tables. */
+fo_status fo_plan_route(fo_plan* plan, const int32_t* row_token, const int32_t* row_slot,
+                        int32_t n_tokens, int32_t top_k, int32_t* dev_status,
+                        void* cuda_stream);
+
 /* Post-communication reorder ([P1] 二 "通信后重排"): for the groups
  * [group_begin, group_end), move every unit from where the consumer left it
  * to its place in the final row-major layout, by the inverse mapping table.
@@ -288,7 +326,8 @@ fo_status fo_consume_group_noalloc(const fo_plan* plan, int32_t group,
  *  RS_ROWBLOCK: src[k] -> dst[k], (M / R) x N, rows k M/R .. (k+1) M/R - 1.
  *  A2A:         src[d] -> dst[d]: the sub-token of routed row (token t,
  *               slot q) lands in row (t / D) * top_k + q of dst[d]
- *               (top_k = 1 + the largest row_slot).
+ *               (top_k = 1 + the largest row_slot, or fo_plan_route's);
+ *               empty rows move nowhere.
  * Stream-ordered after the consumer; no flags. */
 fo_status fo_reorder_back(const fo_plan* plan, int32_t group_begin,
                           int32_t group_end, const void* const* src,

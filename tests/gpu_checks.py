@@ -38,8 +38,18 @@ def gpu_gemm_output(pipe, res, op):
     for s in range(op.tiles):
         rows = op.tile_rows(s)
         r0, c0 = op.tile_row0(s), op.tile_col0(s)
-        C[r0:r0 + rows, c0:c0 + op.tile_n] = res["C_r"][op.unit[s, :rows]]
+        u = op.unit[s, :rows]
+        keep = u >= 0          # rows that hold no token are never stored
+        C[r0:r0 + rows, c0:c0 + op.tile_n][keep] = res["C_r"][u[keep]]
     return C
+
+
+def token_rows(w, inp):
+    """Rows of the stacked GEMM output that hold a token (all of them but
+    the empty capacity rows of an All-to-All routing)."""
+    if inp.row_token is None:
+        return np.ones(w.M, dtype=bool)
+    return np.asarray(inp.row_token) >= 0
 
 
 def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
@@ -54,18 +64,20 @@ def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
     assert res["status"] == 0
     # GEMM (C recovered through the oracle's map of the GPU's C_r)
     C_gpu = gpu_gemm_output(pipe, res, op)
+    stored = token_rows(w, inp)
     if full_gemm:
         C_ref = OG.grouped_gemm_bf16(inp.A, inp.B, inp.expert_rows)
-        frob, ok = gemm_close(C_gpu, C_ref)
+        frob, ok = gemm_close(C_gpu[stored], C_ref[stored])
     else:
         rows = np.asarray(gemm_rows)
+        rows = rows[stored[rows]]
         C_ref = OG.gemm_rows_bf16(inp.A, inp.B, inp.expert_rows, rows)
         frob, ok = gemm_close(C_gpu[rows], C_ref)
     out["gemm_frob"] = frob
     assert frob <= FROB_TOL and ok, f"GEMM off: frob {frob}"
     # pre-comm reorder of the GPU's own output: bit-exact
     C_r_ref = OC.pre_reorder(op, C_gpu)
-    assert np.array_equal(res["C_r"], C_r_ref)
+    assert np.array_equal(res["C_r"][:op.n_units], C_r_ref)
     # consumer, from the GPU's own C_r: bit-exact
     if w.consumer == W.CONS_COPY:
         comm = [OC.consume_copy(op, C_r_ref)]
@@ -84,7 +96,7 @@ def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
     elif w.layout in (W.LAYOUT_RS_SUBTILE, W.LAYOUT_RS_ROWBLOCK):
         final = OC.reorder_back_rs(op, comm)
     else:
-        final = OC.reorder_back_a2a(op, comm, w.top_k)
+        final = OC.reorder_back_a2a(op, comm, w.top_k, n_tokens=w.n_tokens)
     for k, (g, r) in enumerate(zip(res["final"], final)):
         assert np.array_equal(g, r), f"final buffer {k} differs"
     if w.layout == W.LAYOUT_TILE and w.consumer == W.CONS_COPY:

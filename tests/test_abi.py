@@ -47,7 +47,10 @@ def test_status_strings():
     dict(group_waves=(1, 2)),          # does not sum to T = 4
     dict(group_waves=(0, 4)),          # empty group
     dict(layout=fo.FO_LAYOUT_RS_SUBTILE, n_dest=3),   # R does not divide 128
-    dict(layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=8), # no routing given
+    dict(layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=8,  # a routed row without a slot
+         row_token=[0] * 256, row_slot=[-1] * 256),
+    dict(layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=2,  # (token 0, slot 0) twice: rank
+         row_token=[0, 0] + [-1] * 254, row_slot=[0] * 256),  # 0 outgrows its buffer
     dict(wave_width=0),                # host-only plan needs an explicit W
 ])
 def test_bad_descriptions_are_rejected(bad):
@@ -72,5 +75,24 @@ def test_host_only_plan_refuses_launches():
             fo.fo_reorder_back(plan, 0, 3, [16], [16], 0)
         with pytest.raises(fo.FoError):
             fo.fo_consume_group(plan, -1, fo.FO_CONS_COPY, 16, [], [16], 16, 1, 0, 16, 0)
+    finally:
+        fo.fo_plan_destroy(plan)
+
+
+def test_a2a_plan_without_routing_starts_empty():
+    """An All-to-All plan given no routing has every row empty: no units, no
+    output rows; fo_plan_route fills it later (it needs a device plan)."""
+    d = fo.make_desc(M=300, N=512, K=64, tile_n=256, swizzle=2, wave_width=3,
+                     group_waves=(1, 1), layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=4,
+                     expert_rows=[200, 100], host_only=True)
+    plan = fo.fo_plan_groups(d)
+    try:
+        assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_UNITS) == [0] * 4
+        assert fo.fo_plan_table(plan, fo.FO_TAB_FINAL_ROWS) == [0] * 4
+        assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_CAPACITY) == [0] * 4
+        assert set(fo.fo_plan_table(plan, fo.FO_TAB_UNIT)) == {-1}
+        with pytest.raises(fo.FoError) as e:   # host-only: nothing on a device to route
+            fo.fo_plan_route(plan, 16, 16, 10, 2, 16, 0)
+        assert e.value.status == fo.FO_ERR_ARG
     finally:
         fo.fo_plan_destroy(plan)

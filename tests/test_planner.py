@@ -41,6 +41,13 @@ def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
             assert fo.fo_plan_table(plan, which) == ref.reshape(-1).tolist()
         assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_UNITS) == \
             [OP.dest_rows(op, k) for k in range(op.part_start.shape[1])]
+        if layout == fo.FO_LAYOUT_A2A_SUBTOKEN:
+            # output rows: every slot of every token of the rank
+            n_tok, k = int(tok.max()) + 1, int(sl[tok >= 0].max()) + 1
+            fr = fo.fo_plan_table(plan, fo.FO_TAB_FINAL_ROWS)
+            assert fr == [len(range(d, n_tok, R)) * k for d in range(R)]
+            assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_CAPACITY) == \
+                [f * (N // tile_n) for f in fr]
     finally:
         fo.fo_plan_destroy(plan)
 
@@ -80,6 +87,25 @@ def test_ragged_a2a_tables():
     order = np.lexsort((sl, tok, ex))
     er = np.bincount(ex, minlength=E).tolist()
     _compare(er, 512, 64, 128, 3, 7, fo.FO_LAYOUT_A2A_SUBTOKEN, D, tok[order], sl[order])
+
+
+@pytest.mark.parametrize("capacity", [384, 300, 200])
+def test_capacity_padded_a2a_tables(capacity):
+    """Experts of a fixed capacity: rows the routing leaves empty (token -1)
+    get no unit; at 200 rows some routed rows are dropped, at 300 the
+    capacity is not a multiple of 128."""
+    w = W.scaled(W.WORKLOADS["alltoall_dynamic"], M=5 * capacity, N=768, K=64,
+                 n_tokens=700, n_experts=5, capacity=capacity, wave_width=7, swizzle=3)
+    er, tok, sl = W.routing(w, step=2)
+    routed = (tok >= 0).sum()
+    assert (routed < 700 * 2) if capacity == 200 else (routed == 700 * 2 and (tok < 0).any())
+    _compare(er, w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest, tok, sl)
+
+
+def test_alltoall_dynamic_workload_tables():
+    w = W.WORKLOADS["alltoall_dynamic"]
+    er, tok, sl = W.routing(w)
+    _compare(er, w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest, tok, sl)
 
 
 @pytest.mark.parametrize("tm,tn,S,Wd", [(3, 5, 2, 4), (4, 4, 8, 3), (5, 3, 3, 7)])
