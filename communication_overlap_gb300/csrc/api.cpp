@@ -63,6 +63,14 @@ fo_status fo_plan_table(const fo_plan* p, int32_t which, int32_t* out,
     case FO_TAB_DEST_UNITS: v = &p->dest_units; break;
     case FO_TAB_FINAL_ROWS: v = &p->final_rows; break;
     case FO_TAB_DEST_CAPACITY: v = &p->dest_capacity; break;
+    case FO_TAB_SLOT_LIVE:
+      if (p->layout != FO_LAYOUT_A2A_SUBTOKEN) {
+        unit.assign(p->tiles, 1);
+        v = &unit;
+      } else {
+        v = &p->slot_live;
+      }
+      break;
     case FO_TAB_UNIT:
       unit.resize(size_t(p->tiles) * p->tile_m);
       for (int32_t s = 0; s < p->tiles; ++s)

@@ -44,6 +44,8 @@ struct DeviceTables {
   int32_t* row_rank = nullptr;         // [M] A2A: index among the rows of its
                                        //   tile row that go to the same rank
   int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
+  int32_t* slot_live = nullptr;        // [tiles] A2A: 1 if a row of the tile holds
+                                       //   a token (else the GEMM skips it)
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
   int32_t* rwork = nullptr;            // [2P + 1] scratch of the fused consumer+reorder
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
@@ -65,7 +67,7 @@ struct fo_plan {
   std::vector<int32_t> slot_tile, tile_slot, slot_group;
   std::vector<fo::TileInfo> tile;
   std::vector<int32_t> part_start, part_len, part_dst, dest_units, final_rows, dest_capacity;
-  std::vector<int32_t> dest_base, row_dest, row_rank, final_row;
+  std::vector<int32_t> dest_base, row_dest, row_rank, final_row, slot_live;
   int32_t route_blocks = 0;       // A2A: tile-row blocks (ceil(rows / 128) per expert)
   // fo_plan_route rebuilt the routing tables on the device: the host copies
   // above are stale until refresh_routing() downloads them

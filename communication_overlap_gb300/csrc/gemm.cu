@@ -76,6 +76,7 @@ struct GemmArgs {
   const int32_t* dest_base;
   const int32_t* row_dest;
   const int32_t* row_rank;
+  const int32_t* slot_live;  // A2A: [tiles] 0 = no row of the tile holds a token
   uint16_t* c_r;
   int32_t* count;
   uint32_t* flags;
@@ -260,6 +261,17 @@ __device__ __forceinline__ int32_t row_unit(const GemmArgs& a, const TileInfo& t
   return ti.unit_base + r;
 }
 
+// A tile none of whose rows holds a token (All-to-All capacity the routing
+// left empty) has no output: its loads and MMAs are skipped and the tile is
+// only counted.  A pair computes its two tiles with one MMA, so it skips only
+// when both are empty (slots 2i and 2i+1; the partner is slot ^ 1).
+template <bool PAIR>
+__device__ __forceinline__ bool tile_skipped(const GemmArgs& a, int32_t slot) {
+  if (a.slot_live == nullptr) return false;
+  if (PAIR) return (a.slot_live[slot] | a.slot_live[slot ^ 1]) == 0;
+  return a.slot_live[slot] == 0;
+}
+
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     signaled_gemm_kernel(const __grid_constant__ GemmArgs a) {
@@ -341,6 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const CUtensorMap* mb = &a.tmap_b[ti.expert];
         if (slot == int32_t(blockIdx.x))
           for (int e = 0; e <= ti.expert; ++e) prefetch_tmap(&a.tmap_b[e]);
+        if (tile_skipped<PAIR>(a, slot)) continue;
         for (int kb = 0; kb < a.k_blocks; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -395,6 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int32_t slot = blockIdx.x; slot < a.tiles && ok; slot += gridDim.x) {
+        if (tile_skipped<PAIR>(a, slot)) continue;
         if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
@@ -448,6 +462,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     for (int32_t slot = blockIdx.x; slot < a.tiles; slot += gridDim.x) {
       const TileInfo ti = a.tile[slot];
+      if (tile_skipped<PAIR>(a, slot)) {
+        // nothing computed, nothing stored: only counted (and signalled)
+        if (warp == 2 && lane == 0) {
+          if (a.count != nullptr) {
+            const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
+            if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
+          }
+          if (a.trace != nullptr) a.trace[slot] = globaltimer_ns();
+        }
+        __syncwarp();
+        continue;
+      }
       const int32_t my_unit = row_unit(a, ti, slot, q * 32 + lane);
       // one lane waits, the decision is warp-uniform (tcgen05.ld is .aligned)
       int ok = 0;
@@ -656,6 +682,7 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.dest_base = p->dev.dest_base;
   a.row_dest = p->dev.row_dest;
   a.row_rank = p->dev.row_rank;
+  a.slot_live = p->layout == FO_LAYOUT_A2A_SUBTOKEN ? p->dev.slot_live : nullptr;
   a.c_r = static_cast<uint16_t*>(C_r);
   a.count = count;
   a.flags = flags;

@@ -244,6 +244,9 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
     }
     p->group_unit_begin[P] = u;
     p->n_units = u;
+    p->slot_live.assign(tiles, 0);
+    for (int32_t s = 0; s < tiles; ++s)
+      for (int k = 0; k < R; ++k) p->slot_live[s] |= tile_cnt[size_t(s) * R + k] > 0;
   } else if (layout == FO_LAYOUT_RS_SUBTILE) {
     const int32_t h = kTileM / R;
     for (int j = 0; j < P; ++j) {
@@ -389,6 +392,7 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_rd = put(buf, p->row_dest);
   const size_t o_rr = put(buf, p->row_rank);
   const size_t o_fr = put(buf, p->final_row);
+  const size_t o_sl = put(buf, p->slot_live);
   const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
   const size_t o_rwork = put(buf, std::vector<int32_t>(2 * p->P + 1, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
@@ -418,6 +422,7 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.row_dest = reinterpret_cast<int32_t*>(b + o_rd);
   p->dev.row_rank = reinterpret_cast<int32_t*>(b + o_rr);
   p->dev.final_row = reinterpret_cast<int32_t*>(b + o_fr);
+  p->dev.slot_live = reinterpret_cast<int32_t*>(b + o_sl);
   p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
   p->dev.rwork = reinterpret_cast<int32_t*>(b + o_rwork);
   p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
@@ -438,7 +443,8 @@ fo_status refresh_routing(fo_plan* p) {
   if (!get(p->part_start, p->dev.part_start) || !get(p->part_len, p->dev.part_len) ||
       !get(p->part_dst, p->dev.part_dst) || !get(p->group_unit_begin, p->dev.group_unit_begin) ||
       !get(p->dest_base, p->dev.dest_base) || !get(p->row_dest, p->dev.row_dest) ||
-      !get(p->row_rank, p->dev.row_rank) || !get(p->final_row, p->dev.final_row))
+      !get(p->row_rank, p->dev.row_rank) || !get(p->final_row, p->dev.final_row) ||
+      !get(p->slot_live, p->dev.slot_live))
     return FO_ERR_CUDA;
   for (int k = 0; k < p->R; ++k) {
     int32_t off = 0;

@@ -34,7 +34,9 @@
 //                 part_len[j][d]      = E(gsb[j + 1], d) - E(gsb[j], d)
 //                 part_start[j][d]    = group_unit_begin[j] + sum_{d' < d} part_len[j][d']
 //                 dest_base[s][d]     = part_start[j][d] + E(s, d) - E(gsb[j], d)
-//               CTA 0 writes the per-group tables, all CTAs the per-slot one.
+//               CTA 0 writes the per-group tables, all CTAs the per-slot ones
+//               (dest_base, and whether any row of the tile holds a token:
+//               the GEMM skips tiles that hold none).
 //
 // An invalid routing (token >= n_tokens, slot outside [0, top_k), or more
 // units for a rank than its receive buffer holds) routes nothing: every row
@@ -66,6 +68,7 @@ struct RouteArgs {
   int32_t* part_dst;          // [P * R]
   int32_t* group_unit_begin;  // [P + 1]
   int32_t* dest_base;         // [tiles * R]
+  int32_t* slot_live;         // [tiles] 1 if a row of the tile holds a token
   int32_t* status;            // caller's status word
   int32_t expert_row0[kMaxExperts];
   int32_t expert_rows[kMaxExperts];
@@ -225,11 +228,15 @@ __global__ void __launch_bounds__(kPartsThreads) route_parts_kernel(const __grid
     const int32_t s = i / R;
     const int d = i - s * R;
     int32_t v = 0;
-    if (!bad) {
-      const TileInfo& ti = a.tile[s];
-      v = off[ti.group * R + d] + units_before(a, BP, ti.row0, ti.col0, ti.expert, d);
-    }
+    const TileInfo& ti = a.tile[s];
+    if (!bad) v = off[ti.group * R + d] + units_before(a, BP, ti.row0, ti.col0, ti.expert, d);
     a.dest_base[i] = v;
+    if (d == 0) {   // the tile's rows that hold a token: its block's count
+      const int32_t b = a.expert_block0[ti.expert] + (ti.row0 - a.expert_row0[ti.expert]) / kTileM;
+      int32_t n = 0;
+      for (int dd = 0; dd < R; ++dd) n += BP[(b + 1) * R + dd] - BP[b * R + dd];
+      a.slot_live[s] = (!bad && n > 0) ? 1 : 0;
+    }
   }
   if (bad)
     for (int32_t r = first; r < a.M; r += stride) {
@@ -280,6 +287,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
   a.part_dst = p->dev.part_dst;
   a.group_unit_begin = p->dev.group_unit_begin;
   a.dest_base = p->dev.dest_base;
+  a.slot_live = p->dev.slot_live;
   a.status = dev_status;
   const int E = int(p->expert_rows.size());
   int32_t blocks = 0;

@@ -20,7 +20,7 @@ FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
 FO_ACT_NONE, FO_ACT_RELU, FO_ACT_SILU = range(3)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
- FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY) = range(11)
+ FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY, FO_TAB_SLOT_LIVE) = range(12)
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p

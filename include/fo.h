@@ -138,10 +138,14 @@ typedef enum {
   FO_TAB_DEST_UNITS = 8,  /* [R] units each destination buffer receives */
   FO_TAB_FINAL_ROWS = 9,  /* [R] rows of each output of fo_reorder_back
                              (each row has N values) */
-  FO_TAB_DEST_CAPACITY = 10 /* [R] units a destination buffer must hold: A2A
+  FO_TAB_DEST_CAPACITY = 10, /* [R] units a destination buffer must hold: A2A
                              final_rows[k] * (N / tile_n), enough for any
                              routing of the plan's tokens (see
                              fo_plan_route); other layouts DEST_UNITS */
+  FO_TAB_SLOT_LIVE = 11   /* [tiles] 1 if a row of the tile at slot s holds a
+                             token.  A2A only can have 0s: the GEMM skips
+                             such a tile's loads and MMAs (both tiles of a
+                             CTA pair must be empty) and only counts it */
 } fo_table;               /* R = 1 for FO_LAYOUT_TILE, else n_dest */
 
 /* Copy table `which` into out[0 .. capacity); *length = its full length.

@@ -23,7 +23,8 @@ from gpu_checks import check_run, oracle_plan
 pytestmark = pytest.mark.gpu
 
 _TABLES = (fo.FO_TAB_UNIT, fo.FO_TAB_PART_START, fo.FO_TAB_PART_LEN, fo.FO_TAB_PART_DST,
-           fo.FO_TAB_DEST_UNITS, fo.FO_TAB_FINAL_ROWS, fo.FO_TAB_DEST_CAPACITY)
+           fo.FO_TAB_DEST_UNITS, fo.FO_TAB_FINAL_ROWS, fo.FO_TAB_DEST_CAPACITY,
+           fo.FO_TAB_SLOT_LIVE)
 
 
 def _small(capacity=384, **kw):
@@ -151,6 +152,7 @@ def test_invalid_routing_routes_nothing(bad):
         assert res["status"] == fo.FO_ERR_ARG
         assert pipe.dest_units == [0] * w.n_dest
         assert set(fo.fo_plan_table(pipe.plan, fo.FO_TAB_UNIT)) == {-1}
+        assert set(fo.fo_plan_table(pipe.plan, fo.FO_TAB_SLOT_LIVE)) == {0}   # GEMM skips all
         assert res["count"] == pipe.group_tiles      # the GEMM still signals every group
         # recovery
         pipe.buf.status.zero_()
@@ -180,5 +182,32 @@ def test_full_size_dynamic_alltoall():
             res = pipe.results()
             rows = np.sort(rng.choice(w.M, size=512, replace=False))
             check_run(pipe, inp, res, gemm_rows=rows, full_gemm=False)
+    finally:
+        pipe.close()
+
+
+@pytest.mark.parametrize("variant", [fo.FO_GEMM_SINGLE, fo.FO_GEMM_PAIRS])
+def test_empty_tiles_are_skipped_but_counted(variant):
+    """Capacity far above the load leaves whole tiles empty: the GEMM skips
+    their mainloop (single CTAs: each empty tile; pairs: both tiles of a pair
+    empty), still counts them, and every output matches the oracle."""
+    w = _small(768, M=5 * 768, wave_width=8, swizzle=4)
+    base = W.make_inputs(w)
+    pipe = Pipeline(w, base, gemm_variant=variant)
+    try:
+        live = fo.fo_plan_table(pipe.plan, fo.FO_TAB_SLOT_LIVE)
+        assert 0 in live and 1 in live
+        if variant == fo.FO_GEMM_PAIRS:
+            assert pipe.pairable
+        for step in (1, 2):
+            inp = _inputs_for_step(w, base, step)
+            pipe.set_A(inp.A)
+            for f in pipe.buf.final:
+                f.zero_()
+            _route(pipe, inp)
+            pipe.step()
+            res = pipe.results()
+            assert res["count"] == pipe.group_tiles
+            check_run(pipe, inp, res)
     finally:
         pipe.close()

@@ -41,6 +41,8 @@ def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
             assert fo.fo_plan_table(plan, which) == ref.reshape(-1).tolist()
         assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_UNITS) == \
             [OP.dest_rows(op, k) for k in range(op.part_start.shape[1])]
+        live = fo.fo_plan_table(plan, fo.FO_TAB_SLOT_LIVE)
+        assert live == (op.unit >= 0).any(axis=1).astype(int).tolist()
         if layout == fo.FO_LAYOUT_A2A_SUBTOKEN:
             # output rows: every slot of every token of the rank
             n_tok, k = int(tok.max()) + 1, int(sl[tok >= 0].max()) + 1
