@@ -235,27 +235,34 @@ __device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, uin
   }
 }
 
-// One tile's rows from the communication buffers to the final layout: warp
-// w takes every 8th row group; each lane keeps kBatch independent 16-byte
-// loads in flight before its stores.
+// Rows of one reorder work item: every lane of the CTA has kBatch
+// independent 16-byte loads in flight, all issued before the stores, so an
+// item costs one memory round trip.  Items are smaller than a tile (a
+// quarter at tile_n = 256) so that the last group's reorder, which runs
+// after the GEMM has finished, spreads over more CTAs.
 template <int VPU>
-__device__ __forceinline__ void reorder_tile_regs(const FusedArgs& a, uint4* const* src,
-                                                  uint4* const* fin, int32_t s, int tid) {
+constexpr int kItemRows = (kThreads / 32) * (32 / VPU) * 4;
+
+// Rows r0 .. r0 + kItemRows of the tile at slot s from the communication
+// buffers to the final layout: warp w takes row groups w, w + 8, ...
+template <int VPU>
+__device__ __forceinline__ void reorder_rows_regs(const FusedArgs& a, uint4* const* src,
+                                                  uint4* const* fin, int32_t s, int32_t r0,
+                                                  int tid) {
   constexpr int kRowsPerInstr = 32 / VPU;
   constexpr int kWarps = kThreads / 32;
-  constexpr int kBatch = 4;   // loads per lane per round (kept small: this kernel
-                              // shares its register budget with the consumer)
-  constexpr int kRounds = kTileM / kWarps / kRowsPerInstr / kBatch;
+  constexpr int kBatch = 4;   // loads per lane (kept small: this kernel shares
+                              // its register budget with the consumer)
+  static_assert(kItemRows<VPU> == kWarps * kRowsPerInstr * kBatch, "one round per item");
   const int warp = tid / 32, lane = tid % 32, sub = lane / VPU, vl = lane % VPU;
   const TileInfo ti = a.map.tile[s];
-#pragma unroll 1
-  for (int round = 0; round < kRounds; ++round) {
+  {
     uint4 x[kBatch];
     int64_t to[kBatch];
     int kk[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      const int32_t r = ((round * kBatch + i) * kWarps + warp) * kRowsPerInstr + sub;
+      const int32_t r = r0 + (i * kWarps + warp) * kRowsPerInstr + sub;
       kk[i] = -1;
       if (r < ti.rows) {
         int32_t su, dr;
@@ -306,14 +313,17 @@ __global__ void __launch_bounds__(kThreads, 3)
       ok = false;
       return;
     }
-    const int32_t s0 = a.group_slot_begin[j], n = a.group_slot_begin[j + 1] - s0;
+    constexpr int kItems = kTileM / kItemRows<VPU>;   // work items per tile
+    const int32_t s0 = a.group_slot_begin[j];
+    const int32_t n = (a.group_slot_begin[j + 1] - s0) * kItems;
     if (tid == 0) s_chunk[0] = atomicAdd(a.rwork + j, 1);
     __syncthreads();
     for (int buf = 0;; buf ^= 1) {
       const int32_t t = s_chunk[buf];
       if (t >= n) break;
       if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(a.rwork + j, 1);
-      reorder_tile_regs<VPU>(a, s_dst, s_fin, s0 + t, tid);
+      reorder_rows_regs<VPU>(a, s_dst, s_fin, s0 + t / kItems, (t % kItems) * kItemRows<VPU>,
+                             tid);
       __syncthreads();
     }
     __syncthreads();
@@ -425,8 +435,15 @@ int log2_exact(int v) {
   return s;
 }
 
-int default_ctas(const fo_plan* p, int requested) {
-  return requested > 0 ? requested : 4 * p->sm_count;
+// Default grids, measured on GB300 beside the signaled GEMM (step time over
+// 1, 2, 3 and 4 CTAs per SM): the sums are bandwidth-bound with two loads
+// per source in flight and want 4 CTAs per SM; the copy and bucket
+// consumers keep 8 loads in flight per thread and interfere least with the
+// GEMM at 1 per SM; the fused consumer+reorder does best at 3 per SM.
+int default_ctas(const fo_plan* p, int requested, int kind, bool fused) {
+  if (requested > 0) return requested;
+  if (fused) return 3 * p->sm_count;
+  return (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? 4 * p->sm_count : p->sm_count;
 }
 
 // The consumer is launched as a programmatic dependent (when `overlap`):
@@ -489,7 +506,7 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
   a.trace = p->consumer_trace;
-  const int ctas = default_ctas(p, p->consumer_ctas);
+  const int ctas = default_ctas(p, p->consumer_ctas, kind, false);
   const bool ov = p->overlap != 0;
   const int dv = p->device;
   switch (kind) {
@@ -537,7 +554,7 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
   a.rwork = p->dev.rwork;
   a.act = act;
   a.row_vec = p->N / 8;
-  const int ctas = default_ctas(p, p->consumer_ctas);
+  const int ctas = default_ctas(p, p->consumer_ctas, kind, true);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool ov = p->overlap != 0;
   return p->tile_n == 256 ? launch_fused_vpu<32>(kind, a, ctas, ov, p->device, st)
@@ -653,7 +670,7 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.chunk_units = chunk_units_of(kind, p->tile_n);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
-  const int ctas = default_ctas(p, p->consumer_ctas);
+  const int ctas = default_ctas(p, p->consumer_ctas, kind, false);
   const bool ov = p->overlap != 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   switch (kind) {

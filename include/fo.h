@@ -157,8 +157,9 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length);
 
 /* Launch settings of the consumer and reorder kernels.
- *  consumer_ctas, reorder_ctas: grid sizes (<= 0: the defaults, 4 consumer
- *      and 3 reorder CTAs per SM).
+ *  consumer_ctas, reorder_ctas: grid sizes (<= 0: the defaults, measured
+ *      beside the GEMM: consumer 4 CTAs per SM for SUM / RS, 1 per SM for
+ *      COPY / A2A, 3 per SM for fo_consume_reorder; reorder 3 per SM).
  *  overlap: non-zero (default) launches the consumer as a programmatic
  *      dependent launch: issued on the GEMM's stream right after
  *      fo_signaled_gemm, it starts as soon as every GEMM CTA is resident and
