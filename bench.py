@@ -412,6 +412,13 @@ def run_ours(args):
         pipe.consume(s, pipe.epoch)
     t_cons_only = timed(torch, s, cons_only, args.steps, flush)
     t_reo = timed(torch, s, lambda: pipe.reorder(s), args.steps, flush)
+    # the consumer's bandwidth with a full grid (4 CTAs per SM): its roofline
+    # figure; the step uses the library's default grid for running beside the
+    # GEMM, which for copies is smaller and slower alone
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    fo.fo_plan_set_launch(pipe.plan, 4 * sm_count, args.reorder_ctas, False)
+    t_cons_full = timed(torch, s, cons_only, args.steps, flush)
+    fo.fo_plan_set_launch(pipe.plan, args.consumer_ctas, args.reorder_ctas, False)
     pipe.set_overlap(True)
 
     # in-kernel GEMM duration (per-tile stamps) alone and inside the step
@@ -540,6 +547,8 @@ def run_ours(args):
                 "ms_consumer_alone": statistics.mean(t_cons_only),
                 "ms_reorder_alone": statistics.mean(t_reo),
                 "consumer_gbs": cons_bytes / (statistics.mean(t_cons_only) * 1e-3) / 1e9,
+                "ms_consumer_alone_full_grid": statistics.mean(t_cons_full),
+                "consumer_gbs_full_grid": cons_bytes / (statistics.mean(t_cons_full) * 1e-3) / 1e9,
                 "reorder_gbs": reo_bytes / (statistics.mean(t_reo) * 1e-3) / 1e9,
                 "hbm_peak_gbs": hbm,
                 "gemm_in_kernel_ms_alone": statistics.median(span_alone),

@@ -39,6 +39,8 @@ struct ConsumeArgs {
   const int32_t* part_len;
   const int32_t* part_dst;
   int32_t* work;   // [P] chunk counters, then one "CTAs done" counter
+  int32_t* finished;   // [P] chunks finished per group (NULL: no consumed flags)
+  uint32_t* consumed;  // [P] = epoch once every chunk of the group is written
   int32_t g0, g1, n_partials, R, P, vpu_shift, chunk_units;
   uint32_t epoch;
   uint64_t limit_ns;
@@ -137,6 +139,11 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
 // The chunk counters clean up after themselves: the last CTA to finish
 // (counted on work[P]) zeroes them, so the next launch needs no memset and
 // can follow the GEMM directly as a programmatic dependent launch.
+//
+// Each finished chunk is counted per group; the CTA that finishes a group's
+// last chunk publishes consumed[j] = epoch (release, after every chunk's
+// stores), which a post-communication reorder launched as this kernel's
+// programmatic dependent waits for before it moves the group.
 template <int KIND, int U>
 __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant__ ConsumeArgs a) {
   __shared__ int s_ok;
@@ -144,6 +151,9 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
   __shared__ int32_t s_ps[kMaxDest], s_pl[kMaxDest], s_pd[kMaxDest];
   __shared__ uint4* s_dst[kMaxDest];
   const int tid = threadIdx.x;
+  // every CTA of this grid is resident from here on: a dependent reorder may
+  // start (its CTAs can then never hold resources this grid still needs)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid < kMaxDest) s_dst[tid] = a.dst[tid];
   uint64_t t_start = 0;
   int32_t chunks_done = 0;
@@ -162,6 +172,9 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
     }
     const int32_t ub = a.group_unit_begin[j], ue = a.group_unit_begin[j + 1];
     const int32_t n_chunks = (ue - ub + a.chunk_units - 1) / a.chunk_units;
+    if (n_chunks == 0 && a.finished != nullptr && tid == 0)
+      st_release_gpu(a.consumed + j, a.epoch);   // an empty group is consumed at once
+    int32_t group_chunks = 0;
     if (tid == 0) s_chunk[0] = atomicAdd(a.work + j, 1);
     __syncthreads();
     for (int buf = 0;; buf ^= 1) {
@@ -173,6 +186,7 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
       consume_range<KIND, U>(a, s_ps, s_pl, s_pd, s_dst, u0 << a.vpu_shift,
                              u1 << a.vpu_shift, tid);
       __syncthreads();
+      ++group_chunks;
       if (a.trace != nullptr && tid == 0) {
         // the latest chunk end of the group is when it is fully consumed
         atomicMax(reinterpret_cast<unsigned long long*>(a.trace + j),
@@ -181,6 +195,14 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
       }
     }
     __syncthreads();
+    if (a.finished != nullptr && tid == 0 && group_chunks > 0) {
+      // this CTA's stores for the group (all threads, ordered by the
+      // barrier) are visible before its chunks are counted, once per group;
+      // the CTA that completes the count releases the group
+      __threadfence();
+      if (atomicAdd(a.finished + j, group_chunks) + group_chunks == n_chunks)
+        st_release_gpu(a.consumed + j, a.epoch);
+    }
   }
   if (a.trace != nullptr) {
     if (tid == 0) {
@@ -199,7 +221,10 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.work + a.P, 1) == int32_t(gridDim.x) - 1) {
-      for (int j = a.g0; j < a.g1; ++j) atomicExch(a.work + j, 0);
+      for (int j = a.g0; j < a.g1; ++j) {
+        atomicExch(a.work + j, 0);
+        if (a.finished != nullptr) atomicExch(a.finished + j, 0);
+      }
       atomicExch(a.work + a.P, 0);
     }
   }
@@ -423,6 +448,19 @@ fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int 
   return FO_ERR_ARG;
 }
 
+// With overlap on, the consumer publishes each group's completion (per-group
+// finished-chunk counters, then consumed[j] = epoch) for a reorder launched
+// as its programmatic dependent.  Serially the reorder follows in stream
+// order and nothing is published (the counting costs a fence per CTA and
+// group).
+void publish_consumed(const fo_plan* p, ConsumeArgs& a, int32_t* finished, uint32_t epoch) {
+  const bool on = p->overlap != 0;
+  a.finished = on ? finished : nullptr;
+  a.consumed = on ? p->dev.consumed : nullptr;
+  p->consume_epoch = epoch;
+  p->consume_published = on;
+}
+
 int chunk_units_of(int kind, int tile_n) {
   const int bytes = (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? kChunkBytes<FO_CONS_SUM>
                                                                  : kChunkBytes<FO_CONS_COPY>;
@@ -496,6 +534,7 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.part_len = p->dev.part_len;
   a.part_dst = p->dev.part_dst;
   a.work = p->dev.work;
+  publish_consumed(p, a, p->dev.finished, epoch);
   a.g0 = g0;
   a.g1 = g1;
   a.P = p->P;
@@ -577,10 +616,10 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
 // allocates nothing.  The plan's tables and every buffer are still the
 // caller's, created beforehand.
 
-// The shared scratch: chunk counters of up to FO_NOALLOC_MAX_GROUPS groups
-// plus the "CTAs done" counter.  Every GPU that loads the library holds it
-// (16 KB) until the process exits.
-static __device__ __align__(256) int32_t fo_noalloc_scratch[FO_NOALLOC_MAX_GROUPS + 1];
+// The shared scratch: chunk counters of up to FO_NOALLOC_MAX_GROUPS groups,
+// the "CTAs done" counter, then the finished-chunk counters of the groups.
+// Every GPU that loads the library holds it (32 KB) until the process exits.
+static __device__ __align__(256) int32_t fo_noalloc_scratch[2 * FO_NOALLOC_MAX_GROUPS + 1];
 
 namespace fo {
 namespace {
@@ -661,6 +700,8 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.part_len = p->dev.part_len;
   a.part_dst = p->dev.part_dst;
   a.work = scratch;
+  // consumed flags in the plan (allocated when it was built), counters here
+  publish_consumed(p, a, scratch + FO_NOALLOC_MAX_GROUPS + 1, epoch);
   a.g0 = group < 0 ? 0 : group;
   a.g1 = group < 0 ? p->P : group + 1;
   a.P = p->P;

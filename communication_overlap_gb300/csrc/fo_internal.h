@@ -47,6 +47,12 @@ struct DeviceTables {
   int32_t* slot_live = nullptr;        // [tiles] A2A: 1 if a row of the tile holds
                                        //   a token (else the GEMM skips it)
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
+  int32_t* finished = nullptr;         // [P] scratch: chunks the consumer finished
+  uint32_t* consumed = nullptr;        // [P] epoch of the last consume that
+                                       //   finished each group (read by the
+                                       //   overlapped reorder)
+  int32_t* rtile = nullptr;            // [2] scratch of the reorder: tile counter,
+                                       //   CTAs done
   int32_t* rwork = nullptr;            // [2P + 1] scratch of the fused consumer+reorder
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
   int32_t* route_cnt = nullptr;        // [blocks * (R + 1)] A2A scratch of
@@ -77,6 +83,10 @@ struct fo_plan {
   int sm_count = 0;
   int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
   int gemm_variant = 0;   // fo_gemm_variant
+  // epoch of the last consume launched on this plan: a reorder launched as
+  // its programmatic dependent waits until each group is consumed at it
+  mutable uint32_t consume_epoch = 0;
+  mutable bool consume_published = false;   // that consume published its groups
   bool pairable = false;  // launch slots (2i, 2i+1) are vertically adjacent tiles
   uint64_t* trace = nullptr;           // caller's device buffers, see fo_plan_set_trace
   uint64_t* consumer_trace = nullptr;

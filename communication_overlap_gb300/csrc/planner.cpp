@@ -394,6 +394,9 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_fr = put(buf, p->final_row);
   const size_t o_sl = put(buf, p->slot_live);
   const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
+  const size_t o_fin = put(buf, std::vector<int32_t>(p->P, 0));
+  const size_t o_cons = put(buf, std::vector<int32_t>(p->P, 0));
+  const size_t o_rtile = put(buf, std::vector<int32_t>(2, 0));
   const size_t o_rwork = put(buf, std::vector<int32_t>(2 * p->P + 1, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
   const bool a2a = p->layout == FO_LAYOUT_A2A_SUBTOKEN;
@@ -424,6 +427,9 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.final_row = reinterpret_cast<int32_t*>(b + o_fr);
   p->dev.slot_live = reinterpret_cast<int32_t*>(b + o_sl);
   p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
+  p->dev.finished = reinterpret_cast<int32_t*>(b + o_fin);
+  p->dev.consumed = reinterpret_cast<uint32_t*>(b + o_cons);
+  p->dev.rtile = reinterpret_cast<int32_t*>(b + o_rtile);
   p->dev.rwork = reinterpret_cast<int32_t*>(b + o_rwork);
   p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
   p->dev.route_cnt = reinterpret_cast<int32_t*>(b + o_rc);

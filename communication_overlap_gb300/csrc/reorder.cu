@@ -17,7 +17,9 @@
 //    32-row box per subtile for the ReduceScatter layout) into the
 //    row-major output; ragged tiles and All-to-All rows leave as per-row
 //    512-byte bulk stores.
-// Three CTAs per SM keep ~192 KB per SM in flight.
+// Three CTAs per SM keep ~192 KB per SM in flight.  Tiles are handed out in
+// launch order by a counter; launched as the consumer's programmatic
+// dependent, a CTA waits for its tile's group to be consumed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -45,7 +47,30 @@ struct ReorderArgs {
   const uint16_t* bias;   // optional bf16[N] added before the activation
   int32_t act;            // fo_activation
   int32_t unit_bytes, row_bytes, slot0, n_slots;
+  int32_t* counters;         // [0] next tile, [1] CTAs done (reset by the last CTA)
+  const uint32_t* consumed;  // non-NULL: wait until consumed[group] == epoch
+  uint32_t epoch;
 };
+
+// Wait (thread 0) until the consumer has finished the tile's group: acquire
+// loads with __nanosleep back-off, bounded; gives up at once when another
+// CTA already gave up (the status word is set).
+__device__ __forceinline__ bool wait_consumed(const ReorderArgs& a, int32_t group) {
+  const uint32_t* f = a.consumed + group;
+  if (ld_acquire_gpu(f) == a.epoch) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t backoff = 64;
+  while (true) {
+    __nanosleep(backoff);
+    if (ld_acquire_gpu(f) == a.epoch) return true;
+    if (*reinterpret_cast<volatile int32_t*>(a.status) != 0) return false;
+    if (globaltimer_ns() - t0 > kRWaitLimitNs) {
+      atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
+      return false;
+    }
+    if (backoff < 2048) backoff <<= 1;
+  }
+}
 
 __device__ __forceinline__ void reorder_row(const ReorderArgs& a, const TileInfo& ti, int32_t s,
                                             int32_t r, int* k, int32_t* src_unit,
@@ -58,19 +83,42 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   uint8_t* buf = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(buf + kRTileBytes);
-  __shared__ int s_ok;
+  __shared__ int s_ok, s_ready;   // separate words: no barrier lies between
+                                  // the last read of one and the next write
+  __shared__ int32_t s_next[2];
   const int tid = threadIdx.x;
   const uint32_t sbuf = smem_u32(buf), sfull = smem_u32(full);
+  // overlapped (waiting on the consumer): tiles come from a shared counter
+  // in launch order; otherwise CTA b takes tiles b, b + grid, ...
+  const bool dyn = a.consumed != nullptr;
   if (tid == 0) {
     mbar_init(sfull, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_next[0] = dyn ? atomicAdd(a.counters, 1) : int32_t(blockIdx.x);
   }
   __syncthreads();
   const int32_t ub = a.unit_bytes;
   uint32_t phase = 0;
-  for (int32_t t = blockIdx.x; t < a.n_slots; t += gridDim.x, phase ^= 1) {
+  // thread 0 fetches the next index while the CTA works; with the shared
+  // counter, CTAs that start early -- beside a running GEMM and consumer --
+  // take the groups that finish first
+  for (int nb = 0;; nb ^= 1, phase ^= 1) {
+    const int32_t t = s_next[nb];
+    if (t >= a.n_slots) break;
     const int32_t s = a.slot0 + t;
     const TileInfo ti = a.map.tile[s];
+    if (tid == 0) {
+      s_next[nb ^ 1] = dyn ? atomicAdd(a.counters, 1) : t + int32_t(gridDim.x);
+      int ok = 1;
+      if (a.consumed != nullptr) {
+        ok = wait_consumed(a, ti.group) ? 1 : 0;
+        // the consumer's generic stores are read next by the TMA engine
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      s_ready = ok;
+    }
+    __syncthreads();
+    if (!s_ready) break;
     const bool whole = (a.map.layout == FO_LAYOUT_TILE || a.map.layout == FO_LAYOUT_RS_ROWBLOCK);
     const bool a2a = a.map.layout == FO_LAYOUT_A2A_SUBTOKEN;
     // All-to-All: this thread's row (k = -1: it holds no token, moves nowhere)
@@ -163,6 +211,16 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   }
   // every store has completed before the CTA (and its shared memory) ends
   bulk_wait_all();
+  // the last CTA resets the tile counter for the next launch
+  if (!dyn) return;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(a.counters + 1, 1) == int32_t(gridDim.x) - 1) {
+      atomicExch(a.counters, 0);
+      atomicExch(a.counters + 1, 0);
+    }
+  }
 }
 
 }  // namespace
@@ -202,9 +260,29 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   a.row_bytes = p->N * 2;
   a.slot0 = p->group_slot_begin[g0];
   a.n_slots = p->group_slot_begin[g1] - a.slot0;
+  a.counters = p->dev.rtile;
   int ctas = p->reorder_ctas > 0 ? p->reorder_ctas : 3 * p->sm_count;
   if (ctas > a.n_slots) ctas = a.n_slots;
-  reorder_kernel<<<ctas, kRThreads, kRSmem, static_cast<cudaStream_t>(stream)>>>(a);
+  // With overlap on, the reorder is a programmatic dependent of the
+  // consumer launched just before it on the stream: its CTAs start once all
+  // the consumer's CTAs are resident (on SMs the GEMM leaves room on) and
+  // move each group as soon as the consumer has finished it.
+  const bool ov = p->overlap != 0 && p->consume_published;
+  if (ov) {
+    a.consumed = p->dev.consumed;
+    a.epoch = p->consume_epoch;
+  }
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3(kRThreads);
+  cfg.dynamicSmemBytes = kRSmem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = ov ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, reorder_kernel, a) != cudaSuccess) return FO_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 

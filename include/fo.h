@@ -163,8 +163,13 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
  *  overlap: non-zero (default) launches the consumer as a programmatic
  *      dependent launch: issued on the GEMM's stream right after
  *      fo_signaled_gemm, it starts as soon as every GEMM CTA is resident and
- *      runs alongside the GEMM.  Zero launches it as an ordinary kernel
- *      (it then starts after the GEMM has finished: the serial baseline). */
+ *      runs alongside the GEMM.  The consumer then also publishes when each
+ *      group is fully written, and fo_reorder_back issued right after it is
+ *      in turn its programmatic dependent: it starts once every consumer CTA
+ *      is resident and moves each group as soon as that group is consumed.
+ *      Zero launches both as ordinary kernels (the consumer starts after the
+ *      GEMM has finished, the reorder after the consumer: the serial
+ *      baseline). */
 fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
                              int32_t reorder_ctas, int32_t overlap);
 
@@ -277,7 +282,7 @@ fo_status fo_consume_group(const fo_plan* plan, int32_t group,
  * Same arguments, results and launch behaviour as fo_consume_group.  It
  * allocates nothing: instead of the plan's scratch it keeps its chunk
  * counters in a fixed array inside the library's device image, room for
- * FO_NOALLOC_MAX_GROUPS groups (16 KB on every GPU that loads the library,
+ * FO_NOALLOC_MAX_GROUPS groups (32 KB on every GPU that loads the library,
  * held until the process exits).  A plan with more groups gets FO_ERR_ARG
  * and nothing is launched.  The plan's device must be the current device.
  *  - The first call on a device looks up the array's device address
@@ -333,7 +338,13 @@ fo_status fo_plan_route(fo_plan* plan, const int32_t* row_token, const int32_t* 
  *               slot q) lands in row (t / D) * top_k + q of dst[d]
  *               (top_k = 1 + the largest row_slot, or fo_plan_route's);
  *               empty rows move nowhere.
- * Stream-ordered after the consumer; no flags. */
+ * Issue it on the consumer's stream after fo_consume_group.  With overlap
+ * on (fo_plan_set_launch) it may start while the consumer still runs and
+ * waits, bounded, until the plan's last consume call has finished each
+ * group it moves (a wait that runs out sets the plan's status word, see
+ * fo_plan_device_status); tiles are then taken in launch order from a
+ * counter in the plan's scratch, so reorder calls on one plan that overlap
+ * in time race on it.  With overlap off it relies on stream order alone. */
 fo_status fo_reorder_back(const fo_plan* plan, int32_t group_begin,
                           int32_t group_end, const void* const* src,
                           void* const* dst, void* cuda_stream);

@@ -73,3 +73,31 @@ def test_bad_arguments_launch_nothing():
                                 1, 0)
     finally:
         pipe.close()
+
+
+def test_overlapped_reorder_waits_for_its_groups():
+    """With overlap on, fo_reorder_back is the consumer's programmatic
+    dependent and waits until each group it moves has been consumed.  When
+    the consumer gives up (flags never raised for its epoch), the reorder's
+    bounded wait runs out, the plan's status word says so, and the next
+    iteration is clean."""
+    pipe = _pipe()
+    try:
+        pipe.step()
+        torch.cuda.synchronize()
+        pipe.buf.status.zero_()
+        torch.cuda.synchronize()
+        pipe.set_overlap(True)
+        pipe.consume(pipe.s1, epoch=pipe.epoch + 7, spin_limit_ns=2_000_000)
+        pipe.reorder(pipe.s1)
+        torch.cuda.synchronize()
+        assert int(pipe.buf.status.item()) == fo.FO_ERR_TIMEOUT
+        assert fo.fo_plan_device_status(pipe.plan, clear=True) == fo.FO_ERR_TIMEOUT
+        pipe.buf.status.zero_()
+        torch.cuda.synchronize()
+        pipe.step()
+        res = pipe.results()
+        assert res["status"] == 0
+        assert fo.fo_plan_device_status(pipe.plan) == 0
+    finally:
+        pipe.close()
