@@ -93,11 +93,13 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
                                               int tid) {
   constexpr bool kSum = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS);
   constexpr int S = kThreads;
+  // every source vector is read exactly once: evict-first in L2
+  const uint64_t pol = l2_evict_first();
   for (int32_t base = v0 + tid; base < v1; base += S * U) {
     uint4 x[U];
 #pragma unroll
     for (int i = 0; i < U; ++i)
-      if (base + S * i < v1) x[i] = ld_cg(a.src + base + S * i);
+      if (base + S * i < v1) x[i] = ld_once(a.src + base + S * i, pol);
     if constexpr (kSum) {
       float acc[U][8];
 #pragma unroll
@@ -108,7 +110,7 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
         uint4 y[U];
 #pragma unroll
         for (int i = 0; i < U; ++i)
-          if (base + S * i < v1) y[i] = ld_cg(a.partials[q] + base + S * i);
+          if (base + S * i < v1) y[i] = ld_once(a.partials[q] + base + S * i, pol);
 #pragma unroll
         for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[i]);
       }
@@ -281,6 +283,7 @@ __device__ __forceinline__ void reorder_rows_regs(const FusedArgs& a, uint4* con
   static_assert(kItemRows<VPU> == kWarps * kRowsPerInstr * kBatch, "one round per item");
   const int warp = tid / 32, lane = tid % 32, sub = lane / VPU, vl = lane % VPU;
   const TileInfo ti = a.map.tile[s];
+  const uint64_t pol = l2_evict_first();   // the received data is read once
   {
     uint4 x[kBatch];
     int64_t to[kBatch];
@@ -293,7 +296,7 @@ __device__ __forceinline__ void reorder_rows_regs(const FusedArgs& a, uint4* con
         int32_t su, dr;
         map_row(a.map, ti, s, r, &kk[i], &su, &dr);
         if (kk[i] >= 0) {   // not an empty All-to-All row
-          x[i] = ld_cg(src[kk[i]] + int64_t(su) * VPU + vl);
+          x[i] = ld_once(src[kk[i]] + int64_t(su) * VPU + vl, pol);
           to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
         }
       }

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   }
   __syncthreads();
   const int32_t ub = a.unit_bytes;
+  const uint64_t pol = l2_evict_first();   // the received data is read once
   uint32_t phase = 0;
   // thread 0 fetches the next index while the CTA works; with the shared
   // counter, CTAs that start early -- beside a running GEMM and consumer --
@@ -136,18 +137,18 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
         int k;
         int32_t su, dr;
         reorder_row(a, ti, s, 0, &k, &su, &dr);   // rows are contiguous from row 0
-        bulk_load(sbuf, a.src[k] + int64_t(su) * ub, uint32_t(ti.rows * ub), sfull);
+        bulk_load_hint(sbuf, a.src[k] + int64_t(su) * ub, uint32_t(ti.rows * ub), sfull, pol);
       }
     } else if (a.map.layout == FO_LAYOUT_RS_SUBTILE) {
       if (tid < a.map.R) {   // subtile tid: rows tid*h .. +h, contiguous in slice tid
         int k;
         int32_t su, dr;
         reorder_row(a, ti, s, tid * a.map.h, &k, &su, &dr);
-        bulk_load(sbuf + tid * a.map.h * ub, a.src[k] + int64_t(su) * ub, uint32_t(a.map.h * ub),
-                  sfull);
+        bulk_load_hint(sbuf + tid * a.map.h * ub, a.src[k] + int64_t(su) * ub,
+                       uint32_t(a.map.h * ub), sfull, pol);
       }
     } else if (rk >= 0) {  // All-to-All: row by row
-      bulk_load(sbuf + tid * ub, a.src[rk] + int64_t(rsu) * ub, uint32_t(ub), sfull);
+      bulk_load_hint(sbuf + tid * ub, a.src[rk] + int64_t(rsu) * ub, uint32_t(ub), sfull, pol);
     }
     // wait for the tile to land (bounded)
     if (tid == 0) {
