@@ -27,6 +27,13 @@ constexpr int kUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 2 : 8;
 // thread for the copies (32 KB), two passes for the sums (16 KB).
 template <int KIND>
 constexpr int kChunkBytes = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 16 * 1024 : 32 * 1024;
+// The fused consumer+reorder keeps fewer copy loads in flight per thread: it
+// runs at 72 registers (two CTAs beside a GEMM CTA) and also holds the
+// reorder's loads.
+template <int KIND>
+constexpr int kFusedUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 2 : 4;
+// Units of the largest chunk (32 KB of 256-byte units at tile_n = 128).
+constexpr int kMaxChunkUnits = 32 * 1024 / 256;
 
 struct ConsumeArgs {
   const uint4* src;
@@ -40,11 +47,13 @@ struct ConsumeArgs {
   const int32_t* part_dst;
   int32_t* work;   // [P] chunk counters, then one "CTAs done" counter
   int32_t* finished;   // [P] chunks finished per group (NULL: no consumed flags)
-  uint32_t* consumed;  // [P] = epoch once every chunk of the group is written
+  uint32_t* consumed;  // [P] = seq once every chunk of the group is written
+  uint32_t seq;        // this launch's number on the plan (never 0)
   int32_t g0, g1, n_partials, R, P, vpu_shift, chunk_units;
   uint32_t epoch;
   uint64_t limit_ns;
-  uint64_t* trace;  // optional: [P] group fully consumed, then [grid][4] CTA records
+  uint64_t* trace;  // optional: [P] group fully consumed, [P] group reordered
+                    // (fused kernel), then [grid][4] CTA records
 };
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& x) {
@@ -175,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
     const int32_t ub = a.group_unit_begin[j], ue = a.group_unit_begin[j + 1];
     const int32_t n_chunks = (ue - ub + a.chunk_units - 1) / a.chunk_units;
     if (n_chunks == 0 && a.finished != nullptr && tid == 0)
-      st_release_gpu(a.consumed + j, a.epoch);   // an empty group is consumed at once
+      st_release_gpu(a.consumed + j, a.seq);   // an empty group is consumed at once
     int32_t group_chunks = 0;
     if (tid == 0) s_chunk[0] = atomicAdd(a.work + j, 1);
     __syncthreads();
@@ -203,20 +212,26 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
       // the CTA that completes the count releases the group
       __threadfence();
       if (atomicAdd(a.finished + j, group_chunks) + group_chunks == n_chunks)
-        st_release_gpu(a.consumed + j, a.epoch);
+        st_release_gpu(a.consumed + j, a.seq);
     }
   }
   if (a.trace != nullptr) {
     if (tid == 0) {
-      a.trace[a.P + 4 * blockIdx.x + 3] = uint64_t(chunks_done);
+      uint64_t* rec = a.trace + 2 * a.P + 4 * blockIdx.x;
+      rec[3] = uint64_t(chunks_done);
       uint32_t smid;
       asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-      uint64_t* rec = a.trace + a.P + 4 * blockIdx.x;
       rec[0] = smid;
       rec[1] = t_start;
       rec[2] = globaltimer_ns();
     }
   }
+  // A consume launched as the programmatic dependent of the kernel before
+  // it on the stream (the GEMM, or with per-group calls an earlier consume
+  // or reorder of this plan) can run beside that kernel: the scratch
+  // counters below are shared between launches on one plan, so wait until
+  // that kernel has completed before touching them.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // every CTA, finished or timed out, reports; the last one resets the
   // counters of this launch's groups and the report counter
   __syncthreads();
@@ -234,10 +249,17 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
 
 // ---------------------------------------------------------------------------
 // Consumer with the post-communication reorder (and the element-wise
-// epilogue) fused in: one persistent kernel in which a CTA, once it has
-// taken its share of group j's communication, reorders group j-1 back to
-// the final layout -- while the GEMM is still computing later groups.  Only
-// the last group's reorder is left when the GEMM ends.
+// epilogue) fused in: one persistent kernel, on the GEMM's stream, that
+// moves every group to its final layout while the GEMM still computes later
+// groups.
+//  * Tile and ReduceScatter layouts: a CTA that has written a chunk of
+//    units to the communication buffers reads them back from there and
+//    moves each unit to its final place at once (unit_src names the tile
+//    row a unit holds), so a group is final one chunk after it is
+//    communicated, with no wait on other CTAs.
+//  * All-to-All: a unit's final place depends on the routing, so a CTA that
+//    has taken its share of group j's communication reorders group j-1 tile
+//    by tile, after waiting until every chunk of j-1 is counted as consumed.
 
 struct FusedArgs {
   ConsumeArgs c;                  // the communication part (c.dst: its outputs)
@@ -245,6 +267,7 @@ struct FusedArgs {
   RowMap map;
   const uint16_t* bias;
   const int32_t* group_slot_begin;
+  const int32_t* unit_src;  // [units] slot << 7 | row (tile and RS layouts)
   int32_t* rwork;  // [P] reorder chunk counters, [P] units consumed, [1] CTAs done
   int32_t act, row_vec;
 };
@@ -312,9 +335,74 @@ __device__ __forceinline__ void reorder_rows_regs(const FusedArgs& a, uint4* con
   }
 }
 
+// Where the units of a chunk go, computed by threads t < units before the
+// chunk is consumed (their loads overlap the other warps' consume loads):
+// the communication buffer k and unit su it was written to, and its place
+// in final output k (16-byte vector index of the row start) and column.
+struct ChunkMap {
+  int32_t k[kMaxChunkUnits];
+  int32_t su[kMaxChunkUnits];
+  int32_t col[kMaxChunkUnits];
+  int64_t to[kMaxChunkUnits];
+};
+
+__device__ __forceinline__ void map_chunk_units(const FusedArgs& a, ChunkMap& m, int32_t u0,
+                                                int32_t u1, int tid) {
+  if (tid < u1 - u0) {
+    const int32_t us = a.unit_src[u0 + tid];
+    const int32_t s = us >> 7, r = us & (kTileM - 1);
+    const TileInfo ti = a.map.tile[s];
+    int k;
+    int32_t su, dr;
+    map_row(a.map, ti, s, r, &k, &su, &dr);
+    m.k[tid] = k;
+    m.su[tid] = su;
+    m.col[tid] = ti.col0;
+    m.to[tid] = int64_t(dr) * a.row_vec + (ti.col0 >> 3);
+  }
+}
+
+// The chunk's units, just written to the communication buffers by this CTA,
+// read back from there and stored to their final places: thread t moves
+// vectors t, t + 256, ... (one unit per warp instruction), all loads in
+// flight before the stores.
+template <int VPU, int NV>
+__device__ __forceinline__ void reorder_chunk_regs(const FusedArgs& a, const ChunkMap& m,
+                                                   uint4* const* src, uint4* const* fin,
+                                                   int32_t n_units, int tid) {
+  const uint64_t pol = l2_evict_first();   // the received data is read once
+  const int32_t n_vec = n_units * VPU;
+  uint4 x[NV];
+#pragma unroll
+  for (int b = 0; b < NV; ++b) {
+    const int32_t v = tid + kThreads * b;
+    if (v < n_vec) {
+      const int32_t i = v / VPU, vl = v % VPU;
+      x[b] = ld_once(src[m.k[i]] + int64_t(m.su[i]) * VPU + vl, pol);
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NV; ++b) {
+    const int32_t v = tid + kThreads * b;
+    if (v < n_vec) {
+      const int32_t i = v / VPU, vl = v % VPU;
+      uint4 y = x[b];
+      if (a.act != FO_ACT_NONE || a.bias != nullptr)
+        y = epilogue8(y, a.bias, m.col[i] + vl * 8, a.act);
+      st_cs(fin[m.k[i]] + m.to[i] + vl, y);
+    }
+  }
+}
+
+// Launched with 256 threads.  Registers capped at 72: measured, two CTAs at
+// 70 registers run beside each GEMM CTA while the GEMM runs, at 80 only one.
 template <int KIND, int U, int VPU>
-__global__ void __launch_bounds__(kThreads, 3)
-    consume_reorder_kernel(const __grid_constant__ FusedArgs a) {
+__global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ FusedArgs a) {
+  // tile and RS layouts: each chunk is reordered right after it is written
+  constexpr bool kChunkwise = KIND != FO_CONS_A2A;
+  // 16-byte vectors of a chunk per thread
+  constexpr int kNV = kChunkBytes<KIND> / (16 * kThreads);
+  __shared__ ChunkMap s_map;
   const ConsumeArgs& c = a.c;
   __shared__ int s_ok;
   __shared__ int32_t s_chunk[2];
@@ -328,6 +416,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   int32_t* done = a.rwork + c.P;
   bool ok = true;
+  uint64_t t_start = 0;
+  int32_t chunks_done = 0;
+  if (c.trace != nullptr && tid == 0) t_start = globaltimer_ns();
 
   // reorder every tile of group j once its communication is complete
   auto reorder_group = [&](int j) {
@@ -353,12 +444,15 @@ __global__ void __launch_bounds__(kThreads, 3)
       reorder_rows_regs<VPU>(a, s_dst, s_fin, s0 + t / kItems, (t % kItems) * kItemRows<VPU>,
                              tid);
       __syncthreads();
+      if (c.trace != nullptr && tid == 0)   // latest item end: the group is reordered
+        atomicMax(reinterpret_cast<unsigned long long*>(c.trace + c.P + j),
+                  static_cast<unsigned long long>(globaltimer_ns()));
     }
     __syncthreads();
   };
 
   for (int j = c.g0; j < c.g1 && ok; ++j) {
-    if (j > c.g0) {
+    if (!kChunkwise && j > c.g0) {
       reorder_group(j - 1);
       if (!ok) break;
     }
@@ -384,19 +478,46 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(c.work + j, 1);
       const int32_t u0 = ub + ch * c.chunk_units;
       const int32_t u1 = min(u0 + c.chunk_units, ue);
+      if constexpr (kChunkwise) map_chunk_units(a, s_map, u0, u1, tid);
       consume_range<KIND, U>(c, s_ps, s_pl, s_pd, s_dst, u0 << c.vpu_shift, u1 << c.vpu_shift,
                              tid);
-      __syncthreads();
-      if (tid == 0) {
+      __syncthreads();   // the chunk's stores and its map are visible to the whole CTA
+      if constexpr (kChunkwise) {
+        reorder_chunk_regs<VPU, kNV>(a, s_map, s_dst, s_fin, u1 - u0, tid);
+        __syncthreads();   // s_map is free for the next chunk
+        if (c.trace != nullptr && tid == 0) {
+          const unsigned long long now = globaltimer_ns();
+          atomicMax(reinterpret_cast<unsigned long long*>(c.trace + j), now);
+          atomicMax(reinterpret_cast<unsigned long long*>(c.trace + c.P + j), now);
+          ++chunks_done;
+        }
+      } else if (tid == 0) {
         // this chunk's outputs are visible before it is counted as consumed
         __threadfence();
         atomicAdd(done + j, u1 - u0);
+        if (c.trace != nullptr) {
+          atomicMax(reinterpret_cast<unsigned long long*>(c.trace + j),
+                    static_cast<unsigned long long>(globaltimer_ns()));
+          ++chunks_done;
+        }
       }
     }
     __syncthreads();
   }
-  if (ok && c.g1 > c.g0) reorder_group(c.g1 - 1);
+  if (!kChunkwise && ok && c.g1 > c.g0) reorder_group(c.g1 - 1);
+  if (c.trace != nullptr && tid == 0) {
+    uint64_t* rec = c.trace + 2 * c.P + 4 * blockIdx.x;
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    rec[0] = smid;
+    rec[1] = t_start;
+    rec[2] = globaltimer_ns();
+    rec[3] = uint64_t(chunks_done);
+  }
 
+  // the kernel this one depends on has completed before the shared
+  // counters are touched (see consume_kernel)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // every CTA reports; the last one resets this launch's counters
   __syncthreads();
   if (tid == 0) {
@@ -443,24 +564,28 @@ template <int VPU>
 fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int dv,
                            cudaStream_t st) {
   switch (kind) {
-    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>, VPU>(a, ctas, ov, dv, st);
-    case FO_CONS_SUM: return launch_fused_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>, VPU>(a, ctas, ov, dv, st);
-    case FO_CONS_RS: return launch_fused_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>, VPU>(a, ctas, ov, dv, st);
-    case FO_CONS_A2A: return launch_fused_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kFusedUnroll<FO_CONS_COPY>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_SUM: return launch_fused_kind<FO_CONS_SUM, kFusedUnroll<FO_CONS_SUM>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_RS: return launch_fused_kind<FO_CONS_RS, kFusedUnroll<FO_CONS_RS>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_A2A: return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
 }
 
 // With overlap on, the consumer publishes each group's completion (per-group
-// finished-chunk counters, then consumed[j] = epoch) for a reorder launched
-// as its programmatic dependent.  Serially the reorder follows in stream
-// order and nothing is published (the counting costs a fence per CTA and
-// group).
-void publish_consumed(const fo_plan* p, ConsumeArgs& a, int32_t* finished, uint32_t epoch) {
+// finished-chunk counters, then consumed[j] = the launch's sequence number,
+// which no earlier launch on the plan used, so a flag left by one never
+// passes for the next) for a reorder launched as its programmatic
+// dependent.  Serially the reorder follows in stream order and nothing is
+// published (the counting costs a fence per CTA and group).
+void publish_consumed(const fo_plan* p, ConsumeArgs& a, int32_t* finished) {
   const bool on = p->overlap != 0;
   a.finished = on ? finished : nullptr;
   a.consumed = on ? p->dev.consumed : nullptr;
-  p->consume_epoch = epoch;
+  if (on) {
+    if (++p->consume_seq == 0) p->consume_seq = 1;
+    a.seq = p->consume_seq;
+  }
   p->consume_published = on;
 }
 
@@ -537,7 +662,7 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.part_len = p->dev.part_len;
   a.part_dst = p->dev.part_dst;
   a.work = p->dev.work;
-  publish_consumed(p, a, p->dev.finished, epoch);
+  publish_consumed(p, a, p->dev.finished);
   a.g0 = g0;
   a.g1 = g1;
   a.P = p->P;
@@ -590,9 +715,11 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
   c.chunk_units = chunk_units_of(kind, p->tile_n);
   c.epoch = epoch;
   c.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
+  c.trace = p->consumer_trace;
   a.map = make_row_map(p);
   a.bias = static_cast<const uint16_t*>(bias);
   a.group_slot_begin = p->dev.group_slot_begin;
+  a.unit_src = p->dev.unit_src;
   a.rwork = p->dev.rwork;
   a.act = act;
   a.row_vec = p->N / 8;
@@ -704,7 +831,7 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.part_dst = p->dev.part_dst;
   a.work = scratch;
   // consumed flags in the plan (allocated when it was built), counters here
-  publish_consumed(p, a, scratch + FO_NOALLOC_MAX_GROUPS + 1, epoch);
+  publish_consumed(p, a, scratch + FO_NOALLOC_MAX_GROUPS + 1);
   a.g0 = group < 0 ? 0 : group;
   a.g1 = group < 0 ? p->P : group + 1;
   a.P = p->P;

@@ -44,12 +44,14 @@ struct DeviceTables {
   int32_t* row_rank = nullptr;         // [M] A2A: index among the rows of its
                                        //   tile row that go to the same rank
   int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
+  int32_t* unit_src = nullptr;         // [units] tile and RS layouts: slot << 7 | row
+                                       //   of the tile row each unit holds
   int32_t* slot_live = nullptr;        // [tiles] A2A: 1 if a row of the tile holds
                                        //   a token (else the GEMM skips it)
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
   int32_t* finished = nullptr;         // [P] scratch: chunks the consumer finished
-  uint32_t* consumed = nullptr;        // [P] epoch of the last consume that
-                                       //   finished each group (read by the
+  uint32_t* consumed = nullptr;        // [P] sequence number of the last consume
+                                       //   that finished each group (read by the
                                        //   overlapped reorder)
   int32_t* rtile = nullptr;            // [2] scratch of the reorder: tile counter,
                                        //   CTAs done
@@ -73,7 +75,7 @@ struct fo_plan {
   std::vector<int32_t> slot_tile, tile_slot, slot_group;
   std::vector<fo::TileInfo> tile;
   std::vector<int32_t> part_start, part_len, part_dst, dest_units, final_rows, dest_capacity;
-  std::vector<int32_t> dest_base, row_dest, row_rank, final_row, slot_live;
+  std::vector<int32_t> dest_base, row_dest, row_rank, final_row, slot_live, unit_src;
   int32_t route_blocks = 0;       // A2A: tile-row blocks (ceil(rows / 128) per expert)
   // fo_plan_route rebuilt the routing tables on the device: the host copies
   // above are stale until refresh_routing() downloads them
@@ -83,9 +85,9 @@ struct fo_plan {
   int sm_count = 0;
   int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
   int gemm_variant = 0;   // fo_gemm_variant
-  // epoch of the last consume launched on this plan: a reorder launched as
-  // its programmatic dependent waits until each group is consumed at it
-  mutable uint32_t consume_epoch = 0;
+  // sequence number of the last consume launched on this plan: a reorder
+  // launched as its programmatic dependent waits until consumed[j] holds it
+  mutable uint32_t consume_seq = 0;
   mutable bool consume_published = false;   // that consume published its groups
   bool pairable = false;  // launch slots (2i, 2i+1) are vertically adjacent tiles
   uint64_t* trace = nullptr;           // caller's device buffers, see fo_plan_set_trace

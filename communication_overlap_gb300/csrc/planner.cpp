@@ -321,7 +321,14 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   } else {
     p->final_rows.assign(R, d->M / R);
   }
-  if (layout != FO_LAYOUT_A2A_SUBTOKEN) p->dest_capacity = p->dest_units;
+  if (layout != FO_LAYOUT_A2A_SUBTOKEN) {
+    p->dest_capacity = p->dest_units;
+    // the inverse of the unit layout at row granularity: which tile row each
+    // unit holds (read by the fused consumer+reorder)
+    p->unit_src.assign(p->n_units, 0);
+    for (int32_t s = 0; s < tiles; ++s)
+      for (int32_t r = 0; r < p->tile[s].rows; ++r) p->unit_src[unit_of(p, s, r)] = (s << 7) | r;
+  }
   return FO_OK;
 }
 
@@ -393,6 +400,7 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_rr = put(buf, p->row_rank);
   const size_t o_fr = put(buf, p->final_row);
   const size_t o_sl = put(buf, p->slot_live);
+  const size_t o_us = put(buf, p->unit_src);
   const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
   const size_t o_fin = put(buf, std::vector<int32_t>(p->P, 0));
   const size_t o_cons = put(buf, std::vector<int32_t>(p->P, 0));
@@ -426,6 +434,7 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.row_rank = reinterpret_cast<int32_t*>(b + o_rr);
   p->dev.final_row = reinterpret_cast<int32_t*>(b + o_fr);
   p->dev.slot_live = reinterpret_cast<int32_t*>(b + o_sl);
+  p->dev.unit_src = reinterpret_cast<int32_t*>(b + o_us);
   p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
   p->dev.finished = reinterpret_cast<int32_t*>(b + o_fin);
   p->dev.consumed = reinterpret_cast<uint32_t*>(b + o_cons);

@@ -48,8 +48,8 @@ struct ReorderArgs {
   int32_t act;            // fo_activation
   int32_t unit_bytes, row_bytes, slot0, n_slots;
   int32_t* counters;         // [0] next tile, [1] CTAs done (reset by the last CTA)
-  const uint32_t* consumed;  // non-NULL: wait until consumed[group] == epoch
-  uint32_t epoch;
+  const uint32_t* consumed;  // non-NULL: wait until consumed[group] == seq
+  uint32_t seq;              // the preceding consume launch's number
 };
 
 // Wait (thread 0) until the consumer has finished the tile's group: acquire
@@ -57,12 +57,12 @@ struct ReorderArgs {
 // CTA already gave up (the status word is set).
 __device__ __forceinline__ bool wait_consumed(const ReorderArgs& a, int32_t group) {
   const uint32_t* f = a.consumed + group;
-  if (ld_acquire_gpu(f) == a.epoch) return true;
+  if (ld_acquire_gpu(f) == a.seq) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t backoff = 64;
   while (true) {
     __nanosleep(backoff);
-    if (ld_acquire_gpu(f) == a.epoch) return true;
+    if (ld_acquire_gpu(f) == a.seq) return true;
     if (*reinterpret_cast<volatile int32_t*>(a.status) != 0) return false;
     if (globaltimer_ns() - t0 > kRWaitLimitNs) {
       atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
@@ -212,6 +212,10 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   }
   // every store has completed before the CTA (and its shared memory) ends
   bulk_wait_all();
+  // Launched as the consumer's programmatic dependent, this grid completes
+  // only after the consumer has: a later launch on the stream (a consume of
+  // the next group) then never meets the consumer still running.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the last CTA resets the tile counter for the next launch
   if (!dyn) return;
   __syncthreads();
@@ -271,7 +275,7 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   const bool ov = p->overlap != 0 && p->consume_published;
   if (ov) {
     a.consumed = p->dev.consumed;
-    a.epoch = p->consume_epoch;
+    a.seq = p->consume_seq;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(ctas);

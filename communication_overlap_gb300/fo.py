@@ -208,7 +208,7 @@ def fo_plan_set_gemm(plan, variant=FO_GEMM_AUTO):
 
 def fo_plan_set_trace(plan, stamps, consumer_stamps=0):
     """stamps: device uint64[tiles + W]; consumer_stamps: device
-    uint64[P + 4 * consumer CTAs]; 0 stops that trace."""
+    uint64[2P + 4 * consumer CTAs]; 0 stops that trace."""
     _check("fo_plan_set_trace", lib().fo_plan_set_trace(plan, int(stamps) or None,
                                                         int(consumer_stamps) or None))
 

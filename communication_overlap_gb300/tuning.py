@@ -90,7 +90,7 @@ class Tuner:
             p.step(overlap=False)
             torch.cuda.synchronize()
             p.set_overlap(False)
-            trace = torch.zeros(p.P + 4 * ctas, dtype=torch.int64, device=p.device)
+            trace = torch.zeros(2 * p.P + 4 * ctas, dtype=torch.int64, device=p.device)
             fo.fo_plan_set_trace(p.plan, 0, trace.data_ptr())
             spans = []
             for _ in range(self.reps):
@@ -98,7 +98,7 @@ class Tuner:
                 trace.zero_()
                 p.consume(p.s0, p.epoch, group=0)
                 torch.cuda.synchronize()
-                rec = trace[p.P:].view(-1, 4).cpu()
+                rec = trace[2 * p.P:].view(-1, 4).cpu()
                 ran = rec[rec[:, 1] > 0]
                 spans.append(float(ran[:, 2].max() - ran[:, 1].min()) / 1e3)
             fo.fo_plan_set_trace(p.plan, 0, 0)

@@ -201,9 +201,11 @@ fo_status fo_plan_set_gemm(fo_plan* plan, fo_gemm_variant variant, int32_t* pair
  *  stamps [tiles + W]: every GEMM launch writes stamps[slot] = %globaltimer
  *      (ns) when the tile at that launch slot has been stored and counted,
  *      and stamps[tiles + c] = the start time of CTA c.
- *  consumer_stamps [P + 4 * consumer CTAs], zeroed by the caller before the
- *      consume call: [j] = when group j's last chunk was processed; then per
- *      CTA c, [P + 4c ..]: SM id, start time, end time, chunks processed. */
+ *  consumer_stamps [2P + 4 * consumer CTAs], zeroed by the caller before
+ *      the consume call (fo_consume_group or fo_consume_reorder): [j] = when
+ *      group j's last chunk was processed; [P + j] = when group j's last
+ *      reorder item was done (fo_consume_reorder only); then per CTA c,
+ *      [2P + 4c ..]: SM id, start time, end time, chunks processed. */
 fo_status fo_plan_set_trace(fo_plan* plan, uint64_t* stamps, uint64_t* consumer_stamps);
 
 /* Sticky status word of the plan's GEMM and reorder launches (calls with
