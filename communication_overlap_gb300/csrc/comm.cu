@@ -170,7 +170,11 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
   int32_t chunks_done = 0;
   if (a.trace != nullptr && tid == 0) t_start = globaltimer_ns();
   for (int j = a.g0; j < a.g1; ++j) {
-    if (tid == 0) s_ok = wait_flag(a.flags + j, a.epoch, a.limit_ns) ? 1 : 0;
+    // the group's first chunk is taken before the wait on its flag
+    if (tid == 0) {
+      s_chunk[0] = atomicAdd(a.work + j, 1);
+      s_ok = wait_flag(a.flags + j, a.epoch, a.limit_ns) ? 1 : 0;
+    }
     if (tid < a.R) {
       s_ps[tid] = a.part_start[j * a.R + tid];
       s_pl[tid] = a.part_len[j * a.R + tid];
@@ -186,8 +190,6 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
     if (n_chunks == 0 && a.finished != nullptr && tid == 0)
       st_release_gpu(a.consumed + j, a.seq);   // an empty group is consumed at once
     int32_t group_chunks = 0;
-    if (tid == 0) s_chunk[0] = atomicAdd(a.work + j, 1);
-    __syncthreads();
     for (int buf = 0;; buf ^= 1) {
       const int32_t c = s_chunk[buf];
       if (c >= n_chunks) break;
@@ -456,29 +458,40 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
       reorder_group(j - 1);
       if (!ok) break;
     }
-    if (tid == 0) s_ok = wait_flag(c.flags + j, c.epoch, c.limit_ns) ? 1 : 0;
+    // The group's first chunk is taken, and its unit map computed, before
+    // the wait on the group's flag: when the group completes, only the data
+    // moves are left.
+    const int32_t ub = c.group_unit_begin[j], ue = c.group_unit_begin[j + 1];
+    const int32_t n_chunks = (ue - ub + c.chunk_units - 1) / c.chunk_units;
+    if (tid == 0) s_chunk[0] = atomicAdd(c.work + j, 1);
     if (tid < c.R) {
       s_ps[tid] = c.part_start[j * c.R + tid];
       s_pl[tid] = c.part_len[j * c.R + tid];
       s_pd[tid] = c.part_dst[j * c.R + tid];
     }
     __syncthreads();
+    if constexpr (kChunkwise) {
+      const int32_t first = s_chunk[0];
+      if (first < n_chunks) {
+        const int32_t u0 = ub + first * c.chunk_units;
+        map_chunk_units(a, s_map, u0, min(u0 + c.chunk_units, ue), tid);
+      }
+    }
+    if (tid == 0) s_ok = wait_flag(c.flags + j, c.epoch, c.limit_ns) ? 1 : 0;
+    __syncthreads();
     if (!s_ok) {
       if (tid == 0) atomicCAS(c.status, 0, int32_t(FO_ERR_TIMEOUT));
       ok = false;
       break;
     }
-    const int32_t ub = c.group_unit_begin[j], ue = c.group_unit_begin[j + 1];
-    const int32_t n_chunks = (ue - ub + c.chunk_units - 1) / c.chunk_units;
-    if (tid == 0) s_chunk[0] = atomicAdd(c.work + j, 1);
-    __syncthreads();
-    for (int buf = 0;; buf ^= 1) {
+    for (int buf = 0, n = 0;; buf ^= 1, ++n) {
       const int32_t ch = s_chunk[buf];
       if (ch >= n_chunks) break;
       if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(c.work + j, 1);
       const int32_t u0 = ub + ch * c.chunk_units;
       const int32_t u1 = min(u0 + c.chunk_units, ue);
-      if constexpr (kChunkwise) map_chunk_units(a, s_map, u0, u1, tid);
+      if constexpr (kChunkwise)
+        if (n > 0) map_chunk_units(a, s_map, u0, u1, tid);   // the first is mapped
       consume_range<KIND, U>(c, s_ps, s_pl, s_pd, s_dst, u0 << c.vpu_shift, u1 << c.vpu_shift,
                              tid);
       __syncthreads();   // the chunk's stores and its map are visible to the whole CTA
