@@ -397,6 +397,41 @@ def run_ours(args):
     t_gemm = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch), args.steps, flush)
     t_gemm_nosig = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch, signal=False),
                          args.steps, flush)
+    # library reference point: torch.matmul (cuBLAS) on the same operands,
+    # one call per expert for the grouped workload
+    A_bf = pipe.buf.A.view(torch.bfloat16).view(w.M, w.K)
+    B_bf = [b.view(torch.bfloat16).view(w.K, w.N) for b in pipe.buf.B]
+    rows = np.cumsum([0] + list(inp.expert_rows))
+
+    def torch_mm():
+        with torch.cuda.stream(s):
+            for e, Bm in enumerate(B_bf):
+                torch.matmul(A_bf[rows[e]:rows[e + 1]], Bm)
+    for _ in range(3):   # cuBLAS handle, workspace and kernel choice
+        torch_mm()
+    t_mm = timed(torch, s, torch_mm, args.steps, flush)
+
+    # the same path with W = this device's SM count (the workloads fix W)
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    w_sm = None
+    if sm_count != w.wave_width:
+        pipe_sm = Pipeline(w, inp, device=dev, wave_width=sm_count)
+        t_gemm_sm = timed(torch, pipe_sm.s0, lambda: pipe_sm.gemm(pipe_sm.s0, pipe_sm.epoch),
+                          args.steps, flush)
+        for _ in range(3):
+            pipe_sm.step(overlap=True, fused=fused)
+        t_step_sm = timed(torch, pipe_sm.s0,
+                          lambda: pipe_sm.step(overlap=True, sync_current=False, fused=fused),
+                          args.steps, flush)
+        torch.cuda.synchronize()
+        w_sm = {"wave_width": sm_count, "waves": pipe_sm.waves,
+                "partition": pipe_sm.partition, "gemm_pairs": bool(pipe_sm.pairable),
+                "ms_gemm_alone": statistics.mean(t_gemm_sm),
+                "ms_overlapped_step": statistics.mean(t_step_sm),
+                "status_ok": int(pipe_sm.buf.status.item()) == 0}
+        pipe_sm.close()
+        del pipe_sm
+
     # consumer + reorder alone: the flags of the last epoch are already raised;
     # ordinary launches so nothing overlaps the flush before them
     pipe.step(overlap=True)
@@ -415,7 +450,6 @@ def run_ours(args):
     # the consumer's bandwidth with a full grid (4 CTAs per SM): its roofline
     # figure; the step uses the library's default grid for running beside the
     # GEMM, which for copies is smaller and slower alone
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     fo.fo_plan_set_launch(pipe.plan, 4 * sm_count, args.reorder_ctas, False)
     t_cons_full = timed(torch, s, cons_only, args.steps, flush)
     fo.fo_plan_set_launch(pipe.plan, args.consumer_ctas, args.reorder_ctas, False)
@@ -565,6 +599,11 @@ def run_ours(args):
                 "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
                 "gemm_tflops_alone": gemm_tflops,
                 "gemm_frac_of_sustained": gemm_tflops / peak_sust,
+                "ms_torch_matmul": statistics.mean(t_mm),
+                "torch_matmul_tflops": flops / (statistics.mean(t_mm) * 1e-3) / 1e12,
+                "torch_matmul_note": "library reference point: torch.matmul on the same "
+                                     "operands (one call per expert), no reorder or signal",
+                "w_sm_count": w_sm,
                 "ms_consumer_plus_reorder_alone": statistics.mean(t_cons),
                 "ms_consumer_alone": statistics.mean(t_cons_only),
                 "ms_reorder_alone": statistics.mean(t_reo),
