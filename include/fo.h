@@ -397,13 +397,17 @@ fo_status fo_reorder_back_fused(const fo_plan* plan, int32_t group_begin, int32_
 /* fo_consume_group and fo_reorder_back_fused in one persistent kernel, for
  * the same results in both sets of buffers: comm_dst receives what
  * fo_consume_group writes to dst, final_dst what fo_reorder_back_fused
- * writes to dst.  A CTA that has taken its share of group j's
- * communication reorders group j-1 (waiting, bounded, until every chunk of
- * j-1 is counted as consumed), so on the GEMM's stream every group but the
- * last is reordered while the GEMM still runs ([P1] 五: the post-
- * communication reorder fused with the element-wise epilogue to save a
- * launch).  Layouts: TILE (COPY, SUM), RS (RS), A2A (A2A).  Uses the plan's
- * scratch; calls that overlap in time on one plan race on it. */
+ * writes to dst.  Every group is moved to its final layout while the GEMM
+ * still computes later groups ([P1] 五: the post-communication reorder fused
+ * with the element-wise epilogue to save a launch):
+ *  - TILE and RS layouts: a CTA that has written a chunk of units to
+ *    comm_dst reads them back from there and stores them to final_dst at
+ *    once, so a group is final one chunk after its flag rises;
+ *  - A2A: a CTA that has taken its share of group j's communication
+ *    reorders group j-1, after waiting (bounded) until every chunk of j-1
+ *    is counted as consumed.
+ * Layouts: TILE (COPY, SUM), RS (RS), A2A (A2A).  Uses the plan's scratch;
+ * calls that overlap in time on one plan race on it. */
 fo_status fo_consume_reorder(const fo_plan* plan, int32_t group, fo_consumer kind,
                              const void* src_reordered, const void* const* partials,
                              int32_t n_partials, void* const* comm_dst, void* const* final_dst,
