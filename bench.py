@@ -330,7 +330,8 @@ def run_ours(args):
     def flush():
         flush_buf.fill_(1)
 
-    trace = torch.zeros(pipe.tiles + w.wave_width, dtype=torch.int64, device=dev)
+    # tile stamps, CTA starts, and two stamps per split tile of the last wave
+    trace = torch.zeros(pipe.tiles + 3 * w.wave_width, dtype=torch.int64, device=dev)
 
     # Dynamic routing (expert capacities fixed): every step takes the next of
     # a few routings resident in HBM, with its routed A (the dispatch gather,
@@ -488,15 +489,20 @@ def run_ours(args):
         fo.fo_plan_set_trace(pipe.plan, 0, 0)
         stamps = trace.cpu().numpy().astype(np.int64)
         cst = ctrace.cpu().numpy().astype(np.int64)
-        t0 = stamps[pipe.tiles:].min()
+        t0 = stamps[pipe.tiles:pipe.tiles + w.wave_width].min()
         rec = cst[2 * pipe.P:].reshape(-1, 4)
         rec = rec[rec[:, 1] > 0]
 
         def rel(x):
             return [(float(v) - t0) / 1e3 if v > 0 else None for v in x]
         with open(args.trace_out, "w") as f:
+            n_split = fo.fo_plan_set_split(pipe.plan, True)
+            split = stamps[pipe.tiles + w.wave_width:pipe.tiles + w.wave_width + 2 * n_split]
             json.dump({"tile_done_us": ((stamps[:pipe.tiles] - t0) / 1e3).tolist(),
-                       "gemm_cta_start_us": rel(stamps[pipe.tiles:]),
+                       "gemm_cta_start_us": rel(stamps[pipe.tiles:pipe.tiles + w.wave_width]),
+                       "split_tiles": n_split,
+                       "split_helper_done_us": rel(split[0::2]),
+                       "split_owner_half_done_us": rel(split[1::2]),
                        "group_consumed_us": rel(cst[:pipe.P]),
                        "group_reordered_us": rel(cst[pipe.P:2 * pipe.P]),
                        "consumer_cta": [{"sm": int(r[0]), "start_us": (r[1] - t0) / 1e3,

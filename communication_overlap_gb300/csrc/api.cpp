@@ -110,6 +110,13 @@ fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairabl
   return FO_OK;
 }
 
+fo_status fo_plan_set_split(fo_plan* p, int32_t enable, int32_t* split_tiles) {
+  if (!p) return FO_ERR_ARG;
+  p->split_enabled = enable != 0;
+  if (split_tiles) *split_tiles = p->split_enabled ? p->split_n : 0;
+  return FO_OK;
+}
+
 fo_status fo_plan_set_trace(fo_plan* p, uint64_t* stamps, uint64_t* consumer_stamps) {
   if (!p) return FO_ERR_ARG;
   p->trace = stamps;

@@ -253,89 +253,20 @@ __global__ void __launch_bounds__(kThreads) consume_kernel(const __grid_constant
 // Consumer with the post-communication reorder (and the element-wise
 // epilogue) fused in: one persistent kernel, on the GEMM's stream, that
 // moves every group to its final layout while the GEMM still computes later
-// groups.
-//  * Tile and ReduceScatter layouts: a CTA that has written a chunk of
-//    units to the communication buffers reads them back from there and
-//    moves each unit to its final place at once (unit_src names the tile
-//    row a unit holds), so a group is final one chunk after it is
-//    communicated, with no wait on other CTAs.
-//  * All-to-All: a unit's final place depends on the routing, so a CTA that
-//    has taken its share of group j's communication reorders group j-1 tile
-//    by tile, after waiting until every chunk of j-1 is counted as consumed.
+// groups.  A CTA that has written a chunk of units to the communication
+// buffers reads them back from there -- still in L2 -- and moves each unit
+// to its final place at once: unit_src names the tile row a unit holds, the
+// inverse mapping gives its place.  No CTA waits for another, so a group is
+// final one chunk after its flag rises.
 
 struct FusedArgs {
   ConsumeArgs c;                  // the communication part (c.dst: its outputs)
   uint4* fin[kMaxDest];           // final outputs of the reorder
   RowMap map;
   const uint16_t* bias;
-  const int32_t* group_slot_begin;
-  const int32_t* unit_src;  // [units] slot << 7 | row (tile and RS layouts)
-  int32_t* rwork;  // [P] reorder chunk counters, [P] units consumed, [1] CTAs done
+  const int32_t* unit_src;  // [units] slot << 7 | row of the tile row each unit holds
   int32_t act, row_vec;
 };
-
-// Wait until *p >= target (acquire loads, __nanosleep back-off, bounded).
-__device__ __forceinline__ bool wait_count(const int32_t* p, int32_t target, uint64_t limit_ns) {
-  if (int32_t(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p))) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t backoff = 32;
-  while (true) {
-    __nanosleep(backoff);
-    if (int32_t(ld_acquire_gpu(reinterpret_cast<const uint32_t*>(p))) >= target) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-    if (backoff < 1024) backoff <<= 1;
-  }
-}
-
-// Rows of one reorder work item: every lane of the CTA has kBatch
-// independent 16-byte loads in flight, all issued before the stores, so an
-// item costs one memory round trip.  Items are smaller than a tile (a
-// quarter at tile_n = 256) so that the last group's reorder, which runs
-// after the GEMM has finished, spreads over more CTAs.
-template <int VPU>
-constexpr int kItemRows = (kThreads / 32) * (32 / VPU) * 4;
-
-// Rows r0 .. r0 + kItemRows of the tile at slot s from the communication
-// buffers to the final layout: warp w takes row groups w, w + 8, ...
-template <int VPU>
-__device__ __forceinline__ void reorder_rows_regs(const FusedArgs& a, uint4* const* src,
-                                                  uint4* const* fin, int32_t s, int32_t r0,
-                                                  int tid) {
-  constexpr int kRowsPerInstr = 32 / VPU;
-  constexpr int kWarps = kThreads / 32;
-  constexpr int kBatch = 4;   // loads per lane (kept small: this kernel shares
-                              // its register budget with the consumer)
-  static_assert(kItemRows<VPU> == kWarps * kRowsPerInstr * kBatch, "one round per item");
-  const int warp = tid / 32, lane = tid % 32, sub = lane / VPU, vl = lane % VPU;
-  const TileInfo ti = a.map.tile[s];
-  const uint64_t pol = l2_evict_first();   // the received data is read once
-  {
-    uint4 x[kBatch];
-    int64_t to[kBatch];
-    int kk[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int32_t r = r0 + (i * kWarps + warp) * kRowsPerInstr + sub;
-      kk[i] = -1;
-      if (r < ti.rows) {
-        int32_t su, dr;
-        map_row(a.map, ti, s, r, &kk[i], &su, &dr);
-        if (kk[i] >= 0) {   // not an empty All-to-All row
-          x[i] = ld_once(src[kk[i]] + int64_t(su) * VPU + vl, pol);
-          to[i] = int64_t(dr) * a.row_vec + (ti.col0 >> 3) + vl;
-        }
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      if (kk[i] < 0) continue;
-      uint4 y = x[i];
-      if (a.act != FO_ACT_NONE || a.bias != nullptr)
-        y = epilogue8(y, a.bias, ti.col0 + vl * 8, a.act);
-      st_cs(fin[kk[i]] + to[i], y);
-    }
-  }
-}
 
 // Where the units of a chunk go, computed by threads t < units before the
 // chunk is consumed (their loads overlap the other warps' consume loads):
@@ -400,12 +331,9 @@ __device__ __forceinline__ void reorder_chunk_regs(const FusedArgs& a, const Chu
 // 70 registers run beside each GEMM CTA while the GEMM runs, at 80 only one.
 template <int KIND, int U, int VPU>
 __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ FusedArgs a) {
-  // tile and RS layouts: each chunk is reordered right after it is written
-  constexpr bool kChunkwise = KIND != FO_CONS_A2A;
-  // 16-byte vectors of a chunk per thread
-  constexpr int kNV = kChunkBytes<KIND> / (16 * kThreads);
-  __shared__ ChunkMap s_map;
+  constexpr int kNV = kChunkBytes<KIND> / (16 * kThreads);   // vectors of a chunk per thread
   const ConsumeArgs& c = a.c;
+  __shared__ ChunkMap s_map;
   __shared__ int s_ok;
   __shared__ int32_t s_chunk[2];
   __shared__ int32_t s_ps[kMaxDest], s_pl[kMaxDest], s_pd[kMaxDest];
@@ -416,48 +344,11 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
     s_dst[tid] = c.dst[tid];
     s_fin[tid] = a.fin[tid];
   }
-  int32_t* done = a.rwork + c.P;
-  bool ok = true;
   uint64_t t_start = 0;
   int32_t chunks_done = 0;
   if (c.trace != nullptr && tid == 0) t_start = globaltimer_ns();
 
-  // reorder every tile of group j once its communication is complete
-  auto reorder_group = [&](int j) {
-    if (tid == 0) {
-      const int32_t units = c.group_unit_begin[j + 1] - c.group_unit_begin[j];
-      s_ok = wait_count(done + j, units, c.limit_ns) ? 1 : 0;
-    }
-    __syncthreads();
-    if (!s_ok) {
-      if (tid == 0) atomicCAS(c.status, 0, int32_t(FO_ERR_TIMEOUT));
-      ok = false;
-      return;
-    }
-    constexpr int kItems = kTileM / kItemRows<VPU>;   // work items per tile
-    const int32_t s0 = a.group_slot_begin[j];
-    const int32_t n = (a.group_slot_begin[j + 1] - s0) * kItems;
-    if (tid == 0) s_chunk[0] = atomicAdd(a.rwork + j, 1);
-    __syncthreads();
-    for (int buf = 0;; buf ^= 1) {
-      const int32_t t = s_chunk[buf];
-      if (t >= n) break;
-      if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(a.rwork + j, 1);
-      reorder_rows_regs<VPU>(a, s_dst, s_fin, s0 + t / kItems, (t % kItems) * kItemRows<VPU>,
-                             tid);
-      __syncthreads();
-      if (c.trace != nullptr && tid == 0)   // latest item end: the group is reordered
-        atomicMax(reinterpret_cast<unsigned long long*>(c.trace + c.P + j),
-                  static_cast<unsigned long long>(globaltimer_ns()));
-    }
-    __syncthreads();
-  };
-
-  for (int j = c.g0; j < c.g1 && ok; ++j) {
-    if (!kChunkwise && j > c.g0) {
-      reorder_group(j - 1);
-      if (!ok) break;
-    }
+  for (int j = c.g0; j < c.g1; ++j) {
     // The group's first chunk is taken, and its unit map computed, before
     // the wait on the group's flag: when the group completes, only the data
     // moves are left.
@@ -470,18 +361,15 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
       s_pd[tid] = c.part_dst[j * c.R + tid];
     }
     __syncthreads();
-    if constexpr (kChunkwise) {
-      const int32_t first = s_chunk[0];
-      if (first < n_chunks) {
-        const int32_t u0 = ub + first * c.chunk_units;
-        map_chunk_units(a, s_map, u0, min(u0 + c.chunk_units, ue), tid);
-      }
+    const int32_t first = s_chunk[0];
+    if (first < n_chunks) {
+      const int32_t u0 = ub + first * c.chunk_units;
+      map_chunk_units(a, s_map, u0, min(u0 + c.chunk_units, ue), tid);
     }
     if (tid == 0) s_ok = wait_flag(c.flags + j, c.epoch, c.limit_ns) ? 1 : 0;
     __syncthreads();
     if (!s_ok) {
       if (tid == 0) atomicCAS(c.status, 0, int32_t(FO_ERR_TIMEOUT));
-      ok = false;
       break;
     }
     for (int buf = 0, n = 0;; buf ^= 1, ++n) {
@@ -490,34 +378,21 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
       if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(c.work + j, 1);
       const int32_t u0 = ub + ch * c.chunk_units;
       const int32_t u1 = min(u0 + c.chunk_units, ue);
-      if constexpr (kChunkwise)
-        if (n > 0) map_chunk_units(a, s_map, u0, u1, tid);   // the first is mapped
+      if (n > 0) map_chunk_units(a, s_map, u0, u1, tid);   // the first is mapped
       consume_range<KIND, U>(c, s_ps, s_pl, s_pd, s_dst, u0 << c.vpu_shift, u1 << c.vpu_shift,
                              tid);
       __syncthreads();   // the chunk's stores and its map are visible to the whole CTA
-      if constexpr (kChunkwise) {
-        reorder_chunk_regs<VPU, kNV>(a, s_map, s_dst, s_fin, u1 - u0, tid);
-        __syncthreads();   // s_map is free for the next chunk
-        if (c.trace != nullptr && tid == 0) {
-          const unsigned long long now = globaltimer_ns();
-          atomicMax(reinterpret_cast<unsigned long long*>(c.trace + j), now);
-          atomicMax(reinterpret_cast<unsigned long long*>(c.trace + c.P + j), now);
-          ++chunks_done;
-        }
-      } else if (tid == 0) {
-        // this chunk's outputs are visible before it is counted as consumed
-        __threadfence();
-        atomicAdd(done + j, u1 - u0);
-        if (c.trace != nullptr) {
-          atomicMax(reinterpret_cast<unsigned long long*>(c.trace + j),
-                    static_cast<unsigned long long>(globaltimer_ns()));
-          ++chunks_done;
-        }
+      reorder_chunk_regs<VPU, kNV>(a, s_map, s_dst, s_fin, u1 - u0, tid);
+      __syncthreads();   // s_map is free for the next chunk
+      if (c.trace != nullptr && tid == 0) {
+        const unsigned long long now = globaltimer_ns();
+        atomicMax(reinterpret_cast<unsigned long long*>(c.trace + j), now);
+        atomicMax(reinterpret_cast<unsigned long long*>(c.trace + c.P + j), now);
+        ++chunks_done;
       }
     }
     __syncthreads();
   }
-  if (!kChunkwise && ok && c.g1 > c.g0) reorder_group(c.g1 - 1);
   if (c.trace != nullptr && tid == 0) {
     uint64_t* rec = c.trace + 2 * c.P + 4 * blockIdx.x;
     uint32_t smid;
@@ -535,14 +410,9 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    int32_t* exit_count = a.rwork + 2 * c.P;
-    if (atomicAdd(exit_count, 1) == int32_t(gridDim.x) - 1) {
-      for (int j = c.g0; j < c.g1; ++j) {
-        atomicExch(c.work + j, 0);
-        atomicExch(a.rwork + j, 0);
-        atomicExch(done + j, 0);
-      }
-      atomicExch(exit_count, 0);
+    if (atomicAdd(c.work + c.P, 1) == int32_t(gridDim.x) - 1) {
+      for (int j = c.g0; j < c.g1; ++j) atomicExch(c.work + j, 0);
+      atomicExch(c.work + c.P, 0);
     }
   }
 }
@@ -731,9 +601,7 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
   c.trace = p->consumer_trace;
   a.map = make_row_map(p);
   a.bias = static_cast<const uint16_t*>(bias);
-  a.group_slot_begin = p->dev.group_slot_begin;
   a.unit_src = p->dev.unit_src;
-  a.rwork = p->dev.rwork;
   a.act = act;
   a.row_vec = p->N / 8;
   const int ctas = default_ctas(p, p->consumer_ctas, kind, true);

@@ -44,8 +44,8 @@ struct DeviceTables {
   int32_t* row_rank = nullptr;         // [M] A2A: index among the rows of its
                                        //   tile row that go to the same rank
   int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
-  int32_t* unit_src = nullptr;         // [units] tile and RS layouts: slot << 7 | row
-                                       //   of the tile row each unit holds
+  int32_t* unit_src = nullptr;         // [units] slot << 7 | row of the tile row each
+                                       //   unit holds (A2A: room for M * N / tile_n)
   int32_t* slot_live = nullptr;        // [tiles] A2A: 1 if a row of the tile holds
                                        //   a token (else the GEMM skips it)
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
@@ -55,8 +55,10 @@ struct DeviceTables {
                                        //   overlapped reorder)
   int32_t* rtile = nullptr;            // [2] scratch of the reorder: tile counter,
                                        //   CTAs done
-  int32_t* rwork = nullptr;            // [2P + 1] scratch of the fused consumer+reorder
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
+  void* split_ws = nullptr;            // [split_n * 128 * tile_n] fp32 partial sums of
+                                       //   the last wave's split tiles
+  uint32_t* split_flag = nullptr;      // [split_n * 4] per tile quarter: launch seq
   int32_t* route_cnt = nullptr;        // [blocks * (R + 1)] A2A scratch of
                                        //   fo_plan_route: rows per (tile-row
                                        //   block, rank), then a flag per block
@@ -85,6 +87,11 @@ struct fo_plan {
   int sm_count = 0;
   int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
   int gemm_variant = 0;   // fo_gemm_variant
+  // last-wave split: when the last wave holds split_n <= W / 2 tiles, each
+  // is computed by two CTAs over halves of K (0: no split possible)
+  int32_t split_n = 0;
+  bool split_enabled = true;
+  mutable uint32_t gemm_seq = 0;   // GEMM launches on this plan (never 0 once launched)
   // sequence number of the last consume launched on this plan: a reorder
   // launched as its programmatic dependent waits until consumed[j] holds it
   mutable uint32_t consume_seq = 0;

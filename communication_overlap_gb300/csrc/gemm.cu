@@ -65,7 +65,11 @@ struct Cfg {
                                      (uint32_t(BN >> 3) << 17) |
                                      (uint32_t(kMmaM >> 4) << 24);
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(2 * kStages + 7 + 1 <= 32, "barrier area");
+  static_assert(2 * kStages + 8 + 4 <= 32, "barrier area");
+  // a split tile's partial sums, a quarter (32 rows) per epilogue warp, are
+  // received into the pipeline stages (idle by then)
+  static constexpr int kQuarterBytes = 32 * BN * 4;
+  static_assert(4 * kQuarterBytes <= kStages * kStageBytes, "partial sums fit the stages");
 };
 
 struct GemmArgs {
@@ -82,6 +86,12 @@ struct GemmArgs {
   uint32_t* flags;
   int32_t* status;
   uint64_t* trace;  // optional: [tiles] tile done times, then [grid] CTA starts
+  // last-wave split (split_n > 0): the last wave's split_n tiles, from slot
+  // split_slot0 on, are each computed by two CTAs over halves of K
+  float4* split_ws;       // [split_n][4 quarters][BN / 64][16][32] fp32 partials
+  uint32_t* split_flag;   // [split_n * 4] = seq once a quarter's partial is written
+  int32_t split_n, split_slot0, split_wave;
+  uint32_t seq;           // this launch's number on the plan (never 0)
   int32_t tiles, k_blocks, layout, R, h;
   uint32_t epoch;
 };
@@ -261,6 +271,56 @@ __device__ __forceinline__ int32_t row_unit(const GemmArgs& a, const TileInfo& t
   return ti.unit_base + r;
 }
 
+// One item of a CTA's work: the tile at `slot`, k-blocks [kb0, kb1), and
+// its role: 0 a whole tile; 1 the owner of a split tile (first half of K;
+// adds the helper's partial before its epilogue stores, then counts the
+// tile); 2 the helper (second half of K; hands over its fp32 partial).
+struct Work {
+  int32_t slot, kb0, kb1, role;
+};
+
+// Item k of this CTA.  CTA c takes slots c, c + W, ... (wave = slot / W).
+// When the last wave holds n <= W / 2 tiles, its tile c < n is split: CTA c
+// computes the first half of K and CTA c + n (idle in that wave otherwise)
+// the second.  With pairs n is even, so both CTAs of a pair help the two
+// vertically adjacent tiles of one owner pair.
+__device__ __forceinline__ bool next_work(const GemmArgs& a, int32_t k, Work& w) {
+  const int32_t c = blockIdx.x, W = gridDim.x;
+  if (a.split_n > 0 && k == a.split_wave) {
+    const int32_t half = a.k_blocks / 2;
+    if (c < a.split_n) {
+      w = Work{a.split_slot0 + c, 0, half, 1};
+      return true;
+    }
+    if (c < 2 * a.split_n) {
+      w = Work{a.split_slot0 + c - a.split_n, half, a.k_blocks, 2};
+      return true;
+    }
+    return false;
+  }
+  const int32_t slot = c + k * W;
+  if (slot >= a.tiles) return false;
+  w = Work{slot, 0, a.k_blocks, 0};
+  return true;
+}
+
+// Bounded wait (lane 0) for a helper's partial: flag == seq.
+__device__ __noinline__ bool wait_partial(const uint32_t* flag, uint32_t seq,
+                                          volatile int* abort_flag, int32_t* status) {
+  if (ld_acquire_gpu(flag) == seq) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) == seq) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(status, 0, int32_t(FO_ERR_TIMEOUT));
+      return false;
+    }
+  }
+}
+
 // A tile none of whose rows holds a token (All-to-All capacity the routing
 // left empty) has no output: its loads and MMAs are skipped and the tile is
 // only counted.  A pair computes its two tiles with one MMA, so it skips only
@@ -272,9 +332,10 @@ __device__ __forceinline__ bool tile_skipped(const GemmArgs& a, int32_t slot) {
   return a.slot_live[slot] == 0;
 }
 
+// 192 threads; registers capped at 112 so that two 256-thread consumer CTAs
+// at 72 registers fit beside a GEMM CTA on an SM.
 template <int BN, bool PAIR>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    signaled_gemm_kernel(const __grid_constant__ GemmArgs a) {
+__global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ GemmArgs a) {
   using C = Cfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms (the same offsets in
@@ -290,6 +351,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* epi_done = bars + 2 * C::kStages + 4;
   uint64_t* drain = bars + 2 * C::kStages + 6;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 7);
+  uint64_t* part_bar = bars + 2 * C::kStages + 8;   // [4] a quarter of partial sums landed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -306,6 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&epi_done[b]), 4);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&part_bar[b]), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -348,13 +411,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int64_t issued = 0;
-      for (int32_t slot = blockIdx.x; slot < a.tiles && ok; slot += gridDim.x) {
+      Work wk;
+      for (int32_t item = 0; ok && next_work(a, item, wk); ++item) {
+        const int32_t slot = wk.slot;
         const TileInfo ti = a.tile[slot];
         const CUtensorMap* mb = &a.tmap_b[ti.expert];
-        if (slot == int32_t(blockIdx.x))
+        if (item == 0)
           for (int e = 0; e <= ti.expert; ++e) prefetch_tmap(&a.tmap_b[e]);
         if (tile_skipped<PAIR>(a, slot)) continue;
-        for (int kb = 0; kb < a.k_blocks; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
@@ -407,12 +472,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int32_t slot = blockIdx.x; slot < a.tiles && ok; slot += gridDim.x) {
-        if (tile_skipped<PAIR>(a, slot)) continue;
+      Work wk;
+      for (int32_t item = 0; ok && next_work(a, item, wk); ++item) {
+        if (tile_skipped<PAIR>(a, wk.slot)) continue;
         if (!mbar_wait(smem_u32(&acc_empty[acc]), acc_phase ^ 1, abort_flag, a.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-        for (int kb = 0; kb < a.k_blocks; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, a.status)) {
             ok = false;
             break;
@@ -428,10 +494,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // blocks, SBO = 8 K rows x 128 B.
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024);
             const uint64_t bd = smem_desc(sb + kk * 2048, kBlockK * 128, 1024);
+            const uint32_t accumulate = (kb != wk.kb0 || kk != 0) ? 1u : 0u;
             if constexpr (PAIR)
-              mma_bf16_pair(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0);
+              mma_bf16_pair(d_tmem, ad, bd, C::kIdesc, accumulate);
             else
-              mma_bf16(d_tmem, ad, bd, C::kIdesc, (kb | kk) != 0);
+              mma_bf16(d_tmem, ad, bd, C::kIdesc, accumulate);
           }
           if constexpr (PAIR)
             mma_commit_pair(smem_u32(&empty[stage]));
@@ -460,11 +527,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t stage_base = smem_u32(stage_buf);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int32_t slot = blockIdx.x; slot < a.tiles; slot += gridDim.x) {
+    Work wk;
+    for (int32_t item = 0; next_work(a, item, wk); ++item) {
+      const int32_t slot = wk.slot;
       const TileInfo ti = a.tile[slot];
       if (tile_skipped<PAIR>(a, slot)) {
-        // nothing computed, nothing stored: only counted (and signalled)
-        if (warp == 2 && lane == 0) {
+        // nothing computed, nothing stored: only counted (and signalled),
+        // by its owner
+        if (warp == 2 && lane == 0 && wk.role != 2) {
           if (a.count != nullptr) {
             const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
             if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
@@ -480,14 +550,96 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (lane == 0) ok = mbar_wait(smem_u32(&acc_full[acc]), acc_phase, abort_flag, a.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
+      // a split tile's quarter q of the partial sums: [chunk][16 x 4 cols][lane]
+      float4* part = nullptr;
+      uint32_t* part_flag = nullptr;
+      if (wk.role != 0) {
+        const int32_t i = slot - a.split_slot0;
+        part = a.split_ws + size_t(i * 4 + q) * (BN / 64) * 16 * 32;
+        part_flag = a.split_flag + i * 4 + q;
+      }
+      // The owner waits for the helper's quarter and copies it (TMA, one
+      // bulk copy per warp) into the pipeline stages: this is the CTA's last
+      // item, so once its accumulator is full no stage is read or filled any
+      // more.
+      const float* part_smem = reinterpret_cast<const float*>(smem + q * C::kQuarterBytes);
+      if (wk.role == 1) {
+        if (a.trace != nullptr && lane == 0 && q == 0)   // the owner's half is computed
+          a.trace[a.tiles + gridDim.x + 2 * (slot - a.split_slot0) + 1] = globaltimer_ns();
+        const uint32_t pb = smem_u32(&part_bar[q]);
+        if (lane == 0) {
+          ok = wait_partial(part_flag, a.seq, abort_flag, a.status);
+          if (ok) {
+            // the helper's generic stores are read next by the TMA engine
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            mbar_expect_tx(pb, uint32_t(C::kQuarterBytes));
+            bulk_load(smem_u32(part_smem), part, uint32_t(C::kQuarterBytes), pb);
+            ok = mbar_wait(pb, 0, abort_flag, a.status);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // every lane observes the completed copy before reading it
+        if (!mbar_wait(pb, 0, abort_flag, a.status)) break;
+      }
       tc_fence_after();
       const uint32_t t_row = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+      if (wk.role == 2) {
+        // the helper: hand this lane's row of fp32 partial sums over (each
+        // warp instruction writes 512 contiguous bytes), then release the
+        // accumulator and publish the quarter
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 64; ++cc) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(t_row + cc * 64, v0);
+          tmem_ld32(t_row + cc * 64 + 32, v1);
+          tmem_wait_ld();
+          float4* dst = part + cc * 16 * 32 + lane;
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const uint32_t* src = (c4 < 8) ? &v0[c4 * 4] : &v1[(c4 - 8) * 4];
+            __stcg(dst + c4 * 32, make_float4(__uint_as_float(src[0]), __uint_as_float(src[1]),
+                                              __uint_as_float(src[2]), __uint_as_float(src[3])));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          st_release_gpu(part_flag, a.seq);
+          if (a.trace != nullptr && q == 0)   // when the helper handed its partial over
+            a.trace[a.tiles + gridDim.x + 2 * (slot - a.split_slot0)] = globaltimer_ns();
+          mbar_arrive(smem_u32(&epi_done[acc]));
+          if (PAIR && rank != 0)
+            mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[acc]), 0));
+          else
+            mbar_arrive(smem_u32(&acc_empty[acc]));
+        }
+        __syncwarp();
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+        continue;
+      }
 #pragma unroll 1
       for (int cc = 0; cc < BN / 64; ++cc) {
         uint32_t v0[32], v1[32];
         tmem_ld32(t_row + cc * 64, v0);
         tmem_ld32(t_row + cc * 64 + 32, v1);
         tmem_wait_ld();
+        if (wk.role == 1) {   // add the helper's half of K (fp32, from shared memory)
+          const float4* src = reinterpret_cast<const float4*>(part_smem) + cc * 16 * 32 + lane;
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 h = src[c4 * 32];
+            uint32_t* d = (c4 < 8) ? &v0[c4 * 4] : &v1[(c4 - 8) * 4];
+            d[0] = __float_as_uint(__uint_as_float(d[0]) + h.x);
+            d[1] = __float_as_uint(__uint_as_float(d[1]) + h.y);
+            d[2] = __float_as_uint(__uint_as_float(d[2]) + h.z);
+            d[3] = __float_as_uint(__uint_as_float(d[3]) + h.w);
+          }
+        }
         // round to bf16 and write this lane's row (128 B) into the staging
         // buffer, 16-byte pieces rotated by row to spread the banks
 #pragma unroll
@@ -690,6 +842,15 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.trace = p->trace;
   a.tiles = p->tiles;
   a.k_blocks = p->K / kBlockK;
+  if (++p->gemm_seq == 0) p->gemm_seq = 1;
+  a.seq = p->gemm_seq;
+  if (p->split_n > 0 && p->split_enabled) {
+    a.split_ws = static_cast<float4*>(p->dev.split_ws);
+    a.split_flag = p->dev.split_flag;
+    a.split_n = p->split_n;
+    a.split_wave = p->waves - 1;
+    a.split_slot0 = (p->waves - 1) * p->W;
+  }
   a.layout = p->layout;
   a.R = p->R;
   a.h = kTileM / p->R;

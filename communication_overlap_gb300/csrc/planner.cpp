@@ -145,6 +145,13 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
     }
   }
 
+  // Last-wave split: a last wave of n <= W / 2 tiles leaves at least n CTAs
+  // idle; each of its tiles is then computed by two CTAs over halves of K.
+  {
+    const int32_t n_last = tiles - (waves - 1) * W;
+    p->split_n = (waves >= 2 && 2 * n_last <= W && d->K / kBlockK >= 2) ? n_last : 0;
+  }
+
   // CTA pairs: with W even, CTAs 2p and 2p+1 take slots 2i and 2i+1 of every
   // wave; they can share one M = 256 MMA when those are vertically adjacent
   // tiles of the same expert and column.
@@ -321,14 +328,16 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   } else {
     p->final_rows.assign(R, d->M / R);
   }
-  if (layout != FO_LAYOUT_A2A_SUBTOKEN) {
-    p->dest_capacity = p->dest_units;
-    // the inverse of the unit layout at row granularity: which tile row each
-    // unit holds (read by the fused consumer+reorder)
-    p->unit_src.assign(p->n_units, 0);
-    for (int32_t s = 0; s < tiles; ++s)
-      for (int32_t r = 0; r < p->tile[s].rows; ++r) p->unit_src[unit_of(p, s, r)] = (s << 7) | r;
-  }
+  if (layout != FO_LAYOUT_A2A_SUBTOKEN) p->dest_capacity = p->dest_units;
+  // The inverse of the unit layout at row granularity: which tile row each
+  // unit holds (read by the fused consumer+reorder).  All-to-All: room for
+  // every row, since fo_plan_route may route them all.
+  p->unit_src.assign(layout == FO_LAYOUT_A2A_SUBTOKEN ? size_t(d->M) * TN : size_t(p->n_units), 0);
+  for (int32_t s = 0; s < tiles; ++s)
+    for (int32_t r = 0; r < p->tile[s].rows; ++r) {
+      const int32_t u = unit_of(p, s, r);
+      if (u >= 0) p->unit_src[u] = (s << 7) | r;
+    }
   return FO_OK;
 }
 
@@ -405,13 +414,14 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_fin = put(buf, std::vector<int32_t>(p->P, 0));
   const size_t o_cons = put(buf, std::vector<int32_t>(p->P, 0));
   const size_t o_rtile = put(buf, std::vector<int32_t>(2, 0));
-  const size_t o_rwork = put(buf, std::vector<int32_t>(2 * p->P + 1, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
   const bool a2a = p->layout == FO_LAYOUT_A2A_SUBTOKEN;
   if (a2a) {
     p->route_blocks = 0;
     for (int32_t rows : p->expert_rows) p->route_blocks += (rows + kTileM - 1) / kTileM;
   }
+  const size_t o_sws = put(buf, std::vector<float>(size_t(p->split_n) * kTileM * p->tile_n, 0.f));
+  const size_t o_sfl = put(buf, std::vector<int32_t>(size_t(p->split_n) * 4, 0));
   const size_t o_rc =
       put(buf, std::vector<int32_t>(a2a ? size_t(p->route_blocks) * (p->R + 1) : 1, 0));
   void* blob = nullptr;
@@ -439,9 +449,10 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.finished = reinterpret_cast<int32_t*>(b + o_fin);
   p->dev.consumed = reinterpret_cast<uint32_t*>(b + o_cons);
   p->dev.rtile = reinterpret_cast<int32_t*>(b + o_rtile);
-  p->dev.rwork = reinterpret_cast<int32_t*>(b + o_rwork);
   p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
   p->dev.route_cnt = reinterpret_cast<int32_t*>(b + o_rc);
+  p->dev.split_ws = b + o_sws;
+  p->dev.split_flag = reinterpret_cast<uint32_t*>(b + o_sfl);
   return FO_OK;
 }
 

@@ -36,7 +36,8 @@
 //                 dest_base[s][d]     = part_start[j][d] + E(s, d) - E(gsb[j], d)
 //               CTA 0 writes the per-group tables, all CTAs the per-slot ones
 //               (dest_base, and whether any row of the tile holds a token:
-//               the GEMM skips tiles that hold none).
+//               the GEMM skips tiles that hold none) and the per-unit one
+//               (which tile row each unit holds).
 //
 // An invalid routing (token >= n_tokens, slot outside [0, top_k), or more
 // units for a rank than its receive buffer holds) routes nothing: every row
@@ -69,6 +70,7 @@ struct RouteArgs {
   int32_t* group_unit_begin;  // [P + 1]
   int32_t* dest_base;         // [tiles * R]
   int32_t* slot_live;         // [tiles] 1 if a row of the tile holds a token
+  int32_t* unit_src;          // [units] slot << 7 | row of the tile row each unit holds
   int32_t* status;            // caller's status word
   int32_t expert_row0[kMaxExperts];
   int32_t expert_rows[kMaxExperts];
@@ -238,12 +240,28 @@ __global__ void __launch_bounds__(kPartsThreads) route_parts_kernel(const __grid
       a.slot_live[s] = (!bad && n > 0) ? 1 : 0;
     }
   }
-  if (bad)
+  if (bad) {
     for (int32_t r = first; r < a.M; r += stride) {
       a.row_dest[r] = -1;
       a.row_rank[r] = -1;
       a.final_row[r] = -1;
     }
+    return;
+  }
+  // 5. the inverse at row granularity: unit -> the tile row it holds (read by
+  //    the fused consumer+reorder); row r of the tile at slot s is unit
+  //    dest_base[s][d] + rank, computed here from the same closed form
+  for (int64_t i = first; i < int64_t(a.tiles) * kTileM; i += stride) {
+    const int32_t s = int32_t(i / kTileM), r = int32_t(i % kTileM);
+    const TileInfo& ti = a.tile[s];
+    if (r >= ti.rows) continue;
+    const int32_t rho = ti.row0 + r;
+    const int d = a.row_dest[rho];
+    if (d < 0) continue;
+    const int32_t u = off[ti.group * R + d] +
+                      units_before(a, BP, ti.row0, ti.col0, ti.expert, d) + a.row_rank[rho];
+    a.unit_src[u] = (s << 7) | r;
+  }
 }
 
 size_t parts_smem_bytes(const fo_plan* p) {
@@ -288,6 +306,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
   a.group_unit_begin = p->dev.group_unit_begin;
   a.dest_base = p->dev.dest_base;
   a.slot_live = p->dev.slot_live;
+  a.unit_src = p->dev.unit_src;
   a.status = dev_status;
   const int E = int(p->expert_rows.size());
   int32_t blocks = 0;

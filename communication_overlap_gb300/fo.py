@@ -69,6 +69,7 @@ def lib():
                                                   ctypes.c_int32]),
             "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp, _vp]),
             "fo_plan_set_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _i32p]),
+            "fo_plan_set_split": (ctypes.c_int, [_vp, ctypes.c_int32, _i32p]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
             "fo_plan_destroy": (None, [_vp]),
             "fo_counting_table_init": (ctypes.c_int, [_vp, _vp, _vp]),
@@ -204,6 +205,14 @@ def fo_plan_set_gemm(plan, variant=FO_GEMM_AUTO):
     _check("fo_plan_set_gemm", lib().fo_plan_set_gemm(plan, variant, ctypes.byref(pairable),
                                                       ctypes.byref(cap)))
     return bool(pairable.value), cap.value
+
+
+def fo_plan_set_split(plan, enable=True):
+    """Enable or disable the last-wave split; returns the number of split tiles."""
+    n = ctypes.c_int32()
+    _check("fo_plan_set_split", lib().fo_plan_set_split(plan, 1 if enable else 0,
+                                                        ctypes.byref(n)))
+    return n.value
 
 
 def fo_plan_set_trace(plan, stamps, consumer_stamps=0):

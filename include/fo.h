@@ -195,12 +195,27 @@ typedef enum { FO_GEMM_AUTO = 0, FO_GEMM_SINGLE = 1, FO_GEMM_PAIRS = 2 } fo_gemm
 fo_status fo_plan_set_gemm(fo_plan* plan, fo_gemm_variant variant, int32_t* pairable,
                            int32_t* pair_capacity);
 
+/* Last-wave split.  When the last wave holds n <= W / 2 tiles (e.g. 68 of
+ * 148), n CTAs would idle through it; instead each of its tiles is computed
+ * by two CTAs over halves of K: CTA c < n (the tile's own CTA) takes the
+ * first half, CTA c + n the second and hands its fp32 partial sums over
+ * through a workspace in the plan (128 x tile_n x 4 bytes per tile); the
+ * owner adds them and stores, counts and signals the tile as usual.  Waves,
+ * groups, tables and the counting table do not change; only the order of
+ * the fp32 additions of those tiles does.  Enabled by default when the
+ * shape allows it.  *split_tiles (may be NULL): how many tiles are split
+ * (0 when disabled or not possible). */
+fo_status fo_plan_set_split(fo_plan* plan, int32_t enable, int32_t* split_tiles);
+
 /* Timelines ([P2] Figure 3 records each tile's completion time with
  * globaltimer to show the wave pattern).  Device uint64 buffers owned by the
  * caller, kept alive while tracing; NULL stops that trace.
- *  stamps [tiles + W]: every GEMM launch writes stamps[slot] = %globaltimer
- *      (ns) when the tile at that launch slot has been stored and counted,
- *      and stamps[tiles + c] = the start time of CTA c.
+ *  stamps [tiles + W + 2 * split tiles]: every GEMM launch writes
+ *      stamps[slot] = %globaltimer (ns) when the tile at that launch slot has
+ *      been stored and counted, stamps[tiles + c] = the start time of CTA c,
+ *      and for the i-th split tile of the last wave (fo_plan_set_split)
+ *      stamps[tiles + W + 2i] = when its helper handed its partial sums over
+ *      and stamps[tiles + W + 2i + 1] = when its owner's half was computed.
  *  consumer_stamps [2P + 4 * consumer CTAs], zeroed by the caller before
  *      the consume call (fo_consume_group or fo_consume_reorder): [j] = when
  *      group j's last chunk was processed; [P + j] = when group j's last

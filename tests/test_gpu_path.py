@@ -160,3 +160,42 @@ def test_full_size_workload(name):
         check_run(pipe, inp, res, gemm_rows=rows, full_gemm=False)
     finally:
         pipe.close()
+
+
+@pytest.mark.parametrize("variant", [fo.FO_GEMM_SINGLE, fo.FO_GEMM_PAIRS])
+@pytest.mark.parametrize("split", [True, False])
+def test_last_wave_split(variant, split):
+    """16 tiles on W = 12 CTAs: the last wave holds 4 tiles, so CTAs 0-3 and
+    4-7 each compute half of K of those tiles (pairs: CTA pairs), the owners
+    add the helpers' partial sums; everything matches the oracle with and
+    without the split, and the counting table and flags are the same."""
+    w = _small("wave_pattern", M=512, N=1024, K=512, wave_width=12)
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp, gemm_variant=variant)
+    try:
+        n = fo.fo_plan_set_split(pipe.plan, split)
+        assert n == (4 if split else 0)
+        for _ in range(3):
+            pipe.step()
+        res = pipe.results()
+        check_run(pipe, inp, res)
+        assert fo.fo_plan_device_status(pipe.plan) == 0
+    finally:
+        pipe.close()
+
+
+def test_last_wave_split_exact_entries():
+    """Entries in {-1, 0, 1} give exact sums in any order: the split tiles of
+    the last wave equal the oracle bit for bit."""
+    w = _small("wave_pattern", M=512, N=1024, K=256, wave_width=12)
+    rng = np.random.default_rng(7)
+    inp = W.make_inputs(w)
+    inp.A = OB.round_to_bf16(rng.integers(-1, 2, (w.M, w.K)).astype(np.float64))
+    inp.B = [OB.round_to_bf16(rng.integers(-1, 2, (w.K, w.N)).astype(np.float64))]
+    pipe, inp, res = run_workload(w, inp)
+    try:
+        assert fo.fo_plan_set_split(pipe.plan, True) == 4
+        op = oracle_plan(w, inp, pipe.partition)
+        assert np.array_equal(gpu_gemm_output(pipe, res, op), OG.gemm_bf16(inp.A, inp.B[0]))
+    finally:
+        pipe.close()
