@@ -56,6 +56,7 @@ struct DeviceTables {
   int32_t* rtile = nullptr;            // [2] scratch of the reorder: tile counter,
                                        //   CTAs done
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
+  uint32_t* count_ready = nullptr;     // [1] launch seq once the GEMM zeroed the count table
   void* split_ws = nullptr;            // [split_n * 128 * tile_n] fp32 partial sums of
                                        //   the last wave's split tiles
   uint32_t* split_flag = nullptr;      // [split_n * 4] per tile quarter: launch seq

@@ -83,6 +83,8 @@ struct GemmArgs {
   const int32_t* slot_live;  // A2A: [tiles] 0 = no row of the tile holds a token
   uint16_t* c_r;
   int32_t* count;
+  uint32_t* count_ready;  // = seq once CTA 0 has zeroed count[0 .. P)
+  int32_t n_groups;
   uint32_t* flags;
   int32_t* status;
   uint64_t* trace;  // optional: [tiles] tile done times, then [grid] CTA starts
@@ -304,6 +306,26 @@ __device__ __forceinline__ bool next_work(const GemmArgs& a, int32_t k, Work& w)
   return true;
 }
 
+// The counting table is reset by the kernel itself: CTA 0 zeroes it at its
+// start and publishes count_ready = seq; a CTA's first count waits (bounded)
+// for that, which by then -- after its first tile -- has long happened.
+__device__ __forceinline__ bool count_table_ready(const GemmArgs& a, bool& seen,
+                                                  volatile int* abort_flag) {
+  if (seen) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(a.count_ready) != a.seq) {
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
+      return false;
+    }
+    __nanosleep(64);
+  }
+  seen = true;
+  return true;
+}
+
 // Bounded wait (lane 0) for a helper's partial: flag == seq.
 __device__ __noinline__ bool wait_partial(const uint32_t* flag, uint32_t seq,
                                           volatile int* abort_flag, int32_t* status) {
@@ -369,6 +391,12 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
     }
     mbar_init(smem_u32(drain), 1);
     for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&part_bar[b]), 1);
+    if (blockIdx.x == 0 && a.count != nullptr) {
+      // [P1] 一 "组级 Tile 计数": the counting table starts at [0, ..., 0]
+      for (int j = 0; j < a.n_groups; ++j) a.count[j] = 0;
+      __threadfence();
+      st_release_gpu(a.count_ready, a.seq);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -527,6 +555,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
     const uint32_t stage_base = smem_u32(stage_buf);
     int acc = 0;
     uint32_t acc_phase = 0;
+    bool count_seen = false;   // (warp 2, lane 0) the table was reset
     Work wk;
     for (int32_t item = 0; next_work(a, item, wk); ++item) {
       const int32_t slot = wk.slot;
@@ -535,7 +564,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
         // nothing computed, nothing stored: only counted (and signalled),
         // by its owner
         if (warp == 2 && lane == 0 && wk.role != 2) {
-          if (a.count != nullptr) {
+          if (a.count != nullptr && count_table_ready(a, count_seen, abort_flag)) {
             const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
             if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
           }
@@ -691,7 +720,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
       // tile raises the group's flag.
       if (warp == 2 && lane == 0 && (a.count != nullptr || a.trace != nullptr)) {
         if (mbar_wait(smem_u32(&epi_done[acc]), acc_phase, abort_flag, a.status)) {
-          if (a.count != nullptr) {
+          if (a.count != nullptr && count_table_ready(a, count_seen, abort_flag)) {
             __threadfence();
             const int32_t old = atom_add_acq_rel_gpu(a.count + ti.group, 1);
             if (old + 1 == a.group_tiles[ti.group]) st_release_gpu(a.flags + ti.group, a.epoch);
@@ -837,6 +866,8 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.slot_live = p->layout == FO_LAYOUT_A2A_SUBTOKEN ? p->dev.slot_live : nullptr;
   a.c_r = static_cast<uint16_t*>(C_r);
   a.count = count;
+  a.count_ready = p->dev.count_ready;
+  a.n_groups = p->P;
   a.flags = flags;
   a.status = p->dev.gemm_status;
   a.trace = p->trace;

@@ -4,7 +4,7 @@ Plumbing only: torch provides device memory, streams and events; every
 step of the path is a libfo.so call (see ``fo.py``).  One iteration is, on
 one stream:
 
-  fo_counting_table_init, fo_signaled_gemm(epoch),
+  fo_signaled_gemm(epoch) (which resets the counting table itself),
   fo_consume_group(all groups, epoch)   -- a programmatic dependent launch:
                                            runs alongside the GEMM
   fo_reorder_back(all groups)
@@ -144,9 +144,8 @@ class Pipeline:
 
     # ------------------------------------------------------------ calls
     def gemm(self, stream, epoch, signal=True):
+        # (the kernel resets the counting table itself before counting)
         b = self.buf
-        if signal:
-            fo.fo_counting_table_init(self.plan, b.count.data_ptr(), stream.cuda_stream)
         fo.fo_signaled_gemm(self.plan, b.A.data_ptr(), [x.data_ptr() for x in b.B],
                             b.C_r.data_ptr(), b.count.data_ptr() if signal else 0,
                             b.flags.data_ptr() if signal else 0, epoch, stream.cuda_stream)

@@ -234,7 +234,9 @@ void fo_plan_destroy(fo_plan* plan);
 
 /* Counting table initialisation ([P1] 一 "实现方法: 组级 Tile 计数": the table
  * starts at [0, ..., 0]): cudaMemsetAsync of count_table[0 .. P) on the
- * stream the GEMM will run on.  count_table: device int32[P]. */
+ * stream the GEMM will run on.  count_table: device int32[P].  Optional:
+ * fo_signaled_gemm resets the table itself; this call is for callers that
+ * want it cleared earlier (to read it before the next launch). */
 fo_status fo_counting_table_init(const fo_plan* plan, int32_t* count_table,
                                  void* cuda_stream);
 
@@ -250,8 +252,10 @@ fo_status fo_counting_table_init(const fo_plan* plan, int32_t* count_table,
  *  B:  host array of n_experts (1 for a plain GEMM) device pointers, each
  *      K x N bf16 row-major.
  *  C_reordered: device, M * N bf16 (M * N / tile_n units).
- *  count_table: device int32[P], zeroed by the caller before the launch
- *      (cudaMemsetAsync on the same stream); ends equal to |G_j|.
+ *  count_table: device int32[P].  The kernel resets it to [0, ..., 0]
+ *      itself (CTA 0, before any tile is counted), so the caller need not
+ *      (fo_counting_table_init does the same as a separate memset); it ends
+ *      equal to |G_j|.
  *  flags: device uint32[P].  count_table and flags may both be NULL: the
  *      GEMM then signals nothing.
  *  epoch: the value this iteration's flags take; use a new one per

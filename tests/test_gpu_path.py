@@ -199,3 +199,21 @@ def test_last_wave_split_exact_entries():
         assert np.array_equal(gpu_gemm_output(pipe, res, op), OG.gemm_bf16(inp.A, inp.B[0]))
     finally:
         pipe.close()
+
+
+def test_gemm_resets_the_counting_table():
+    """Whatever the counting table holds before the launch, the kernel resets
+    it before counting: after the step it holds |G_j| again."""
+    w = _small("wave_pattern", M=512, N=1024, K=256, wave_width=6)
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp)
+    try:
+        for junk in (7, -3, 1 << 20):
+            pipe.buf.count.fill_(junk)
+            pipe.step()
+            res = pipe.results()
+            assert res["count"] == pipe.group_tiles
+            assert res["status"] == 0
+            check_run(pipe, inp, res)
+    finally:
+        pipe.close()
