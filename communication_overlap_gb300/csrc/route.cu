@@ -333,9 +333,11 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   route_rows_kernel<<<a.B, kTileM, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return FO_ERR_CUDA;
-  const int64_t entries = int64_t(p->tiles) * p->R;
+  // enough CTAs that each thread takes a handful of the tiles x 128 rows of
+  // the unit table (each needs a dependent global load), up to 4 per SM
+  const int64_t entries = int64_t(p->tiles) * kTileM;
   int ctas = int((entries + 4 * kPartsThreads - 1) / (4 * kPartsThreads));
-  ctas = ctas < 1 ? 1 : (ctas > p->sm_count ? p->sm_count : ctas);
+  ctas = ctas < 1 ? 1 : (ctas > 4 * p->sm_count ? 4 * p->sm_count : ctas);
   route_parts_kernel<<<ctas, kPartsThreads, smem, st>>>(a);
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
