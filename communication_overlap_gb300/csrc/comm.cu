@@ -1,12 +1,18 @@
-// Consumer kernel: the communication stand-in.
+// Consumer kernels: the communication stand-in, alone (consume_kernel) and
+// with the post-communication reorder fused in (consume_reorder_kernel).
 //
 // Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 核心设计 "通信侧" (the
 // communication runs as its own kernel on another stream), 五、CUTLASS 扩展实现
-// "专用监控内核" (a monitor kernel tracks progress through atomic counters),
-// 二、重排机制 (a group's data is contiguous so one collective call covers it).
+// "专用监控内核" (a monitor kernel tracks progress through atomic counters) and
+// "Epilogue 集成" (the reorder fused with element-wise operations), 二、重排机制
+// (a group's data is contiguous so one collective call covers it).
 //
-// The kernel is an HBM-bound stream of 16-byte vectors over each group's
-// contiguous unit range: every warp instruction moves 512 contiguous bytes.
+// Both are HBM-bound streams of 16-byte vectors over each group's contiguous
+// unit range (every warp instruction moves 512 contiguous bytes), launched as
+// programmatic dependents of the GEMM so that they run beside it: per group,
+// one thread polls the group's flag, then the CTAs take chunks of the range
+// from a per-group counter.  The plain consumer also publishes when each
+// group is fully written, for a reorder launched as its own dependent.
 #include <cuda_runtime.h>
 
 #include <mutex>
