@@ -597,6 +597,9 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "detail": {
                 "ms_overlapped_step": ms_ov,
+                "ms_overlapped_step_median": statistics.median(t_ov),
+                "ms_serial_step_median": statistics.median(t_ser),
+                "ms_gemm_alone_median": statistics.median(t_gemm),
                 "overlapped_step_kernels": "consumer+reorder fused" if fused else "separate",
                 "ms_overlapped_step_other_variant": statistics.mean(t_alt),
                 "ms_serial_step": ms_ser,
