@@ -117,6 +117,13 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
+// The same, with the first attempt inline: the pipeline loops call it once
+// per k-block and almost always find the phase complete.
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int32_t* status) {
+  return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, abort_flag, status);
+}
+
 // Bounded wait that ignores the abort flag (used while winding down).
 __device__ __noinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
@@ -448,7 +455,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
           for (int e = 0; e <= ti.expert; ++e) prefetch_tmap(&a.tmap_b[e]);
         if (tile_skipped<PAIR>(a, slot)) continue;
         for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
+          if (!mbar_wait_fast(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
@@ -507,7 +514,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
-          if (!mbar_wait(smem_u32(&full[stage]), phase, abort_flag, a.status)) {
+          if (!mbar_wait_fast(smem_u32(&full[stage]), phase, abort_flag, a.status)) {
             ok = false;
             break;
           }
