@@ -296,7 +296,9 @@ struct Work {
 __device__ __forceinline__ bool next_work(const GemmArgs& a, int32_t k, Work& w) {
   const int32_t c = blockIdx.x, W = gridDim.x;
   if (a.split_n > 0 && k == a.split_wave) {
-    const int32_t half = a.k_blocks / 2;
+    // the owner takes 9/16 of K: the helper also has to hand its partial
+    // sums over, so with equal halves the owner would wait for it
+    const int32_t half = (a.k_blocks * 9 + 8) / 16;
     if (c < a.split_n) {
       w = Work{a.split_slot0 + c, 0, half, 1};
       return true;
