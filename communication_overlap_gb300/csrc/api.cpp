@@ -113,7 +113,9 @@ fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairabl
 fo_status fo_plan_set_split(fo_plan* p, int32_t enable, int32_t* split_tiles) {
   if (!p) return FO_ERR_ARG;
   p->split_enabled = enable != 0;
-  if (split_tiles) *split_tiles = p->split_enabled ? p->split_n : 0;
+  // (split only when every CTA of the grid can be resident at once)
+  const bool fits = p->blob == nullptr || p->W <= p->sm_count;
+  if (split_tiles) *split_tiles = (p->split_enabled && fits) ? p->split_n : 0;
   return FO_OK;
 }
 

@@ -884,7 +884,9 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.k_blocks = p->K / kBlockK;
   if (++p->gemm_seq == 0) p->gemm_seq = 1;
   a.seq = p->gemm_seq;
-  if (p->split_n > 0 && p->split_enabled) {
+  // an owner waits for its helper's partial sums, so the split needs every
+  // CTA of the grid resident at once (W no larger than the SM count)
+  if (p->split_n > 0 && p->split_enabled && p->W <= p->sm_count) {
     a.split_ws = static_cast<float4*>(p->dev.split_ws);
     a.split_flag = p->dev.split_flag;
     a.split_n = p->split_n;

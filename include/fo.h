@@ -203,8 +203,10 @@ fo_status fo_plan_set_gemm(fo_plan* plan, fo_gemm_variant variant, int32_t* pair
  * owner adds them and stores, counts and signals the tile as usual.  Waves,
  * groups, tables and the counting table do not change; only the order of
  * the fp32 additions of those tiles does.  Enabled by default when the
- * shape allows it.  *split_tiles (may be NULL): how many tiles are split
- * (0 when disabled or not possible). */
+ * shape allows it and W does not exceed the device's SM count (an owner
+ * waits for its helper, so every CTA must be resident at once).
+ * *split_tiles (may be NULL): how many tiles are split (0 when disabled or
+ * not possible). */
 fo_status fo_plan_set_split(fo_plan* plan, int32_t enable, int32_t* split_tiles);
 
 /* Timelines ([P2] Figure 3 records each tile's completion time with
