@@ -19,6 +19,10 @@ Readings taken where the pages are silent (each is also stated where used):
   R2  wave(slot) = slot // W, W = number of persistent GEMM workers
   R3  |G_j| is counted in tiles, partitions are given in waves
   R6  intra-tile order is row-major; a "unit" is one tile row (tile_n values)
+  R16 All-to-All with an even W: each expert's grid of tile rows is padded to
+      an even count with one empty tile row (no valid rows), so that every
+      band has an even height and launch slots 2i, 2i+1 hold vertically
+      adjacent tiles; empty tiles take slots and count in |G_j| like others
 """
 from dataclasses import dataclass, field
 from itertools import product
@@ -142,9 +146,9 @@ class Plan:
 
     def tile_rows(self, slot):
         """Valid rows of the tile at ``slot`` (the last tile-row of an expert
-        may be ragged)."""
+        may be ragged; a padding tile row (R16) has none)."""
         e, tm, _ = self.slot_tile[slot]
-        return min(self.tile_m, self.expert_rows[e] - tm * self.tile_m)
+        return max(0, min(self.tile_m, self.expert_rows[e] - tm * self.tile_m))
 
     def tile_row0(self, slot):
         """First row of the tile at ``slot`` in the stacked GEMM output."""
@@ -203,10 +207,14 @@ def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
              None if row_token is None else np.asarray(row_token),
              None if row_slot is None else np.asarray(row_slot))
     p.tiles_n = N // tile_n
+    # Reading R16: All-to-All grids with an even W get an even number of tile
+    # rows per expert (one empty row added when odd)
+    pad_even = layout == LAYOUT_A2A and wave_width % 2 == 0
     row0 = 0
     for m_e in p.expert_rows:
         p.expert_row0.append(row0)
-        p.expert_tiles_m.append(-(-m_e // tile_m))
+        tm = -(-m_e // tile_m)
+        p.expert_tiles_m.append(tm + (tm % 2) if pad_even else tm)
         row0 += m_e
     for e, tm_count in enumerate(p.expert_tiles_m):
         for tm, tn in launch_order(tm_count, p.tiles_n, swizzle):

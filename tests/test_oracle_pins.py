@@ -280,6 +280,37 @@ def test_a2a_every_routed_row_lands_once():
     assert sum(o.shape[0] for o in outs) == p.M
 
 
+def test_a2a_even_width_pads_expert_grids():
+    """Reading R16: with an even W every expert's grid gets an even number of
+    tile rows (one empty row added when odd), so launch slots 2i, 2i+1 are
+    vertically adjacent tiles of one expert and column; the empty tiles hold
+    no rows, take slots and count in |G_j|; every routed row still lands
+    once.  With an odd W nothing is padded."""
+    D, k = 4, 2
+    er, tok, sl = _tiny_routing(n_tok=100, E=3, D=D)     # 200 rows over 3 experts
+    tm = [-(-m // 128) for m in er]
+    assert any(t % 2 for t in tm)
+    for W, pad in ((6, True), (5, False)):
+        tiles = sum(t + (t % 2 if pad else 0) for t in tm) * 3
+        p = P.build_plan(er, 3 * 64, 64, 128, 64, 4, W,
+                         P.one_then_two(P.wave_count(tiles, W)), P.LAYOUT_A2A, D, tok, sl)
+        assert p.tiles == tiles
+        assert p.expert_tiles_m == [t + (t % 2 if pad else 0) for t in tm]
+        assert int(p.group_tiles.sum()) == p.tiles
+        empty = [s for s in range(p.tiles) if p.tile_rows(s) == 0]
+        assert len(empty) == (sum(t % 2 for t in tm) * 3 if pad else 0)
+        if pad:
+            for s in range(0, p.tiles, 2):
+                e0, tm0, tn0 = p.slot_tile[s]
+                e1, tm1, tn1 = p.slot_tile[s + 1]
+                assert (e0, tn0, tm1) == (e1, tn1, tm0 + 1)
+        C = np.random.default_rng(8).integers(0, 65535, (p.M, p.N)).astype(np.uint16)
+        outs = cm.reorder_back_a2a(p, cm.consume_a2a(p, cm.pre_reorder(p, C)), k)
+        for rho in range(p.M):
+            t, q = int(tok[rho]), int(sl[rho])
+            assert np.array_equal(outs[t % D][(t // D) * k + q], C[rho])
+
+
 def _padded_routing(capacity, n_tok=40, E=3, k=2, D=4, seed=0):
     """The routing of ``_tiny_routing`` with every expert's rows padded to a
     fixed capacity by rows that hold no token (token -1): the static layout a
