@@ -74,6 +74,7 @@ struct fo_plan {
   int32_t P = 0, R = 1, layout = 0, n_dest = 1, n_experts = 0, top_k = 1, n_tokens = 0;
   int32_t tiles = 0, tiles_n = 0, waves = 0, n_units = 0;
   std::vector<int32_t> expert_rows, expert_row0, expert_tile0;
+  std::vector<int32_t> expert_tm;   // tile rows of each expert's grid (incl. padding)
   std::vector<int32_t> group_waves, group_tiles, group_slot_begin, group_unit_begin;
   std::vector<int32_t> slot_tile, tile_slot, slot_group;
   std::vector<fo::TileInfo> tile;
@@ -110,6 +111,7 @@ namespace fo {
 fo_status check_shape(const fo_plan_desc* d, int32_t* W, int32_t* tiles,
                       int32_t* waves);
 fo_status build_plan(const fo_plan_desc* d, fo_plan* p);
+int32_t expert_tile_rows(int layout, int32_t W, int32_t rows);
 fo_status upload_plan(fo_plan* p);
 int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r);
 void set_a2a_outputs(fo_plan* p, int32_t n_tokens, int32_t top_k);

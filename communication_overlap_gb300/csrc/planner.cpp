@@ -27,6 +27,15 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
+// Tile rows of an expert's grid.  Reading: in the All-to-All layout with an
+// even W, an odd count gets one empty tile row, so that every band of the
+// launch order has an even height and launch slots 2i, 2i+1 are vertically
+// adjacent tiles (CTA pairs); the empty tiles take slots and are counted.
+int32_t expert_tile_rows(int layout, int32_t W, int32_t rows) {
+  const int32_t tm = int32_t(ceil_div(rows, kTileM));
+  return (layout == FO_LAYOUT_A2A_SUBTOKEN && W % 2 == 0) ? tm + (tm & 1) : tm;
+}
+
 fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
                       int32_t* waves_out) {
   if (!d) return FO_ERR_ARG;
@@ -36,23 +45,6 @@ fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
   if (d->N % d->tile_n != 0 || d->K % kBlockK != 0) return FO_ERR_ARG;
   if (d->swizzle < 1) return FO_ERR_ARG;
   if (d->n_experts < 0 || d->n_experts > kMaxExperts) return FO_ERR_ARG;
-  int64_t tiles_m = 0;
-  if (d->n_experts > 0) {
-    if (!d->expert_rows) return FO_ERR_ARG;
-    int64_t sum = 0;
-    for (int e = 0; e < d->n_experts; ++e) {
-      if (d->expert_rows[e] < 0) return FO_ERR_ARG;
-      sum += d->expert_rows[e];
-      tiles_m += ceil_div(d->expert_rows[e], kTileM);
-    }
-    if (sum != d->M) return FO_ERR_ARG;
-  } else {
-    tiles_m = ceil_div(d->M, kTileM);
-  }
-  int64_t tiles = tiles_m * (d->N / d->tile_n);
-  if (tiles <= 0 || tiles > (int64_t(1) << 24)) return FO_ERR_ARG;
-  // units (tile rows) index the reordered buffer in int32
-  if (int64_t(d->M) * (d->N / d->tile_n) >= (int64_t(1) << 31)) return FO_ERR_ARG;
   int32_t W = d->wave_width;
   if (W <= 0) {
     if (d->host_only) return FO_ERR_ARG;
@@ -61,6 +53,23 @@ fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
     if (cudaDeviceGetAttribute(&W, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return FO_ERR_CUDA;
   }
+  int64_t tiles_m = 0;
+  if (d->n_experts > 0) {
+    if (!d->expert_rows) return FO_ERR_ARG;
+    int64_t sum = 0;
+    for (int e = 0; e < d->n_experts; ++e) {
+      if (d->expert_rows[e] < 0) return FO_ERR_ARG;
+      sum += d->expert_rows[e];
+      tiles_m += expert_tile_rows(d->layout, W, d->expert_rows[e]);
+    }
+    if (sum != d->M) return FO_ERR_ARG;
+  } else {
+    tiles_m = expert_tile_rows(d->layout, W, d->M);
+  }
+  int64_t tiles = tiles_m * (d->N / d->tile_n);
+  if (tiles <= 0 || tiles > (int64_t(1) << 24)) return FO_ERR_ARG;
+  // units (tile rows) index the reordered buffer in int32
+  if (int64_t(d->M) * (d->N / d->tile_n) >= (int64_t(1) << 31)) return FO_ERR_ARG;
   if (W_out) *W_out = W;
   if (tiles_out) *tiles_out = int32_t(tiles);
   if (waves_out) *waves_out = int32_t(ceil_div(tiles, W));
@@ -112,10 +121,11 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   const int E = int(p->expert_rows.size());
   p->expert_row0.assign(E, 0);
   p->expert_tile0.assign(E, 0);
+  p->expert_tm.assign(E, 0);
+  for (int e = 0; e < E; ++e) p->expert_tm[e] = expert_tile_rows(layout, W, p->expert_rows[e]);
   for (int e = 1; e < E; ++e) {
     p->expert_row0[e] = p->expert_row0[e - 1] + p->expert_rows[e - 1];
-    p->expert_tile0[e] = p->expert_tile0[e - 1] +
-                         int32_t(ceil_div(p->expert_rows[e - 1], kTileM)) * TN;
+    p->expert_tile0[e] = p->expert_tile0[e - 1] + p->expert_tm[e - 1] * TN;
   }
 
   // Launch order: experts in turn; inside an expert, band b covers tile rows
@@ -127,7 +137,7 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   {
     int32_t s = 0;
     for (int e = 0; e < E; ++e) {
-      const int32_t tm_count = int32_t(ceil_div(p->expert_rows[e], kTileM));
+      const int32_t tm_count = p->expert_tm[e];
       for (int32_t top = 0; top < tm_count; top += d->swizzle) {
         const int32_t h = std::min<int32_t>(d->swizzle, tm_count - top);
         for (int32_t o = 0; o < h * TN; ++o, ++s) {
@@ -138,7 +148,8 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
           TileInfo& ti = p->tile[s];
           ti.row0 = p->expert_row0[e] + tm * kTileM;
           ti.col0 = tn * d->tile_n;
-          ti.rows = std::min<int32_t>(kTileM, p->expert_rows[e] - tm * kTileM);
+          // (a padding tile row holds no rows)
+          ti.rows = std::max<int32_t>(0, std::min<int32_t>(kTileM, p->expert_rows[e] - tm * kTileM));
           ti.expert = e;
         }
       }
@@ -419,7 +430,7 @@ fo_status upload_plan(fo_plan* p) {
   const bool a2a = p->layout == FO_LAYOUT_A2A_SUBTOKEN;
   if (a2a) {
     p->route_blocks = 0;
-    for (int32_t rows : p->expert_rows) p->route_blocks += (rows + kTileM - 1) / kTileM;
+    for (int32_t tm : p->expert_tm) p->route_blocks += tm;
   }
   const size_t o_sws = put(buf, std::vector<float>(size_t(p->split_n) * kTileM * p->tile_n, 0.f));
   const size_t o_sfl = put(buf, std::vector<int32_t>(size_t(p->split_n) * 4, 0));

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
     if (tid == 0) mbar_expect_tx(sfull, uint32_t(in_rows * ub));
     __syncthreads();
     if (whole) {
-      if (tid == 0) {
+      if (tid == 0 && ti.rows > 0) {   // (a padding tile holds no rows)
         int k;
         int32_t su, dr;
         reorder_row(a, ti, s, 0, &k, &su, &dr);   // rows are contiguous from row 0

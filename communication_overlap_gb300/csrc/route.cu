@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(kTileM) route_rows_kernel(const __grid_constan
   int e = 0;
   while (e + 1 < a.n_experts && a.expert_block0[e + 1] <= b) ++e;
   const int32_t row0 = a.expert_row0[e] + (b - a.expert_block0[e]) * kTileM;
-  const int32_t rows = min(kTileM, a.expert_row0[e] + a.expert_rows[e] - row0);
+  // (a padding tile row of an expert's grid holds no rows)
+  const int32_t rows = max(0, min(kTileM, a.expert_row0[e] + a.expert_rows[e] - row0));
   for (int i = tid; i < kWarps * kMaxDest; i += kTileM) (&warp_cnt[0][0])[i] = 0;
   int32_t d = -1, t = -1, q = 0;
   int bad = 0;
@@ -314,7 +315,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
     a.expert_row0[e] = p->expert_row0[e];
     a.expert_rows[e] = p->expert_rows[e];
     a.expert_block0[e] = blocks;
-    blocks += (p->expert_rows[e] + kTileM - 1) / kTileM;
+    blocks += p->expert_tm[e];   // (incl. a padding tile row)
   }
   a.expert_block0[E] = blocks;
   for (int k = 0; k < p->R; ++k) a.cap[k] = p->dest_capacity[k];

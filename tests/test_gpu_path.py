@@ -72,6 +72,24 @@ def test_small_alltoall_ragged_experts():
         pipe.close()
 
 
+@pytest.mark.parametrize("fused", [False, True])
+def test_alltoall_padded_grids_run_as_pairs(fused):
+    """An even W pads odd expert grids with an empty tile row, so the GEMM
+    runs as CTA pairs; everything matches the oracle."""
+    w = _small("alltoall", M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5,
+               wave_width=8)
+    inp = W.make_inputs(w)
+    assert any(-(-m // 128) % 2 for m in inp.expert_rows)
+    pipe = Pipeline(w, inp, gemm_variant=fo.FO_GEMM_PAIRS)
+    try:
+        assert pipe.pairable
+        for _ in range(2):
+            pipe.step(fused=fused)
+        check_run(pipe, inp, pipe.results())
+    finally:
+        pipe.close()
+
+
 def test_gemm_exact_unit_entries_and_identity():
     """Entries in {-1, 0, 1} with K <= 256 give exact integer sums: the GPU
     result must equal the oracle bit for bit; an identity A returns B."""

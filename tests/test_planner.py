@@ -117,3 +117,18 @@ def test_every_partition_tables(tm, tn, S, Wd):
         _compare([tm * 128], tn * 128, 64, 128, S, Wd, fo.FO_LAYOUT_TILE, partition=part)
         _compare([tm * 128], tn * 128, 64, 128, S, Wd, fo.FO_LAYOUT_RS_SUBTILE, R=4,
                  partition=part)
+
+
+def test_padded_a2a_tables_even_width():
+    """All-to-All with an even W: odd expert grids get an empty tile row; the
+    host planner's tables equal the oracle's, and launch slots pair up."""
+    rng = np.random.default_rng(3)
+    n_tok, E, k, D = 150, 3, 2, 4
+    picks = np.argsort(rng.random((n_tok, E)), axis=1)[:, :k]
+    tok = np.repeat(np.arange(n_tok), k)
+    sl = np.tile(np.arange(k), n_tok)
+    ex = picks.reshape(-1)
+    order = np.lexsort((sl, tok, ex))
+    er = np.bincount(ex, minlength=E).tolist()
+    assert any(-(-m // 128) % 2 for m in er)
+    _compare(er, 512, 64, 256, 4, 6, fo.FO_LAYOUT_A2A_SUBTOKEN, D, tok[order], sl[order])
