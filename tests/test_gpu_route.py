@@ -61,9 +61,11 @@ def _route(pipe, inp):
     pipe.route(tok, sl)
 
 
-@pytest.mark.parametrize("capacity", [384, 300, 200])
-def test_device_tables_equal_host_tables(capacity):
-    w = _small(capacity)
+@pytest.mark.parametrize("capacity,wave_width", [(384, 7), (300, 7), (200, 7), (300, 8)])
+def test_device_tables_equal_host_tables(capacity, wave_width):
+    """(300 rows = 3 tile rows per expert: with W = 8 each expert's grid is
+    padded with an empty tile row, which the routing kernels count too.)"""
+    w = _small(capacity, wave_width=wave_width)
     base = W.make_inputs(w)
     pipe = Pipeline(w, base)
     try:
@@ -89,12 +91,12 @@ def test_device_tables_equal_host_tables(capacity):
         pipe.close()
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_steps_on_device_routings_match_oracle(fused):
+@pytest.mark.parametrize("fused,wave_width", [(False, 7), (True, 7), (True, 8)])
+def test_steps_on_device_routings_match_oracle(fused, wave_width):
     """Three steps, each on a routing handed over in device memory; after
     each, every table, the reorders and the consumer match the oracle for
-    that step's routing, bit for bit."""
-    w = _small(384)
+    that step's routing, bit for bit (W = 8: padded grids, CTA pairs)."""
+    w = _small(300 if wave_width == 8 else 384, wave_width=wave_width)
     base = W.make_inputs(w)
     pipe = Pipeline(w, base)
     try:
