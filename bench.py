@@ -6,9 +6,10 @@
 A step is one pass of the whole path on the workload (default: the
 wave-pattern GEMM M=2048, N=8192, K=8192, 128x256 tiles, 148-CTA waves,
 groups of 1 then 2 waves, copy consumer + reorder back), inputs resident in
-HBM: counting-table reset, signaled GEMM, consumer (a programmatic
-dependent launch running alongside the GEMM) and post-communication
-reorder.  ``value`` is the GEMM's FLOPs per step divided by the step time
+HBM: signaled GEMM (it resets its own counting table), then the consumer
+and the post-communication reorder, by default as one kernel that stores
+every unit straight to its final place (a programmatic dependent launch
+running alongside the GEMM; ``--step-kernels`` picks the others).  ``value`` is the GEMM's FLOPs per step divided by the step time
 (TFLOPS of the whole overlapped step); for the dynamic-routing workload
 only the rows that hold a token count (2 x routed rows x N x K).  L2 is flushed (a 256 MiB write)
 before every timed step, outside the timed events.
@@ -52,9 +53,11 @@ def parse():
     ap.add_argument("--trace-out", default="", help="write per-tile stamps (json)")
     ap.add_argument("--consumer-ctas", type=int, default=0,
                     help="consumer grid (0: library default, by consumer kind)")
-    ap.add_argument("--step-kernels", default="auto", choices=["auto", "fused", "separate"],
+    ap.add_argument("--step-kernels", default="auto",
+                    choices=["auto", "fused", "separate", "direct"],
                     help="consumer and reorder as one kernel (fo_consume_reorder) or two; "
-                         "auto: fused except for the plain sum")
+                         "direct: the fused kernel without communication buffers; "
+                         "auto: direct")
     ap.add_argument("--reorder-ctas", type=int, default=0,
                     help="reorder grid (0: library default, 3 per SM)")
     return ap.parse_args()
@@ -305,6 +308,14 @@ def workload_name(w):
 
 # ----------------------------------------------------------------- our path
 
+STEP_KERNELS = {
+    "direct": "signaled GEMM + one consumer kernel that stores every unit straight to "
+              "its final place (communication and post-communication reorder fused)",
+    "fused": "signaled GEMM + one consumer kernel that writes the communication buffers "
+             "and moves each chunk on to its final place",
+    "separate": "signaled GEMM + consumer + post-communication reorder",
+}
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -362,16 +373,15 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     # warm-up (also the first correctness evidence: status and counting table)
-    # measured (both variants timed in one process): the fused kernel wins
-    # for the copy, scatter and bucket consumers; for the plain sum, whose
-    # eight sources already saturate HBM beside the GEMM, the two are even
-    # and the separate kernels are kept
-    if args.step_kernels == "auto":
-        fused = w.consumer != W.CONS_SUM
-    else:
-        fused = args.step_kernels == "fused"
+    # measured (all three variants timed in one process, interleaved): the
+    # direct fused kernel gives the shortest step on every workload; the
+    # fused kernel that writes the communication buffers and the separate
+    # kernels are timed below as well
+    kernels = "direct" if args.step_kernels == "auto" else args.step_kernels
+    fused = kernels in ("fused", "direct")
+    direct = kernels == "direct"
     for _ in range(max(3, args.warmup)):
-        step(overlap=True, fused=fused)
+        step(overlap=True, fused=fused, direct=direct)
     torch.cuda.synchronize()
     assert int(pipe.buf.status.item()) == 0, "consumer wait timed out"
     assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
@@ -379,16 +389,21 @@ def run_ours(args):
     # the headline: overlapped steps
     barrier()
     with Clocks(local) as clk:
-        t_ov = timed(torch, s, lambda: step(overlap=True, sync_current=False, fused=fused),
+        t_ov = timed(torch, s,
+                     lambda: step(overlap=True, sync_current=False, fused=fused, direct=direct),
                      args.steps, flush)
     barrier()
     ms_ov = statistics.mean(t_ov)
     status_ok = int(pipe.buf.status.item()) == 0
 
     # serial baseline: consumer after the GEMM
-    # the other overlapped variant (separate kernels, or fused)
-    t_alt = timed(torch, s, lambda: step(overlap=True, sync_current=False, fused=not fused),
-                  args.steps, flush)
+    # every overlapped variant: separate kernels, fused, fused direct (no
+    # communication buffers, each unit stored straight to its final place)
+    t_var = {}
+    for name, kw in (("separate", dict(fused=False)), ("fused", dict(fused=True)),
+                     ("direct", dict(fused=True, direct=True))):
+        t_var[name] = timed(torch, s, lambda: step(overlap=True, sync_current=False, **kw),
+                            args.steps, flush)
     t_ser = timed(torch, s, lambda: step(overlap=False, sync_current=False),
                   args.steps, flush)
     t_route = []
@@ -420,9 +435,10 @@ def run_ours(args):
         t_gemm_sm = timed(torch, pipe_sm.s0, lambda: pipe_sm.gemm(pipe_sm.s0, pipe_sm.epoch),
                           args.steps, flush)
         for _ in range(3):
-            pipe_sm.step(overlap=True, fused=fused)
+            pipe_sm.step(overlap=True, fused=fused, direct=direct)
         t_step_sm = timed(torch, pipe_sm.s0,
-                          lambda: pipe_sm.step(overlap=True, sync_current=False, fused=fused),
+                          lambda: pipe_sm.step(overlap=True, sync_current=False, fused=fused,
+                                               direct=direct),
                           args.steps, flush)
         torch.cuda.synchronize()
         w_sm = {"wave_width": sm_count, "waves": pipe_sm.waves,
@@ -448,6 +464,8 @@ def run_ours(args):
         pipe.consume(s, pipe.epoch)
     t_cons_only = timed(torch, s, cons_only, args.steps, flush)
     t_reo = timed(torch, s, lambda: pipe.reorder(s), args.steps, flush)
+    t_direct_alone = timed(torch, s, lambda: pipe.consume_reorder(s, pipe.epoch, direct=True),
+                           args.steps, flush)
     # the consumer's bandwidth with a full grid (4 CTAs per SM): its roofline
     # figure; the step uses the library's default grid for running beside the
     # GEMM, which for copies is smaller and slower alone
@@ -473,7 +491,7 @@ def run_ours(args):
         span_alone.append(gemm_span()[0])
         with torch.cuda.stream(s):
             flush()
-        pipe.step(overlap=True, fused=fused)
+        pipe.step(overlap=True, fused=fused, direct=direct)
         torch.cuda.synchronize()
         sp, stamps = gemm_span()
         span_step.append(sp)
@@ -484,7 +502,7 @@ def run_ours(args):
         fo.fo_plan_set_trace(pipe.plan, trace.data_ptr(), ctrace.data_ptr())
         with torch.cuda.stream(s):
             flush()
-        pipe.step(overlap=True, fused=fused)
+        pipe.step(overlap=True, fused=fused, direct=direct)
         torch.cuda.synchronize()
         fo.fo_plan_set_trace(pipe.plan, 0, 0)
         stamps = trace.cpu().numpy().astype(np.int64)
@@ -508,7 +526,7 @@ def run_ours(args):
                        "consumer_cta": [{"sm": int(r[0]), "start_us": (r[1] - t0) / 1e3,
                                          "end_us": (r[2] - t0) / 1e3, "chunks": int(r[3])}
                                         for r in rec],
-                       "step_kernels": "fused" if fused else "separate",
+                       "step_kernels": kernels,
                        "wave_width": w.wave_width, "partition": pipe.partition}, f)
 
     # end to end through the C ABI with host buffers
@@ -542,7 +560,7 @@ def run_ours(args):
                 d_.copy_(h_, non_blocking=True)
         if dyn:
             pipe.route(d_tok, d_sl)
-        pipe.step(overlap=True, sync_current=False, fused=fused)
+        pipe.step(overlap=True, sync_current=False, fused=fused, direct=direct)
         with torch.cuda.stream(s):
             for h_, d_ in zip(hOut, pipe.buf.final):
                 h_.copy_(d_, non_blocking=True)
@@ -583,6 +601,7 @@ def run_ours(args):
                        "groups_tiles": pipe.group_tiles, "consumer": consumer_name(w),
                        "l2": "flushed before every timed step (256 MiB write)",
                        "consumer_ctas": args.consumer_ctas or "library default",
+                       "step_kernels": STEP_KERNELS[kernels],
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_burst,
                          "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,
@@ -600,8 +619,8 @@ def run_ours(args):
                 "ms_overlapped_step_median": statistics.median(t_ov),
                 "ms_serial_step_median": statistics.median(t_ser),
                 "ms_gemm_alone_median": statistics.median(t_gemm),
-                "overlapped_step_kernels": "consumer+reorder fused" if fused else "separate",
-                "ms_overlapped_step_other_variant": statistics.mean(t_alt),
+                "overlapped_step_kernels": kernels,
+                "ms_overlapped_step_by_kernels": {k: statistics.mean(v) for k, v in t_var.items()},
                 "ms_serial_step": ms_ser,
                 "overlap_speedup": ms_ser / ms_ov,
                 "ms_gemm_alone": ms_gemm,
@@ -620,6 +639,8 @@ def run_ours(args):
                 "ms_consumer_alone_full_grid": statistics.mean(t_cons_full),
                 "consumer_gbs_full_grid": cons_bytes / (statistics.mean(t_cons_full) * 1e-3) / 1e9,
                 "reorder_gbs": reo_bytes / (statistics.mean(t_reo) * 1e-3) / 1e9,
+                "ms_direct_alone": statistics.mean(t_direct_alone),
+                "direct_gbs": cons_bytes / (statistics.mean(t_direct_alone) * 1e-3) / 1e9,
                 "hbm_peak_gbs": hbm,
                 "gemm_in_kernel_ms_alone": statistics.median(span_alone),
                 "gemm_in_kernel_ms_in_step": statistics.median(span_step),

@@ -71,6 +71,11 @@ fo_status fo_plan_table(const fo_plan* p, int32_t which, int32_t* out,
         v = &p->slot_live;
       }
       break;
+    case FO_TAB_UNIT_PLACE:
+      if (!p->place_ok) return FO_ERR_UNSUPPORTED;
+      unit.assign(p->unit_place.begin(), p->unit_place.begin() + p->n_units);
+      v = &unit;
+      break;
     case FO_TAB_UNIT:
       unit.resize(size_t(p->tiles) * p->tile_m);
       for (int32_t s = 0; s < p->tiles; ++s)
@@ -200,8 +205,7 @@ fo_status fo_consume_reorder(const fo_plan* p, int32_t group, fo_consumer kind,
                              void* const* comm_dst, void* const* final_dst, const void* bias,
                              fo_activation act, const uint32_t* flags, uint32_t epoch,
                              uint64_t spin_limit_ns, int32_t* dev_status, void* stream) {
-  if (!p || !p->blob || !src || !comm_dst || !final_dst || !flags || !dev_status)
-    return FO_ERR_ARG;
+  if (!p || !p->blob || !src || !final_dst || !flags || !dev_status) return FO_ERR_ARG;
   if (group < -1 || group >= p->P) return FO_ERR_ARG;
   if (act < FO_ACT_NONE || act > FO_ACT_SILU) return FO_ERR_ARG;
   if (bias && (reinterpret_cast<uintptr_t>(bias) & 15)) return FO_ERR_ARG;
@@ -228,7 +232,7 @@ fo_status fo_consume_reorder(const fo_plan* p, int32_t group, fo_consumer kind,
     if (!partials[i]) return FO_ERR_ARG;
   const int n = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
   for (int k = 0; k < n; ++k)
-    if (!comm_dst[k] || !final_dst[k]) return FO_ERR_ARG;
+    if ((comm_dst && !comm_dst[k]) || !final_dst[k]) return FO_ERR_ARG;
   const int32_t g0 = group < 0 ? 0 : group, g1 = group < 0 ? p->P : group + 1;
   return fo::launch_consume_reorder(p, g0, g1, int(kind), src, partials, n_partials, comm_dst,
                                     final_dst, bias, int(act), flags, epoch, spin_limit_ns,

@@ -271,7 +271,9 @@ struct FusedArgs {
   RowMap map;
   const uint16_t* bias;
   const int32_t* unit_src;  // [units] slot << 7 | row of the tile row each unit holds
+  const int32_t* unit_place;   // [units] output << kPlaceShift | vector index
   int32_t act, row_vec;
+  int32_t direct;  // no communication buffers: each unit goes straight to its final place
 };
 
 // Where the units of a chunk go, computed by threads t < units before the
@@ -333,9 +335,64 @@ __device__ __forceinline__ void reorder_chunk_regs(const FusedArgs& a, const Chu
   }
 }
 
+// The direct variant: the chunk's vectors [v0, v1) of the reordered buffer,
+// consumed as in consume_range (same loads, same fp32 sums in the same
+// order), then stored straight to their final places, so the communication
+// buffers are neither written nor read back.  Each lane reads its unit's
+// place from the plan's unit_place table (one load, which a warp's lanes
+// share: a unit is 512 or 256 contiguous bytes), issued before the data
+// loads so that both are in flight together.
+template <int KIND, int U>
+__device__ __forceinline__ void consume_direct(const FusedArgs& a, uint4* const* fin,
+                                               int32_t v0, int32_t v1, int tid) {
+  const ConsumeArgs& c = a.c;
+  constexpr bool kSum = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS);
+  constexpr int S = kThreads;
+  const uint64_t pol = l2_evict_first();
+  const int32_t vmask = (1 << c.vpu_shift) - 1;
+  for (int32_t base = v0 + tid; base < v1; base += S * U) {
+    int32_t place[U];   // output << kPlaceShift | vector index; -1 past the chunk
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      const int32_t v = base + S * i;
+      place[i] = v < v1 ? a.unit_place[v >> c.vpu_shift] + (v & vmask) : -1;
+    }
+    uint4 x[U];
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+      if (base + S * i < v1) x[i] = ld_once(c.src + base + S * i, pol);
+    if constexpr (kSum) {
+      float acc[U][8];
+#pragma unroll
+      for (int i = 0; i < U; ++i) set_bf16x8(acc[i], x[i]);
+#pragma unroll
+      for (int q = 0; q < kMaxPartials; ++q) {
+        if (q >= c.n_partials) break;
+        uint4 y[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+          if (base + S * i < v1) y[i] = ld_once(c.partials[q] + base + S * i, pol);
+#pragma unroll
+        for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i) x[i] = pack8(acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+      if (place[i] < 0) continue;   // past the chunk
+      const int32_t to = place[i] & ((1 << kPlaceShift) - 1);
+      uint4 y = x[i];
+      if (a.act != FO_ACT_NONE || a.bias != nullptr)
+        y = epilogue8(y, a.bias, (to % a.row_vec) * 8, a.act);
+      st_cs(fin[place[i] >> kPlaceShift] + to, y);
+    }
+  }
+}
+
 // Launched with 256 threads.  Registers capped at 72: measured, two CTAs at
 // 70 registers run beside each GEMM CTA while the GEMM runs, at 80 only one.
-template <int KIND, int U, int VPU>
+template <int KIND, int U, int VPU, bool DIRECT>
 __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ FusedArgs a) {
   constexpr int kNV = kChunkBytes<KIND> / (16 * kThreads);   // vectors of a chunk per thread
   const ConsumeArgs& c = a.c;
@@ -368,7 +425,7 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
     }
     __syncthreads();
     const int32_t first = s_chunk[0];
-    if (first < n_chunks) {
+    if (!DIRECT && first < n_chunks) {
       const int32_t u0 = ub + first * c.chunk_units;
       map_chunk_units(a, s_map, u0, min(u0 + c.chunk_units, ue), tid);
     }
@@ -384,12 +441,17 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
       if (tid == 0) s_chunk[buf ^ 1] = atomicAdd(c.work + j, 1);
       const int32_t u0 = ub + ch * c.chunk_units;
       const int32_t u1 = min(u0 + c.chunk_units, ue);
-      if (n > 0) map_chunk_units(a, s_map, u0, u1, tid);   // the first is mapped
-      consume_range<KIND, U>(c, s_ps, s_pl, s_pd, s_dst, u0 << c.vpu_shift, u1 << c.vpu_shift,
-                             tid);
-      __syncthreads();   // the chunk's stores and its map are visible to the whole CTA
-      reorder_chunk_regs<VPU, kNV>(a, s_map, s_dst, s_fin, u1 - u0, tid);
-      __syncthreads();   // s_map is free for the next chunk
+      if constexpr (DIRECT) {
+        consume_direct<KIND, U>(a, s_fin, u0 << c.vpu_shift, u1 << c.vpu_shift, tid);
+        __syncthreads();   // the next chunk index is visible to the whole CTA
+      } else {
+        if (n > 0) map_chunk_units(a, s_map, u0, u1, tid);   // the first is mapped
+        consume_range<KIND, U>(c, s_ps, s_pl, s_pd, s_dst, u0 << c.vpu_shift,
+                               u1 << c.vpu_shift, tid);
+        __syncthreads();   // the chunk's stores and its map are visible to the whole CTA
+        reorder_chunk_regs<VPU, kNV>(a, s_map, s_dst, s_fin, u1 - u0, tid);
+        __syncthreads();   // s_map is free for the next chunk
+      }
       if (c.trace != nullptr && tid == 0) {
         const unsigned long long now = globaltimer_ns();
         atomicMax(reinterpret_cast<unsigned long long*>(c.trace + j), now);
@@ -423,14 +485,14 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
   }
 }
 
-template <int KIND, int U, int VPU>
+template <int KIND, int U, int VPU, bool DIRECT>
 fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int device,
                             cudaStream_t st) {
   static std::once_flag once[64];
   static cudaError_t err[64];
   const int d = device < 64 ? device : 63;
   std::call_once(once[d], [&] {
-    err[d] = cudaFuncSetAttribute(consume_reorder_kernel<KIND, U, VPU>,
+    err[d] = cudaFuncSetAttribute(consume_reorder_kernel<KIND, U, VPU, DIRECT>,
                                   cudaFuncAttributePreferredSharedMemoryCarveout,
                                   int(cudaSharedmemCarveoutMaxShared));
   });
@@ -444,19 +506,19 @@ fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int devi
   attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, consume_reorder_kernel<KIND, U, VPU>, a) != cudaSuccess)
+  if (cudaLaunchKernelEx(&cfg, consume_reorder_kernel<KIND, U, VPU, DIRECT>, a) != cudaSuccess)
     return FO_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
-template <int VPU>
+template <int VPU, bool DIRECT>
 fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int dv,
                            cudaStream_t st) {
   switch (kind) {
-    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kFusedUnroll<FO_CONS_COPY>, VPU>(a, ctas, ov, dv, st);
-    case FO_CONS_SUM: return launch_fused_kind<FO_CONS_SUM, kFusedUnroll<FO_CONS_SUM>, VPU>(a, ctas, ov, dv, st);
-    case FO_CONS_RS: return launch_fused_kind<FO_CONS_RS, kFusedUnroll<FO_CONS_RS>, VPU>(a, ctas, ov, dv, st);
-    case FO_CONS_A2A: return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU>(a, ctas, ov, dv, st);
+    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kFusedUnroll<FO_CONS_COPY>, VPU, DIRECT>(a, ctas, ov, dv, st);
+    case FO_CONS_SUM: return launch_fused_kind<FO_CONS_SUM, kFusedUnroll<FO_CONS_SUM>, VPU, DIRECT>(a, ctas, ov, dv, st);
+    case FO_CONS_RS: return launch_fused_kind<FO_CONS_RS, kFusedUnroll<FO_CONS_RS>, VPU, DIRECT>(a, ctas, ov, dv, st);
+    case FO_CONS_A2A: return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU, DIRECT>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
 }
@@ -494,10 +556,12 @@ int log2_exact(int v) {
 // 1, 2, 3 and 4 CTAs per SM): the sums are bandwidth-bound with two loads
 // per source in flight and want 4 CTAs per SM; the copy and bucket
 // consumers keep 8 loads in flight per thread and interfere least with the
-// GEMM at 1 per SM; the fused consumer+reorder does best at 3 per SM.
-int default_ctas(const fo_plan* p, int requested, int kind, bool fused) {
+// GEMM at 1 per SM; the fused consumer+reorder does best at 3 per SM, and
+// so does its direct variant except for the All-to-All bucket, where the
+// GEMM dominates the step and 1 CTA per SM slows it least.
+int default_ctas(const fo_plan* p, int requested, int kind, bool fused, bool direct) {
   if (requested > 0) return requested;
-  if (fused) return 3 * p->sm_count;
+  if (fused) return (direct && kind == FO_CONS_A2A ? 1 : 3) * p->sm_count;
   return (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? 4 * p->sm_count : p->sm_count;
 }
 
@@ -562,7 +626,7 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
   a.trace = p->consumer_trace;
-  const int ctas = default_ctas(p, p->consumer_ctas, kind, false);
+  const int ctas = default_ctas(p, p->consumer_ctas, kind, false, false);
   const bool ov = p->overlap != 0;
   const int dv = p->device;
   switch (kind) {
@@ -585,7 +649,11 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
   c.src = static_cast<const uint4*>(src);
   for (int i = 0; i < n_partials; ++i) c.partials[i] = static_cast<const uint4*>(partials[i]);
   const int n_comm = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
-  for (int k = 0; k < n_comm; ++k) c.dst[k] = static_cast<uint4*>(comm_dst[k]);
+  a.direct = comm_dst == nullptr ? 1 : 0;
+  // the direct variant names each place in 28 bits of 16-byte vectors
+  if (a.direct && !p->place_ok) return FO_ERR_UNSUPPORTED;
+  if (comm_dst != nullptr)
+    for (int k = 0; k < n_comm; ++k) c.dst[k] = static_cast<uint4*>(comm_dst[k]);
   const int n_fin = p->layout == FO_LAYOUT_TILE ? 1 : p->R;
   for (int k = 0; k < n_fin; ++k) a.fin[k] = static_cast<uint4*>(final_dst[k]);
   c.flags = flags;
@@ -608,13 +676,17 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
   a.map = make_row_map(p);
   a.bias = static_cast<const uint16_t*>(bias);
   a.unit_src = p->dev.unit_src;
+  a.unit_place = p->dev.unit_place;
   a.act = act;
   a.row_vec = p->N / 8;
-  const int ctas = default_ctas(p, p->consumer_ctas, kind, true);
+  const int ctas = default_ctas(p, p->consumer_ctas, kind, true, a.direct != 0);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool ov = p->overlap != 0;
-  return p->tile_n == 256 ? launch_fused_vpu<32>(kind, a, ctas, ov, p->device, st)
-                          : launch_fused_vpu<16>(kind, a, ctas, ov, p->device, st);
+  if (a.direct)
+    return p->tile_n == 256 ? launch_fused_vpu<32, true>(kind, a, ctas, ov, p->device, st)
+                            : launch_fused_vpu<16, true>(kind, a, ctas, ov, p->device, st);
+  return p->tile_n == 256 ? launch_fused_vpu<32, false>(kind, a, ctas, ov, p->device, st)
+                          : launch_fused_vpu<16, false>(kind, a, ctas, ov, p->device, st);
 }
 
 }  // namespace fo
@@ -728,7 +800,7 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.chunk_units = chunk_units_of(kind, p->tile_n);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
-  const int ctas = default_ctas(p, p->consumer_ctas, kind, false);
+  const int ctas = default_ctas(p, p->consumer_ctas, kind, false, false);
   const bool ov = p->overlap != 0;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   switch (kind) {

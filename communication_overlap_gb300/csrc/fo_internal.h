@@ -46,6 +46,9 @@ struct DeviceTables {
   int32_t* final_row = nullptr;        // [M] A2A: row in the rank's output
   int32_t* unit_src = nullptr;         // [units] slot << 7 | row of the tile row each
                                        //   unit holds (A2A: room for M * N / tile_n)
+  int32_t* unit_place = nullptr;       // [units, as unit_src] final place of each unit:
+                                       //   output k << 28 | 16-byte vector index of
+                                       //   its first element there
   int32_t* slot_live = nullptr;        // [tiles] A2A: 1 if a row of the tile holds
                                        //   a token (else the GEMM skips it)
   int32_t* work = nullptr;             // [P + 1] scratch: consumer chunk counters
@@ -80,6 +83,10 @@ struct fo_plan {
   std::vector<fo::TileInfo> tile;
   std::vector<int32_t> part_start, part_len, part_dst, dest_units, final_rows, dest_capacity;
   std::vector<int32_t> dest_base, row_dest, row_rank, final_row, slot_live, unit_src;
+  std::vector<int32_t> unit_place;
+  // every output holds fewer than 2^28 16-byte vectors, so unit_place can
+  // name any place in it (the direct consumer+reorder needs this)
+  bool place_ok = false;
   int32_t route_blocks = 0;       // A2A: tile-row blocks (ceil(rows / 128) per expert)
   // fo_plan_route rebuilt the routing tables on the device: the host copies
   // above are stale until refresh_routing() downloads them
@@ -114,6 +121,9 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p);
 int32_t expert_tile_rows(int layout, int32_t W, int32_t rows);
 fo_status upload_plan(fo_plan* p);
 int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r);
+int32_t place_of(const fo_plan* p, int32_t slot, int32_t r);
+// bits of unit_place that hold the vector index; the output is above them
+constexpr int kPlaceShift = 28;
 void set_a2a_outputs(fo_plan* p, int32_t n_tokens, int32_t top_k);
 fo_status refresh_routing(fo_plan* p);
 

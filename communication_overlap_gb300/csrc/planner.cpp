@@ -344,12 +344,42 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   // unit holds (read by the fused consumer+reorder).  All-to-All: room for
   // every row, since fo_plan_route may route them all.
   p->unit_src.assign(layout == FO_LAYOUT_A2A_SUBTOKEN ? size_t(d->M) * TN : size_t(p->n_units), 0);
+  // and each unit's final place, for the direct consumer+reorder
+  p->place_ok = true;
+  for (int32_t rows : p->final_rows)
+    if (int64_t(rows) * (d->N / 8) >= (int64_t(1) << kPlaceShift)) p->place_ok = false;
+  p->unit_place.assign(p->unit_src.size(), 0);
   for (int32_t s = 0; s < tiles; ++s)
     for (int32_t r = 0; r < p->tile[s].rows; ++r) {
       const int32_t u = unit_of(p, s, r);
-      if (u >= 0) p->unit_src[u] = (s << 7) | r;
+      if (u < 0) continue;
+      p->unit_src[u] = (s << 7) | r;
+      if (p->place_ok) p->unit_place[u] = place_of(p, s, r);
     }
   return FO_OK;
+}
+
+// Final place of row r of the tile at slot s (a row that holds a token):
+// output k << kPlaceShift | the 16-byte vector index, in output k, of the
+// row's element at the tile's first column.  The rows are those of the
+// post-communication reorder: TILE row row0 + r; RS_SUBTILE subtile k = r / h
+// of tile row tm goes to slice row h tm + r - h k; RS_ROWBLOCK the tile's
+// rank, row row0 + r - k M / R; A2A the row's rank and its final row.
+int32_t place_of(const fo_plan* p, int32_t slot, int32_t r) {
+  const TileInfo& ti = p->tile[slot];
+  int32_t k = 0, row = ti.row0 + r;
+  if (p->layout == FO_LAYOUT_RS_SUBTILE) {
+    const int32_t h = kTileM / p->R;
+    k = r / h;
+    row = (ti.row0 / kTileM) * h + r - k * h;
+  } else if (p->layout == FO_LAYOUT_RS_ROWBLOCK) {
+    k = ti.dest;
+    row = ti.row0 + r - k * (p->M / p->R);
+  } else if (p->layout == FO_LAYOUT_A2A_SUBTOKEN) {
+    k = p->row_dest[ti.row0 + r];
+    row = p->final_row[ti.row0 + r];
+  }
+  return (k << kPlaceShift) | (row * (p->N / 8) + ti.col0 / 8);
 }
 
 // All-to-All outputs for routings of n_tokens tokens with top_k slots each:
@@ -421,6 +451,7 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_fr = put(buf, p->final_row);
   const size_t o_sl = put(buf, p->slot_live);
   const size_t o_us = put(buf, p->unit_src);
+  const size_t o_up = put(buf, p->unit_place);
   const size_t o_work = put(buf, std::vector<int32_t>(p->P + 1, 0));
   const size_t o_fin = put(buf, std::vector<int32_t>(p->P, 0));
   const size_t o_cons = put(buf, std::vector<int32_t>(p->P, 0));
@@ -457,6 +488,7 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.final_row = reinterpret_cast<int32_t*>(b + o_fr);
   p->dev.slot_live = reinterpret_cast<int32_t*>(b + o_sl);
   p->dev.unit_src = reinterpret_cast<int32_t*>(b + o_us);
+  p->dev.unit_place = reinterpret_cast<int32_t*>(b + o_up);
   p->dev.work = reinterpret_cast<int32_t*>(b + o_work);
   p->dev.finished = reinterpret_cast<int32_t*>(b + o_fin);
   p->dev.consumed = reinterpret_cast<uint32_t*>(b + o_cons);
@@ -483,7 +515,7 @@ fo_status refresh_routing(fo_plan* p) {
       !get(p->part_dst, p->dev.part_dst) || !get(p->group_unit_begin, p->dev.group_unit_begin) ||
       !get(p->dest_base, p->dev.dest_base) || !get(p->row_dest, p->dev.row_dest) ||
       !get(p->row_rank, p->dev.row_rank) || !get(p->final_row, p->dev.final_row) ||
-      !get(p->slot_live, p->dev.slot_live))
+      !get(p->slot_live, p->dev.slot_live) || !get(p->unit_place, p->dev.unit_place))
     return FO_ERR_CUDA;
   for (int k = 0; k < p->R; ++k) {
     int32_t off = 0;

@@ -71,12 +71,14 @@ struct RouteArgs {
   int32_t* dest_base;         // [tiles * R]
   int32_t* slot_live;         // [tiles] 1 if a row of the tile holds a token
   int32_t* unit_src;          // [units] slot << 7 | row of the tile row each unit holds
+  int32_t* unit_place;        // [units] final place: rank << kPlaceShift | vector index
+                              //   (NULL: the plan's outputs are too large for it)
   int32_t* status;            // caller's status word
   int32_t expert_row0[kMaxExperts];
   int32_t expert_rows[kMaxExperts];
   int32_t expert_block0[kMaxExperts + 1];
   int32_t cap[kMaxDest];      // units each receive buffer holds
-  int32_t n_experts, R, n_tokens, top_k, B, P, tiles, TN, swizzle, tile_n, M;
+  int32_t n_experts, R, n_tokens, top_k, B, P, tiles, TN, swizzle, tile_n, M, N;
 };
 
 __global__ void __launch_bounds__(kTileM) route_rows_kernel(const __grid_constant__ RouteArgs a) {
@@ -250,8 +252,9 @@ __global__ void __launch_bounds__(kPartsThreads) route_parts_kernel(const __grid
     return;
   }
   // 5. the inverse at row granularity: unit -> the tile row it holds (read by
-  //    the fused consumer+reorder); row r of the tile at slot s is unit
-  //    dest_base[s][d] + rank, computed here from the same closed form
+  //    the fused consumer+reorder) and its final place (read by its direct
+  //    variant); row r of the tile at slot s is unit dest_base[s][d] + rank,
+  //    computed here from the same closed form
   for (int64_t i = first; i < int64_t(a.tiles) * kTileM; i += stride) {
     const int32_t s = int32_t(i / kTileM), r = int32_t(i % kTileM);
     const TileInfo& ti = a.tile[s];
@@ -262,6 +265,8 @@ __global__ void __launch_bounds__(kPartsThreads) route_parts_kernel(const __grid
     const int32_t u = off[ti.group * R + d] +
                       units_before(a, BP, ti.row0, ti.col0, ti.expert, d) + a.row_rank[rho];
     a.unit_src[u] = (s << 7) | r;
+    if (a.unit_place != nullptr)
+      a.unit_place[u] = (d << kPlaceShift) | (a.final_row[rho] * (a.N / 8) + ti.col0 / 8);
   }
 }
 
@@ -308,6 +313,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
   a.dest_base = p->dev.dest_base;
   a.slot_live = p->dev.slot_live;
   a.unit_src = p->dev.unit_src;
+  a.unit_place = p->place_ok ? p->dev.unit_place : nullptr;
   a.status = dev_status;
   const int E = int(p->expert_rows.size());
   int32_t blocks = 0;
@@ -330,6 +336,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
   a.swizzle = p->swizzle;
   a.tile_n = p->tile_n;
   a.M = p->M;
+  a.N = p->N;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   route_rows_kernel<<<a.B, kTileM, 0, st>>>(a);

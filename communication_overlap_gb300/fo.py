@@ -20,7 +20,7 @@ FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
 FO_ACT_NONE, FO_ACT_RELU, FO_ACT_SILU = range(3)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
- FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY, FO_TAB_SLOT_LIVE) = range(12)
+ FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY, FO_TAB_SLOT_LIVE, FO_TAB_UNIT_PLACE) = range(13)
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _vp = ctypes.c_void_p
@@ -281,9 +281,12 @@ def fo_reorder_back_fused(plan, group_begin, group_end, src, dst, bias, act, str
 
 def fo_consume_reorder(plan, group, kind, src, partials, comm_dst, final_dst, bias, act,
                        flags, epoch, spin_limit_ns, dev_status, stream):
+    """comm_dst: device addresses, or None for the direct variant (no
+    communication buffers written)."""
     _check("fo_consume_reorder",
            lib().fo_consume_reorder(plan, group, kind, int(src), _ptrs(partials), len(partials),
-                                    _ptrs(comm_dst), _ptrs(final_dst), int(bias) or None, act,
+                                    None if comm_dst is None else _ptrs(comm_dst),
+                                    _ptrs(final_dst), int(bias) or None, act,
                                     int(flags), epoch & 0xffffffff, spin_limit_ns,
                                     int(dev_status), stream or None))
 

@@ -164,11 +164,14 @@ class Pipeline:
                            stream.cuda_stream)
 
     def consume_reorder(self, stream, epoch, group=-1, spin_limit_ns=0, bias=0,
-                        act=fo.FO_ACT_NONE):
+                        act=fo.FO_ACT_NONE, direct=False):
+        """direct: no communication buffers; every unit goes straight to
+        its final place."""
         b = self.buf
         fo.fo_consume_reorder(self.plan, group, self.kind, b.C_r.data_ptr(),
                               [p.data_ptr() for p in b.partials],
-                              [c.data_ptr() for c in b.comm], [f.data_ptr() for f in b.final],
+                              None if direct else [c.data_ptr() for c in b.comm],
+                              [f.data_ptr() for f in b.final],
                               bias, act, b.flags.data_ptr(), epoch, spin_limit_ns,
                               b.status.data_ptr(), stream.cuda_stream)
 
@@ -177,11 +180,12 @@ class Pipeline:
             fo.fo_plan_set_launch(self.plan, self.consumer_ctas, self.reorder_ctas, overlap)
             self._overlap = overlap
 
-    def step(self, overlap=True, sync_current=True, fused=False):
+    def step(self, overlap=True, sync_current=True, fused=False, direct=False):
         """One pass of the whole path with a fresh epoch, on stream s0.  With
         overlap the consumer runs alongside the GEMM (dependent launch);
         without, it starts after the GEMM (the serial baseline).  fused: the
-        consumer and the post-communication reorder in one kernel."""
+        consumer and the post-communication reorder in one kernel; direct
+        (with fused): without the communication buffers."""
         self.set_overlap(overlap)
         self.epoch = (self.epoch + 1) & 0xffffffff or 1
         e = self.epoch
@@ -190,7 +194,7 @@ class Pipeline:
             self.s0.wait_stream(cur)
         self.gemm(self.s0, e)
         if fused:
-            self.consume_reorder(self.s0, e)
+            self.consume_reorder(self.s0, e, direct=direct)
         else:
             self.consume(self.s0, e)
             self.reorder(self.s0)

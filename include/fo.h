@@ -142,10 +142,16 @@ typedef enum {
                              final_rows[k] * (N / tile_n), enough for any
                              routing of the plan's tokens (see
                              fo_plan_route); other layouts DEST_UNITS */
-  FO_TAB_SLOT_LIVE = 11   /* [tiles] 1 if a row of the tile at slot s holds a
+  FO_TAB_SLOT_LIVE = 11,  /* [tiles] 1 if a row of the tile at slot s holds a
                              token.  A2A only can have 0s: the GEMM skips
                              such a tile's loads and MMAs (both tiles of a
                              CTA pair must be empty) and only counts it */
+  FO_TAB_UNIT_PLACE = 12  /* [units] final place of each unit of C_r, as
+                             the post-communication reorder puts it:
+                             k << 28 | the 16-byte vector index, in output k,
+                             of the unit's first element (its row x N / 8 +
+                             its first column / 8).  FO_ERR_UNSUPPORTED when
+                             an output holds 2^28 or more vectors */
 } fo_table;               /* R = 1 for FO_LAYOUT_TILE, else n_dest */
 
 /* Copy table `which` into out[0 .. capacity); *length = its full length.
@@ -159,7 +165,8 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
 /* Launch settings of the consumer and reorder kernels.
  *  consumer_ctas, reorder_ctas: grid sizes (<= 0: the defaults, measured
  *      beside the GEMM: consumer 4 CTAs per SM for SUM / RS, 1 per SM for
- *      COPY / A2A, 3 per SM for fo_consume_reorder; reorder 3 per SM).
+ *      COPY / A2A, 3 per SM for fo_consume_reorder (its direct variant: 1
+ *      per SM for A2A); reorder 3 per SM).
  *  overlap: non-zero (default) launches the consumer as a programmatic
  *      dependent launch: issued on the GEMM's stream right after
  *      fo_signaled_gemm, it starts as soon as every GEMM CTA is resident and
@@ -421,12 +428,19 @@ fo_status fo_reorder_back_fused(const fo_plan* plan, int32_t group_begin, int32_
  * writes to dst.  Every group is moved to its final layout while the GEMM
  * still computes later groups ([P1] 五: the post-communication reorder fused
  * with the element-wise epilogue to save a launch):
- *  - TILE and RS layouts: a CTA that has written a chunk of units to
- *    comm_dst reads them back from there and stores them to final_dst at
- *    once, so a group is final one chunk after its flag rises;
- *  - A2A: a CTA that has taken its share of group j's communication
- *    reorders group j-1, after waiting (bounded) until every chunk of j-1
- *    is counted as consumed.
+ * a CTA that has written a chunk of units to comm_dst reads them back from
+ * there (still in L2) and stores them to final_dst at once, so a group is
+ * final one chunk after its flag rises.  No CTA waits for another.
+ *  comm_dst: as fo_consume_group's dst, or NULL for the direct variant: the
+ *      communication buffers are then neither written nor read, and each
+ *      consumed unit (the same copy or the same fp32 sum, in the same
+ *      order) is stored straight to its final place.  final_dst is
+ *      bit-identical either way; the direct variant moves fewer bytes
+ *      (SUM with n partials: (n + 2) x C rather than (n + 4) x C; COPY and
+ *      A2A: 2 x C rather than 4 x C, for C the output's bytes).
+ *      Each unit's place comes from FO_TAB_UNIT_PLACE (one table load).
+ *      FO_ERR_UNSUPPORTED if an output holds 2^28 or more 16-byte vectors
+ *      (4 GiB), which that table cannot name.
  * Layouts: TILE (COPY, SUM), RS (RS), A2A (A2A).  Uses the plan's scratch;
  * calls that overlap in time on one plan race on it. */
 fo_status fo_consume_reorder(const fo_plan* plan, int32_t group, fo_consumer kind,

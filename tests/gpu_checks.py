@@ -1,6 +1,7 @@
 """Shared checks of the CUDA path against the oracle (used by -m gpu tests
 and by __graft_entry__.smoke)."""
 import numpy as np
+import torch
 
 from communication_overlap_gb300 import workloads as W
 from communication_overlap_gb300.pipeline import Pipeline
@@ -52,9 +53,28 @@ def token_rows(w, inp):
     return np.asarray(inp.row_token) >= 0
 
 
-def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
+# A bf16 NaN pattern no output carries: the communication buffers hold it
+# before a step of the direct variant, which must leave them untouched.
+COMM_SENTINEL = 0x7FC1
+
+
+def fill_comm_sentinel(pipe):
+    for c in pipe.buf.comm:
+        c.view(torch.int16).fill_(COMM_SENTINEL)
+
+
+def step_mode(mode):
+    """Pipeline.step keywords of a test mode: False (separate kernels), True
+    (fused) or "direct" (fused, without communication buffers)."""
+    return dict(fused=bool(mode), direct=mode == "direct")
+
+
+def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True, direct=False):
     """Every check of one GPU pass.  Returns a dict of findings; raises
-    AssertionError on the first mismatch."""
+    AssertionError on the first mismatch.  direct: the pass used the direct
+    variant, so the communication buffers must still hold COMM_SENTINEL and
+    the final buffers are checked against the oracle's reorder of the
+    oracle's consumer output."""
     w = pipe.w
     op = oracle_plan(w, inp, pipe.partition)
     out = {}
@@ -89,7 +109,10 @@ def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
         comm = OC.consume_a2a(op, C_r_ref)
     assert len(comm) == len(res["comm"])
     for k, (g, r) in enumerate(zip(res["comm"], comm)):
-        assert np.array_equal(g, r), f"consumer buffer {k} differs"
+        if direct:
+            assert (g == COMM_SENTINEL).all(), f"consumer buffer {k} was written"
+        else:
+            assert np.array_equal(g, r), f"consumer buffer {k} differs"
     # post-comm reorder: bit-exact
     if w.layout == W.LAYOUT_TILE:
         final = [OC.reorder_back_tile(op, comm[0])]
@@ -105,11 +128,14 @@ def check_run(pipe, inp, res, gemm_rows=None, full_gemm=True):
 
 
 def run_workload(w, inp=None, overlap=True, steps=2, fused=False, **kw):
+    """fused: a test mode of step_mode."""
     inp = inp or W.make_inputs(w)
     pipe = Pipeline(w, inp, **kw)
     try:
+        if fused == "direct":
+            fill_comm_sentinel(pipe)
         for _ in range(steps):
-            pipe.step(overlap=overlap, fused=fused)
+            pipe.step(overlap=overlap, **step_mode(fused))
         res = pipe.results()
     except Exception:
         pipe.close()

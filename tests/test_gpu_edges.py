@@ -10,7 +10,7 @@ from communication_overlap_gb300 import fo
 from communication_overlap_gb300 import workloads as W
 from communication_overlap_gb300.pipeline import Pipeline
 
-from gpu_checks import check_run, run_workload
+from gpu_checks import check_run, fill_comm_sentinel, run_workload, step_mode
 
 pytestmark = pytest.mark.gpu
 
@@ -19,17 +19,19 @@ def _run(w, partition=None, fused=False, variant=None, **kw):
     inp = W.make_inputs(w)
     pipe = Pipeline(w, inp, partition=partition, gemm_variant=variant, **kw)
     try:
+        if fused == "direct":
+            fill_comm_sentinel(pipe)
         for _ in range(2):
-            pipe.step(fused=fused)
+            pipe.step(**step_mode(fused))
         res = pipe.results()
-        check_run(pipe, inp, res)
+        check_run(pipe, inp, res, direct=fused == "direct")
         assert fo.fo_plan_device_status(pipe.plan) == 0
         return pipe.tiles, pipe.waves, pipe.partition
     finally:
         pipe.close()
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "direct"])
 @pytest.mark.parametrize("case", [
     dict(M=128, N=256, K=64, wave_width=1),           # one tile, one k-block
     dict(M=1, N=256, K=128, wave_width=1),            # one row
@@ -61,7 +63,7 @@ def test_split_with_two_k_blocks(variant):
         pipe.close()
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "direct"])
 def test_tile_n_128_pairs_and_split(fused):
     """128 x 128 tiles: 32 tiles on W = 20 (last wave 12, not split) and on
     W = 24 (last wave 8, split), with CTA pairs."""
@@ -72,8 +74,10 @@ def test_tile_n_128_pairs_and_split(fused):
         pipe = Pipeline(w, inp, gemm_variant=fo.FO_GEMM_PAIRS)
         try:
             assert fo.fo_plan_set_split(pipe.plan, True) == n_split
-            pipe.step(fused=fused)
-            check_run(pipe, inp, pipe.results())
+            if fused == "direct":
+                fill_comm_sentinel(pipe)
+            pipe.step(**step_mode(fused))
+            check_run(pipe, inp, pipe.results(), direct=fused == "direct")
         finally:
             pipe.close()
 

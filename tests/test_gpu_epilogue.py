@@ -12,7 +12,8 @@ from oracle import bf16 as OB
 from oracle import comm as OC
 from oracle import epilogue as OE
 
-from gpu_checks import check_run, gpu_gemm_output, oracle_plan, run_workload
+from gpu_checks import (COMM_SENTINEL, check_run, fill_comm_sentinel, gpu_gemm_output,
+                        oracle_plan, run_workload)
 
 pytestmark = pytest.mark.gpu
 
@@ -130,5 +131,34 @@ def test_fused_consume_reorder(case):
         assert got["status"] == 0
         for g, r in zip(got["final"], res["final"]):
             assert _close(g, OE.elementwise(r, bias, fo.FO_ACT_SILU), fo.FO_ACT_SILU)
+    finally:
+        pipe.close()
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_fused_direct(case):
+    """The direct variant (no communication buffers): the final buffers equal
+    the oracle's reorder of the oracle's consumer output, bit for bit, and
+    the communication buffers are never touched; with an epilogue, the
+    oracle's element-wise result."""
+    w = _workload(case)
+    pipe, inp, res = run_workload(w, steps=2, fused="direct")
+    try:
+        check_run(pipe, inp, res, direct=True)
+        bias = _bias(w.N, 6)
+        dbias = torch.from_numpy(bias.view(np.int16)).cuda()
+        want = [OE.elementwise(r, bias, fo.FO_ACT_RELU) for r in res["final"]]
+        for f in pipe.buf.final:
+            f.zero_()
+        pipe.epoch += 1
+        pipe.gemm(pipe.s0, pipe.epoch)
+        pipe.consume_reorder(pipe.s0, pipe.epoch, bias=dbias.data_ptr(), act=fo.FO_ACT_RELU,
+                             direct=True)
+        got = pipe.results()
+        assert got["status"] == 0
+        for c in got["comm"]:
+            assert (c == COMM_SENTINEL).all()
+        for g, r in zip(got["final"], want):
+            assert np.array_equal(g, r)
     finally:
         pipe.close()

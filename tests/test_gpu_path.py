@@ -15,7 +15,8 @@ from communication_overlap_gb300.pipeline import Pipeline
 from oracle import bf16 as OB
 from oracle import gemm as OG
 
-from gpu_checks import check_run, run_workload, gpu_gemm_output, oracle_plan
+from gpu_checks import (COMM_SENTINEL, check_run, fill_comm_sentinel, gpu_gemm_output,
+                        oracle_plan, run_workload, step_mode)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +73,7 @@ def test_small_alltoall_ragged_experts():
         pipe.close()
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "direct"])
 def test_alltoall_padded_grids_run_as_pairs(fused):
     """An even W pads odd expert grids with an empty tile row, so the GEMM
     runs as CTA pairs; everything matches the oracle."""
@@ -83,9 +84,11 @@ def test_alltoall_padded_grids_run_as_pairs(fused):
     pipe = Pipeline(w, inp, gemm_variant=fo.FO_GEMM_PAIRS)
     try:
         assert pipe.pairable
+        if fused == "direct":
+            fill_comm_sentinel(pipe)
         for _ in range(2):
-            pipe.step(fused=fused)
-        check_run(pipe, inp, pipe.results())
+            pipe.step(**step_mode(fused))
+        check_run(pipe, inp, pipe.results(), direct=fused == "direct")
     finally:
         pipe.close()
 
@@ -176,6 +179,19 @@ def test_full_size_workload(name):
         rng = np.random.default_rng(123)
         rows = np.sort(rng.choice(w.M, size=512, replace=False))
         check_run(pipe, inp, res, gemm_rows=rows, full_gemm=False)
+        # the direct fused variant, as the benchmark also times it: the same
+        # final buffers, bit for bit, and the communication buffers untouched
+        fill_comm_sentinel(pipe)
+        for f in pipe.buf.final:
+            f.zero_()
+        for _ in range(2):
+            pipe.step(fused=True, direct=True)
+        got = pipe.results()
+        assert got["status"] == 0
+        for g, r in zip(got["final"], res["final"]):
+            assert np.array_equal(g, r)
+        for c in got["comm"]:
+            assert (c == COMM_SENTINEL).all()
     finally:
         pipe.close()
 

@@ -18,13 +18,13 @@ from communication_overlap_gb300 import fo
 from communication_overlap_gb300 import workloads as W
 from communication_overlap_gb300.pipeline import Pipeline
 
-from gpu_checks import check_run, oracle_plan
+from gpu_checks import check_run, fill_comm_sentinel, oracle_plan, step_mode
 
 pytestmark = pytest.mark.gpu
 
 _TABLES = (fo.FO_TAB_UNIT, fo.FO_TAB_PART_START, fo.FO_TAB_PART_LEN, fo.FO_TAB_PART_DST,
            fo.FO_TAB_DEST_UNITS, fo.FO_TAB_FINAL_ROWS, fo.FO_TAB_DEST_CAPACITY,
-           fo.FO_TAB_SLOT_LIVE)
+           fo.FO_TAB_SLOT_LIVE, fo.FO_TAB_UNIT_PLACE)
 
 
 def _small(capacity=384, **kw):
@@ -91,7 +91,7 @@ def test_device_tables_equal_host_tables(capacity, wave_width):
         pipe.close()
 
 
-@pytest.mark.parametrize("fused,wave_width", [(False, 7), (True, 7), (True, 8)])
+@pytest.mark.parametrize("fused,wave_width", [(False, 7), (True, 7), (True, 8), ("direct", 8)])
 def test_steps_on_device_routings_match_oracle(fused, wave_width):
     """Three steps, each on a routing handed over in device memory; after
     each, every table, the reorders and the consumer match the oracle for
@@ -106,9 +106,11 @@ def test_steps_on_device_routings_match_oracle(fused, wave_width):
             for f in pipe.buf.final:
                 f.zero_()
             _route(pipe, inp)
-            pipe.step(fused=fused)
+            if fused == "direct":
+                fill_comm_sentinel(pipe)
+            pipe.step(**step_mode(fused))
             res = pipe.results()
-            check_run(pipe, inp, res)
+            check_run(pipe, inp, res, direct=fused == "direct")
     finally:
         pipe.close()
 

@@ -6,7 +6,8 @@ are cleared.  A consumer that ever read a unit before the GEMM had stored it
 and raised the group's flag would copy the sentinel.  Over many steps the
 consumer's and the reorder's outputs must equal, bit for bit, those of the
 first step, which is checked against the oracle.  Covers the separate and
-the fused kernels, and all four consumers.
+the fused kernels (with and without the communication buffers), and all
+four consumers.
 """
 import numpy as np
 import pytest
@@ -15,7 +16,7 @@ import torch
 from communication_overlap_gb300 import workloads as W
 from communication_overlap_gb300.pipeline import Pipeline
 
-from gpu_checks import check_run
+from gpu_checks import check_run, fill_comm_sentinel, step_mode
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +40,7 @@ def _digest(tensors):
     return out
 
 
-@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("fused", [False, True, "direct"])
 @pytest.mark.parametrize("name,kw", CASES)
 def test_repeated_overlapped_steps(name, kw, fused):
     w = W.scaled(W.WORKLOADS[name], **kw)
@@ -53,11 +54,13 @@ def test_repeated_overlapped_steps(name, kw, fused):
             pipe.buf.C_r.copy_(sentinel)
             for c in pipe.buf.comm + pipe.buf.final:
                 c.zero_()
-            pipe.step(fused=fused)
+            if fused == "direct":
+                fill_comm_sentinel(pipe)
+            pipe.step(**step_mode(fused))
             if rep == 0:
                 res = pipe.results()
-                check_run(pipe, inp, res)
-                assert not any((c == 0xFFFF).any() for c in res["comm"])
+                check_run(pipe, inp, res, direct=fused == "direct")
+                assert not any((c == 0xFFFF).any() for c in res["comm"] + res["final"])
                 first = _digest(pipe.buf.comm + pipe.buf.final)
             else:
                 assert _digest(pipe.buf.comm + pipe.buf.final) == first, rep

@@ -5,11 +5,40 @@ import pytest
 
 from communication_overlap_gb300 import fo
 from communication_overlap_gb300 import workloads as W
+from oracle import comm as OC
 from oracle import plan as OP
 
 _LAYOUT_NAME = {fo.FO_LAYOUT_TILE: OP.LAYOUT_TILE, fo.FO_LAYOUT_RS_SUBTILE: OP.LAYOUT_RS_SUBTILE,
                 fo.FO_LAYOUT_RS_ROWBLOCK: OP.LAYOUT_RS_ROWBLOCK,
                 fo.FO_LAYOUT_A2A_SUBTOKEN: OP.LAYOUT_A2A}
+
+
+def _oracle_places(op, layout, tok, sl):
+    """Each unit's final place as the oracle's consumer and post-communication
+    reorder put it: every unit of C_r carries its number + 1 in its first
+    three columns (14 bits each: finite bf16 patterns, which a one-source
+    fp32 sum keeps), the oracle moves the units, and the outputs are read
+    back.  Place = k << 28 | row x N / 8 + first column / 8."""
+    n = op.n_units
+    ids = np.arange(1, n + 1, dtype=np.int64)
+    C_r = np.zeros((n, op.tile_n), dtype=np.uint16)
+    for c in range(3):
+        C_r[:, c] = (ids >> (14 * c)) & 0x3FFF
+    if layout == fo.FO_LAYOUT_TILE:
+        outs = [OC.reorder_back_tile(op, OC.consume_copy(op, C_r))]
+    elif layout == fo.FO_LAYOUT_A2A_SUBTOKEN:
+        top_k = int(sl[tok >= 0].max()) + 1
+        outs = OC.reorder_back_a2a(op, OC.consume_a2a(op, C_r), top_k,
+                                   n_tokens=int(tok.max()) + 1)
+    else:
+        outs = OC.reorder_back_rs(op, OC.consume_rs(op, C_r, []))
+    place = np.full(n, -1, dtype=np.int64)
+    for k, out in enumerate(outs):
+        blocks = out.reshape(out.shape[0], -1, op.tile_n).astype(np.int64)
+        got = blocks[..., 0] | (blocks[..., 1] << 14) | (blocks[..., 2] << 28)
+        r, c = np.nonzero(got)
+        place[got[r, c] - 1] = (k << 28) | (r * (op.N // 8) + c * (op.tile_n // 8))
+    return place
 
 
 def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
@@ -43,6 +72,9 @@ def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
             [OP.dest_rows(op, k) for k in range(op.part_start.shape[1])]
         live = fo.fo_plan_table(plan, fo.FO_TAB_SLOT_LIVE)
         assert live == (op.unit >= 0).any(axis=1).astype(int).tolist()
+        if op.n_units * tile_n <= (1 << 26):   # the id payload stays small
+            place = fo.fo_plan_table(plan, fo.FO_TAB_UNIT_PLACE)
+            assert place == _oracle_places(op, layout, tok, sl).tolist()
         if layout == fo.FO_LAYOUT_A2A_SUBTOKEN:
             # output rows: every slot of every token of the rank
             n_tok, k = int(tok.max()) + 1, int(sl[tok >= 0].max()) + 1
