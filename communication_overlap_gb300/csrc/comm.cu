@@ -26,18 +26,19 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// 16-byte vectors each lane keeps in flight per source (per iteration).
+// 16-byte vectors each lane keeps in flight per source (per iteration): the
+// sums keep one per source, all sources at once (sum_partials).
 template <int KIND>
-constexpr int kUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 2 : 8;
+constexpr int kUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 1 : 8;
 // Bytes of the source a CTA takes per chunk: one pass of U vectors per
-// thread for the copies (32 KB), two passes for the sums (16 KB).
+// thread for the copies (32 KB), four passes for the sums (16 KB).
 template <int KIND>
 constexpr int kChunkBytes = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 16 * 1024 : 32 * 1024;
 // The fused consumer+reorder keeps fewer copy loads in flight per thread: it
 // runs at 72 registers (two CTAs beside a GEMM CTA) and also holds the
 // reorder's loads.
 template <int KIND>
-constexpr int kFusedUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 2 : 4;
+constexpr int kFusedUnroll = (KIND == FO_CONS_SUM || KIND == FO_CONS_RS) ? 1 : 4;
 // Units of the largest chunk (32 KB of 256-byte units at tile_n = 128).
 constexpr int kMaxChunkUnits = 32 * 1024 / 256;
 
@@ -85,6 +86,33 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
 }
 
+// x[i] (U vectors of the own buffer at base + kThreads * i, those below v1)
+// becomes the fp32 sum of itself and the same vectors of every partial, in
+// order, rounded once to bf16.  Every partial's loads are issued before the
+// first addition (predicated per partial, no early exit), so a thread keeps
+// all its sources' loads in flight at once instead of one source at a time.
+template <int U>
+__device__ __forceinline__ void sum_partials(const ConsumeArgs& a, int32_t base, int32_t v1,
+                                             uint64_t pol, uint4 (&x)[U]) {
+  uint4 y[kMaxPartials][U];
+#pragma unroll
+  for (int q = 0; q < kMaxPartials; ++q)
+#pragma unroll
+    for (int i = 0; i < U; ++i)
+      if (q < a.n_partials && base + kThreads * i < v1)
+        y[q][i] = ld_once(a.partials[q] + base + kThreads * i, pol);
+  float acc[U][8];
+#pragma unroll
+  for (int i = 0; i < U; ++i) set_bf16x8(acc[i], x[i]);
+#pragma unroll
+  for (int q = 0; q < kMaxPartials; ++q)
+    if (q < a.n_partials)
+#pragma unroll
+      for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[q][i]);
+#pragma unroll
+  for (int i = 0; i < U; ++i) x[i] = pack8(acc[i]);
+}
+
 // Where vector v (unit v >> vpu_shift) of the group goes: destination k's
 // part (j, k) starts at unit part_dst there.
 __device__ __forceinline__ uint4* route(const int32_t* ps, const int32_t* pl,
@@ -115,23 +143,7 @@ __device__ __forceinline__ void consume_range(const ConsumeArgs& a, const int32_
 #pragma unroll
     for (int i = 0; i < U; ++i)
       if (base + S * i < v1) x[i] = ld_once(a.src + base + S * i, pol);
-    if constexpr (kSum) {
-      float acc[U][8];
-#pragma unroll
-      for (int i = 0; i < U; ++i) set_bf16x8(acc[i], x[i]);
-#pragma unroll
-      for (int q = 0; q < kMaxPartials; ++q) {
-        if (q >= a.n_partials) break;
-        uint4 y[U];
-#pragma unroll
-        for (int i = 0; i < U; ++i)
-          if (base + S * i < v1) y[i] = ld_once(a.partials[q] + base + S * i, pol);
-#pragma unroll
-        for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < U; ++i) x[i] = pack8(acc[i]);
-    }
+    if constexpr (kSum) sum_partials<U>(a, base, v1, pol, x);
 #pragma unroll
     for (int i = 0; i < U; ++i) {
       const int32_t v = base + S * i;
@@ -361,23 +373,7 @@ __device__ __forceinline__ void consume_direct(const FusedArgs& a, uint4* const*
 #pragma unroll
     for (int i = 0; i < U; ++i)
       if (base + S * i < v1) x[i] = ld_once(c.src + base + S * i, pol);
-    if constexpr (kSum) {
-      float acc[U][8];
-#pragma unroll
-      for (int i = 0; i < U; ++i) set_bf16x8(acc[i], x[i]);
-#pragma unroll
-      for (int q = 0; q < kMaxPartials; ++q) {
-        if (q >= c.n_partials) break;
-        uint4 y[U];
-#pragma unroll
-        for (int i = 0; i < U; ++i)
-          if (base + S * i < v1) y[i] = ld_once(c.partials[q] + base + S * i, pol);
-#pragma unroll
-        for (int i = 0; i < U; ++i) add_bf16x8(acc[i], y[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < U; ++i) x[i] = pack8(acc[i]);
-    }
+    if constexpr (kSum) sum_partials<U>(c, base, v1, pol, x);
 #pragma unroll
     for (int i = 0; i < U; ++i) {
       if (place[i] < 0) continue;   // past the chunk
