@@ -75,6 +75,39 @@ def test_host_only_plan_refuses_launches():
             fo.fo_reorder_back(plan, 0, 3, [16], [16], 0)
         with pytest.raises(fo.FoError):
             fo.fo_consume_group(plan, -1, fo.FO_CONS_COPY, 16, [], [16], 16, 1, 0, 16, 0)
+        for comm in ([16], None):    # with communication buffers, and direct
+            with pytest.raises(fo.FoError) as e:
+                fo.fo_consume_reorder(plan, -1, fo.FO_CONS_COPY, 16, [], comm, [16], 0,
+                                      fo.FO_ACT_NONE, 16, 1, 0, 16, 0)
+            assert e.value.status == fo.FO_ERR_ARG
+    finally:
+        fo.fo_plan_destroy(plan)
+
+
+def test_unit_place_table():
+    """Every unit's final place, as k << 28 | 16-byte vector index; a plan
+    whose output holds 2^28 vectors or more cannot name them."""
+    d = fo.make_desc(M=256, N=512, K=256, tile_n=128, swizzle=2, wave_width=2,
+                     group_waves=(1, 2, 1), host_only=True)
+    plan = fo.fo_plan_groups(d)
+    try:
+        place = fo.fo_plan_table(plan, fo.FO_TAB_UNIT_PLACE)
+        unit = fo.fo_plan_table(plan, fo.FO_TAB_UNIT)
+        tile_of_slot = fo.fo_plan_table(plan, fo.FO_TAB_SLOT_TILE)
+        assert sorted(place) == list(range(0, 256 * 512 // 8, 128 // 8))
+        for s, t in enumerate(tile_of_slot):   # tile t = tm * 4 + tn (row-major)
+            for r in range(128):
+                row, col = 128 * (t // 4) + r, 128 * (t % 4)
+                assert place[unit[128 * s + r]] == row * 512 // 8 + col // 8
+    finally:
+        fo.fo_plan_destroy(plan)
+    big = dict(M=65536, N=32768, K=64, tile_n=256, swizzle=8, wave_width=148, host_only=True)
+    _, T = fo.fo_wave_count(fo.make_desc(**big))
+    plan = fo.fo_plan_groups(fo.make_desc(**big, group_waves=(T,)))
+    try:
+        with pytest.raises(fo.FoError) as e:
+            fo.fo_plan_table(plan, fo.FO_TAB_UNIT_PLACE)
+        assert e.value.status == fo.FO_ERR_UNSUPPORTED
     finally:
         fo.fo_plan_destroy(plan)
 
@@ -91,6 +124,7 @@ def test_a2a_plan_without_routing_starts_empty():
         assert fo.fo_plan_table(plan, fo.FO_TAB_FINAL_ROWS) == [0] * 4
         assert fo.fo_plan_table(plan, fo.FO_TAB_DEST_CAPACITY) == [0] * 4
         assert set(fo.fo_plan_table(plan, fo.FO_TAB_UNIT)) == {-1}
+        assert fo.fo_plan_table(plan, fo.FO_TAB_UNIT_PLACE) == []
         with pytest.raises(fo.FoError) as e:   # host-only: nothing on a device to route
             fo.fo_plan_route(plan, 16, 16, 10, 2, 16, 0)
         assert e.value.status == fo.FO_ERR_ARG

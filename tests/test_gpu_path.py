@@ -143,7 +143,8 @@ def test_signals_off_and_repeat_epochs():
 
 def test_per_group_calls_match_whole_call():
     """Consuming and reordering group by group gives the same bytes as the
-    single all-groups call."""
+    single all-groups call; so does the direct consumer+reorder called group
+    by group."""
     w = _small("allreduce", M=512, N=1024, K=256, wave_width=3)
     inp = W.make_inputs(w)
     pipe = Pipeline(w, inp)
@@ -161,6 +162,20 @@ def test_per_group_calls_match_whole_call():
         parts = pipe.results()
         for a, b in zip(whole["comm"] + whole["final"], parts["comm"] + parts["final"]):
             assert np.array_equal(a, b)
+        # the direct consumer+reorder, group by group (last group first)
+        for f in pipe.buf.final:
+            f.zero_()
+        fill_comm_sentinel(pipe)
+        torch.cuda.synchronize()
+        for j in reversed(range(pipe.P)):
+            pipe.consume_reorder(pipe.s1, e, group=j, direct=True)
+        torch.cuda.synchronize()
+        direct = pipe.results()
+        assert direct["status"] == 0
+        for a, b in zip(whole["final"], direct["final"]):
+            assert np.array_equal(a, b)
+        for c in direct["comm"]:
+            assert (c == COMM_SENTINEL).all()
     finally:
         pipe.close()
 
