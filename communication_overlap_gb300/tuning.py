@@ -6,7 +6,8 @@ and a check of the prediction against measured step times.
 Offline ([P1] "FlashOverlap: 信号驱动计算通信重叠论文详解", 四、实时调优, 离线阶段):
   * GEMM configuration: our own signaled GEMM, its duration timed alone;
   * "bandwidth curve": on one GPU the communication is the consumer
-    stand-in, so the curve is the consumer's latency against group bytes,
+    stand-in (by default the direct consumer+reorder the benchmark's step
+    runs), so the curve is the consumer's latency against group bytes,
     sampled on a first group of k waves (k = 1 .. T), its flag already
     raised.  The latency is taken inside the kernel (first CTA start to last
     CTA end, from the consumer's globaltimer trace): in the overlapped step
@@ -58,10 +59,16 @@ def _time(fn, stream, reps, flush):
 
 
 class Tuner:
-    def __init__(self, w, inp=None, reps=20):
+    """kernels: the step's consumer kernels, "direct" (the consumer+reorder
+    storing straight to the final layout, the benchmark's default) or
+    "separate" (consumer, then reorder); the curve and the validation steps
+    both use them."""
+
+    def __init__(self, w, inp=None, reps=20, kernels="direct"):
         self.w = w
         self.inp = inp or W.make_inputs(w)
         self.reps = reps
+        self.direct = kernels == "direct"
         self.pipe = Pipeline(w, self.inp)
         self.flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         self.tile_bytes = w.tile_m * w.tile_n * 2
@@ -96,7 +103,10 @@ class Tuner:
             for _ in range(self.reps):
                 self.flush()
                 trace.zero_()
-                p.consume(p.s0, p.epoch, group=0)
+                if self.direct:
+                    p.consume_reorder(p.s0, p.epoch, group=0, direct=True)
+                else:
+                    p.consume(p.s0, p.epoch, group=0)
                 torch.cuda.synchronize()
                 rec = trace[2 * p.P:].view(-1, 4).cpu()
                 ran = rec[rec[:, 1] > 0]
@@ -108,25 +118,26 @@ class Tuner:
     def step_us(self, partition):
         p = self.pipe
         p.replan(partition)
+        kw = dict(fused=True, direct=True) if self.direct else {}
         for _ in range(3):
-            p.step(overlap=True)
+            p.step(overlap=True, **kw)
         torch.cuda.synchronize()
         assert int(p.buf.status.item()) == 0
-        return _time(lambda: p.step(overlap=True, sync_current=False), p.s0, self.reps,
+        return _time(lambda: p.step(overlap=True, sync_current=False, **kw), p.s0, self.reps,
                      self.flush)
 
     def desc(self, partition=()):
         return fo.make_desc(**self.pipe.desc_args, group_waves=partition, host_only=True)
 
 
-def run(name, validate=False, reps=20):
+def run(name, validate=False, reps=20, kernels="direct"):
     w = W.WORKLOADS[name]
-    t = Tuner(w, reps=reps)
+    t = Tuner(w, reps=reps, kernels=kernels)
     try:
         gemm = t.gemm_us()
         curve = t.curve()
         best, pred = fo.fo_tune_partition(t.desc(), gemm, curve)
-        out = {"workload": name, "waves": t.pipe.waves, "gemm_us": gemm,
+        out = {"workload": name, "kernels": kernels, "waves": t.pipe.waves, "gemm_us": gemm,
                "curve": curve, "tuned": best, "tuned_predicted_us": pred}
         base = fo.partition_one_then_two(t.pipe.waves)
         out["one_then_two_predicted_us"] = fo.fo_predict_partition(t.desc(base), gemm, curve)
@@ -162,8 +173,9 @@ def main(argv=None):
     ap.add_argument("--validate", action="store_true")
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--out", default="")
+    ap.add_argument("--kernels", default="direct", choices=["direct", "separate"])
     a = ap.parse_args(argv)
-    res = run(a.workload, a.validate, a.reps)
+    res = run(a.workload, a.validate, a.reps, a.kernels)
     text = json.dumps(res)
     if a.out:
         with open(a.out, "w") as f:

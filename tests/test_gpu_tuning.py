@@ -13,9 +13,10 @@ from gpu_checks import check_run
 pytestmark = pytest.mark.gpu
 
 
-def test_tuner_small_allreduce():
+@pytest.mark.parametrize("kernels", ["direct", "separate"])
+def test_tuner_small_allreduce(kernels):
     w = W.scaled(W.WORKLOADS["allreduce"], M=1024, N=2048, K=256, wave_width=8)
-    t = Tuner(w, reps=3)
+    t = Tuner(w, reps=3, kernels=kernels)
     try:
         gemm = t.gemm_us()
         curve = t.curve()
