@@ -172,20 +172,26 @@ def test_invalid_routing_routes_nothing(bad):
 
 def test_full_size_dynamic_alltoall():
     """The 8 x 5120-row capacity layer at full size: two device routings,
-    every table and data movement bit-exact, the GEMM on sampled rows."""
+    the first with the separate kernels, the second with the direct
+    consumer+reorder the benchmark's step runs; every table and data
+    movement bit-exact, the GEMM on 2048 sampled rows."""
     w = W.WORKLOADS["alltoall_dynamic"]
     base = W.make_inputs(w)
     pipe = Pipeline(w, base)
     try:
         rng = np.random.default_rng(321)
-        for step in (1, 2):
+        for step, mode in ((1, False), (2, "direct")):
             inp = _inputs_for_step(w, base, step)
             pipe.set_A(inp.A)
+            for f in pipe.buf.final:
+                f.zero_()
             _route(pipe, inp)
-            pipe.step()
+            if mode == "direct":
+                fill_comm_sentinel(pipe)
+            pipe.step(**step_mode(mode))
             res = pipe.results()
-            rows = np.sort(rng.choice(w.M, size=512, replace=False))
-            check_run(pipe, inp, res, gemm_rows=rows, full_gemm=False)
+            rows = np.sort(rng.choice(w.M, size=2048, replace=False))
+            check_run(pipe, inp, res, gemm_rows=rows, full_gemm=False, direct=mode == "direct")
     finally:
         pipe.close()
 
