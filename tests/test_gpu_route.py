@@ -221,3 +221,48 @@ def test_empty_tiles_are_skipped_but_counted(variant):
             check_run(pipe, inp, res)
     finally:
         pipe.close()
+
+
+@pytest.mark.parametrize("wave_width", [7, 8])
+def test_many_steps_cycling_device_routings(wave_width):
+    """As the benchmark runs the dynamic layer: four routings resident in
+    device memory, taken in turn for 60 overlapped steps of the direct
+    consumer+reorder, each step routed on the device first.  The first time
+    a routing comes up its outputs are checked against the oracle; every
+    later step on it must give the same final bytes (device digests), with
+    the communication buffers never written.  (W = 8: padded grids, CTA
+    pairs.)"""
+    w = _small(300, wave_width=wave_width)
+    base = W.make_inputs(w)
+    pipe = Pipeline(w, base)
+    try:
+        dev = pipe.device
+        routes = []
+        for k in range(1, 5):
+            inp = _inputs_for_step(w, base, k)
+            routes.append((inp,
+                           torch.from_numpy(np.asarray(inp.row_token, np.int32)).to(dev),
+                           torch.from_numpy(np.asarray(inp.row_slot, np.int32)).to(dev),
+                           torch.from_numpy(inp.A.view(np.int16)).to(dev)))
+        fill_comm_sentinel(pipe)
+        first = {}
+        for step in range(60):
+            k = step % len(routes)
+            inp, tok, sl, A = routes[k]
+            pipe.buf.A = A
+            for f in pipe.buf.final:
+                f.zero_()
+            pipe.route(tok, sl)
+            pipe.step(fused=True, direct=True)
+            digest = [(int(f.view(torch.int16).to(torch.int64).sum()),
+                       int((f.view(torch.int16).to(torch.int64).reshape(-1) *
+                            (torch.arange(f.numel(), device=dev) % 65521 + 1)).sum()))
+                      for f in pipe.buf.final]
+            if k not in first:
+                check_run(pipe, inp, pipe.results(), direct=True)
+                first[k] = digest
+            else:
+                assert digest == first[k], step
+                assert int(pipe.buf.status.item()) == 0, step
+    finally:
+        pipe.close()
