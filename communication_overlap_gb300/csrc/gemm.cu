@@ -132,12 +132,13 @@ __device__ __noinline__ bool mbar_wait_plain(uint32_t bar, uint32_t parity, uint
   return true;
 }
 
+// TMA tile loads carry an L2 cache policy (`policy`, from createpolicy).
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c0, int32_t c1) {
+                                            int32_t c0, int32_t c1, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 
@@ -233,11 +234,12 @@ __device__ __forceinline__ void cluster_sync() {
 // TMA load into this CTA's shared memory whose completion is counted on the
 // pair leader's mbarrier (`bar` is a cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar, int32_t c0, int32_t c1) {
+                                                 uint32_t bar, int32_t c0, int32_t c1,
+                                                 uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
       : "memory");
 }
 
@@ -448,6 +450,12 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
       uint32_t phase = 0;
       bool ok = true;
       int64_t issued = 0;
+      // A and B tiles are reused by the other tiles of their band and column
+      // and the consumer's streams pass through L2 beside them (read once,
+      // evict-first): keep the operands, evict them last.  Measured: the
+      // overlapped step 1-2% shorter on every workload.
+      uint64_t keep;
+      asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
       Work wk;
       for (int32_t item = 0; ok && next_work(a, item, wk); ++item) {
         const int32_t slot = wk.slot;
@@ -471,18 +479,18 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
               mbar_expect_tx(smem_u32(&full[stage]), C::kStageBytes);
             else
               mbar_expect_tx_cluster_relaxed(fb, C::kStageBytes);
-            tma_load_2d_pair(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
+            tma_load_2d_pair(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0, keep);
 #pragma unroll
             for (int c = 0; c < C::kBCols / 64; ++c)
               tma_load_2d_pair(sb + c * (kBlockK * 128), mb, fb,
-                               ti.col0 + int32_t(rank) * C::kBCols + c * 64, kb * kBlockK);
+                               ti.col0 + int32_t(rank) * C::kBCols + c * 64, kb * kBlockK, keep);
           } else {
             const uint32_t fb = smem_u32(&full[stage]);
             mbar_expect_tx(fb, C::kStageBytes);
-            tma_load_2d(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0);
+            tma_load_2d(sa, &a.tmap_a, fb, kb * kBlockK, ti.row0, keep);
 #pragma unroll
             for (int c = 0; c < C::kBCols / 64; ++c)
-              tma_load_2d(sb + c * (kBlockK * 128), mb, fb, ti.col0 + c * 64, kb * kBlockK);
+              tma_load_2d(sb + c * (kBlockK * 128), mb, fb, ti.col0 + c * 64, kb * kBlockK, keep);
           }
           ++issued;
           if (++stage == C::kStages) {
