@@ -1,5 +1,8 @@
 // Consumer kernels: the communication stand-in, alone (consume_kernel) and
-// with the post-communication reorder fused in (consume_reorder_kernel).
+// with the post-communication reorder fused in (consume_reorder_kernel,
+// which either writes the communication buffers and moves each chunk on to
+// its final place, or -- the direct variant -- stores every unit straight
+// to its final place).
 //
 // Pages: "FlashOverlap: 信号驱动计算通信重叠论文详解" -- 核心设计 "通信侧" (the
 // communication runs as its own kernel on another stream), 五、CUTLASS 扩展实现
@@ -557,8 +560,8 @@ int log2_exact(int v) {
 }
 
 // Default grids, measured on GB300 beside the signaled GEMM (step time over
-// 1, 2, 3 and 4 CTAs per SM): the sums are bandwidth-bound with two loads
-// per source in flight and want 4 CTAs per SM; the copy and bucket
+// 1, 2, 3 and 4 CTAs per SM): the sums are bandwidth-bound with a load per
+// source in flight and want 4 CTAs per SM; the copy and bucket
 // consumers keep 8 loads in flight per thread and interfere least with the
 // GEMM at 1 per SM; the fused consumer+reorder does best at 3 per SM, and
 // so does its direct variant except for the All-to-All bucket, where the
