@@ -58,6 +58,17 @@ def _time(fn, stream, reps, flush):
     return statistics.median(ms) * 1e3   # us
 
 
+def sample_waves(T):
+    """Group sizes at which to sample the curve for a GEMM of T waves: every
+    size up to 8, then about four per doubling, and T itself (the predictor
+    interpolates between them)."""
+    ks, k = [], 1
+    while k < T:
+        ks.append(k)
+        k = k + 1 if k < 8 else k + max(1, k // 4)
+    return ks + [T]
+
+
 class Tuner:
     """kernels: the step's consumer kernels, "direct" (the consumer+reorder
     storing straight to the final layout, the benchmark's default) or
@@ -86,13 +97,14 @@ class Tuner:
             p.gemm(p.s0, p.epoch)
         return _time(lambda: p.gemm(p.s0, p.epoch), p.s0, self.reps, self.flush)
 
-    def curve(self):
-        """[(bytes, us)] for first groups of 1 .. T waves (in-kernel time)."""
+    def curve(self, waves=None):
+        """[(bytes, us)] for first groups of k waves (in-kernel time), k in
+        `waves` (default every k = 1 .. T)."""
         p = self.pipe
         T = p.waves
         ctas = 4 * torch.cuda.get_device_properties(p.device).multi_processor_count
         pts = []
-        for k in range(1, T + 1):
+        for k in (waves or range(1, T + 1)):
             p.replan([k, T - k] if k < T else [T])
             p.step(overlap=False)
             torch.cuda.synchronize()
