@@ -61,3 +61,17 @@ def test_bad_curves_rejected():
     for curve in ([(1, 2.0)], [(1, 2.0), (1, 3.0)], [(1, float("nan")), (2, 1.0)]):
         with pytest.raises(fo.FoError):
             fo.fo_tune_partition(d, 10.0, curve)
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 8, 9, 98, 122])
+def test_curve_sample_points(T):
+    """The group sizes at which the benchmark samples the latency curve:
+    strictly increasing, every size up to 8, T itself, and gaps that grow
+    no faster than a quarter of the size (so interpolation stays local)."""
+    pytest.importorskip("torch")
+    from communication_overlap_gb300.tuning import sample_waves
+    ks = sample_waves(T)
+    assert ks[-1] == T and ks[0] == 1
+    assert all(b > a for a, b in zip(ks, ks[1:]))
+    assert [k for k in ks if k <= 8] == list(range(1, min(T, 8) + 1))
+    assert all(b - a <= max(1, a // 4) for a, b in zip(ks, ks[1:-1]))
