@@ -474,6 +474,8 @@ def run_ours(args):
     # GEMM, which for copies is smaller and slower alone
     fo.fo_plan_set_launch(pipe.plan, 4 * sm_count, args.reorder_ctas, False)
     t_cons_full = timed(torch, s, cons_only, args.steps, flush)
+    t_direct_full = timed(torch, s, lambda: pipe.consume_reorder(s, pipe.epoch, direct=True),
+                          args.steps, flush)
     fo.fo_plan_set_launch(pipe.plan, args.consumer_ctas, args.reorder_ctas, False)
     pipe.set_overlap(True)
 
@@ -734,6 +736,8 @@ def run_ours(args):
                 "reorder_gbs": reo_bytes / (statistics.mean(t_reo) * 1e-3) / 1e9,
                 "ms_direct_alone": statistics.mean(t_direct_alone),
                 "direct_gbs": cons_bytes / (statistics.mean(t_direct_alone) * 1e-3) / 1e9,
+                "ms_direct_alone_full_grid": statistics.mean(t_direct_full),
+                "direct_gbs_full_grid": cons_bytes / (statistics.mean(t_direct_full) * 1e-3) / 1e9,
                 "hbm_peak_gbs": hbm,
                 "gemm_in_kernel_ms_alone": statistics.median(span_alone),
                 "gemm_in_kernel_ms_in_step": statistics.median(span_step),
