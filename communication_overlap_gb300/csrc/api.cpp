@@ -125,7 +125,7 @@ fo_status fo_plan_set_split(fo_plan* p, int32_t enable, int32_t* split_tiles) {
 }
 
 fo_status fo_plan_set_trace(fo_plan* p, uint64_t* stamps, uint64_t* consumer_stamps) {
-  if (!p) return FO_ERR_ARG;
+  if (!p || !fo::aligned8(stamps) || !fo::aligned8(consumer_stamps)) return FO_ERR_ARG;
   p->trace = stamps;
   p->consumer_trace = consumer_stamps;
   return FO_OK;
@@ -161,6 +161,7 @@ fo_status fo_signaled_gemm(const fo_plan* p, const void* A, const void* const* B
                            uint32_t epoch, void* stream) {
   if (!p || !p->blob || !A || !B || !C_r) return FO_ERR_ARG;
   if ((count == nullptr) != (flags == nullptr)) return FO_ERR_ARG;
+  if (!fo::aligned4(count) || !fo::aligned4(flags)) return FO_ERR_ARG;
   return fo::launch_signaled_gemm(p, A, B, C_r, count, flags, epoch, stream);
 }
 
@@ -171,6 +172,7 @@ fo_status fo_consume_group(const fo_plan* p, int32_t group, fo_consumer kind,
                            uint64_t spin_limit_ns, int32_t* dev_status,
                            void* stream) {
   if (!p || !p->blob || !src || !dst || !flags || !dev_status) return FO_ERR_ARG;
+  if (!fo::aligned4(flags) || !fo::aligned4(dev_status)) return FO_ERR_ARG;
   if (group < -1 || group >= p->P) return FO_ERR_ARG;
   const int32_t g0 = group < 0 ? 0 : group, g1 = group < 0 ? p->P : group + 1;
   switch (kind) {
@@ -191,11 +193,13 @@ fo_status fo_consume_group(const fo_plan* p, int32_t group, fo_consumer kind,
     default: return FO_ERR_ARG;
   }
   if (n_partials > 0 && !partials) return FO_ERR_ARG;
+  // the kernels move 16-byte vectors: every buffer starts on a 16-byte boundary
+  if (!fo::aligned16(src)) return FO_ERR_ARG;
   for (int i = 0; i < n_partials; ++i)
-    if (!partials[i]) return FO_ERR_ARG;
+    if (!partials[i] || !fo::aligned16(partials[i])) return FO_ERR_ARG;
   const int n_dst = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
   for (int k = 0; k < n_dst; ++k)
-    if (!dst[k]) return FO_ERR_ARG;
+    if (!dst[k] || !fo::aligned16(dst[k])) return FO_ERR_ARG;
   return fo::launch_consume(p, g0, g1, int(kind), src, partials, n_partials, dst,
                             flags, epoch, spin_limit_ns, dev_status, stream);
 }
@@ -206,6 +210,7 @@ fo_status fo_consume_reorder(const fo_plan* p, int32_t group, fo_consumer kind,
                              fo_activation act, const uint32_t* flags, uint32_t epoch,
                              uint64_t spin_limit_ns, int32_t* dev_status, void* stream) {
   if (!p || !p->blob || !src || !final_dst || !flags || !dev_status) return FO_ERR_ARG;
+  if (!fo::aligned4(flags) || !fo::aligned4(dev_status)) return FO_ERR_ARG;
   if (group < -1 || group >= p->P) return FO_ERR_ARG;
   if (act < FO_ACT_NONE || act > FO_ACT_SILU) return FO_ERR_ARG;
   if (bias && (reinterpret_cast<uintptr_t>(bias) & 15)) return FO_ERR_ARG;
@@ -228,11 +233,15 @@ fo_status fo_consume_reorder(const fo_plan* p, int32_t group, fo_consumer kind,
     default: return FO_ERR_ARG;
   }
   if (n_partials > 0 && !partials) return FO_ERR_ARG;
+  if (!fo::aligned16(src)) return FO_ERR_ARG;
   for (int i = 0; i < n_partials; ++i)
-    if (!partials[i]) return FO_ERR_ARG;
+    if (!partials[i] || !fo::aligned16(partials[i])) return FO_ERR_ARG;
   const int n = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
-  for (int k = 0; k < n; ++k)
-    if ((comm_dst && !comm_dst[k]) || !final_dst[k]) return FO_ERR_ARG;
+  for (int k = 0; k < n; ++k) {
+    if ((comm_dst && (!comm_dst[k] || !fo::aligned16(comm_dst[k]))) || !final_dst[k] ||
+        !fo::aligned16(final_dst[k]))
+      return FO_ERR_ARG;
+  }
   const int32_t g0 = group < 0 ? 0 : group, g1 = group < 0 ? p->P : group + 1;
   return fo::launch_consume_reorder(p, g0, g1, int(kind), src, partials, n_partials, comm_dst,
                                     final_dst, bias, int(act), flags, epoch, spin_limit_ns,

@@ -754,6 +754,7 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
                                               void* stream) {
   using namespace fo;
   if (!p || !p->blob || !src || !dst || !flags || !dev_status) return FO_ERR_ARG;
+  if (!aligned4(flags) || !aligned4(dev_status)) return FO_ERR_ARG;
   if (p->P > FO_NOALLOC_MAX_GROUPS) return FO_ERR_ARG;  // scratch too small for this plan
   if (group < -1 || group >= p->P) return FO_ERR_ARG;
   switch (kind) {
@@ -774,11 +775,12 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
     default: return FO_ERR_ARG;
   }
   if (n_partials > 0 && !partials) return FO_ERR_ARG;
+  if (!aligned16(src)) return FO_ERR_ARG;
   for (int i = 0; i < n_partials; ++i)
-    if (!partials[i]) return FO_ERR_ARG;
+    if (!partials[i] || !aligned16(partials[i])) return FO_ERR_ARG;
   const int n_dst = (kind == FO_CONS_RS || kind == FO_CONS_A2A) ? p->R : 1;
   for (int k = 0; k < n_dst; ++k)
-    if (!dst[k]) return FO_ERR_ARG;
+    if (!dst[k] || !aligned16(dst[k])) return FO_ERR_ARG;
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return FO_ERR_CUDA;
   if (device != p->device) return FO_ERR_ARG;  // the plan's device must be current

@@ -34,7 +34,11 @@
  *    A failed CUDA call returns FO_ERR_CUDA.  Device-side waits are bounded:
  *    a wait that runs out writes FO_ERR_TIMEOUT into the caller's status word
  *    (read it after synchronising); no kernel traps or asserts.
- *  - Device pointers must be 16-byte aligned.
+ *  - Device data buffers (A, B, C_reordered, partials, communication and
+ *    final buffers, bias) must be 16-byte aligned; counting tables, flags,
+ *    status words and routing arrays 4-byte aligned; trace stamps 8-byte
+ *    aligned.  A misaligned pointer is an argument error (FO_ERR_ARG),
+ *    checked before anything is launched.
  */
 #ifndef FO_H
 #define FO_H

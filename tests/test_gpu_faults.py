@@ -101,3 +101,49 @@ def test_overlapped_reorder_waits_for_its_groups():
         assert fo.fo_plan_device_status(pipe.plan) == 0
     finally:
         pipe.close()
+
+
+def test_misaligned_buffers_are_argument_errors():
+    """Buffers that are not 16-byte aligned (data) or 4-byte aligned
+    (counters, flags, status) are refused on the host with FO_ERR_ARG,
+    before any launch; the plan stays usable."""
+    w = W.scaled(W.WORKLOADS["allreduce"], M=256, N=512, K=128, wave_width=2)
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp)
+    try:
+        b = pipe.buf
+        s = pipe.s0.cuda_stream
+        parts = [p.data_ptr() for p in b.partials]
+        bad = [
+            lambda: fo.fo_consume_group(pipe.plan, -1, fo.FO_CONS_SUM, b.C_r.data_ptr() + 2,
+                                        parts, [b.comm[0].data_ptr()], b.flags.data_ptr(), 1,
+                                        0, b.status.data_ptr(), s),
+            lambda: fo.fo_consume_group(pipe.plan, -1, fo.FO_CONS_SUM, b.C_r.data_ptr(),
+                                        parts[:-1] + [parts[-1] + 8], [b.comm[0].data_ptr()],
+                                        b.flags.data_ptr(), 1, 0, b.status.data_ptr(), s),
+            lambda: fo.fo_consume_group(pipe.plan, -1, fo.FO_CONS_SUM, b.C_r.data_ptr(), parts,
+                                        [b.comm[0].data_ptr() + 4], b.flags.data_ptr(), 1, 0,
+                                        b.status.data_ptr(), s),
+            lambda: fo.fo_consume_group(pipe.plan, -1, fo.FO_CONS_SUM, b.C_r.data_ptr(), parts,
+                                        [b.comm[0].data_ptr()], b.flags.data_ptr() + 2, 1, 0,
+                                        b.status.data_ptr(), s),
+            lambda: fo.fo_consume_reorder(pipe.plan, -1, fo.FO_CONS_SUM, b.C_r.data_ptr(), parts,
+                                          None, [b.final[0].data_ptr() + 2], 0, fo.FO_ACT_NONE,
+                                          b.flags.data_ptr(), 1, 0, b.status.data_ptr(), s),
+            lambda: fo.fo_consume_group_noalloc(pipe.plan, -1, fo.FO_CONS_SUM,
+                                                b.C_r.data_ptr() + 8, parts,
+                                                [b.comm[0].data_ptr()], b.flags.data_ptr(), 1, 0,
+                                                b.status.data_ptr(), s),
+            lambda: fo.fo_signaled_gemm(pipe.plan, b.A.data_ptr(), [x.data_ptr() for x in b.B],
+                                        b.C_r.data_ptr(), b.count.data_ptr() + 1,
+                                        b.flags.data_ptr(), 1, s),
+        ]
+        for call in bad:
+            with pytest.raises(fo.FoError) as e:
+                call()
+            assert e.value.status == fo.FO_ERR_ARG
+        torch.cuda.synchronize()
+        pipe.step(fused=True, direct=True)          # still usable
+        assert pipe.results()["status"] == 0
+    finally:
+        pipe.close()
