@@ -70,6 +70,10 @@ struct Cfg {
   // received into the pipeline stages (idle by then)
   static constexpr int kQuarterBytes = 32 * BN * 4;
   static_assert(4 * kQuarterBytes <= kStages * kStageBytes, "partial sums fit the stages");
+  // when a quarter fills exactly one stage (pairs, BN = 256), the producer
+  // receives quarter q into stage q as soon as that stage's last k-block has
+  // been consumed, overlapping the copies with the owner's last MMAs
+  static constexpr bool kEarlyPartial = kStageBytes == kQuarterBytes && kStages >= 4;
 };
 
 struct GemmArgs {
@@ -457,6 +461,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
       uint64_t keep;
       asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
       Work wk;
+      int32_t owner_slot = -1;   // the split tile this CTA owns (its last item)
       for (int32_t item = 0; ok && next_work(a, item, wk); ++item) {
         const int32_t slot = wk.slot;
         const TileInfo ti = a.tile[slot];
@@ -464,6 +469,7 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
         if (item == 0)
           for (int e = 0; e <= ti.expert; ++e) prefetch_tmap(&a.tmap_b[e]);
         if (tile_skipped<PAIR>(a, slot)) continue;
+        if (wk.role == 1) owner_slot = slot;
         for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           if (!mbar_wait_fast(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -497,6 +503,39 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
             stage = 0;
             phase ^= 1;
           }
+        }
+      }
+      if constexpr (C::kEarlyPartial) {
+        if (ok && owner_slot >= 0) {
+          // Continue around the ring: each stage is free once the MMA has
+          // consumed its last k-block.  Stage q < 4 then receives quarter q
+          // of the helper's partial sums (after the helper has published
+          // it), while the owner's last MMAs still run; the epilogue waits
+          // on part_bar[q].
+          const int32_t i = owner_slot - a.split_slot0;
+          uint32_t sent = 0;   // quarters whose copy was issued (bit q)
+          for (int v = 0; v < C::kStages; ++v) {
+            if (!mbar_wait_fast(smem_u32(&empty[stage]), phase ^ 1, abort_flag, a.status)) break;
+            if (stage < 4) {
+              const int q = stage;
+              if (!wait_partial(a.split_flag + i * 4 + q, a.seq, abort_flag, a.status)) break;
+              // the helper's generic stores are read next by the TMA engine
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              const uint32_t pb = smem_u32(&part_bar[q]);
+              mbar_expect_tx(pb, uint32_t(C::kQuarterBytes));
+              bulk_load(smem_u32(smem + q * C::kQuarterBytes),
+                        a.split_ws + size_t(i * 4 + q) * (BN / 64) * 16 * 32,
+                        uint32_t(C::kQuarterBytes), pb);
+              sent |= 1u << q;
+            }
+            if (++stage == C::kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          // the copies land before the CTA can exit, whatever happened
+          for (int q = 0; q < 4; ++q)
+            if ((sent >> q) & 1u) mbar_wait_plain(smem_u32(&part_bar[q]), 0, 10000000ull);
         }
       }
       if (!ok && !PAIR) {
@@ -613,18 +652,20 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
         if (a.trace != nullptr && lane == 0 && q == 0)   // the owner's half is computed
           a.trace[a.tiles + gridDim.x + 2 * (slot - a.split_slot0) + 1] = globaltimer_ns();
         const uint32_t pb = smem_u32(&part_bar[q]);
-        if (lane == 0) {
-          ok = wait_partial(part_flag, a.seq, abort_flag, a.status);
-          if (ok) {
-            // the helper's generic stores are read next by the TMA engine
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            mbar_expect_tx(pb, uint32_t(C::kQuarterBytes));
-            bulk_load(smem_u32(part_smem), part, uint32_t(C::kQuarterBytes), pb);
-            ok = mbar_wait(pb, 0, abort_flag, a.status);
+        if constexpr (!C::kEarlyPartial) {   // (else the producer sends it)
+          if (lane == 0) {
+            ok = wait_partial(part_flag, a.seq, abort_flag, a.status);
+            if (ok) {
+              // the helper's generic stores are read next by the TMA engine
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              mbar_expect_tx(pb, uint32_t(C::kQuarterBytes));
+              bulk_load(smem_u32(part_smem), part, uint32_t(C::kQuarterBytes), pb);
+              ok = mbar_wait(pb, 0, abort_flag, a.status);
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
         // every lane observes the completed copy before reading it
         if (!mbar_wait(pb, 0, abort_flag, a.status)) break;
       }
