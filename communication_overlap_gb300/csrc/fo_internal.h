@@ -60,6 +60,7 @@ struct DeviceTables {
                                        //   CTAs done
   int32_t* gemm_status = nullptr;      // [1] sticky status of the GEMM's waits
   uint32_t* count_ready = nullptr;     // [1] launch seq once the GEMM zeroed the count table
+  int32_t* gemm_exit = nullptr;        // [1] CTAs of the GEMM that finished (reset by the last)
   void* split_ws = nullptr;            // [split_n * 128 * tile_n] fp32 partial sums of
                                        //   the last wave's split tiles
   uint32_t* split_flag = nullptr;      // [split_n * 4] per tile quarter: launch seq

@@ -88,6 +88,7 @@ struct GemmArgs {
   uint16_t* c_r;
   int32_t* count;
   uint32_t* count_ready;  // = seq once CTA 0 has zeroed count[0 .. P)
+  int32_t* exit_count;    // CTAs finished; the last withdraws count_ready
   int32_t n_groups;
   uint32_t* flags;
   int32_t* status;
@@ -407,8 +408,15 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
     mbar_init(smem_u32(drain), 1);
     for (int b = 0; b < 4; ++b) mbar_init(smem_u32(&part_bar[b]), 1);
     if (blockIdx.x == 0 && a.count != nullptr) {
-      // [P1] 一 "组级 Tile 计数": the counting table starts at [0, ..., 0]
-      for (int j = 0; j < a.n_groups; ++j) a.count[j] = 0;
+      // [P1] 一 "组级 Tile 计数": the counting table starts at [0, ..., 0].
+      // The flags are cleared too, before any consumer of this launch can
+      // start (it starts once every CTA has passed launch_dependents below),
+      // so a step replayed with the same epoch -- a captured CUDA graph --
+      // never sees the previous replay's flags.
+      for (int j = 0; j < a.n_groups; ++j) {
+        a.count[j] = 0;
+        a.flags[j] = 0;
+      }
       __threadfence();
       st_release_gpu(a.count_ready, a.seq);
     }
@@ -519,6 +527,8 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
             if (stage < 4) {
               const int q = stage;
               if (!wait_partial(a.split_flag + i * 4 + q, a.seq, abort_flag, a.status)) break;
+              // taken: clear it for the next launch (a replay reuses a.seq)
+              *reinterpret_cast<volatile uint32_t*>(a.split_flag + i * 4 + q) = 0u;
               // the helper's generic stores are read next by the TMA engine
               asm volatile("fence.proxy.async.global;" ::: "memory");
               const uint32_t pb = smem_u32(&part_bar[q]);
@@ -656,6 +666,8 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
           if (lane == 0) {
             ok = wait_partial(part_flag, a.seq, abort_flag, a.status);
             if (ok) {
+              // taken: clear it for the next launch (a replay reuses a.seq)
+              *reinterpret_cast<volatile uint32_t*>(part_flag) = 0u;
               // the helper's generic stores are read next by the TMA engine
               asm volatile("fence.proxy.async.global;" ::: "memory");
               mbar_expect_tx(pb, uint32_t(C::kQuarterBytes));
@@ -796,6 +808,16 @@ __global__ void __maxnreg__(112) signaled_gemm_kernel(const __grid_constant__ Ge
 
   // ------------------------------------------------------------ teardown
   __syncthreads();
+  // Every tile of this CTA is counted.  The last CTA to get here withdraws
+  // the table-ready word, so the next launch's CTAs wait for its own reset
+  // even when it carries the same sequence number (a replayed graph).
+  if (threadIdx.x == 0 && a.count != nullptr) {
+    __threadfence();
+    if (atomicAdd(a.exit_count, 1) == int32_t(gridDim.x) - 1) {
+      atomicExch(a.count_ready, 0u);
+      atomicExch(a.exit_count, 0);
+    }
+  }
   if (warp == 1) {
     // every MMA has completed before the tensor memory is released
     // (immediate on the normal path: the epilogue saw them all)
@@ -925,6 +947,7 @@ fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* cons
   a.c_r = static_cast<uint16_t*>(C_r);
   a.count = count;
   a.count_ready = p->dev.count_ready;
+  a.exit_count = p->dev.gemm_exit;
   a.n_groups = p->P;
   a.flags = flags;
   a.status = p->dev.gemm_status;

@@ -457,7 +457,7 @@ fo_status upload_plan(fo_plan* p) {
   const size_t o_cons = put(buf, std::vector<int32_t>(p->P, 0));
   const size_t o_rtile = put(buf, std::vector<int32_t>(2, 0));
   const size_t o_gst = put(buf, std::vector<int32_t>(1, 0));
-  const size_t o_crd = put(buf, std::vector<int32_t>(1, 0));
+  const size_t o_crd = put(buf, std::vector<int32_t>(2, 0));   // count_ready, gemm_exit
   const bool a2a = p->layout == FO_LAYOUT_A2A_SUBTOKEN;
   if (a2a) {
     p->route_blocks = 0;
@@ -495,6 +495,7 @@ fo_status upload_plan(fo_plan* p) {
   p->dev.rtile = reinterpret_cast<int32_t*>(b + o_rtile);
   p->dev.gemm_status = reinterpret_cast<int32_t*>(b + o_gst);
   p->dev.count_ready = reinterpret_cast<uint32_t*>(b + o_crd);
+  p->dev.gemm_exit = reinterpret_cast<int32_t*>(b + o_crd) + 1;
   p->dev.route_cnt = reinterpret_cast<int32_t*>(b + o_rc);
   p->dev.split_ws = b + o_sws;
   p->dev.split_flag = reinterpret_cast<uint32_t*>(b + o_sfl);

@@ -48,8 +48,9 @@ struct ReorderArgs {
   int32_t act;            // fo_activation
   int32_t unit_bytes, row_bytes, slot0, n_slots;
   int32_t* counters;         // [0] next tile, [1] CTAs done (reset by the last CTA)
-  const uint32_t* consumed;  // non-NULL: wait until consumed[group] == seq
+  uint32_t* consumed;        // non-NULL: wait until consumed[group] == seq
   uint32_t seq;              // the preceding consume launch's number
+  int32_t g0, g1;            // the groups this launch covers
 };
 
 // Wait (thread 0) until the consumer has finished the tile's group: acquire
@@ -222,6 +223,10 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.counters + 1, 1) == int32_t(gridDim.x) - 1) {
+      // every tile is done: clear the groups' consumed flags too, so a
+      // launch that carries the same sequence number (a replayed graph)
+      // waits for its own consumer
+      for (int32_t j = a.g0; j < a.g1; ++j) atomicExch(a.consumed + j, 0u);
       atomicExch(a.counters, 0);
       atomicExch(a.counters + 1, 0);
     }
@@ -266,6 +271,8 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   a.slot0 = p->group_slot_begin[g0];
   a.n_slots = p->group_slot_begin[g1] - a.slot0;
   a.counters = p->dev.rtile;
+  a.g0 = g0;
+  a.g1 = g1;
   int ctas = p->reorder_ctas > 0 ? p->reorder_ctas : 3 * p->sm_count;
   if (ctas > a.n_slots) ctas = a.n_slots;
   // With overlap on, the reorder is a programmatic dependent of the
@@ -276,6 +283,9 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   if (ov) {
     a.consumed = p->dev.consumed;
     a.seq = p->consume_seq;
+    // this launch clears the consumed flags once it has used them: a later
+    // reorder without a consume in between runs as an ordinary launch
+    p->consume_published = false;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(ctas);

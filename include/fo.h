@@ -269,10 +269,15 @@ fo_status fo_counting_table_init(const fo_plan* plan, int32_t* count_table,
  *      itself (CTA 0, before any tile is counted), so the caller need not
  *      (fo_counting_table_init does the same as a separate memset); it ends
  *      equal to |G_j|.
- *  flags: device uint32[P].  count_table and flags may both be NULL: the
- *      GEMM then signals nothing.
- *  epoch: the value this iteration's flags take; use a new one per
- *      iteration so flags never need resetting.
+ *  flags: device uint32[P].  CTA 0 clears them with the counting table,
+ *      before any consumer launched after this call can start.  count_table
+ *      and flags may both be NULL: the GEMM then signals nothing.
+ *  epoch: the value this iteration's flags take.  A new one per iteration
+ *      is the simplest; a step captured in a CUDA graph may replay with the
+ *      same one (the flags are cleared at every launch, and the kernels'
+ *      per-launch handshakes -- the counting table's reset, the split
+ *      tiles' partial sums, the reorder's consumed flags -- are withdrawn
+ *      by each launch when it has used them).
  * Requires K % 64 == 0 and a device with compute capability 10.3. */
 fo_status fo_signaled_gemm(const fo_plan* plan, const void* A,
                            const void* const* B, void* C_reordered,
