@@ -400,6 +400,28 @@ def run_ours(args):
     status_ok = int(pipe.buf.status.item()) == 0
 
     # serial baseline: consumer after the GEMM
+    # the same step captured once in a CUDA graph and replayed (same epoch
+    # and kernel parameters every time; the kernels clear their own signals)
+    t_graph = []
+    if not dyn:
+        g_epoch = pipe.epoch + 1
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            pipe.gemm(s, g_epoch)
+            if fused:
+                pipe.consume_reorder(s, g_epoch, direct=direct)
+            else:
+                pipe.consume(s, g_epoch)
+                pipe.reorder(s)
+        pipe.epoch = g_epoch
+        def replay():
+            with torch.cuda.stream(s):   # replay on the step's stream
+                graph.replay()
+        t_graph = timed(torch, s, replay, args.steps, flush)
+        assert int(pipe.buf.status.item()) == 0
+        assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
+        del graph
+
     # every overlapped variant: separate kernels, fused, fused direct (no
     # communication buffers, each unit stored straight to its final place)
     t_var = {}
@@ -716,6 +738,7 @@ def run_ours(args):
                 "ms_gemm_alone_median": statistics.median(t_gemm),
                 "overlapped_step_kernels": kernels,
                 "ms_overlapped_step_by_kernels": {k: statistics.mean(v) for k, v in t_var.items()},
+                "ms_overlapped_step_graph_replay": statistics.mean(t_graph) if t_graph else None,
                 "ms_serial_step": ms_ser,
                 "overlap_speedup": ms_ser / ms_ov,
                 "ms_gemm_alone": ms_gemm,
