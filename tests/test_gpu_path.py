@@ -121,7 +121,8 @@ def test_gemm_exact_unit_entries_and_identity():
 
 def test_signals_off_and_repeat_epochs():
     """With count/flags NULL the GEMM writes the same C_r and signals
-    nothing; repeated epochs keep flags monotone without resets."""
+    nothing (it leaves the flags alone); with signals, every step's flags
+    hold its own epoch."""
     w = _small("wave_pattern", M=512, N=1024, K=256, wave_width=6)
     inp = W.make_inputs(w)
     pipe = Pipeline(w, inp)
