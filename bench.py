@@ -15,7 +15,8 @@ only the rows that hold a token count (2 x routed rows x N x K).  L2 is flushed 
 before every timed step, outside the timed events.
 
 Extra keys: the GEMM alone (signals on and off), the consumer+reorder alone
-(flags already raised), the serial step (consumer after the GEMM), the
+(flags already raised), the serial step (the same kernels, the consumer as an
+ordinary launch after the GEMM; also with the separate kernels), the
 overlap ratio serial/overlapped, the GEMM's in-kernel duration inside the
 overlapped step (per-tile globaltimer stamps) and its slowdown against the
 GEMM alone, ``roofline`` of the dominant kernel (the GEMM), ``e2e`` through
@@ -429,8 +430,13 @@ def run_ours(args):
                      ("direct", dict(fused=True, direct=True))):
         t_var[name] = timed(torch, s, lambda: step(overlap=True, sync_current=False, **kw),
                             args.steps, flush)
-    t_ser = timed(torch, s, lambda: step(overlap=False, sync_current=False),
+    # serial = the same kernels as the overlapped step, the consumer as an
+    # ordinary launch after the GEMM; and the separate kernels serially
+    t_ser = timed(torch, s,
+                  lambda: step(overlap=False, sync_current=False, fused=fused, direct=direct),
                   args.steps, flush)
+    t_ser_sep = timed(torch, s, lambda: step(overlap=False, sync_current=False),
+                      args.steps, flush)
     t_route = []
     if dyn:   # the two routing kernels alone
         t_route = timed(torch, s, lambda: pipe.route(*routes[0][:2]), args.steps, flush)
@@ -740,6 +746,8 @@ def run_ours(args):
                 "ms_overlapped_step_by_kernels": {k: statistics.mean(v) for k, v in t_var.items()},
                 "ms_overlapped_step_graph_replay": statistics.mean(t_graph) if t_graph else None,
                 "ms_serial_step": ms_ser,
+                "serial_step_kernels": kernels,
+                "ms_serial_step_separate_kernels": statistics.mean(t_ser_sep),
                 "overlap_speedup": ms_ser / ms_ov,
                 "ms_gemm_alone": ms_gemm,
                 "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
