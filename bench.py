@@ -400,7 +400,6 @@ def run_ours(args):
     ms_ov = statistics.mean(t_ov)
     status_ok = int(pipe.buf.status.item()) == 0
 
-    # serial baseline: consumer after the GEMM
     # the same step captured once in a CUDA graph and replayed (same epoch
     # and kernel parameters every time; the kernels clear their own signals)
     t_graph = []
