@@ -255,18 +255,46 @@ __global__ void __launch_bounds__(kPartsThreads) route_parts_kernel(const __grid
   //    the fused consumer+reorder) and its final place (read by its direct
   //    variant); row r of the tile at slot s is unit dest_base[s][d] + rank,
   //    computed here from the same closed form
-  for (int64_t i = first; i < int64_t(a.tiles) * kTileM; i += stride) {
-    const int32_t s = int32_t(i / kTileM), r = int32_t(i % kTileM);
-    const TileInfo& ti = a.tile[s];
-    if (r >= ti.rows) continue;
-    const int32_t rho = ti.row0 + r;
-    const int d = a.row_dest[rho];
-    if (d < 0) continue;
-    const int32_t u = off[ti.group * R + d] +
-                      units_before(a, BP, ti.row0, ti.col0, ti.expert, d) + a.row_rank[rho];
-    a.unit_src[u] = (s << 7) | r;
-    if (a.unit_place != nullptr)
-      a.unit_place[u] = (d << kPlaceShift) | (a.final_row[rho] * (a.N / 8) + ti.col0 / 8);
+  //    Four entries per thread and pass, their table loads issued together:
+  //    each entry is a chain of two dependent global loads (the tile, then
+  //    the row's rank, destination and output row).
+  constexpr int kE = 4;
+  const int64_t n_entries = int64_t(a.tiles) * kTileM;
+  for (int64_t i0 = first; i0 < n_entries; i0 += int64_t(stride) * kE) {
+    TileInfo ti[kE];
+    int32_t rho[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      const int64_t i = i0 + int64_t(stride) * e;
+      rho[e] = -1;
+      if (i < n_entries) {
+        ti[e] = a.tile[i / kTileM];
+        const int32_t r = int32_t(i % kTileM);
+        if (r < ti[e].rows) rho[e] = ti[e].row0 + r;
+      }
+    }
+    int d[kE];
+    int32_t rank[kE], frow[kE];
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      d[e] = -1;
+      if (rho[e] >= 0) {
+        d[e] = a.row_dest[rho[e]];
+        rank[e] = a.row_rank[rho[e]];
+        frow[e] = a.unit_place != nullptr ? a.final_row[rho[e]] : 0;
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kE; ++e) {
+      if (d[e] < 0) continue;
+      const int64_t i = i0 + int64_t(stride) * e;
+      const int32_t s = int32_t(i / kTileM), r = int32_t(i % kTileM);
+      const int32_t u = off[ti[e].group * R + d[e]] +
+                        units_before(a, BP, ti[e].row0, ti[e].col0, ti[e].expert, d[e]) + rank[e];
+      a.unit_src[u] = (s << 7) | r;
+      if (a.unit_place != nullptr)
+        a.unit_place[u] = (d[e] << kPlaceShift) | (frow[e] * (a.N / 8) + ti[e].col0 / 8);
+    }
   }
 }
 
