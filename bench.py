@@ -1,32 +1,39 @@
 """Benchmark of the signaled-GEMM + reorder path (one JSON line on rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--per-workload LIST|none]
 
-A step is one pass of the whole path on the workload (default: the
-wave-pattern GEMM M=2048, N=8192, K=8192, 128x256 tiles, 148-CTA waves,
-groups of 1 then 2 waves, copy consumer + reorder back), inputs resident in
-HBM: signaled GEMM (it resets its own counting table), then the consumer
-and the post-communication reorder, by default as one kernel that stores
-every unit straight to its final place (a programmatic dependent launch
-running alongside the GEMM; ``--step-kernels`` picks the others).  ``value`` is the GEMM's FLOPs per step divided by the step time
-(TFLOPS of the whole overlapped step); for the dynamic-routing workload
-only the rows that hold a token count (2 x routed rows x N x K).  L2 is flushed (a 256 MiB write)
-before every timed step, outside the timed events.
+A step is one pass of the whole path on a workload, inputs resident in HBM:
+the signaled GEMM (it resets its own counting table), then the consumer and
+the post-communication reorder, by default as one kernel that stores every
+unit straight to its final place (a programmatic dependent launch running
+alongside the GEMM; ``--step-kernels`` picks the others).  ``value`` is the
+GEMM's FLOPs per step divided by the step time (TFLOPS of the whole
+overlapped step); for the All-to-All layers only the rows that hold a token
+count (2 x routed rows x N x K).  L2 is flushed (a 256 MiB write) before
+every timed step, outside the timed events.
 
-Extra keys: the GEMM alone (signals on and off), the consumer+reorder alone
-(flags already raised), the serial step (the same kernels, the consumer as an
-ordinary launch after the GEMM; also with the separate kernels), the
-overlap ratio serial/overlapped, the GEMM's in-kernel duration inside the
-overlapped step (per-tile globaltimer stamps) and its slowdown against the
-GEMM alone, ``roofline`` of the dominant kernel (the GEMM), ``e2e`` through
-the C ABI with host buffers (every step's inputs copied in from pinned host
-memory and its output copied back, pipelined over two buffer sets), and ``cpu_baseline`` (the CPU oracle on a
-bounded sample).
+The headline workload (default: alltoall, the largest one, 16384 tokens x
+top-2 over 8 experts, N=14336, K=4096) gets every measurement: the GEMM
+alone (signals on and off), the consumer and the reorder alone, the serial
+step (the same kernels, the consumer as an ordinary launch after the GEMM),
+the overlap ratio, the GEMM's in-kernel duration inside the step and its
+slowdown, the consumer's in-kernel bandwidth inside the step, ``roofline``
+of the dominant kernel (the GEMM) against the measured and the nominal
+peak, ``e2e`` through the C ABI with host buffers (every step's inputs
+copied in from pinned host memory and its output copied back, pipelined
+over two buffer sets), and ``cpu_baseline`` (the CPU oracle on a bounded
+sample).  Every other workload (``--per-workload``) is timed in the same
+process, one after another, with the same step and a compact set of the
+same measurements, under ``per_workload``.
 
-For N > 1 (torchrun) every rank runs its own replica of the workload (the
-path has no data exchange on one node: "replicas only"); value sums the
-ranks' FLOPs over the slowest rank's time.
+For N > 1 (torchrun) every rank runs its own replica of the headline
+workload (the path has no data exchange on one node: "replicas only");
+value sums the ranks' FLOPs over the slowest rank's time.
+
+``--ncu-gemm`` runs only a few GEMM launches of the workload (the grouped
+one optionally cut to ``--experts`` experts): the small case for ncu
+captures of the GEMM.
 """
 import argparse
 import hashlib
@@ -41,14 +48,26 @@ sys.path.insert(0, ROOT)
 
 import numpy as np
 
+METRIC = "signaled GEMM TFLOPS (% of bf16 peak); overlap time vs serial GEMM+consumer"
+HEADLINE = "alltoall"
+PER_WORKLOAD = "wave_pattern,allreduce,reducescatter,alltoall_dynamic"
+# Nominal GB300 figures, for fractions beside the measured ones: dense bf16
+# tensor throughput (NVIDIA's figures with 2:4 sparsity are twice this) and
+# the HBM3e bandwidth.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 8000.0
+
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="wave_pattern")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--per-workload", default=PER_WORKLOAD,
+                    help="comma-separated workloads timed after the headline in the same "
+                         "process ('none': skip)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -64,6 +83,10 @@ def parse():
                          "auto: direct")
     ap.add_argument("--reorder-ctas", type=int, default=0,
                     help="reorder grid (0: library default, 3 per SM)")
+    ap.add_argument("--ncu-gemm", action="store_true",
+                    help="only GEMM launches (warm-up + --steps), for ncu captures")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="with --ncu-gemm: the grouped workload cut to its first experts")
     return ap.parse_args()
 
 
@@ -191,10 +214,11 @@ def timed(torch, stream, fn, steps, flush=None):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def traffic_from_profile(kernel_src):
-    """Per-launch DRAM bytes of the GEMM from the committed ncu summary, if
-    it was taken on the current source of the kernel (else None)."""
-    path = os.path.join(ROOT, "profiles", "signaled_gemm_wave_pattern_ncu.md")
+def traffic_from_profile(workload, kernel_src):
+    """Per-launch DRAM bytes of the GEMM on `workload` from the committed ncu
+    summary (profiles/signaled_gemm_<workload>_ncu.md), if it was taken on
+    the current source of the kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", f"signaled_gemm_{workload}_ncu.md")
     try:
         txt = open(path).read()
     except OSError:
@@ -231,35 +255,77 @@ def calibrate_rows(w, inp, cpu_seconds):
 _LAYOUT_NAMES = {0: "tile", 1: "rs_subtile", 2: "rs_rowblock", 3: "a2a"}
 
 
-def oracle_sample(w, inp, partition, rows):
+def oracle_plan(w, inp, partition):
+    from oracle import plan as OPN
+    return OPN.build_plan(inp.expert_rows, w.N, w.K, w.tile_m, w.tile_n, w.swizzle,
+                          w.wave_width, partition, _LAYOUT_NAMES[w.layout], w.n_dest,
+                          inp.row_token, inp.row_slot,
+                          pad_expert_tile_rows=w.pad_expert_tile_rows)
+
+
+def oracle_rest(w, inp, p, C, groups):
+    """Pre-reorder, consumer and post-reorder of the oracle over `groups`
+    (None: all), on the GEMM output C."""
+    from oracle import comm as OC
+    C_r = OC.pre_reorder(p, C, groups)
+    if w.consumer == 0:
+        recv = OC.consume_copy(p, C_r, groups)
+    elif w.consumer == 1:
+        recv = OC.consume_sum(p, C_r, inp.partials, groups)
+    elif w.consumer == 2:
+        recv = OC.consume_rs(p, C_r, inp.partials, groups)
+    else:
+        recv = OC.consume_a2a(p, C_r, groups)
+    if w.layout == 0:
+        OC.reorder_back_tile(p, recv, groups)
+    elif w.layout in (1, 2):
+        OC.reorder_back_rs(p, recv, groups)
+    else:
+        OC.reorder_back_a2a(p, recv, w.top_k or 2, groups, n_tokens=w.n_tokens or None)
+
+
+def oracle_sample(w, inp, partition, rows, rest_seconds):
     """Time the CPU oracle on a bounded sample of the workload: the fp64 GEMM
     on the first `rows` output rows, plus pre-reorder, consumer and
-    post-reorder on the full output (the plan is built once per shape and
-    not counted).  Returns (seconds per full step estimate, description,
-    cores)."""
+    post-reorder on the first wave groups (all of them when that fits in
+    about `rest_seconds`), each scaled to the full step.  The plan is built
+    once per shape and not counted, except with a routing that changes every
+    step.  Returns (seconds per full step estimate, description, cores)."""
     from oracle import gemm as OG
-    from oracle import pipeline as OPL
 
     t0 = time.perf_counter()
     OG.gemm_rows_bf16(inp.A, inp.B, inp.expert_rows, np.arange(rows))
     t_rows = time.perf_counter() - t0
     gemm_full = t_rows * (w.M / rows)
-    # the rest of the path on the full output (values do not matter for time)
+    t0 = time.perf_counter()
+    p = oracle_plan(w, inp, partition)
+    t_plan = time.perf_counter() - t0
+    # the rest of the path (values do not matter for the time): group 0
+    # first, then as many leading groups as the budget allows
     C = np.zeros((w.M, w.N), dtype=np.uint16)
-    cons = {0: "copy", 1: "sum", 2: "rs", 3: "a2a"}[w.consumer]
-    res = OPL.run(inp.expert_rows, w.N, w.K, w.tile_m, w.tile_n, w.swizzle, w.wave_width,
-                  partition, _LAYOUT_NAMES[w.layout], cons, inp.A, inp.B, inp.partials,
-                  w.n_dest, inp.row_token, inp.row_slot, w.top_k or 2, C_given=C)
-    # with dynamic routing the routing tables are rebuilt every step: the
-    # plan is part of the step
-    skip = ("gemm",) if w.capacity else ("gemm", "plan")
-    rest = sum(v for k, v in res.seconds.items() if k not in skip)
-    plan_note = (f"plan ({res.seconds['plan']:.2f} s) included: the routing changes every step"
-                 if w.capacity else f"plan ({res.seconds['plan']:.2f} s) excluded")
+    units = [int(p.part_len[j].sum()) for j in range(p.n_groups)]
+    t0 = time.perf_counter()
+    oracle_rest(w, inp, p, C, [0])
+    t0_rest = time.perf_counter() - t0
+    per_unit = t0_rest / max(1, units[0])
+    g = 1
+    while g < p.n_groups and sum(units[:g + 1]) * per_unit <= rest_seconds:
+        g += 1
+    if g > 1:
+        t0 = time.perf_counter()
+        oracle_rest(w, inp, p, C, list(range(g)))
+        t_rest = time.perf_counter() - t0
+    else:
+        t_rest = t0_rest
+    rest_full = t_rest * p.n_units / max(1, sum(units[:g]))
+    plan_s = t_plan if w.capacity else 0.0
+    plan_note = (f"plan ({t_plan:.2f} s) included: the routing changes every step"
+                 if w.capacity else f"plan ({t_plan:.2f} s) excluded")
     desc = (f"fp64 GEMM on {rows} of {w.M} output rows ({t_rows:.2f} s, scaled x"
-            f"{w.M / rows:.1f}) + pre-reorder, consumer and post-reorder on the full "
-            f"output ({rest:.2f} s); {plan_note}")
-    return gemm_full + rest, desc, os.cpu_count()
+            f"{w.M / rows:.1f}) + pre-reorder, consumer and post-reorder on the first "
+            f"{g} of {p.n_groups} wave groups ({t_rest:.2f} s, scaled x"
+            f"{p.n_units / max(1, sum(units[:g])):.2f}); {plan_note}")
+    return gemm_full + rest_full + plan_s, desc, os.cpu_count()
 
 
 def run_reference(args):
@@ -271,21 +337,24 @@ def run_reference(args):
     from oracle import plan as OPN
     w = W.WORKLOADS[args.workload]
     inp = W.make_inputs(w)
-    tiles = sum(-(-m // w.tile_m) for m in inp.expert_rows) * (w.N // w.tile_n)
+    tiles_m = [-(-m // w.tile_m) for m in inp.expert_rows]
+    if w.pad_expert_tile_rows:
+        tiles_m = [t + t % 2 for t in tiles_m]
+    tiles = sum(tiles_m) * (w.N // w.tile_n)
     partition = OPN.one_then_two(OPN.wave_count(tiles, w.wave_width))
     per = []
+    # a few seconds of CPU work per step, so the whole run ends in minutes
     budget = max(2.0, 150.0 / max(1, args.steps + args.warmup))
-    rows = calibrate_rows(w, inp, budget)
+    rows = calibrate_rows(w, inp, budget / 2)
     desc = ""
     for i in range(args.warmup + args.steps):
-        secs, desc, cores = oracle_sample(w, inp, partition, rows)
+        secs, desc, cores = oracle_sample(w, inp, partition, rows, budget / 2)
         if i >= args.warmup:
             per.append(secs)
     step_s = statistics.mean(per)
     value = 2.0 * moved_rows(w, inp) * w.N * w.K / step_s / 1e12
     line = {
-        "impl": "reference", "metric": "signaled GEMM TFLOPS (% of bf16 peak); "
-        "overlap time vs serial GEMM+consumer", "value": value, "unit": "TFLOPS",
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -303,9 +372,11 @@ def workload_name(w):
     if w.grouped:
         cap = (f", capacity {w.capacity} rows per expert (M={w.M}), a new routing built on "
                f"the device every step" if w.capacity else "")
+        pad = (", expert grids padded to even tile-row counts (CTA pairs)"
+               if w.pad_expert_tile_rows else "")
         return (f"{w.name}: grouped bf16 GEMM {w.n_tokens} tokens x top-{w.top_k} over "
                 f"{w.n_experts} experts, N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
-                f"W={w.wave_width}, swizzle {w.swizzle}{cap}")
+                f"W={w.wave_width}, swizzle {w.swizzle}{cap}{pad}")
     return (f"{w.name}: bf16 GEMM M={w.M} N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
             f"W={w.wave_width}, swizzle {w.swizzle}")
 
@@ -320,56 +391,312 @@ STEP_KERNELS = {
     "separate": "signaled GEMM + consumer + post-communication reorder",
 }
 
+
+class Bench:
+    """One workload planned and resident, with the step and the timing legs
+    the headline and the per-workload records share."""
+
+    def __init__(self, ctx, w, args):
+        from communication_overlap_gb300 import workloads as W
+        from communication_overlap_gb300.pipeline import Pipeline
+        self.ctx, self.w, self.args = ctx, w, args
+        torch, dev = ctx["torch"], ctx["dev"]
+        self.inp = W.make_inputs(w)
+        self.pipe = Pipeline(w, self.inp, device=dev, consumer_ctas=args.consumer_ctas,
+                             reorder_ctas=args.reorder_ctas)
+        self.s = self.pipe.s0
+        # FLOPs of the rows that hold a token: with fixed expert capacities
+        # the empty rows are not work (the GEMM skips tiles that have none)
+        self.flops = 2.0 * moved_rows(w, self.inp) * w.N * w.K
+        self.kernels = "direct" if args.step_kernels == "auto" else args.step_kernels
+        self.fused = self.kernels in ("fused", "direct")
+        self.direct = self.kernels == "direct"
+        # Dynamic routing (expert capacities fixed): every step takes the
+        # next of a few routings resident in HBM, with its routed A (the
+        # dispatch gather, outside the path), and rebuilds the routing tables
+        # on the device (fo_plan_route) before its GEMM.
+        self.dyn = w.capacity > 0
+        self.routes = []
+        if self.dyn:
+            X = W.token_matrix(w)
+            for k in range(1, 5):
+                _, tok, sl = W.routing(w, k)
+                self.routes.append((torch.from_numpy(tok).to(dev),
+                                    torch.from_numpy(sl).to(dev),
+                                    torch.from_numpy(W.gather_rows(X, tok).view(np.int16))
+                                    .to(dev)))
+            del X
+        self.turn = 0
+
+    def step(self, **kw):
+        if self.dyn:
+            tok, sl, A = self.routes[self.turn % len(self.routes)]
+            self.turn += 1
+            self.pipe.buf.A = A
+            self.pipe.route(tok, sl)
+        return self.pipe.step(**kw)
+
+    def ovl(self):
+        self.step(overlap=True, sync_current=False, fused=self.fused, direct=self.direct)
+
+    def timed(self, fn, steps=None):
+        return timed(self.ctx["torch"], self.s, fn, steps or self.args.steps, self.ctx["flush"])
+
+    def close(self):
+        self.pipe.close()
+
+    # ------------------------------------------------------------------ legs
+    def warm(self):
+        torch = self.ctx["torch"]
+        for _ in range(max(3, self.args.warmup)):
+            self.step(overlap=True, fused=self.fused, direct=self.direct)
+        torch.cuda.synchronize()
+        assert int(self.pipe.buf.status.item()) == 0, "consumer wait timed out"
+        assert self.pipe.buf.count.cpu().tolist() == self.pipe.group_tiles
+
+    def consumer_bytes(self):
+        return consumer_bytes(self.w, self.inp)
+
+    def gemm_spans(self):
+        """The GEMM's in-kernel duration (first CTA start to last tile, from
+        the per-tile globaltimer stamps) alone and inside the overlapped
+        step, `steps` times each, L2 flushed before each."""
+        torch, fo = self.ctx["torch"], self.ctx["fo"]
+        pipe, w = self.pipe, self.w
+        trace = torch.zeros(pipe.tiles + 3 * w.wave_width, dtype=torch.int64,
+                            device=pipe.device)
+        fo.fo_plan_set_trace(pipe.plan, trace.data_ptr())
+
+        def span():
+            t = trace.cpu().numpy().astype(np.int64)
+            starts = t[pipe.tiles:pipe.tiles + min(w.wave_width, pipe.tiles)]
+            return (t[:pipe.tiles].max() - starts.min()) / 1e6
+
+        alone, in_step = [], []
+        for _ in range(self.args.steps):
+            with torch.cuda.stream(self.s):
+                self.ctx["flush"]()
+            pipe.gemm(self.s, pipe.epoch)
+            torch.cuda.synchronize()
+            alone.append(span())
+            with torch.cuda.stream(self.s):
+                self.ctx["flush"]()
+            self.step(overlap=True, fused=self.fused, direct=self.direct)
+            torch.cuda.synchronize()
+            in_step.append(span())
+        fo.fo_plan_set_trace(pipe.plan, 0)
+        return statistics.median(alone), statistics.median(in_step)
+
+    def consumer_in_step(self, reps=3):
+        """The consumer's bandwidth inside the overlapped step, from one
+        traced step: group j's flag rises with its last tile (GEMM stamps);
+        its consumer is busy from max(flag_j, end of group j-1) to the end of
+        its last chunk (consumer stamps).  Bytes are the consumer's
+        algorithmic bytes of the group (sources read once, output written
+        once).  Median over `reps` steps of: all groups, the groups that
+        complete while the GEMM still runs, and the last group (after it)."""
+        torch, fo = self.ctx["torch"], self.ctx["fo"]
+        pipe, w = self.pipe, self.w
+        sm = self.ctx["sm_count"]
+        trace = torch.zeros(pipe.tiles + 3 * w.wave_width, dtype=torch.int64,
+                            device=pipe.device)
+        ctrace = torch.zeros(2 * pipe.P + 4 * 4 * sm, dtype=torch.int64, device=pipe.device)
+        per_unit = self.consumer_bytes() / max(1, moved_rows(w, self.inp) * (w.N // w.tile_n))
+        out = {"all": [], "during_gemm": [], "last_group": [], "busy_us": []}
+        for _ in range(reps):
+            fo.fo_plan_set_trace(pipe.plan, trace.data_ptr(), ctrace.data_ptr())
+            with torch.cuda.stream(self.s):
+                self.ctx["flush"]()
+                ctrace.zero_()
+            self.step(overlap=True, fused=self.fused, direct=self.direct)
+            torch.cuda.synchronize()
+            fo.fo_plan_set_trace(pipe.plan, 0, 0)
+            st = trace.cpu().numpy().astype(np.int64)
+            cs = ctrace.cpu().numpy().astype(np.int64)
+            slot_group = np.asarray(fo.fo_plan_table(pipe.plan, fo.FO_TAB_SLOT_GROUP))
+            part_len = np.asarray(fo.fo_plan_table(pipe.plan, fo.FO_TAB_PART_LEN))
+            units = part_len.reshape(pipe.P, -1).sum(axis=1)
+            tile_done = st[:pipe.tiles]
+            flag = np.array([tile_done[slot_group == j].max() for j in range(pipe.P)])
+            done = cs[:pipe.P]
+            start = np.maximum(flag, np.concatenate(([flag[0]], done[:-1])))
+            busy = np.maximum(done - start, 1)
+            nbytes = units * per_unit
+            gemm_end = tile_done.max()
+            during = flag < gemm_end
+            if units.sum() == 0 or (done == 0).any():
+                continue
+            out["all"].append(nbytes.sum() / busy.sum())
+            if during.any():
+                out["during_gemm"].append(nbytes[during].sum() / busy[during].sum())
+            out["last_group"].append(nbytes[-1] / busy[-1])
+            out["busy_us"].append(busy.sum() / 1e3)
+        res = {}
+        for k, v in out.items():
+            res[k] = statistics.median(v) if v else None
+        hbm = self.ctx["hbm"]
+        return {"gbs": res["all"], "gbs_groups_during_gemm": res["during_gemm"],
+                "gbs_last_group": res["last_group"], "busy_us": res["busy_us"],
+                "frac_of_measured": res["all"] / hbm if res["all"] else None,
+                "frac_of_nominal": res["all"] / NOMINAL_HBM_GBS if res["all"] else None,
+                "how": "per group: algorithmic bytes / (end of its last chunk - max(its "
+                       "flag, end of the previous group)), from globaltimer stamps of one "
+                       "traced overlapped step (median of 3)"}
+
+    def alone_legs(self):
+        """Consumer and reorder alone (flags of the last epoch already raised;
+        ordinary launches so nothing overlaps the flush before them)."""
+        fo, pipe, s = self.ctx["fo"], self.pipe, self.s
+        torch = self.ctx["torch"]
+        sm = self.ctx["sm_count"]
+        pipe.step(overlap=True)
+        torch.cuda.synchronize()
+        pipe.set_overlap(False)
+        r = {}
+        r["direct"] = self.timed(lambda: pipe.consume_reorder(s, pipe.epoch, direct=True))
+        r["consumer"] = self.timed(lambda: pipe.consume(s, pipe.epoch))
+        r["reorder"] = self.timed(lambda: pipe.reorder(s))
+        # a full grid (4 CTAs per SM): the bandwidth roofline figure; the step
+        # uses the library's default grid for running beside the GEMM
+        fo.fo_plan_set_launch(pipe.plan, 4 * sm, self.args.reorder_ctas, False)
+        r["direct_full"] = self.timed(lambda: pipe.consume_reorder(s, pipe.epoch, direct=True))
+        r["consumer_full"] = self.timed(lambda: pipe.consume(s, pipe.epoch))
+        fo.fo_plan_set_launch(pipe.plan, self.args.consumer_ctas, self.args.reorder_ctas, False)
+        pipe.set_overlap(True)
+        return {k: statistics.mean(v) for k, v in r.items()}
+
+    def torch_mm(self):
+        """torch.matmul (cuBLAS) on the same operands, one call per expert."""
+        torch, w = self.ctx["torch"], self.w
+        A_bf = self.pipe.buf.A.view(torch.bfloat16).view(w.M, w.K)
+        B_bf = [b.view(torch.bfloat16).view(w.K, w.N) for b in self.pipe.buf.B]
+        rows = np.cumsum([0] + list(self.inp.expert_rows))
+
+        def mm():
+            with torch.cuda.stream(self.s):
+                for e, Bm in enumerate(B_bf):
+                    torch.matmul(A_bf[rows[e]:rows[e + 1]], Bm)
+        for _ in range(3):   # cuBLAS handle, workspace and kernel choice
+            mm()
+        return statistics.mean(self.timed(mm))
+
+    def record(self, ms_ov, ms_ser, ms_gemm, clk):
+        """The per-workload record (shared by the headline's detail)."""
+        w, pipe = self.w, self.pipe
+        ctx = self.ctx
+        hbm, peak = ctx["hbm"], ctx["peak_burst"]
+        alone = self.alone_legs()
+        span_alone, span_step = self.gemm_spans()
+        cb = self.consumer_bytes()
+        reo_bytes = 2 * moved_rows(w, self.inp) * w.N * 2
+        ms_mm = self.torch_mm()
+        gemm_tf = self.flops / (ms_gemm * 1e-3) / 1e12
+
+        def bw(nbytes, ms):
+            g = nbytes / (ms * 1e-3) / 1e9
+            return {"ms": ms, "gbs": g, "frac_of_measured": g / hbm,
+                    "frac_of_nominal": g / NOMINAL_HBM_GBS}
+        return {
+            "config": workload_name(w),
+            "partition": pipe.partition, "groups_tiles": pipe.group_tiles,
+            "consumer": consumer_name(w), "gemm_pairs": bool(pipe.pairable),
+            "value_tflops": self.flops / (ms_ov * 1e-3) / 1e12,
+            "ms_overlapped_step": ms_ov, "ms_serial_step": ms_ser,
+            "overlap_speedup": ms_ser / ms_ov,
+            "ms_gemm_alone": ms_gemm, "gemm_tflops_alone": gemm_tf,
+            "gemm_frac_of_measured_peak": gemm_tf / peak,
+            "gemm_frac_of_nominal_peak": gemm_tf / NOMINAL_BF16_TFLOPS,
+            "ms_torch_matmul": ms_mm,
+            "torch_matmul_tflops": self.flops / (ms_mm * 1e-3) / 1e12,
+            "gemm_in_kernel_ms_alone": span_alone, "gemm_in_kernel_ms_in_step": span_step,
+            "gemm_slowdown": span_step / span_alone,
+            "consumer_bytes": cb,
+            "direct_alone_step_grid": bw(cb, alone["direct"]),
+            "direct_alone_full_grid": bw(cb, alone["direct_full"]),
+            "consumer_in_step": self.consumer_in_step(),
+            "consumer_alone_step_grid": bw(cb, alone["consumer"]),
+            "consumer_alone_full_grid": bw(cb, alone["consumer_full"]),
+            "reorder_alone": bw(reo_bytes, alone["reorder"]),
+            "clocks": clk,
+            "status_ok": int(pipe.buf.status.item()) == 0,
+        }
+
+
+def measure_compact(ctx, w, args):
+    """A workload other than the headline: the overlapped and serial steps,
+    the GEMM alone, the GEMM's slowdown, the consumer's bandwidth (alone and
+    inside the step) and the clocks of the overlapped steps."""
+    torch = ctx["torch"]
+    b = Bench(ctx, w, args)
+    try:
+        b.warm()
+        with Clocks(ctx["local"]) as clk:
+            t_ov = b.timed(b.ovl)
+        t_ser = b.timed(lambda: b.step(overlap=False, sync_current=False, fused=b.fused,
+                                       direct=b.direct))
+        t_gemm = b.timed(lambda: b.pipe.gemm(b.s, b.pipe.epoch))
+        rec = b.record(statistics.mean(t_ov), statistics.mean(t_ser), statistics.mean(t_gemm),
+                       clk.summary())
+        rec["step_kernels"] = b.kernels
+        return rec
+    finally:
+        b.close()
+        del b
+        torch.cuda.empty_cache()
+
+
+def run_ncu_gemm(args):
+    """Only GEMM launches of the workload (optionally its first --experts
+    experts): the small case for ncu captures of the GEMM."""
+    import torch
+    from communication_overlap_gb300 import workloads as W
+    from communication_overlap_gb300.pipeline import Pipeline
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    if w.grouped and args.experts:
+        e = args.experts
+        rows = int(sum(inp.expert_rows[:e]))
+        tok = np.asarray(inp.row_token[:rows])
+        w = W.scaled(w, M=rows, n_experts=e, n_tokens=int(tok.max()) + 1)
+        inp.A, inp.B = inp.A[:rows], inp.B[:e]
+        inp.expert_rows = inp.expert_rows[:e]
+        inp.row_token, inp.row_slot = inp.row_token[:rows], inp.row_slot[:rows]
+    pipe = Pipeline(w, inp)
+    for _ in range(args.warmup):
+        pipe.gemm(pipe.s0, 1)
+    for _ in range(args.steps):
+        pipe.gemm(pipe.s0, 1)
+    torch.cuda.synchronize()
+    ok = pipe.buf.count.cpu().tolist() == pipe.group_tiles
+    print(json.dumps({"ncu_gemm": w.name, "M": w.M, "experts": w.n_experts,
+                      "tiles": pipe.tiles, "launches": args.warmup + args.steps,
+                      "flops_per_launch": 2.0 * moved_rows(w, inp) * w.N * w.K,
+                      "count_ok": ok}))
+    pipe.close()
+    return 0 if ok else 1
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
     from communication_overlap_gb300 import fo
     from communication_overlap_gb300 import workloads as W
-    from communication_overlap_gb300.pipeline import Pipeline
 
     rank, local, world = dist_env()
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
-    w = W.WORKLOADS[args.workload]
-    inp = W.make_inputs(w)
-    pipe = Pipeline(w, inp, device=dev, consumer_ctas=args.consumer_ctas,
-                    reorder_ctas=args.reorder_ctas)
-    s = pipe.s0
-    # FLOPs of the rows that hold a token: with fixed expert capacities the
-    # empty rows are not work (the GEMM skips tiles that have none)
-    flops = 2.0 * moved_rows(w, inp) * w.N * w.K
+    hbm, peak_burst, peak_sust, peak_kind = measured_peaks()
     flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def flush():
-        flush_buf.fill_(1)
-
-    # tile stamps, CTA starts, and two stamps per split tile of the last wave
-    trace = torch.zeros(pipe.tiles + 3 * w.wave_width, dtype=torch.int64, device=dev)
-
-    # Dynamic routing (expert capacities fixed): every step takes the next of
-    # a few routings resident in HBM, with its routed A (the dispatch gather,
-    # outside the path), and rebuilds the routing tables on the device
-    # (fo_plan_route) before its GEMM.
-    dyn = w.capacity > 0
-    routes = []
-    if dyn:
-        X = W.token_matrix(w)
-        for k in range(1, 5):
-            _, tok, sl = W.routing(w, k)
-            routes.append((torch.from_numpy(tok).to(dev), torch.from_numpy(sl).to(dev),
-                           torch.from_numpy(W.gather_rows(X, tok).view(np.int16)).to(dev)))
-        del X
-    turn = [0]
-
-    def step(**kw):
-        if dyn:
-            tok, sl, A = routes[turn[0] % len(routes)]
-            turn[0] += 1
-            pipe.buf.A = A
-            pipe.route(tok, sl)
-        return pipe.step(**kw)
+    ctx = dict(torch=torch, fo=fo, dev=dev, local=local, hbm=hbm, peak_burst=peak_burst,
+               sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
+               flush=lambda: flush_buf.fill_(1))
+    w = W.WORKLOADS[args.workload]
+    b = Bench(ctx, w, args)
+    pipe, s, flops, inp = b.pipe, b.s, b.flops, b.inp
+    fused, direct, dyn, kernels = b.fused, b.direct, b.dyn, b.kernels
+    sm_count = ctx["sm_count"]
 
     def barrier():
         if world > 1:
@@ -377,204 +704,228 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     # warm-up (also the first correctness evidence: status and counting table)
-    # measured (all three variants timed in one process, interleaved): the
-    # direct fused kernel gives the shortest step on every workload; the
-    # fused kernel that writes the communication buffers and the separate
-    # kernels are timed below as well
-    kernels = "direct" if args.step_kernels == "auto" else args.step_kernels
-    fused = kernels in ("fused", "direct")
-    direct = kernels == "direct"
-    for _ in range(max(3, args.warmup)):
-        step(overlap=True, fused=fused, direct=direct)
-    torch.cuda.synchronize()
-    assert int(pipe.buf.status.item()) == 0, "consumer wait timed out"
-    assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
+    b.warm()
 
     # the headline: overlapped steps
     barrier()
     with Clocks(local) as clk:
-        t_ov = timed(torch, s,
-                     lambda: step(overlap=True, sync_current=False, fused=fused, direct=direct),
-                     args.steps, flush)
+        t_ov = b.timed(b.ovl)
     barrier()
     ms_ov = statistics.mean(t_ov)
     status_ok = int(pipe.buf.status.item()) == 0
 
-    # the same step captured once in a CUDA graph and replayed (same epoch
-    # and kernel parameters every time; the kernels clear their own signals)
-    t_graph = []
-    if not dyn:
-        g_epoch = pipe.epoch + 1
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=s):
-            pipe.gemm(s, g_epoch)
-            if fused:
-                pipe.consume_reorder(s, g_epoch, direct=direct)
-            else:
-                pipe.consume(s, g_epoch)
-                pipe.reorder(s)
-        pipe.epoch = g_epoch
-        def replay():
-            with torch.cuda.stream(s):   # replay on the step's stream
-                graph.replay()
-        t_graph = timed(torch, s, replay, args.steps, flush)
-        assert int(pipe.buf.status.item()) == 0
-        assert pipe.buf.count.cpu().tolist() == pipe.group_tiles
-        del graph
-
-    # every overlapped variant: separate kernels, fused, fused direct (no
-    # communication buffers, each unit stored straight to its final place)
+    # every overlapped variant: separate kernels, fused, fused direct
     t_var = {}
     for name, kw in (("separate", dict(fused=False)), ("fused", dict(fused=True)),
                      ("direct", dict(fused=True, direct=True))):
-        t_var[name] = timed(torch, s, lambda: step(overlap=True, sync_current=False, **kw),
-                            args.steps, flush)
+        t_var[name] = b.timed(lambda: b.step(overlap=True, sync_current=False, **kw))
     # serial = the same kernels as the overlapped step, the consumer as an
     # ordinary launch after the GEMM; and the separate kernels serially
-    t_ser = timed(torch, s,
-                  lambda: step(overlap=False, sync_current=False, fused=fused, direct=direct),
-                  args.steps, flush)
-    t_ser_sep = timed(torch, s, lambda: step(overlap=False, sync_current=False),
-                      args.steps, flush)
+    t_ser = b.timed(lambda: b.step(overlap=False, sync_current=False, fused=fused,
+                                   direct=direct))
+    t_ser_sep = b.timed(lambda: b.step(overlap=False, sync_current=False))
     t_route = []
     if dyn:   # the two routing kernels alone
-        t_route = timed(torch, s, lambda: pipe.route(*routes[0][:2]), args.steps, flush)
+        t_route = b.timed(lambda: pipe.route(*b.routes[0][:2]))
     # GEMM alone (signals on, as in the step; and off)
-    t_gemm = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch), args.steps, flush)
-    t_gemm_nosig = timed(torch, s, lambda: pipe.gemm(s, pipe.epoch, signal=False),
-                         args.steps, flush)
-    # library reference point: torch.matmul (cuBLAS) on the same operands,
-    # one call per expert for the grouped workload
-    A_bf = pipe.buf.A.view(torch.bfloat16).view(w.M, w.K)
-    B_bf = [b.view(torch.bfloat16).view(w.K, w.N) for b in pipe.buf.B]
-    rows = np.cumsum([0] + list(inp.expert_rows))
+    t_gemm = b.timed(lambda: pipe.gemm(s, pipe.epoch))
+    t_gemm_nosig = b.timed(lambda: pipe.gemm(s, pipe.epoch, signal=False))
+    ms_gemm_local = statistics.mean(t_gemm)
+    rec = b.record(ms_ov, statistics.mean(t_ser), ms_gemm_local, clk.summary())
 
-    def torch_mm():
-        with torch.cuda.stream(s):
-            for e, Bm in enumerate(B_bf):
-                torch.matmul(A_bf[rows[e]:rows[e + 1]], Bm)
-    for _ in range(3):   # cuBLAS handle, workspace and kernel choice
-        torch_mm()
-    t_mm = timed(torch, s, torch_mm, args.steps, flush)
-
-    # the same path with W = this device's SM count (the workloads fix W)
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    w_sm = None
-    if sm_count != w.wave_width:
-        pipe_sm = Pipeline(w, inp, device=dev, wave_width=sm_count)
-        t_gemm_sm = timed(torch, pipe_sm.s0, lambda: pipe_sm.gemm(pipe_sm.s0, pipe_sm.epoch),
-                          args.steps, flush)
-        for _ in range(3):
-            pipe_sm.step(overlap=True, fused=fused, direct=direct)
-        t_step_sm = timed(torch, pipe_sm.s0,
-                          lambda: pipe_sm.step(overlap=True, sync_current=False, fused=fused,
-                                               direct=direct),
-                          args.steps, flush)
-        torch.cuda.synchronize()
-        w_sm = {"wave_width": sm_count, "waves": pipe_sm.waves,
-                "partition": pipe_sm.partition, "gemm_pairs": bool(pipe_sm.pairable),
-                "ms_gemm_alone": statistics.mean(t_gemm_sm),
-                "ms_overlapped_step": statistics.mean(t_step_sm),
-                "status_ok": int(pipe_sm.buf.status.item()) == 0}
-        pipe_sm.close()
-        del pipe_sm
-
-    # consumer + reorder alone: the flags of the last epoch are already raised;
-    # ordinary launches so nothing overlaps the flush before them
-    pipe.step(overlap=True)
-    torch.cuda.synchronize()
-    pipe.set_overlap(False)
-
-    def cons_alone():
-        pipe.consume(s, pipe.epoch)
-        pipe.reorder(s)
-    t_cons = timed(torch, s, cons_alone, args.steps, flush)
-
-    def cons_only():
-        pipe.consume(s, pipe.epoch)
-    t_cons_only = timed(torch, s, cons_only, args.steps, flush)
-    t_reo = timed(torch, s, lambda: pipe.reorder(s), args.steps, flush)
-    t_direct_alone = timed(torch, s, lambda: pipe.consume_reorder(s, pipe.epoch, direct=True),
-                           args.steps, flush)
-    # the consumer's bandwidth with a full grid (4 CTAs per SM): its roofline
-    # figure; the step uses the library's default grid for running beside the
-    # GEMM, which for copies is smaller and slower alone
-    fo.fo_plan_set_launch(pipe.plan, 4 * sm_count, args.reorder_ctas, False)
-    t_cons_full = timed(torch, s, cons_only, args.steps, flush)
-    t_direct_full = timed(torch, s, lambda: pipe.consume_reorder(s, pipe.epoch, direct=True),
-                          args.steps, flush)
-    fo.fo_plan_set_launch(pipe.plan, args.consumer_ctas, args.reorder_ctas, False)
-    pipe.set_overlap(True)
-
-    # in-kernel GEMM duration (per-tile stamps) alone and inside the step
-    fo.fo_plan_set_trace(pipe.plan, trace.data_ptr())
-
-    def gemm_span():
-        t = trace.cpu().numpy().astype(np.int64)
-        starts = t[pipe.tiles:pipe.tiles + min(w.wave_width, pipe.tiles)]
-        return (t[:pipe.tiles].max() - starts.min()) / 1e6, t
-
-    span_alone, span_step = [], []
-    for _ in range(args.steps):
-        with torch.cuda.stream(s):
-            flush()
-        pipe.gemm(s, pipe.epoch)
-        torch.cuda.synchronize()
-        span_alone.append(gemm_span()[0])
-        with torch.cuda.stream(s):
-            flush()
-        pipe.step(overlap=True, fused=fused, direct=direct)
-        torch.cuda.synchronize()
-        sp, stamps = gemm_span()
-        span_step.append(sp)
-    fo.fo_plan_set_trace(pipe.plan, 0)
     if args.trace_out:
-        # one more overlapped step with the consumer's stamps as well
-        ctrace = torch.zeros(2 * pipe.P + 16 * sm_count, dtype=torch.int64, device=dev)
-        fo.fo_plan_set_trace(pipe.plan, trace.data_ptr(), ctrace.data_ptr())
-        with torch.cuda.stream(s):
-            flush()
-        pipe.step(overlap=True, fused=fused, direct=direct)
-        torch.cuda.synchronize()
-        fo.fo_plan_set_trace(pipe.plan, 0, 0)
-        stamps = trace.cpu().numpy().astype(np.int64)
-        cst = ctrace.cpu().numpy().astype(np.int64)
-        t0 = stamps[pipe.tiles:pipe.tiles + w.wave_width].min()
-        rec = cst[2 * pipe.P:].reshape(-1, 4)
-        rec = rec[rec[:, 1] > 0]
+        write_trace(ctx, b, args.trace_out)
 
-        def rel(x):
-            return [(float(v) - t0) / 1e3 if v > 0 else None for v in x]
-        with open(args.trace_out, "w") as f:
-            n_split = fo.fo_plan_set_split(pipe.plan, True)
-            split = stamps[pipe.tiles + w.wave_width:pipe.tiles + w.wave_width + 2 * n_split]
-            json.dump({"tile_done_us": ((stamps[:pipe.tiles] - t0) / 1e3).tolist(),
-                       "gemm_cta_start_us": rel(stamps[pipe.tiles:pipe.tiles + w.wave_width]),
-                       "split_tiles": n_split,
-                       "split_helper_done_us": rel(split[0::2]),
-                       "split_owner_half_done_us": rel(split[1::2]),
-                       "group_consumed_us": rel(cst[:pipe.P]),
-                       "group_reordered_us": rel(cst[pipe.P:2 * pipe.P]),
-                       "consumer_cta": [{"sm": int(r[0]), "start_us": (r[1] - t0) / 1e3,
-                                         "end_us": (r[2] - t0) / 1e3, "chunks": int(r[3])}
-                                        for r in rec],
-                       "step_kernels": kernels,
-                       "wave_width": w.wave_width, "partition": pipe.partition}, f)
+    e2e = measure_e2e(ctx, b, args)
 
-    # end to end through the C ABI with host buffers
+    # Algorithm 1 on this workload: the offline inputs (this run's GEMM time
+    # and the consumer's latency curve, sampled) and the exact search; then
+    # the overlapped step with the tuned partition against the workload's
+    # own, alternating.  Reported beside the headline, which keeps the
+    # workload's partition.
+    tuned = None
+    if not args.no_tune:
+        try:
+            tuned = tune_partition(w, inp, ms_gemm_for_tuning=ms_gemm_local,
+                                   partition=pipe.partition, steps=max(10, args.steps // 2))
+        except Exception as e:   # a report, not the benchmark: keep the line
+            tuned = {"error": f"{type(e).__name__}: {e}"}
+    group_tiles, partition = pipe.group_tiles, pipe.partition
+    b.close()
+    del b
+    torch.cuda.empty_cache()
+
+    # every other workload, in the same process (one GPU, one replica)
+    per = {}
+    names = [] if args.per_workload in ("", "none") else args.per_workload.split(",")
+    if world == 1:
+        for name in names:
+            if name == args.workload:
+                continue
+            try:
+                per[name] = measure_compact(ctx, W.WORKLOADS[name], args)
+            except Exception as e:   # keep the headline line
+                per[name] = {"error": f"{type(e).__name__}: {e}"}
+
+    # max over ranks
+    def rmax(x):
+        return max_over_ranks(x, dist if world > 1 else None, dev)
+
+    ms_ov = rmax(ms_ov)
+    ms_ser = rmax(statistics.mean(t_ser))
+    ms_gemm = rmax(ms_gemm_local)
+    ms_e2e = rmax(e2e["ms_pipelined"])
+    ms_e2e_serial = rmax(e2e["ms_one_step_at_a_time"])
+
+    gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
+    traffic = traffic_from_profile(w.name, os.path.join(ROOT, "communication_overlap_gb300",
+                                                         "csrc", "gemm.cu"))
+    out = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            rows = calibrate_rows(w, inp, args.cpu_seconds / 2)
+            secs, desc, cores = oracle_sample(w, inp, partition, rows, args.cpu_seconds / 2)
+            cpu = {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": cores,
+                   "kind": "oracle", "sample": desc}
+        headline = dict(rec)
+        headline.update({
+            "overlapped_step_kernels": kernels,
+            "ms_overlapped_step_median": statistics.median(t_ov),
+            "ms_overlapped_step_by_kernels": {k: statistics.mean(v) for k, v in t_var.items()},
+            "ms_serial_step_separate_kernels": statistics.mean(t_ser_sep),
+            "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
+            "gemm_frac_of_sustained": gemm_tflops / peak_sust,
+            "hbm_peak_gbs": hbm, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+            "nominal_bf16_tflops": NOMINAL_BF16_TFLOPS,
+            "status_ok": status_ok,
+            "tuned_partition": tuned,
+        })
+        if dyn:
+            headline.update({"ms_route_alone": statistics.mean(t_route),
+                             "routings": "4 routings resident in HBM, taken in turn, one "
+                                         "per step"})
+        out = {
+            "metric": METRIC,
+            "value": whole_job_tflops(world, flops, ms_ov),
+            "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_ov, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(w), "partition": partition,
+                       "groups_tiles": group_tiles, "consumer": consumer_name(w),
+                       "l2": "flushed before every timed step (256 MiB write)",
+                       "consumer_ctas": args.consumer_ctas or "library default",
+                       "step_kernels": STEP_KERNELS[kernels],
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_burst,
+                         "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,
+                         "frac_nominal": gemm_tflops / NOMINAL_BF16_TFLOPS,
+                         "nominal_peak": NOMINAL_BF16_TFLOPS,
+                         "traffic": traffic,
+                         "kernel": "signaled_gemm_kernel (alone, signals on)",
+                         "peak_source": f"{peak_kind} bf16 burst (frac); nominal GB300 "
+                                        "dense bf16 (frac_nominal)"},
+            "clocks": clk.summary(),
+            "e2e": {"value": whole_job_tflops(world, flops, ms_e2e), "unit": "TFLOPS",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "ms_per_step": ms_e2e,
+                    "pipelined": "two sets of device inputs and outputs: step k+1's "
+                                 "host-to-device copies and step k-1's device-to-host copy "
+                                 "overlap step k",
+                    "value_one_step_at_a_time": whole_job_tflops(world, flops, ms_e2e_serial),
+                    "ms_per_step_one_step_at_a_time": ms_e2e_serial},
+            "gpu_launches": ((2 if fused else 3) + (2 if dyn else 0)) * args.steps,
+            "cpu_baseline": cpu,
+            "detail": headline,
+            "per_workload": {k: compact_view(v) for k, v in per.items()},
+        }
+        print(json.dumps(out))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def compact_view(rec):
+    """The per-workload record as printed: times, fractions and clocks."""
+    if "error" in rec:
+        return rec
+    keep = ("config", "partition", "gemm_pairs", "consumer", "value_tflops",
+            "ms_overlapped_step", "ms_serial_step", "overlap_speedup", "ms_gemm_alone",
+            "gemm_tflops_alone", "gemm_frac_of_measured_peak", "gemm_frac_of_nominal_peak",
+            "ms_torch_matmul", "gemm_slowdown", "gemm_in_kernel_ms_alone",
+            "gemm_in_kernel_ms_in_step", "consumer_bytes", "direct_alone_step_grid",
+            "direct_alone_full_grid", "consumer_in_step", "reorder_alone", "clocks",
+            "status_ok", "step_kernels")
+    out = {k: rec[k] for k in keep if k in rec}
+    if isinstance(out.get("consumer_in_step"), dict):
+        out["consumer_in_step"] = {k: v for k, v in out["consumer_in_step"].items()
+                                   if k != "how"}
+    return out
+
+
+def write_trace(ctx, b, path):
+    """One more overlapped step with the GEMM's and the consumer's stamps."""
+    torch, fo = ctx["torch"], ctx["fo"]
+    pipe, w = b.pipe, b.w
+    sm_count = ctx["sm_count"]
+    trace = torch.zeros(pipe.tiles + 3 * w.wave_width, dtype=torch.int64, device=pipe.device)
+    ctrace = torch.zeros(2 * pipe.P + 16 * sm_count, dtype=torch.int64, device=pipe.device)
+    fo.fo_plan_set_trace(pipe.plan, trace.data_ptr(), ctrace.data_ptr())
+    with torch.cuda.stream(b.s):
+        ctx["flush"]()
+    b.step(overlap=True, fused=b.fused, direct=b.direct)
+    torch.cuda.synchronize()
+    fo.fo_plan_set_trace(pipe.plan, 0, 0)
+    stamps = trace.cpu().numpy().astype(np.int64)
+    cst = ctrace.cpu().numpy().astype(np.int64)
+    t0 = stamps[pipe.tiles:pipe.tiles + w.wave_width].min()
+    rec = cst[2 * pipe.P:].reshape(-1, 4)
+    rec = rec[rec[:, 1] > 0]
+
+    def rel(x):
+        return [(float(v) - t0) / 1e3 if v > 0 else None for v in x]
+    n_split = fo.fo_plan_set_split(pipe.plan, True)
+    split = stamps[pipe.tiles + w.wave_width:pipe.tiles + w.wave_width + 2 * n_split]
+    with open(path, "w") as f:
+        json.dump({"tile_done_us": ((stamps[:pipe.tiles] - t0) / 1e3).tolist(),
+                   "gemm_cta_start_us": rel(stamps[pipe.tiles:pipe.tiles + w.wave_width]),
+                   "split_tiles": n_split,
+                   "split_helper_done_us": rel(split[0::2]),
+                   "split_owner_half_done_us": rel(split[1::2]),
+                   "group_consumed_us": rel(cst[:pipe.P]),
+                   "group_reordered_us": rel(cst[pipe.P:2 * pipe.P]),
+                   "consumer_cta": [{"sm": int(r[0]), "start_us": (r[1] - t0) / 1e3,
+                                     "end_us": (r[2] - t0) / 1e3, "chunks": int(r[3])}
+                                    for r in rec],
+                   "step_kernels": b.kernels,
+                   "wave_width": w.wave_width, "partition": pipe.partition}, f)
+
+
+def measure_e2e(ctx, b, args):
+    """End to end through the C ABI with host buffers: every step copies its
+    inputs in from pinned host memory and its output back.  One step at a
+    time, and pipelined as a serving loop runs it."""
+    torch = ctx["torch"]
+    pipe, w, s, inp, dyn = b.pipe, b.w, b.s, b.inp, b.dyn
+    fused, direct = b.fused, b.direct
+    dev = pipe.device
     hA = torch.from_numpy(inp.A.view(np.int16)).pin_memory()
     h_route = []
+    d_tok = d_sl = None
     if dyn:   # each step's routing and routed A come from the host
         h_route = [(t.cpu().pin_memory(), q.cpu().pin_memory(), a.cpu().pin_memory())
-                   for t, q, a in routes]
-        d_tok, d_sl = torch.empty_like(routes[0][0]), torch.empty_like(routes[0][1])
-        pipe.buf.A = torch.empty_like(routes[0][2])
-    hB = [torch.from_numpy(b.view(np.int16)).pin_memory() for b in inp.B]
+                   for t, q, a in b.routes]
+        d_tok, d_sl = torch.empty_like(b.routes[0][0]), torch.empty_like(b.routes[0][1])
+        pipe.buf.A = torch.empty_like(b.routes[0][2])
+    hB = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in inp.B]
     hP = [torch.from_numpy(p.view(np.int16)).pin_memory() for p in inp.partials]
     hOut = [torch.empty(f.shape, dtype=torch.int16).pin_memory() for f in pipe.buf.final]
-    h2d = hA.numel() * 2 + sum(b.numel() * 2 for b in hB) + sum(p.numel() * 2 for p in hP)
+    h2d = hA.numel() * 2 + sum(x.numel() * 2 for x in hB) + sum(p.numel() * 2 for p in hP)
     h2d += 2 * w.M * 4 if dyn else 0
     d2h = sum(o.numel() * 2 for o in hOut)
+    turn = [0]
 
     def e2e_step():
         with torch.cuda.stream(s):
@@ -597,14 +948,14 @@ def run_ours(args):
             for h_, d_ in zip(hOut, pipe.buf.final):
                 h_.copy_(d_, non_blocking=True)
     # one step at a time: its copies in, the step, its copy out
-    t_e2e_serial = timed(torch, s, e2e_step, args.steps, flush)
+    t_serial = b.timed(e2e_step)
 
-    # pipelined, as a serving loop runs it: two sets of device inputs and
-    # outputs; step k+1's inputs are copied in (one copy stream) and step
-    # k-1's output copied out (another) while step k computes.  Every step
-    # still copies all its inputs in and its output out; the region is timed
-    # from before the first copy to after the last, over all steps.  Each
-    # step's copies write more than L2 holds (no flush between steps).
+    # pipelined: two sets of device inputs and outputs; step k+1's inputs are
+    # copied in (one copy stream) and step k-1's output copied out (another)
+    # while step k computes.  Every step still copies all its inputs in and
+    # its output out; the region is timed from before the first copy to
+    # after the last, over all steps.  Each step's copies write more than L2
+    # holds (no flush between steps).
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     sets = [dict(A=pipe.buf.A, B=pipe.buf.B, partials=pipe.buf.partials,
                  final=pipe.buf.final, hOut=hOut)]
@@ -617,7 +968,7 @@ def run_ours(args):
             st_["tok"], st_["sl"] = torch.empty_like(d_tok), torch.empty_like(d_sl)
     ev = [{k: torch.cuda.Event() for k in ("h2d", "comp", "d2h")} for _ in sets]
 
-    def e2e_pipelined(n):
+    def pipelined(n):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(s)
@@ -659,132 +1010,14 @@ def run_ours(args):
         e1.record(s)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
-    e2e_pipelined(2)   # warm-up of the streams and events
-    ms_e2e_pipe = e2e_pipelined(args.steps)
+    pipelined(2)   # warm-up of the streams and events
+    ms_pipe = pipelined(args.steps)
     assert int(pipe.buf.status.item()) == 0
-    for st_ in sets[1:]:
-        for kk in ("A", "B", "partials", "final"):
-            st_[kk] = None
     pipe.buf.A, pipe.buf.B = sets[0]["A"], sets[0]["B"]
     pipe.buf.partials, pipe.buf.final = sets[0]["partials"], sets[0]["final"]
     del sets
-
-    # Algorithm 1 on this workload: the offline inputs (this run's GEMM time
-    # and the consumer's latency curve, sampled) and the exact search; then
-    # the overlapped step with the tuned partition against the workload's
-    # own, in one pipeline, alternating.  Reported beside the headline, which
-    # keeps the workload's partition.
-    tuned = None
-    if not args.no_tune:
-        try:
-            tuned = tune_partition(w, inp, ms_gemm_for_tuning=statistics.mean(t_gemm),
-                                   partition=pipe.partition, steps=max(10, args.steps // 5))
-        except Exception as e:   # a report, not the benchmark: keep the line
-            tuned = {"error": f"{type(e).__name__}: {e}"}
-
-    # max over ranks
-    def rmax(x):
-        return max_over_ranks(x, dist if world > 1 else None, dev)
-
-    ms_ov = rmax(ms_ov)
-    ms_ser = rmax(statistics.mean(t_ser))
-    ms_gemm = rmax(statistics.mean(t_gemm))
-    ms_e2e = rmax(ms_e2e_pipe)
-    ms_e2e_serial = rmax(statistics.mean(t_e2e_serial))
-
-    hbm, peak_burst, peak_sust, peak_kind = measured_peaks()
-    gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
-    traffic = traffic_from_profile(os.path.join(ROOT, "communication_overlap_gb300",
-                                                "csrc", "gemm.cu"))
-    cons_bytes = consumer_bytes(w, inp)
-    reo_bytes = 2 * moved_rows(w, inp) * w.N * 2
-    out = None
-    if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline:
-            rows = calibrate_rows(w, inp, args.cpu_seconds)
-            secs, desc, cores = oracle_sample(w, inp, pipe.partition, rows)
-            cpu = {"value": flops / secs / 1e12, "unit": "TFLOPS", "cores": cores,
-                   "kind": "oracle", "sample": desc}
-        out = {
-            "metric": "signaled GEMM TFLOPS (% of bf16 peak); overlap time vs serial "
-                      "GEMM+consumer",
-            "value": whole_job_tflops(world, flops, ms_ov),
-            "unit": "TFLOPS",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_ov, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_name(w), "partition": pipe.partition,
-                       "groups_tiles": pipe.group_tiles, "consumer": consumer_name(w),
-                       "l2": "flushed before every timed step (256 MiB write)",
-                       "consumer_ctas": args.consumer_ctas or "library default",
-                       "step_kernels": STEP_KERNELS[kernels],
-                       "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_burst,
-                         "unit": "TFLOP/s", "frac": gemm_tflops / peak_burst,
-                         "traffic": traffic,
-                         "kernel": "signaled_gemm_kernel<256> (alone, signals on)",
-                         "peak_source": f"{peak_kind} bf16 burst"},
-            "clocks": clk.summary(),
-            "e2e": {"value": whole_job_tflops(world, flops, ms_e2e), "unit": "TFLOPS",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": ms_e2e,
-                    "pipelined": "two sets of device inputs and outputs: step k+1's "
-                                 "host-to-device copies and step k-1's device-to-host copy "
-                                 "overlap step k",
-                    "value_one_step_at_a_time": whole_job_tflops(world, flops, ms_e2e_serial),
-                    "ms_per_step_one_step_at_a_time": ms_e2e_serial},
-            "gpu_launches": ((2 if fused else 3) + (2 if dyn else 0)) * args.steps,
-            "cpu_baseline": cpu,
-            "detail": {
-                "ms_overlapped_step": ms_ov,
-                "ms_overlapped_step_median": statistics.median(t_ov),
-                "ms_serial_step_median": statistics.median(t_ser),
-                "ms_gemm_alone_median": statistics.median(t_gemm),
-                "overlapped_step_kernels": kernels,
-                "ms_overlapped_step_by_kernels": {k: statistics.mean(v) for k, v in t_var.items()},
-                "ms_overlapped_step_graph_replay": statistics.mean(t_graph) if t_graph else None,
-                "ms_serial_step": ms_ser,
-                "serial_step_kernels": kernels,
-                "ms_serial_step_separate_kernels": statistics.mean(t_ser_sep),
-                "overlap_speedup": ms_ser / ms_ov,
-                "ms_gemm_alone": ms_gemm,
-                "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
-                "gemm_tflops_alone": gemm_tflops,
-                "gemm_frac_of_sustained": gemm_tflops / peak_sust,
-                "ms_torch_matmul": statistics.mean(t_mm),
-                "torch_matmul_tflops": flops / (statistics.mean(t_mm) * 1e-3) / 1e12,
-                "torch_matmul_note": "library reference point: torch.matmul on the same "
-                                     "operands (one call per expert), no reorder or signal",
-                "w_sm_count": w_sm,
-                "ms_consumer_plus_reorder_alone": statistics.mean(t_cons),
-                "ms_consumer_alone": statistics.mean(t_cons_only),
-                "ms_reorder_alone": statistics.mean(t_reo),
-                "consumer_gbs": cons_bytes / (statistics.mean(t_cons_only) * 1e-3) / 1e9,
-                "ms_consumer_alone_full_grid": statistics.mean(t_cons_full),
-                "consumer_gbs_full_grid": cons_bytes / (statistics.mean(t_cons_full) * 1e-3) / 1e9,
-                "reorder_gbs": reo_bytes / (statistics.mean(t_reo) * 1e-3) / 1e9,
-                "ms_direct_alone": statistics.mean(t_direct_alone),
-                "direct_gbs": cons_bytes / (statistics.mean(t_direct_alone) * 1e-3) / 1e9,
-                "ms_direct_alone_full_grid": statistics.mean(t_direct_full),
-                "direct_gbs_full_grid": cons_bytes / (statistics.mean(t_direct_full) * 1e-3) / 1e9,
-                "hbm_peak_gbs": hbm,
-                "gemm_in_kernel_ms_alone": statistics.median(span_alone),
-                "gemm_in_kernel_ms_in_step": statistics.median(span_step),
-                "gemm_slowdown": statistics.median(span_step) / statistics.median(span_alone),
-                "status_ok": status_ok,
-                "tuned_partition": tuned,
-                **({"ms_route_alone": statistics.mean(t_route),
-                    "routings": "4 routings resident in HBM, taken in turn, one per step"}
-                   if dyn else {}),
-            },
-        }
-        print(json.dumps(out))
-    pipe.close()
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
+    return {"ms_pipelined": ms_pipe, "ms_one_step_at_a_time": statistics.mean(t_serial),
+            "h2d": h2d, "d2h": d2h}
 
 
 def tune_partition(w, inp, ms_gemm_for_tuning, partition, steps):
@@ -861,6 +1094,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.ncu_gemm:
+        return run_ncu_gemm(args)
     return run_ours(args)
 
 

@@ -162,7 +162,9 @@ fo_status fo_signaled_gemm(const fo_plan* p, const void* A, const void* const* B
   if (!p || !p->blob || !A || !B || !C_r) return FO_ERR_ARG;
   if ((count == nullptr) != (flags == nullptr)) return FO_ERR_ARG;
   if (!fo::aligned4(count) || !fo::aligned4(flags)) return FO_ERR_ARG;
-  return fo::launch_signaled_gemm(p, A, B, C_r, count, flags, epoch, stream);
+  const fo_status st = fo::launch_signaled_gemm(p, A, B, C_r, count, flags, epoch, stream);
+  if (st == FO_OK) fo::noalloc_note_ordinary_launch(p->device, stream);
+  return st;
 }
 
 fo_status fo_consume_group(const fo_plan* p, int32_t group, fo_consumer kind,

@@ -19,6 +19,8 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <utility>
+#include <vector>
 
 #include "device_common.cuh"
 #include "row_map.cuh"
@@ -729,10 +731,15 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
 // allocates nothing.  The plan's tables and every buffer are still the
 // caller's, created beforehand.
 
-// The shared scratch: chunk counters of up to FO_NOALLOC_MAX_GROUPS groups,
-// the "CTAs done" counter, then the finished-chunk counters of the groups.
-// Every GPU that loads the library holds it (32 KB) until the process exits.
-static __device__ __align__(256) int32_t fo_noalloc_scratch[2 * FO_NOALLOC_MAX_GROUPS + 1];
+// The shared scratch.  Layout for a plan of P groups (P <= MAX =
+// FO_NOALLOC_MAX_GROUPS):
+//   [MAX - P, MAX)        chunk counters of groups 0 .. P-1
+//   [MAX]                 "CTAs done" counter (the same slot for every plan)
+//   [MAX + 1, MAX + 1 + P) finished-chunk counters of groups 0 .. P-1
+// Zero when the library is loaded; every launch leaves what it used at zero
+// (its last CTA resets it, also after a timeout).  Every GPU that loads the
+// library holds the array (32 KB) until the process exits.
+static __device__ __align__(256) int32_t fo_noalloc_scratch[2 * FO_NOALLOC_MAX_GROUPS + 1] = {0};
 
 namespace fo {
 namespace {
@@ -740,18 +747,33 @@ namespace {
 std::mutex g_noalloc_mutex;
 int32_t* g_noalloc_addr[64] = {};
 
+// Streams (device, stream) on which a no-alloc consume was launched with no
+// ordinary (non-programmatic) library launch after it.  A consume is a
+// programmatic dependent launch that lets its own dependents start at once,
+// so a second no-alloc consume issued on the same stream -- directly after
+// the first, or after a reorder that is in turn the first's dependent --
+// could start while the first still runs, and both would take chunks from
+// the one array.  Such a consume is launched as an ordinary kernel instead:
+// it starts once everything before it on the stream has finished.  An
+// ordinary launch (fo_signaled_gemm) ends that: it waits for all earlier
+// work, so a consume that depends on it cannot meet an earlier consume.
+std::vector<std::pair<int, cudaStream_t>> g_noalloc_pending;
+
+bool noalloc_take_pending(int device, cudaStream_t st) {
+  for (auto& e : g_noalloc_pending)
+    if (e.first == device && e.second == st) return true;
+  g_noalloc_pending.emplace_back(device, st);
+  return false;
+}
+
 // Device address of fo_noalloc_scratch on the current device.  In host code
 // the array's name only stands for it; its address on a device comes from
-// cudaGetSymbolAddress, taken once per device with that device current.  The
-// first call on a device also clears the array (synchronous cudaMemset);
-// every consumer launch leaves the counters at zero again.
+// cudaGetSymbolAddress, taken once per device with that device current.
 fo_status noalloc_scratch(int device, int32_t** out) {
   if (device < 0 || device >= 64) return FO_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (g_noalloc_addr[device] == nullptr) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, fo_noalloc_scratch) != cudaSuccess) return FO_ERR_CUDA;
-    if (cudaMemset(ptr, 0, sizeof(fo_noalloc_scratch)) != cudaSuccess) return FO_ERR_CUDA;
     g_noalloc_addr[device] = static_cast<int32_t*>(ptr);
   }
   *out = g_noalloc_addr[device];
@@ -759,6 +781,18 @@ fo_status noalloc_scratch(int device, int32_t** out) {
 }
 
 }  // namespace
+
+void noalloc_note_ordinary_launch(int device, void* stream) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (size_t i = 0; i < g_noalloc_pending.size(); ++i)
+    if (g_noalloc_pending[i].first == device && g_noalloc_pending[i].second == st) {
+      g_noalloc_pending[i] = g_noalloc_pending.back();
+      g_noalloc_pending.pop_back();
+      return;
+    }
+}
+
 }  // namespace fo
 
 extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
@@ -800,6 +834,8 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   int device = -1;
   if (cudaGetDevice(&device) != cudaSuccess) return FO_ERR_CUDA;
   if (device != p->device) return FO_ERR_ARG;  // the plan's device must be current
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   int32_t* scratch = nullptr;
   const fo_status st = noalloc_scratch(device, &scratch);
   if (st != FO_OK) return st;
@@ -814,8 +850,9 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.part_start = p->dev.part_start;
   a.part_len = p->dev.part_len;
   a.part_dst = p->dev.part_dst;
-  a.work = scratch;
-  // consumed flags in the plan (allocated when it was built), counters here
+  // work[j] for j < P just below the fixed "CTAs done" slot work[P] =
+  // scratch[MAX]; consumed flags in the plan (allocated when it was built)
+  a.work = scratch + (FO_NOALLOC_MAX_GROUPS - p->P);
   publish_consumed(p, a, scratch + FO_NOALLOC_MAX_GROUPS + 1);
   a.g0 = group < 0 ? 0 : group;
   a.g1 = group < 0 ? p->P : group + 1;
@@ -826,9 +863,11 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   a.chunk_units = chunk_units_of(kind, p->tile_n);
   a.epoch = epoch;
   a.limit_ns = spin_limit_ns ? spin_limit_ns : 2000000000ull;
+  a.trace = p->consumer_trace;
   const int ctas = default_ctas(p, p->consumer_ctas, kind, false, false);
-  const bool ov = p->overlap != 0;
-  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  // overlap as fo_consume_group does, unless a no-alloc consume launched
+  // earlier on this stream may still be running (see g_noalloc_pending)
+  const bool ov = p->overlap != 0 && !noalloc_take_pending(device, cs);
   switch (kind) {
     case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, device, cs);
     case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, device, cs);

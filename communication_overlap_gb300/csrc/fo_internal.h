@@ -119,7 +119,7 @@ namespace fo {
 fo_status check_shape(const fo_plan_desc* d, int32_t* W, int32_t* tiles,
                       int32_t* waves);
 fo_status build_plan(const fo_plan_desc* d, fo_plan* p);
-int32_t expert_tile_rows(int layout, int32_t W, int32_t rows);
+int32_t expert_tile_rows(int32_t pad, int32_t rows);
 fo_status upload_plan(fo_plan* p);
 int32_t unit_of(const fo_plan* p, int32_t slot, int32_t r);
 int32_t place_of(const fo_plan* p, int32_t slot, int32_t r);
@@ -160,6 +160,11 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
 fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
                               const void* const* src, void* const* dst,
                               const void* bias, int act, void* stream);
+// An ordinary (not programmatic) launch of the library on `stream` (the
+// signaled GEMM): every earlier kernel on the stream has finished before it
+// starts, so a no-alloc consume issued after it cannot run beside an
+// earlier one (comm.cu, fo_consume_group_noalloc).
+void noalloc_note_ordinary_launch(int device, void* stream);
 fo_status launch_allgather_rows(const fo_plan* p, const void* const* slices, void* out,
                                 const void* bias, int act, void* stream);
 

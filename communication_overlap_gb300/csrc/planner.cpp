@@ -27,13 +27,15 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
-// Tile rows of an expert's grid.  Reading: in the All-to-All layout with an
-// even W, an odd count gets one empty tile row, so that every band of the
-// launch order has an even height and launch slots 2i, 2i+1 are vertically
-// adjacent tiles (CTA pairs); the empty tiles take slots and are counted.
-int32_t expert_tile_rows(int layout, int32_t W, int32_t rows) {
+// Tile rows of an expert's grid: ceil(rows / 128), the GEMM's output tiles.
+// With pad_expert_tile_rows (an explicit plan input, All-to-All layout
+// only), an odd count gets one empty tile row, so that every band of the
+// launch order has an even height and launch slots 2i, 2i+1 can be
+// vertically adjacent tiles (CTA pairs); the empty tiles take slots and are
+// counted like the others.
+int32_t expert_tile_rows(int32_t pad, int32_t rows) {
   const int32_t tm = int32_t(ceil_div(rows, kTileM));
-  return (layout == FO_LAYOUT_A2A_SUBTOKEN && W % 2 == 0) ? tm + (tm & 1) : tm;
+  return pad ? tm + (tm & 1) : tm;
 }
 
 fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
@@ -45,6 +47,10 @@ fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
   if (d->N % d->tile_n != 0 || d->K % kBlockK != 0) return FO_ERR_ARG;
   if (d->swizzle < 1) return FO_ERR_ARG;
   if (d->n_experts < 0 || d->n_experts > kMaxExperts) return FO_ERR_ARG;
+  if (d->pad_expert_tile_rows != 0 &&
+      (d->pad_expert_tile_rows != 1 || d->layout != FO_LAYOUT_A2A_SUBTOKEN))
+    return FO_ERR_ARG;
+  const int32_t pad = d->pad_expert_tile_rows;
   int32_t W = d->wave_width;
   if (W <= 0) {
     if (d->host_only) return FO_ERR_ARG;
@@ -60,11 +66,11 @@ fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
     for (int e = 0; e < d->n_experts; ++e) {
       if (d->expert_rows[e] < 0) return FO_ERR_ARG;
       sum += d->expert_rows[e];
-      tiles_m += expert_tile_rows(d->layout, W, d->expert_rows[e]);
+      tiles_m += expert_tile_rows(pad, d->expert_rows[e]);
     }
     if (sum != d->M) return FO_ERR_ARG;
   } else {
-    tiles_m = expert_tile_rows(d->layout, W, d->M);
+    tiles_m = expert_tile_rows(pad, d->M);
   }
   int64_t tiles = tiles_m * (d->N / d->tile_n);
   if (tiles <= 0 || tiles > (int64_t(1) << 24)) return FO_ERR_ARG;
@@ -122,7 +128,8 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
   p->expert_row0.assign(E, 0);
   p->expert_tile0.assign(E, 0);
   p->expert_tm.assign(E, 0);
-  for (int e = 0; e < E; ++e) p->expert_tm[e] = expert_tile_rows(layout, W, p->expert_rows[e]);
+  for (int e = 0; e < E; ++e)
+    p->expert_tm[e] = expert_tile_rows(d->pad_expert_tile_rows, p->expert_rows[e]);
   for (int e = 1; e < E; ++e) {
     p->expert_row0[e] = p->expert_row0[e - 1] + p->expert_rows[e - 1];
     p->expert_tile0[e] = p->expert_tile0[e - 1] + p->expert_tm[e - 1] * TN;

@@ -38,6 +38,7 @@ class fo_plan_desc(ctypes.Structure):
         ("n_experts", ctypes.c_int32), ("expert_rows", _i32p),
         ("row_token", _i32p), ("row_slot", _i32p),
         ("host_only", ctypes.c_int32),
+        ("pad_expert_tile_rows", ctypes.c_int32),
     ]
 
 
@@ -132,7 +133,7 @@ def fo_status_string(status):
 
 def make_desc(M, N, K, tile_m=128, tile_n=256, swizzle=8, wave_width=0,
               group_waves=(), layout=FO_LAYOUT_TILE, n_dest=1, expert_rows=None,
-              row_token=None, row_slot=None, host_only=False):
+              row_token=None, row_slot=None, host_only=False, pad_expert_tile_rows=False):
     """Build an fo_plan_desc; the returned object keeps its arrays alive."""
     d = fo_plan_desc()
     d.M, d.N, d.K = M, N, K
@@ -152,6 +153,7 @@ def make_desc(M, N, K, tile_m=128, tile_n=256, swizzle=8, wave_width=0,
         keep += [rt, rs]
         d.row_token, d.row_slot = ctypes.cast(rt, _i32p), ctypes.cast(rs, _i32p)
     d.host_only = 1 if host_only else 0
+    d.pad_expert_tile_rows = 1 if pad_expert_tile_rows else 0
     d._keep = keep
     return d
 

@@ -60,7 +60,8 @@ class Pipeline:
             M=w.M, N=w.N, K=w.K, tile_m=w.tile_m, tile_n=w.tile_n, swizzle=w.swizzle,
             wave_width=W, layout=w.layout, n_dest=w.n_dest,
             expert_rows=inp.expert_rows if w.grouped else None,
-            row_token=inp.row_token, row_slot=inp.row_slot)
+            row_token=inp.row_token, row_slot=inp.row_slot,
+            pad_expert_tile_rows=w.pad_expert_tile_rows)
         probe = fo.make_desc(**self.desc_args, host_only=True)
         self.tiles, self.waves = fo.fo_wave_count(probe)
         self.partition = list(partition) if partition else fo.partition_one_then_two(self.waves)

@@ -16,7 +16,9 @@ Workloads (the shapes of the pages' workloads; synthetic data, no weights):
                   consumer: sum with 3 partials, scatter to 4 slices
   alltoall        16384 tokens x top-2 = 32768 routed rows over 8 experts,
                   N=14336 K=4096 (Mixtral-8x7B-shaped expert up-projection);
-                  consumer: bucket rows by token mod 8 into 8 buffers
+                  consumer: bucket rows by token mod 8 into 8 buffers; each
+                  expert's grid is padded to an even number of tile rows
+                  (an explicit plan input) so the GEMM runs as CTA pairs
   alltoall_dynamic  the same layer with a fixed capacity of 5120 rows per
                   expert (1.25 x the mean load, a multiple of 128): the GEMM
                   shape never changes, each step draws a new routing, and the
@@ -59,6 +61,9 @@ class Workload:
     n_experts: int = 0
     top_k: int = 0
     capacity: int = 0     # rows per expert (0: exactly the routed rows)
+    # each expert's grid padded to an even number of tile rows (one empty
+    # tile row when odd), so the GEMM can run as CTA pairs; a plan input
+    pad_expert_tile_rows: bool = False
 
     @property
     def grouped(self):
@@ -79,7 +84,7 @@ WORKLOADS = {
                               n_dest=4, n_partials=3),
     "alltoall": Workload("alltoall", 5, 32768, 14336, 4096,
                          layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
-                         n_tokens=16384, n_experts=8, top_k=2),
+                         n_tokens=16384, n_experts=8, top_k=2, pad_expert_tile_rows=True),
     "alltoall_dynamic": Workload("alltoall_dynamic", 6, 8 * 5120, 14336, 4096,
                                  layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
                                  n_tokens=16384, n_experts=8, top_k=2, capacity=5120),

@@ -107,6 +107,16 @@ typedef struct {
                                  for a routing given by fo_plan_route */
   const int32_t* row_slot;    /* [M] A2A: top-k slot of each routed row */
   int32_t host_only;      /* 1: build host tables only (no device needed) */
+  int32_t pad_expert_tile_rows; /* 0 (default): each expert's grid has
+                                 ceil(rows / tile_m) tile rows, the GEMM's
+                                 output tiles.  1 (A2A layout only): an odd
+                                 count gets one empty tile row, so that every
+                                 band of the launch order has an even height
+                                 and CTA pairs (fo_plan_set_gemm) can take
+                                 launch slots 2i, 2i+1; empty tiles take
+                                 slots, count in waves and |G_j|, and are
+                                 skipped by the GEMM.  Not in the pages: a
+                                 choice of this library's pair kernel */
 } fo_plan_desc;
 
 typedef struct fo_plan fo_plan;   /* opaque, library-owned */
@@ -318,19 +328,26 @@ fo_status fo_consume_group(const fo_plan* plan, int32_t group,
  * pool owns all device memory and forbids allocations on the request path,
  * and latency-critical loops that cannot wait for the allocator.
  *
- * Same arguments, results and launch behaviour as fo_consume_group.  It
- * allocates nothing: instead of the plan's scratch it keeps its chunk
- * counters in a fixed array inside the library's device image, room for
- * FO_NOALLOC_MAX_GROUPS groups (32 KB on every GPU that loads the library,
- * held until the process exits).  A plan with more groups gets FO_ERR_ARG
- * and nothing is launched.  The plan's device must be the current device.
+ * Same arguments and results as fo_consume_group, and the same launch: a
+ * programmatic dependent launch after fo_signaled_gemm with overlap on
+ * (fo_plan_set_launch), also feeding an overlapped fo_reorder_back, with
+ * the plan's consumer trace if one is set.  It allocates nothing: instead
+ * of the plan's scratch it keeps its chunk counters in a fixed array inside
+ * the library's device image, room for FO_NOALLOC_MAX_GROUPS groups (32 KB
+ * on every GPU that loads the library, held until the process exits).  A
+ * plan with more groups gets FO_ERR_ARG and nothing is launched.  The
+ * plan's device must be the current device.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) and clears it with a synchronous cudaMemset;
- *    make that first call before any stream capture.  Every launch leaves
- *    the counters at zero for the next one.
+ *    (cudaGetSymbolAddress, once per device); make that first call before
+ *    any stream capture.  The array is zero when the library loads and
+ *    every launch leaves its counters at zero for the next one, also after
+ *    a wait that ran out.
  *  - All calls share the one array: calls whose kernels overlap on the GPU
- *    (other streams, other plans) race on it.  Issue them one after
- *    another, e.g. on one stream. */
+ *    (on other streams, without an ordering between them) race on it.
+ *    Calls on one stream are ordered: when an earlier no-alloc consume on
+ *    the same stream could still be running (no fo_signaled_gemm issued on
+ *    that stream since it), the call is launched as an ordinary kernel, so
+ *    it starts only after that consume has finished. */
 #define FO_NOALLOC_MAX_GROUPS 4096
 fo_status fo_consume_group_noalloc(const fo_plan* plan, int32_t group,
                                    fo_consumer kind, const void* src_reordered,

@@ -27,11 +27,18 @@ def _groups(p, groups):
     return range(p.n_groups) if groups is None else groups
 
 
-def pre_reorder(p, C_bits):
+def _slots(p, groups):
+    for j in _groups(p, groups):
+        s0, s1 = p.group_slots[j]
+        yield from range(s0, s1)
+
+
+def pre_reorder(p, C_bits, groups=None, out=None):
     """C_r[unit(slot, r)] = C[row0(slot) + r, col0(slot) : col0 + tile_n]
-    for every valid row of every tile ([P1] 二 "预通信重排")."""
-    C_r = np.zeros((p.n_units, p.tile_n), dtype=np.uint16)
-    for s in range(p.tiles):
+    for every valid row of every tile ([P1] 二 "预通信重排"); with ``groups``,
+    only the tiles of those groups."""
+    C_r = np.zeros((p.n_units, p.tile_n), dtype=np.uint16) if out is None else out
+    for s in _slots(p, groups):
         rows = p.tile_rows(s)
         r0, c0 = p.tile_row0(s), p.tile_col0(s)
         u = p.unit[s, :rows]
@@ -106,12 +113,6 @@ def consume_a2a(p, C_r, groups=None, out=None):
                         int(p.part_dst[j, d]))
             recv[d][o:o + n] = C_r[st:st + n]
     return recv
-
-
-def _slots(p, groups):
-    for j in _groups(p, groups):
-        s0, s1 = p.group_slots[j]
-        yield from range(s0, s1)
 
 
 def reorder_back_tile(p, recv, groups=None, out=None):

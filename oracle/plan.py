@@ -19,10 +19,12 @@ Readings taken where the pages are silent (each is also stated where used):
   R2  wave(slot) = slot // W, W = number of persistent GEMM workers
   R3  |G_j| is counted in tiles, partitions are given in waves
   R6  intra-tile order is row-major; a "unit" is one tile row (tile_n values)
-  R16 All-to-All with an even W: each expert's grid of tile rows is padded to
-      an even count with one empty tile row (no valid rows), so that every
-      band has an even height and launch slots 2i, 2i+1 hold vertically
-      adjacent tiles; empty tiles take slots and count in |G_j| like others
+  R16 an expert's grid has ceil(m_e / tile_m) tile rows, the GEMM's output
+      tiles.  Only when the plan asks for it (``pad_expert_tile_rows``, an
+      explicit input, All-to-All layout only) is an odd count padded with
+      one empty tile row (no valid rows), so that every band has an even
+      height; empty tiles then take slots and count in |G_j| like others.
+      The pages know no such padding: it is an input, never inferred.
 """
 from dataclasses import dataclass, field
 from itertools import product
@@ -187,7 +189,8 @@ def _row_dests(plan, slot):
 
 
 def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
-               partition, layout, n_dest=1, row_token=None, row_slot=None):
+               partition, layout, n_dest=1, row_token=None, row_slot=None,
+               pad_expert_tile_rows=False):
     """Build every table of the path for one problem.
 
     * launch slots: experts in order, each expert's ceil(m_e/tile_m) x
@@ -199,6 +202,10 @@ def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
     * groups: group j holds the waves partition[j] after the earlier groups'
       ([P1] 一 "Wave Group 设计"); |G_j| counts its tiles (reading R3).
     * the reordered layout ``unit[slot, r]`` (see ``_assign_units``).
+
+    pad_expert_tile_rows (reading R16; All-to-All only): give each expert's
+    grid an even number of tile rows by adding one empty tile row when odd.
+    Off by default: the grid is then exactly the GEMM's output tiles.
     """
     if N % tile_n:
         raise ValueError("N must be a multiple of tile_n")
@@ -207,9 +214,10 @@ def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
              None if row_token is None else np.asarray(row_token),
              None if row_slot is None else np.asarray(row_slot))
     p.tiles_n = N // tile_n
-    # Reading R16: All-to-All grids with an even W get an even number of tile
-    # rows per expert (one empty row added when odd)
-    pad_even = layout == LAYOUT_A2A and wave_width % 2 == 0
+    # Reading R16: padding only when asked for, and only in the A2A layout
+    if pad_expert_tile_rows and layout != LAYOUT_A2A:
+        raise ValueError("expert grid padding is an All-to-All option")
+    pad_even = bool(pad_expert_tile_rows)
     row0 = 0
     for m_e in p.expert_rows:
         p.expert_row0.append(row0)

@@ -21,7 +21,8 @@ CASES = [
     dict(name="allreduce", M=512, N=1024, K=256, wave_width=4),
     dict(name="reducescatter", M=1024, N=512, K=192, wave_width=8),
     dict(name="reducescatter", M=1024, N=512, K=192, wave_width=3, layout=W.LAYOUT_RS_ROWBLOCK),
-    dict(name="alltoall", M=2 * 600, N=768, K=128, n_tokens=600, n_experts=4, wave_width=7),
+    dict(name="alltoall", M=2 * 600, N=768, K=128, n_tokens=600, n_experts=4, wave_width=7,
+         pad_expert_tile_rows=False),
     dict(name="worked_example"),
 ]
 ACTS = [(fo.FO_ACT_NONE, False), (fo.FO_ACT_RELU, True), (fo.FO_ACT_SILU, True)]

@@ -38,9 +38,11 @@ def _case(i):
                      layout=W.LAYOUT_RS_ROWBLOCK, **kw)
     else:
         n_tok = int(rng.integers(40, 700))
+        # expert grids padded to even tile-row counts when W is even (CTA
+        # pairs), unpadded when it is odd
         w = W.scaled(W.WORKLOADS[kind], M=2 * n_tok, n_tokens=n_tok,
                      n_experts=int(rng.integers(2, 7)), n_dest=int(rng.choice([2, 4, 8])),
-                     **kw)
+                     pad_expert_tile_rows=kw["wave_width"] % 2 == 0, **kw)
     return w, rng, MODES[i % len(MODES)]
 
 
@@ -58,7 +60,8 @@ def test_random_shape(i):
     probe = fo.make_desc(M=w.M, N=w.N, K=w.K, tile_n=w.tile_n, swizzle=w.swizzle,
                          wave_width=w.wave_width, layout=w.layout, n_dest=w.n_dest,
                          expert_rows=inp.expert_rows if w.grouped else None,
-                         row_token=inp.row_token, row_slot=inp.row_slot, host_only=True)
+                         row_token=inp.row_token, row_slot=inp.row_slot, host_only=True,
+                         pad_expert_tile_rows=w.pad_expert_tile_rows)
     _, T = fo.fo_wave_count(probe)
     pipe = Pipeline(w, inp, partition=_partition(rng, T))
     try:

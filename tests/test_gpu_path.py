@@ -64,7 +64,7 @@ def test_rowblock_layout():
 
 def test_small_alltoall_ragged_experts():
     w = _small("alltoall", M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5,
-               wave_width=9)
+               wave_width=9, pad_expert_tile_rows=False)
     pipe, inp, res = run_workload(w)
     try:
         assert any(m % 128 for m in inp.expert_rows)
@@ -75,10 +75,10 @@ def test_small_alltoall_ragged_experts():
 
 @pytest.mark.parametrize("fused", [False, True, "direct"])
 def test_alltoall_padded_grids_run_as_pairs(fused):
-    """An even W pads odd expert grids with an empty tile row, so the GEMM
-    runs as CTA pairs; everything matches the oracle."""
+    """Expert grids padded to even tile-row counts (an explicit plan input)
+    let the GEMM run as CTA pairs; everything matches the oracle."""
     w = _small("alltoall", M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5,
-               wave_width=8)
+               wave_width=8, pad_expert_tile_rows=True)
     inp = W.make_inputs(w)
     assert any(-(-m // 128) % 2 for m in inp.expert_rows)
     pipe = Pipeline(w, inp, gemm_variant=fo.FO_GEMM_PAIRS)

@@ -46,7 +46,8 @@ def _host_tables(w, inp, partition):
     desc = fo.make_desc(M=w.M, N=w.N, K=w.K, tile_n=w.tile_n, swizzle=w.swizzle,
                         wave_width=w.wave_width, group_waves=partition, layout=w.layout,
                         n_dest=w.n_dest, expert_rows=inp.expert_rows,
-                        row_token=inp.row_token, row_slot=inp.row_slot, host_only=True)
+                        row_token=inp.row_token, row_slot=inp.row_slot, host_only=True,
+                        pad_expert_tile_rows=w.pad_expert_tile_rows)
     plan = fo.fo_plan_groups(desc)
     try:
         return {t: fo.fo_plan_table(plan, t) for t in _TABLES}

@@ -280,20 +280,22 @@ def test_a2a_every_routed_row_lands_once():
     assert sum(o.shape[0] for o in outs) == p.M
 
 
-def test_a2a_even_width_pads_expert_grids():
-    """Reading R16: with an even W every expert's grid gets an even number of
-    tile rows (one empty row added when odd), so launch slots 2i, 2i+1 are
-    vertically adjacent tiles of one expert and column; the empty tiles hold
-    no rows, take slots and count in |G_j|; every routed row still lands
-    once.  With an odd W nothing is padded."""
+def test_a2a_expert_grid_padding_is_an_explicit_input():
+    """Reading R16: an expert's grid is ceil(m_e / 128) tile rows -- the
+    GEMM's output tiles -- whatever W is.  Only with pad_expert_tile_rows
+    does an odd count get one empty tile row, so that launch slots 2i, 2i+1
+    are vertically adjacent tiles of one expert and column; the empty tiles
+    hold no rows, take slots and count in |G_j|; every routed row still
+    lands once either way."""
     D, k = 4, 2
     er, tok, sl = _tiny_routing(n_tok=100, E=3, D=D)     # 200 rows over 3 experts
     tm = [-(-m // 128) for m in er]
     assert any(t % 2 for t in tm)
-    for W, pad in ((6, True), (5, False)):
+    for W, pad in ((6, True), (6, False), (5, True), (5, False)):
         tiles = sum(t + (t % 2 if pad else 0) for t in tm) * 3
         p = P.build_plan(er, 3 * 64, 64, 128, 64, 4, W,
-                         P.one_then_two(P.wave_count(tiles, W)), P.LAYOUT_A2A, D, tok, sl)
+                         P.one_then_two(P.wave_count(tiles, W)), P.LAYOUT_A2A, D, tok, sl,
+                         pad_expert_tile_rows=pad)
         assert p.tiles == tiles
         assert p.expert_tiles_m == [t + (t % 2 if pad else 0) for t in tm]
         assert int(p.group_tiles.sum()) == p.tiles
@@ -309,6 +311,9 @@ def test_a2a_even_width_pads_expert_grids():
         for rho in range(p.M):
             t, q = int(tok[rho]), int(sl[rho])
             assert np.array_equal(outs[t % D][(t // D) * k + q], C[rho])
+    with pytest.raises(ValueError):   # an All-to-All option only
+        P.build_plan([256], 128, 64, 128, 64, 2, 2, (1, 1), P.LAYOUT_TILE,
+                     pad_expert_tile_rows=True)
 
 
 def _padded_routing(capacity, n_tok=40, E=3, k=2, D=4, seed=0):

@@ -42,19 +42,19 @@ def _oracle_places(op, layout, tok, sl):
 
 
 def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
-             partition=None):
+             partition=None, pad=False):
     M = int(sum(expert_rows))
     grouped = tok is not None or len(expert_rows) > 1
     args = dict(M=M, N=N, K=K, tile_n=tile_n, swizzle=S, wave_width=Wd, layout=layout,
                 n_dest=R, expert_rows=list(expert_rows) if grouped else None,
-                row_token=tok, row_slot=sl, host_only=True)
+                row_token=tok, row_slot=sl, host_only=True, pad_expert_tile_rows=pad)
     tiles, T = fo.fo_wave_count(fo.make_desc(**args))
     if partition is None:
         partition = OP.one_then_two(OP.wave_count(tiles, Wd))
     plan = fo.fo_plan_groups(fo.make_desc(**args, group_waves=partition))
     try:
         op = OP.build_plan(list(expert_rows), N, K, 128, tile_n, S, Wd, partition,
-                           _LAYOUT_NAME[layout], R, tok, sl)
+                           _LAYOUT_NAME[layout], R, tok, sl, pad_expert_tile_rows=pad)
         assert (tiles, T) == (op.tiles, op.waves)
         t, waves, gt, t2s = fo.fo_plan_info(plan)
         assert (t, waves) == (op.tiles, op.waves)
@@ -99,6 +99,10 @@ def test_workload_tables(name):
 def test_alltoall_workload_tables():
     w = W.WORKLOADS["alltoall"]
     er, tok, sl = W.routing(w)
+    assert w.pad_expert_tile_rows
+    _compare(er, w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest, tok, sl,
+             pad=True)
+    # the same layer unpadded: the grids are exactly the GEMM's output tiles
     _compare(er, w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest, tok, sl)
 
 
@@ -151,9 +155,11 @@ def test_every_partition_tables(tm, tn, S, Wd):
                  partition=part)
 
 
-def test_padded_a2a_tables_even_width():
-    """All-to-All with an even W: odd expert grids get an empty tile row; the
-    host planner's tables equal the oracle's, and launch slots pair up."""
+@pytest.mark.parametrize("Wd,pad", [(6, True), (6, False), (5, True)])
+def test_padded_a2a_tables(Wd, pad):
+    """All-to-All with pad_expert_tile_rows: odd expert grids get an empty
+    tile row (whatever W); without it the grids are the GEMM's output tiles
+    (even W included).  The host planner's tables equal the oracle's."""
     rng = np.random.default_rng(3)
     n_tok, E, k, D = 150, 3, 2, 4
     picks = np.argsort(rng.random((n_tok, E)), axis=1)[:, :k]
@@ -163,4 +169,23 @@ def test_padded_a2a_tables_even_width():
     order = np.lexsort((sl, tok, ex))
     er = np.bincount(ex, minlength=E).tolist()
     assert any(-(-m // 128) % 2 for m in er)
-    _compare(er, 512, 64, 256, 4, 6, fo.FO_LAYOUT_A2A_SUBTOKEN, D, tok[order], sl[order])
+    _compare(er, 512, 64, 256, 4, Wd, fo.FO_LAYOUT_A2A_SUBTOKEN, D, tok[order], sl[order],
+             pad=pad)
+    tiles, _ = fo.fo_wave_count(fo.make_desc(
+        M=int(sum(er)), N=512, K=64, tile_n=256, swizzle=4, wave_width=Wd,
+        layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=D, expert_rows=er, row_token=tok[order],
+        row_slot=sl[order], host_only=True, pad_expert_tile_rows=pad))
+    tm = [-(-m // 128) for m in er]
+    assert tiles == 2 * sum(t + (t % 2 if pad else 0) for t in tm)
+
+
+def test_padding_is_an_all_to_all_option():
+    """The padding of expert grids is refused for the other layouts."""
+    d = fo.make_desc(M=384, N=512, K=64, tile_n=256, swizzle=2, wave_width=4,
+                     group_waves=(1, 1), host_only=True, pad_expert_tile_rows=True)
+    with pytest.raises(fo.FoError) as e:
+        fo.fo_plan_groups(d)
+    assert e.value.status == fo.FO_ERR_ARG
+    with pytest.raises(ValueError):
+        OP.build_plan([384], 512, 64, 128, 256, 2, 4, (1, 1), OP.LAYOUT_TILE,
+                      pad_expert_tile_rows=True)
