@@ -83,11 +83,24 @@ def parse():
                          "auto: direct")
     ap.add_argument("--reorder-ctas", type=int, default=0,
                     help="reorder grid (0: library default, 3 per SM)")
+    ap.add_argument("--band-order", default="workload",
+                    choices=["workload", "forward", "serpentine"],
+                    help="column order inside the launch order's bands (default: each "
+                         "workload's own)")
     ap.add_argument("--ncu-gemm", action="store_true",
                     help="only GEMM launches (warm-up + --steps), for ncu captures")
     ap.add_argument("--experts", type=int, default=0,
                     help="with --ncu-gemm: the grouped workload cut to its first experts")
     return ap.parse_args()
+
+
+def workload(args, name):
+    """The named workload, with the launch order's band order if given."""
+    from communication_overlap_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    if args.band_order != "workload":
+        w = W.scaled(w, serpentine=args.band_order == "serpentine")
+    return w
 
 
 def dist_env():
@@ -260,7 +273,8 @@ def oracle_plan(w, inp, partition):
     return OPN.build_plan(inp.expert_rows, w.N, w.K, w.tile_m, w.tile_n, w.swizzle,
                           w.wave_width, partition, _LAYOUT_NAMES[w.layout], w.n_dest,
                           inp.row_token, inp.row_slot,
-                          pad_expert_tile_rows=w.pad_expert_tile_rows)
+                          pad_expert_tile_rows=w.pad_expert_tile_rows,
+                          serpentine=w.serpentine)
 
 
 def oracle_rest(w, inp, p, C, groups):
@@ -335,7 +349,7 @@ def run_reference(args):
         return 0
     from communication_overlap_gb300 import workloads as W
     from oracle import plan as OPN
-    w = W.WORKLOADS[args.workload]
+    w = workload(args, args.workload)
     inp = W.make_inputs(w)
     tiles_m = [-(-m // w.tile_m) for m in inp.expert_rows]
     if w.pad_expert_tile_rows:
@@ -374,11 +388,13 @@ def workload_name(w):
                f"the device every step" if w.capacity else "")
         pad = (", expert grids padded to even tile-row counts (CTA pairs)"
                if w.pad_expert_tile_rows else "")
+        pad += ", serpentine bands" if w.serpentine else ""
         return (f"{w.name}: grouped bf16 GEMM {w.n_tokens} tokens x top-{w.top_k} over "
                 f"{w.n_experts} experts, N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
                 f"W={w.wave_width}, swizzle {w.swizzle}{cap}{pad}")
     return (f"{w.name}: bf16 GEMM M={w.M} N={w.N} K={w.K}, {w.tile_m}x{w.tile_n} tiles, "
-            f"W={w.wave_width}, swizzle {w.swizzle}")
+            f"W={w.wave_width}, swizzle {w.swizzle}"
+            + (", serpentine bands" if w.serpentine else ""))
 
 
 # ----------------------------------------------------------------- our path
@@ -517,15 +533,18 @@ class Bench:
             part_len = np.asarray(fo.fo_plan_table(pipe.plan, fo.FO_TAB_PART_LEN))
             units = part_len.reshape(pipe.P, -1).sum(axis=1)
             tile_done = st[:pipe.tiles]
-            flag = np.array([tile_done[slot_group == j].max() for j in range(pipe.P)])
-            done = cs[:pipe.P]
+            gemm_end = tile_done.max()
+            # groups with units (a group of empty All-to-All tiles has none
+            # and leaves no consumer stamp)
+            live = np.nonzero(units > 0)[0]
+            if live.size == 0 or (cs[live] == 0).any():
+                continue
+            flag = np.array([tile_done[slot_group == j].max() for j in live])
+            done = cs[live]
             start = np.maximum(flag, np.concatenate(([flag[0]], done[:-1])))
             busy = np.maximum(done - start, 1)
-            nbytes = units * per_unit
-            gemm_end = tile_done.max()
+            nbytes = units[live] * per_unit
             during = flag < gemm_end
-            if units.sum() == 0 or (done == 0).any():
-                continue
             out["all"].append(nbytes.sum() / busy.sum())
             if during.any():
                 out["during_gemm"].append(nbytes[during].sum() / busy[during].sum())
@@ -651,7 +670,7 @@ def run_ncu_gemm(args):
     import torch
     from communication_overlap_gb300 import workloads as W
     from communication_overlap_gb300.pipeline import Pipeline
-    w = W.WORKLOADS[args.workload]
+    w = workload(args, args.workload)
     inp = W.make_inputs(w)
     if w.grouped and args.experts:
         e = args.experts
@@ -692,7 +711,7 @@ def run_ours(args):
     ctx = dict(torch=torch, fo=fo, dev=dev, local=local, hbm=hbm, peak_burst=peak_burst,
                sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
                flush=lambda: flush_buf.fill_(1))
-    w = W.WORKLOADS[args.workload]
+    w = workload(args, args.workload)
     b = Bench(ctx, w, args)
     pipe, s, flops, inp = b.pipe, b.s, b.flops, b.inp
     fused, direct, dyn, kernels = b.fused, b.direct, b.dyn, b.kernels
@@ -763,7 +782,7 @@ def run_ours(args):
             if name == args.workload:
                 continue
             try:
-                per[name] = measure_compact(ctx, W.WORKLOADS[name], args)
+                per[name] = measure_compact(ctx, workload(args, name), args)
             except Exception as e:   # keep the headline line
                 per[name] = {"error": f"{type(e).__name__}: {e}"}
 

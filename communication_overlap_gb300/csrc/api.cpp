@@ -101,6 +101,12 @@ fo_status fo_plan_set_launch(fo_plan* p, int32_t consumer_ctas, int32_t reorder_
   return FO_OK;
 }
 
+fo_status fo_plan_set_pacing(fo_plan* p, int32_t ctas_during_gemm) {
+  if (!p || ctas_during_gemm < 0) return FO_ERR_ARG;
+  p->consumer_pace = ctas_during_gemm;
+  return FO_OK;
+}
+
 fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairable,
                            int32_t* pair_capacity) {
   if (!p) return FO_ERR_ARG;

@@ -297,6 +297,7 @@ struct FusedArgs {
   const int32_t* unit_place;   // [units] output << kPlaceShift | vector index
   int32_t act, row_vec;
   int32_t direct;  // no communication buffers: each unit goes straight to its final place
+  int32_t pace;    // > 0: CTAs from this index on first wait for the last group's flag
 };
 
 // Where the units of a chunk go, computed by threads t < units before the
@@ -418,7 +419,20 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
   int32_t chunks_done = 0;
   if (c.trace != nullptr && tid == 0) t_start = globaltimer_ns();
 
-  for (int j = c.g0; j < c.g1; ++j) {
+  // Pacing: while the GEMM still runs, only the first `pace` CTAs consume;
+  // the others wait until the last group's flag rises (the GEMM's end) and
+  // then take whatever chunks are left, from the first group on.
+  bool paced_ok = true;
+  if (a.pace > 0 && int32_t(blockIdx.x) >= a.pace && c.g1 > c.g0) {
+    if (tid == 0) s_ok = wait_flag(c.flags + (c.g1 - 1), c.epoch, c.limit_ns) ? 1 : 0;
+    __syncthreads();
+    if (!s_ok) {
+      if (tid == 0) atomicCAS(c.status, 0, int32_t(FO_ERR_TIMEOUT));
+      paced_ok = false;
+    }
+  }
+
+  for (int j = c.g0; paced_ok && j < c.g1; ++j) {
     // The group's first chunk is taken, and its unit map computed, before
     // the wait on the group's flag: when the group completes, only the data
     // moves are left.
@@ -706,6 +720,8 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
   a.act = act;
   a.row_vec = p->N / 8;
   const int ctas = default_ctas(p, p->consumer_ctas, kind, true, a.direct != 0);
+  a.pace = (p->overlap != 0 && p->consumer_pace > 0 && p->consumer_pace < ctas)
+               ? p->consumer_pace : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool ov = p->overlap != 0;
   if (a.direct)

@@ -75,6 +75,7 @@ struct DeviceTables {
 struct fo_plan {
   // description
   int32_t M = 0, N = 0, K = 0, tile_m = 0, tile_n = 0, swizzle = 0, W = 0;
+  int32_t band_order = 0;   // fo_band_order
   int32_t P = 0, R = 1, layout = 0, n_dest = 1, n_experts = 0, top_k = 1, n_tokens = 0;
   int32_t tiles = 0, tiles_n = 0, waves = 0, n_units = 0;
   std::vector<int32_t> expert_rows, expert_row0, expert_tile0;
@@ -96,6 +97,10 @@ struct fo_plan {
   int device = -1;
   int sm_count = 0;
   int consumer_ctas = 0, reorder_ctas = 0, overlap = 1;
+  // fo_consume_reorder with overlap on: consumer CTAs with an index of at
+  // least this many wait for the last group's flag before taking work
+  // (0: every CTA works from the first flag on)
+  int consumer_pace = 0;
   int gemm_variant = 0;   // fo_gemm_variant
   // last-wave split: when the last wave holds split_n <= W / 2 tiles, each
   // is computed by two CTAs over halves of K (0: no split possible)

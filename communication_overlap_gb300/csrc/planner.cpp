@@ -46,6 +46,8 @@ fo_status check_shape(const fo_plan_desc* d, int32_t* W_out, int32_t* tiles_out,
   if (d->tile_n != 128 && d->tile_n != 256) return FO_ERR_UNSUPPORTED;
   if (d->N % d->tile_n != 0 || d->K % kBlockK != 0) return FO_ERR_ARG;
   if (d->swizzle < 1) return FO_ERR_ARG;
+  if (d->band_order != FO_BAND_FORWARD && d->band_order != FO_BAND_SERPENTINE)
+    return FO_ERR_ARG;
   if (d->n_experts < 0 || d->n_experts > kMaxExperts) return FO_ERR_ARG;
   if (d->pad_expert_tile_rows != 0 &&
       (d->pad_expert_tile_rows != 1 || d->layout != FO_LAYOUT_A2A_SUBTOKEN))
@@ -115,6 +117,7 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
 
   p->M = d->M; p->N = d->N; p->K = d->K;
   p->tile_m = d->tile_m; p->tile_n = d->tile_n; p->swizzle = d->swizzle;
+  p->band_order = d->band_order;
   p->W = W; p->P = d->n_groups; p->R = R; p->layout = layout;
   p->n_dest = d->n_dest; p->n_experts = d->n_experts;
   p->tiles = tiles; p->waves = waves; p->tiles_n = d->N / d->tile_n;
@@ -137,7 +140,8 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
 
   // Launch order: experts in turn; inside an expert, band b covers tile rows
   // [b*S, b*S + h) with h = min(S, rows left); position o inside the band is
-  // column o / h, row b*S + o % h.
+  // column o / h (serpentine: TN - 1 - o / h in the expert's odd bands), row
+  // b*S + o % h.
   p->slot_tile.assign(tiles, 0);
   p->tile_slot.assign(tiles, 0);
   p->tile.assign(tiles, TileInfo{});
@@ -148,7 +152,8 @@ fo_status build_plan(const fo_plan_desc* d, fo_plan* p) {
       for (int32_t top = 0; top < tm_count; top += d->swizzle) {
         const int32_t h = std::min<int32_t>(d->swizzle, tm_count - top);
         for (int32_t o = 0; o < h * TN; ++o, ++s) {
-          const int32_t tm = top + o % h, tn = o / h;
+          const bool back = d->band_order == FO_BAND_SERPENTINE && (top / d->swizzle) % 2;
+          const int32_t tm = top + o % h, tn = back ? TN - 1 - o / h : o / h;
           const int32_t t = p->expert_tile0[e] + tm * TN + tn;
           p->slot_tile[s] = t;
           p->tile_slot[t] = s;

@@ -24,7 +24,9 @@
 //               blocks, redone in every CTA's shared memory), the units for d
 //               before launch slot s follow in closed form from the banded
 //               launch order (bands of `swizzle` tile rows walked column by
-//               column):
+//               column; in a serpentine order the expert's odd bands walk
+//               them right to left, and tn below is the column's position
+//               in its band, TN - 1 - column there):
 //                 E(s, d) = TN * BP[b0][d] + tn * (BP[b0 + h][d] - BP[b0][d])
 //                           + BP[b][d] - BP[b0][d]
 //               for the tile of block b, column tn, in the band of blocks
@@ -79,6 +81,7 @@ struct RouteArgs {
   int32_t expert_block0[kMaxExperts + 1];
   int32_t cap[kMaxDest];      // units each receive buffer holds
   int32_t n_experts, R, n_tokens, top_k, B, P, tiles, TN, swizzle, tile_n, M, N;
+  int32_t serpentine;   // odd bands of each expert walk their columns right to left
 };
 
 __global__ void __launch_bounds__(kTileM) route_rows_kernel(const __grid_constant__ RouteArgs a) {
@@ -139,7 +142,9 @@ __device__ __forceinline__ int32_t units_before(const RouteArgs& a, const int32_
   const int32_t top = tm - tm % a.swizzle;
   const int32_t h = min(a.swizzle, tm_count - top);
   const int32_t b0 = a.expert_block0[e] + top, b = a.expert_block0[e] + tm;
-  const int32_t tn = col0 / a.tile_n;
+  const int32_t col = col0 / a.tile_n;
+  // the column's position in its band's order
+  const int32_t tn = (a.serpentine && (top / a.swizzle) % 2) ? a.TN - 1 - col : col;
   const int32_t p0 = BP[b0 * a.R + d];
   return a.TN * p0 + tn * (BP[(b0 + h) * a.R + d] - p0) + (BP[b * a.R + d] - p0);
 }
@@ -362,6 +367,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
   a.tiles = p->tiles;
   a.TN = p->tiles_n;
   a.swizzle = p->swizzle;
+  a.serpentine = p->band_order == FO_BAND_SERPENTINE ? 1 : 0;
   a.tile_n = p->tile_n;
   a.M = p->M;
   a.N = p->N;

@@ -18,6 +18,7 @@ FO_LAYOUT_TILE, FO_LAYOUT_RS_SUBTILE, FO_LAYOUT_RS_ROWBLOCK, FO_LAYOUT_A2A_SUBTO
 FO_CONS_COPY, FO_CONS_SUM, FO_CONS_RS, FO_CONS_A2A = range(4)
 FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
 FO_ACT_NONE, FO_ACT_RELU, FO_ACT_SILU = range(3)
+FO_BAND_FORWARD, FO_BAND_SERPENTINE = range(2)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
  FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY, FO_TAB_SLOT_LIVE, FO_TAB_UNIT_PLACE) = range(13)
@@ -39,6 +40,7 @@ class fo_plan_desc(ctypes.Structure):
         ("row_token", _i32p), ("row_slot", _i32p),
         ("host_only", ctypes.c_int32),
         ("pad_expert_tile_rows", ctypes.c_int32),
+        ("band_order", ctypes.c_int32),
     ]
 
 
@@ -69,6 +71,7 @@ def lib():
             "fo_plan_set_launch": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32,
                                                   ctypes.c_int32]),
             "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp, _vp]),
+            "fo_plan_set_pacing": (ctypes.c_int, [_vp, ctypes.c_int32]),
             "fo_plan_set_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _i32p]),
             "fo_plan_set_split": (ctypes.c_int, [_vp, ctypes.c_int32, _i32p]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
@@ -133,7 +136,8 @@ def fo_status_string(status):
 
 def make_desc(M, N, K, tile_m=128, tile_n=256, swizzle=8, wave_width=0,
               group_waves=(), layout=FO_LAYOUT_TILE, n_dest=1, expert_rows=None,
-              row_token=None, row_slot=None, host_only=False, pad_expert_tile_rows=False):
+              row_token=None, row_slot=None, host_only=False, pad_expert_tile_rows=False,
+              band_order=FO_BAND_FORWARD):
     """Build an fo_plan_desc; the returned object keeps its arrays alive."""
     d = fo_plan_desc()
     d.M, d.N, d.K = M, N, K
@@ -154,6 +158,7 @@ def make_desc(M, N, K, tile_m=128, tile_n=256, swizzle=8, wave_width=0,
         d.row_token, d.row_slot = ctypes.cast(rt, _i32p), ctypes.cast(rs, _i32p)
     d.host_only = 1 if host_only else 0
     d.pad_expert_tile_rows = 1 if pad_expert_tile_rows else 0
+    d.band_order = int(band_order)
     d._keep = keep
     return d
 
@@ -199,6 +204,11 @@ def fo_plan_route(plan, row_token, row_slot, n_tokens, top_k, dev_status, stream
 def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):
     _check("fo_plan_set_launch",
            lib().fo_plan_set_launch(plan, consumer_ctas, reorder_ctas, 1 if overlap else 0))
+
+
+def fo_plan_set_pacing(plan, ctas_during_gemm=0):
+    """Consumer CTAs that take work while the GEMM runs (0: all)."""
+    _check("fo_plan_set_pacing", lib().fo_plan_set_pacing(plan, int(ctas_during_gemm)))
 
 
 def fo_plan_set_gemm(plan, variant=FO_GEMM_AUTO):

@@ -61,7 +61,8 @@ class Pipeline:
             wave_width=W, layout=w.layout, n_dest=w.n_dest,
             expert_rows=inp.expert_rows if w.grouped else None,
             row_token=inp.row_token, row_slot=inp.row_slot,
-            pad_expert_tile_rows=w.pad_expert_tile_rows)
+            pad_expert_tile_rows=w.pad_expert_tile_rows,
+            band_order=fo.FO_BAND_SERPENTINE if w.serpentine else fo.FO_BAND_FORWARD)
         probe = fo.make_desc(**self.desc_args, host_only=True)
         self.tiles, self.waves = fo.fo_wave_count(probe)
         self.partition = list(partition) if partition else fo.partition_one_then_two(self.waves)

@@ -19,6 +19,8 @@ Workloads (the shapes of the pages' workloads; synthetic data, no weights):
                   consumer: bucket rows by token mod 8 into 8 buffers; each
                   expert's grid is padded to an even number of tile rows
                   (an explicit plan input) so the GEMM runs as CTA pairs
+  Every workload but the worked example launches its bands in serpentine
+  order (odd bands right to left; an explicit plan input).
   alltoall_dynamic  the same layer with a fixed capacity of 5120 rows per
                   expert (1.25 x the mean load, a multiple of 128): the GEMM
                   shape never changes, each step draws a new routing, and the
@@ -64,6 +66,9 @@ class Workload:
     # each expert's grid padded to an even number of tile rows (one empty
     # tile row when odd), so the GEMM can run as CTA pairs; a plan input
     pad_expert_tile_rows: bool = False
+    # launch order: the odd bands (of each expert) walk their columns right
+    # to left (serpentine) instead of left to right; a plan input
+    serpentine: bool = False
 
     @property
     def grouped(self):
@@ -73,21 +78,26 @@ class Workload:
         return 2.0 * self.M * self.N * self.K
 
 
+# The large workloads launch their bands in serpentine order (measured: the
+# GEMM 0.7-2.7% shorter, fewer re-reads of B); the worked example has one
+# band, where both orders are the same.
 WORKLOADS = {
     "worked_example": Workload("worked_example", 1, 256, 512, 256, tile_n=128,
                                swizzle=2, wave_width=2, uniform=True),
-    "wave_pattern": Workload("wave_pattern", 2, 2048, 8192, 8192),
+    "wave_pattern": Workload("wave_pattern", 2, 2048, 8192, 8192, serpentine=True),
     "allreduce": Workload("allreduce", 3, 4096, 8192, 3584,
-                          consumer=CONS_SUM, n_partials=7),
+                          consumer=CONS_SUM, n_partials=7, serpentine=True),
     "reducescatter": Workload("reducescatter", 4, 8192, 4096, 2752,
                               layout=LAYOUT_RS_SUBTILE, consumer=CONS_RS,
-                              n_dest=4, n_partials=3),
+                              n_dest=4, n_partials=3, serpentine=True),
     "alltoall": Workload("alltoall", 5, 32768, 14336, 4096,
                          layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
-                         n_tokens=16384, n_experts=8, top_k=2, pad_expert_tile_rows=True),
+                         n_tokens=16384, n_experts=8, top_k=2, pad_expert_tile_rows=True,
+                         serpentine=True),
     "alltoall_dynamic": Workload("alltoall_dynamic", 6, 8 * 5120, 14336, 4096,
                                  layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
-                                 n_tokens=16384, n_experts=8, top_k=2, capacity=5120),
+                                 n_tokens=16384, n_experts=8, top_k=2, capacity=5120,
+                                 serpentine=True),
 }
 
 

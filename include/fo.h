@@ -117,7 +117,20 @@ typedef struct {
                                  slots, count in waves and |G_j|, and are
                                  skipped by the GEMM.  Not in the pages: a
                                  choice of this library's pair kernel */
+  int32_t band_order;     /* FO_BAND_FORWARD (0, default) or
+                             FO_BAND_SERPENTINE, see fo_band_order */
 } fo_plan_desc;
+
+/* Column order inside the bands of the launch order.  Tiles are launched
+ * band by band (`swizzle` tile rows per band, per expert); inside a band,
+ * column by column, each column top to bottom.
+ *  FO_BAND_FORWARD:    every band walks its columns left to right.
+ *  FO_BAND_SERPENTINE: the odd bands of each expert walk them right to
+ *      left, so a band starts on the columns of B the band before it ended
+ *      on, while they may still be in L2.
+ * Either way a band's tiles are consecutive launch slots, waves are slot / W
+ * and the CTA pairs of fo_plan_set_gemm stay vertically adjacent. */
+typedef enum { FO_BAND_FORWARD = 0, FO_BAND_SERPENTINE = 1 } fo_band_order;
 
 typedef struct fo_plan fo_plan;   /* opaque, library-owned */
 
@@ -193,6 +206,16 @@ fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
  *      baseline). */
 fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
                              int32_t reorder_ctas, int32_t overlap);
+
+/* Pacing of fo_consume_reorder beside the GEMM (overlap on).  While the GEMM
+ * still runs, only consumer CTAs 0 .. ctas_during_gemm-1 take work; the
+ * others first wait (bounded, like every flag wait) for the last group's
+ * flag -- the GEMM's end -- and then take whatever is left, from the first
+ * group on.  A consumer that moves less data while the GEMM runs competes
+ * less with it for HBM and SM time, and catches up once it has finished.
+ * 0 (default) or a value of at least the grid: every CTA works from the
+ * first flag on.  The results do not depend on it. */
+fo_status fo_plan_set_pacing(fo_plan* plan, int32_t ctas_during_gemm);
 
 /* How fo_signaled_gemm maps tiles onto CTAs.  Either way W CTAs take the
  * launch slots c, c + W, ... (wave = slot / W) and every tile gets the same

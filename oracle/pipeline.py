@@ -29,14 +29,15 @@ class Result:
 
 def run(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width, partition,
         layout, consumer, A, B_list, partials=(), n_dest=1, row_token=None,
-        row_slot=None, top_k=2, C_given=None, pad_expert_tile_rows=False):
+        row_slot=None, top_k=2, C_given=None, pad_expert_tile_rows=False,
+        serpentine=False):
     """Run the path once.  ``C_given`` may be passed to skip the GEMM stage
     (to check the later stages on a given GEMM output)."""
     res = Result(plan=None)
     t = time.perf_counter()
     p = P.build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
                      partition, layout, n_dest, row_token, row_slot,
-                     pad_expert_tile_rows=pad_expert_tile_rows)
+                     pad_expert_tile_rows=pad_expert_tile_rows, serpentine=serpentine)
     res.plan = p
     res.seconds["plan"] = time.perf_counter() - t
 

@@ -16,6 +16,8 @@ shared with the CUDA path's planner.
 
 Readings taken where the pages are silent (each is also stated where used):
   R1  block swizzle: bands of ``swizzle`` tile-rows, walked column by column
+      (left to right; with the serpentine band order, an explicit plan
+      input, the odd bands of each expert walk right to left)
   R2  wave(slot) = slot // W, W = number of persistent GEMM workers
   R3  |G_j| is counted in tiles, partitions are given in waves
   R6  intra-tile order is row-major; a "unit" is one tile row (tile_n values)
@@ -41,7 +43,7 @@ LAYOUT_A2A = "a2a"                  # All-to-All: sub-tokens by destination
 # --------------------------------------------------------------------------
 # tile order, waves, groups
 
-def launch_order(tiles_m, tiles_n, swizzle):
+def launch_order(tiles_m, tiles_n, swizzle, serpentine=False):
     """Launch order of a tiles_m x tiles_n grid as a list of (tm, tn).
 
     [P1] 一 "Block Swizzling 的影响" and 二 "挑战: 不规则的 Tile 执行顺序": tiles are
@@ -49,16 +51,21 @@ def launch_order(tiles_m, tiles_n, swizzle):
     The pages never define the swizzle.  Reading R1: tile-rows form bands of
     ``swizzle`` rows (the last band may be shorter); bands are taken in
     order, and inside a band the tiles are taken column by column, top to
-    bottom.
+    bottom.  Columns go left to right; with ``serpentine`` (a plan input, not
+    the pages') the odd bands (second, fourth, ...) go right to left.
     """
     order = []
-    top = 0
+    top, band = 0, 0
     while top < tiles_m:
         h = min(swizzle, tiles_m - top)
-        for tn in range(tiles_n):
+        cols = range(tiles_n)
+        if serpentine and band % 2 == 1:
+            cols = reversed(cols)
+        for tn in cols:
             for dm in range(h):
                 order.append((top + dm, tn))
         top += h
+        band += 1
     return order
 
 
@@ -190,7 +197,7 @@ def _row_dests(plan, slot):
 
 def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
                partition, layout, n_dest=1, row_token=None, row_slot=None,
-               pad_expert_tile_rows=False):
+               pad_expert_tile_rows=False, serpentine=False):
     """Build every table of the path for one problem.
 
     * launch slots: experts in order, each expert's ceil(m_e/tile_m) x
@@ -206,6 +213,9 @@ def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
     pad_expert_tile_rows (reading R16; All-to-All only): give each expert's
     grid an even number of tile rows by adding one empty tile row when odd.
     Off by default: the grid is then exactly the GEMM's output tiles.
+
+    serpentine (reading R1, a plan input): the odd bands of each expert walk
+    their columns right to left.
     """
     if N % tile_n:
         raise ValueError("N must be a multiple of tile_n")
@@ -225,7 +235,7 @@ def build_plan(expert_rows, N, K, tile_m, tile_n, swizzle, wave_width,
         p.expert_tiles_m.append(tm + (tm % 2) if pad_even else tm)
         row0 += m_e
     for e, tm_count in enumerate(p.expert_tiles_m):
-        for tm, tn in launch_order(tm_count, p.tiles_n, swizzle):
+        for tm, tn in launch_order(tm_count, p.tiles_n, swizzle, serpentine):
             p.slot_tile.append((e, tm, tn))
     p.tiles = len(p.slot_tile)
     p.waves = wave_count(p.tiles, wave_width)

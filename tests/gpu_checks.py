@@ -22,7 +22,8 @@ def oracle_plan(w, inp, partition):
     return OP.build_plan(inp.expert_rows, w.N, w.K, w.tile_m, w.tile_n, w.swizzle,
                          w.wave_width, partition, _LAYOUT[w.layout], w.n_dest,
                          inp.row_token, inp.row_slot,
-                         pad_expert_tile_rows=w.pad_expert_tile_rows)
+                         pad_expert_tile_rows=w.pad_expert_tile_rows,
+                         serpentine=w.serpentine)
 
 
 def gemm_close(got_bits, ref_bits):

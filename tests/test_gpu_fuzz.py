@@ -2,7 +2,8 @@
 
 Each case draws a workload kind, tile width, M (ragged where the layout
 allows), N, K, wave width, band height and wave-group partition, and for the
-All-to-All layer the token count, experts and ranks, from one fixed seed;
+All-to-All layer the token count, experts and ranks, and the band order
+(forward or serpentine), from one fixed seed;
 the cases rotate through the separate kernels, the fused kernel and the
 direct consumer+reorder.  Every table, reorder and consumer output must be
 bit-exact, the GEMM within the tolerance, as in the hand-picked cases.
@@ -28,7 +29,7 @@ def _case(i):
     tile_n = int(rng.choice([128, 256]))
     kw = dict(N=tile_n * int(rng.integers(1, 7)), K=64 * int(rng.integers(1, 9)),
               tile_n=tile_n, wave_width=int(rng.integers(1, 25)),
-              swizzle=int(rng.integers(1, 10)))
+              swizzle=int(rng.integers(1, 10)), serpentine=bool(rng.integers(0, 2)))
     if kind in ("wave_pattern", "allreduce"):
         w = W.scaled(W.WORKLOADS[kind], M=int(rng.integers(1, 1600)), **kw)
     elif kind == "reducescatter":
@@ -61,7 +62,8 @@ def test_random_shape(i):
                          wave_width=w.wave_width, layout=w.layout, n_dest=w.n_dest,
                          expert_rows=inp.expert_rows if w.grouped else None,
                          row_token=inp.row_token, row_slot=inp.row_slot, host_only=True,
-                         pad_expert_tile_rows=w.pad_expert_tile_rows)
+                         pad_expert_tile_rows=w.pad_expert_tile_rows,
+                         band_order=fo.FO_BAND_SERPENTINE if w.serpentine else fo.FO_BAND_FORWARD)
     _, T = fo.fo_wave_count(probe)
     pipe = Pipeline(w, inp, partition=_partition(rng, T))
     try:

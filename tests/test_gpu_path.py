@@ -267,3 +267,32 @@ def test_gemm_resets_the_counting_table():
             check_run(pipe, inp, res)
     finally:
         pipe.close()
+
+
+@pytest.mark.parametrize("mode", [True, "direct"])
+@pytest.mark.parametrize("name,kw", [
+    ("allreduce", dict(M=1024, N=1024, K=256, wave_width=6)),
+    ("reducescatter", dict(M=1024, N=512, K=192, wave_width=7)),
+    ("alltoall", dict(M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5, wave_width=8)),
+])
+def test_paced_consumer(name, kw, mode):
+    """fo_plan_set_pacing: with only a few consumer CTAs working while the
+    GEMM runs (the rest joining at the last group's flag), every output is
+    still the oracle's, bit for bit, over repeated steps."""
+    w = _small(name, **kw)
+    inp = W.make_inputs(w)
+    pipe = Pipeline(w, inp)
+    try:
+        for pace in (1, 3, 40):
+            fo.fo_plan_set_pacing(pipe.plan, pace)
+            if mode == "direct":
+                fill_comm_sentinel(pipe)
+            for f in pipe.buf.final:
+                f.zero_()
+            for _ in range(3):
+                pipe.step(**step_mode(mode))
+            check_run(pipe, inp, pipe.results(), direct=mode == "direct")
+        with pytest.raises(fo.FoError):
+            fo.fo_plan_set_pacing(pipe.plan, -1)
+    finally:
+        pipe.close()

@@ -51,6 +51,18 @@ CASES = {
     "a2a_padded_pairs": ("alltoall", dict(M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5,
                                           wave_width=8, pad_expert_tile_rows=True),
                          dict(gemm_variant=fo.FO_GEMM_PAIRS)),
+    # the serpentine band order: odd bands walk their columns right to left
+    "serp_tile_pairs": ("allreduce", dict(M=1024, N=1024, K=256, wave_width=6, swizzle=2,
+                                          serpentine=True),
+                        dict(gemm_variant=fo.FO_GEMM_PAIRS)),
+    "serp_tile_single": ("wave_pattern", dict(M=640, N=768, K=128, wave_width=7, swizzle=2,
+                                              serpentine=True), {}),
+    "serp_rs_subtile": ("reducescatter", dict(M=1024, N=768, K=192, wave_width=6, swizzle=3,
+                                              serpentine=True), {}),
+    "serp_a2a_padded_pairs": ("alltoall", dict(M=2 * 700, N=768, K=256, n_tokens=700,
+                                               n_experts=5, wave_width=8, swizzle=2,
+                                               pad_expert_tile_rows=True, serpentine=True),
+                              dict(gemm_variant=fo.FO_GEMM_PAIRS)),
 }
 
 
@@ -77,14 +89,14 @@ def test_exact_placement(case, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("pad", [False, True])
-def test_exact_placement_device_routing(mode, pad):
+@pytest.mark.parametrize("pad,serp", [(False, False), (True, False), (True, True)])
+def test_exact_placement_device_routing(mode, pad, serp):
     """A routing rebuilt on the device (fo_plan_route): the GEMM stores each
     sub-token to the place the device tables give, bit for bit as the oracle
     places it for that routing; with padded and unpadded expert grids."""
     w = W.scaled(W.WORKLOADS["alltoall_dynamic"], M=5 * 384, N=768, K=256, n_tokens=700,
-                 n_experts=5, capacity=384, wave_width=8, swizzle=3,
-                 pad_expert_tile_rows=pad)
+                 n_experts=5, capacity=384, wave_width=8, swizzle=2,
+                 pad_expert_tile_rows=pad, serpentine=serp)
     inp = exact_inputs(w)
     pipe = Pipeline(w, inp)
     try:

@@ -47,7 +47,8 @@ def _host_tables(w, inp, partition):
                         wave_width=w.wave_width, group_waves=partition, layout=w.layout,
                         n_dest=w.n_dest, expert_rows=inp.expert_rows,
                         row_token=inp.row_token, row_slot=inp.row_slot, host_only=True,
-                        pad_expert_tile_rows=w.pad_expert_tile_rows)
+                        pad_expert_tile_rows=w.pad_expert_tile_rows,
+                        band_order=fo.FO_BAND_SERPENTINE if w.serpentine else fo.FO_BAND_FORWARD)
     plan = fo.fo_plan_groups(desc)
     try:
         return {t: fo.fo_plan_table(plan, t) for t in _TABLES}

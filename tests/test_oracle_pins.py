@@ -141,6 +141,24 @@ def test_swizzle_reading_worked_grid():
     assert P.launch_order(3, 2, 8) == [(0, 0), (1, 0), (2, 0), (0, 1), (1, 1), (2, 1)]
 
 
+def test_serpentine_launch_order():
+    """The serpentine band order (a plan input): the second band of a 5 x 3
+    grid in bands of 2 walks its columns right to left, the third left to
+    right again; every tile is launched once, a band's tiles stay
+    consecutive, and vertical neighbours stay in consecutive slots."""
+    got = P.launch_order(5, 3, 2, serpentine=True)
+    assert got == [(0, 0), (1, 0), (0, 1), (1, 1), (0, 2), (1, 2),
+                   (2, 2), (3, 2), (2, 1), (3, 1), (2, 0), (3, 0),
+                   (4, 0), (4, 1), (4, 2)]
+    fwd = P.launch_order(5, 3, 2)
+    assert sorted(got) == sorted(fwd) and len(set(got)) == 15
+    for a, b in zip(range(0, 12, 2), range(1, 12, 2)):
+        (ra, ca), (rb, cb) = got[a], got[b]
+        assert ca == cb and rb == ra + 1
+    # one band: the same order as the forward one (the worked example)
+    assert P.launch_order(2, 4, 2, serpentine=True) == P.launch_order(2, 4, 2)
+
+
 @pytest.mark.parametrize("tm,tn,S,W", [(3, 5, 2, 4), (4, 4, 8, 3), (5, 3, 3, 7),
                                        (2, 4, 2, 2), (7, 2, 4, 5)])
 def test_every_partition_brute_force(tm, tn, S, W):

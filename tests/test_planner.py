@@ -42,19 +42,21 @@ def _oracle_places(op, layout, tok, sl):
 
 
 def _compare(expert_rows, N, K, tile_n, S, Wd, layout, R=1, tok=None, sl=None,
-             partition=None, pad=False):
+             partition=None, pad=False, serp=False):
     M = int(sum(expert_rows))
     grouped = tok is not None or len(expert_rows) > 1
     args = dict(M=M, N=N, K=K, tile_n=tile_n, swizzle=S, wave_width=Wd, layout=layout,
                 n_dest=R, expert_rows=list(expert_rows) if grouped else None,
-                row_token=tok, row_slot=sl, host_only=True, pad_expert_tile_rows=pad)
+                row_token=tok, row_slot=sl, host_only=True, pad_expert_tile_rows=pad,
+                band_order=fo.FO_BAND_SERPENTINE if serp else fo.FO_BAND_FORWARD)
     tiles, T = fo.fo_wave_count(fo.make_desc(**args))
     if partition is None:
         partition = OP.one_then_two(OP.wave_count(tiles, Wd))
     plan = fo.fo_plan_groups(fo.make_desc(**args, group_waves=partition))
     try:
         op = OP.build_plan(list(expert_rows), N, K, 128, tile_n, S, Wd, partition,
-                           _LAYOUT_NAME[layout], R, tok, sl, pad_expert_tile_rows=pad)
+                           _LAYOUT_NAME[layout], R, tok, sl, pad_expert_tile_rows=pad,
+                           serpentine=serp)
         assert (tiles, T) == (op.tiles, op.waves)
         t, waves, gt, t2s = fo.fo_plan_info(plan)
         assert (t, waves) == (op.tiles, op.waves)
@@ -189,3 +191,37 @@ def test_padding_is_an_all_to_all_option():
     with pytest.raises(ValueError):
         OP.build_plan([384], 512, 64, 128, 256, 2, 4, (1, 1), OP.LAYOUT_TILE,
                       pad_expert_tile_rows=True)
+
+
+@pytest.mark.parametrize("tm,tn,S,Wd", [(5, 3, 2, 4), (4, 4, 1, 3), (7, 2, 3, 6)])
+def test_serpentine_tables(tm, tn, S, Wd):
+    """The serpentine band order (odd bands right to left): every table
+    equals the oracle's, for every partition of a small grid, in the tile
+    and ReduceScatter layouts."""
+    T = OP.wave_count(tm * tn, Wd)
+    for part in OP.design_space(T):
+        _compare([tm * 128], tn * 128, 64, 128, S, Wd, fo.FO_LAYOUT_TILE, partition=part,
+                 serp=True)
+        _compare([tm * 128], tn * 128, 64, 128, S, Wd, fo.FO_LAYOUT_RS_SUBTILE, R=4,
+                 partition=part, serp=True)
+
+
+@pytest.mark.parametrize("pad", [False, True])
+def test_serpentine_a2a_tables(pad):
+    rng = np.random.default_rng(4)
+    n_tok, E, k, D = 500, 4, 2, 8
+    picks = np.argsort(rng.random((n_tok, E)), axis=1)[:, :k]
+    tok = np.repeat(np.arange(n_tok), k)
+    sl = np.tile(np.arange(k), n_tok)
+    ex = picks.reshape(-1)
+    order = np.lexsort((sl, tok, ex))
+    er = np.bincount(ex, minlength=E).tolist()
+    _compare(er, 768, 64, 256, 2, 6, fo.FO_LAYOUT_A2A_SUBTOKEN, D, tok[order], sl[order],
+             pad=pad, serp=True)
+
+
+@pytest.mark.parametrize("name", ["wave_pattern", "allreduce", "reducescatter"])
+def test_serpentine_workload_tables(name):
+    w = W.WORKLOADS[name]
+    _compare([w.M], w.N, w.K, w.tile_n, w.swizzle, w.wave_width, w.layout, w.n_dest,
+             serp=True)
