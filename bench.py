@@ -87,6 +87,10 @@ def parse():
                     choices=["workload", "forward", "serpentine"],
                     help="column order inside the launch order's bands (default: each "
                          "workload's own)")
+    ap.add_argument("--partition", default="workload", choices=["workload", "tuned"],
+                    help="the headline's wave-group partition: the workload's own (one wave, "
+                         "then groups of two) or Algorithm 1's with the interference factors, "
+                         "tuned in this run before the timed steps")
     ap.add_argument("--ncu-gemm", action="store_true",
                     help="only GEMM launches (warm-up + --steps), for ncu captures")
     ap.add_argument("--experts", type=int, default=0,
@@ -722,6 +726,16 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    # --partition tuned: Algorithm 1 (with the interference factors) picks the
+    # headline's partition, its offline inputs measured here first
+    pre_tuned = None
+    if args.partition == "tuned":
+        b.warm()
+        ms_g = statistics.mean(b.timed(lambda: pipe.gemm(s, pipe.epoch)))
+        pre_tuned = tune_partition(w, inp, ms_gemm_for_tuning=ms_g, partition=pipe.partition,
+                                   steps=max(10, args.steps // 2))
+        pipe.replan(pre_tuned["partition_interference"])
+
     # warm-up (also the first correctness evidence: status and counting table)
     b.warm()
 
@@ -734,10 +748,12 @@ def run_ours(args):
     status_ok = int(pipe.buf.status.item()) == 0
 
     # every overlapped variant: separate kernels, fused, fused direct
-    t_var = {}
+    t_var, clk_var = {}, {}
     for name, kw in (("separate", dict(fused=False)), ("fused", dict(fused=True)),
                      ("direct", dict(fused=True, direct=True))):
-        t_var[name] = b.timed(lambda: b.step(overlap=True, sync_current=False, **kw))
+        with Clocks(local) as c_:
+            t_var[name] = b.timed(lambda: b.step(overlap=True, sync_current=False, **kw))
+        clk_var[name] = c_.summary()
     # serial = the same kernels as the overlapped step, the consumer as an
     # ordinary launch after the GEMM; and the separate kernels serially
     t_ser = b.timed(lambda: b.step(overlap=False, sync_current=False, fused=fused,
@@ -752,6 +768,20 @@ def run_ours(args):
     ms_gemm_local = statistics.mean(t_gemm)
     rec = b.record(ms_ov, statistics.mean(t_ser), ms_gemm_local, clk.summary())
 
+    # the overlapped step again after about a second of back-to-back steps:
+    # the power-limited steady state of a long run
+    n_hot = max(args.steps, int(1000.0 / max(ms_ov, 1e-3)))
+    for _ in range(n_hot):
+        b.ovl()
+    with Clocks(local) as clk_hot:
+        t_hot = b.timed(b.ovl)
+    sustained = {"ms_overlapped_step": statistics.mean(t_hot),
+                 "value_tflops": flops / (statistics.mean(t_hot) * 1e-3) / 1e12,
+                 "steps_before": n_hot, "clocks": clk_hot.summary(),
+                 "note": "the same overlapped step timed after about 1 s of back-to-back "
+                         "steps (no flush between them); the headline is timed after the "
+                         "warm-up"}
+
     if args.trace_out:
         write_trace(ctx, b, args.trace_out)
 
@@ -763,7 +793,7 @@ def run_ours(args):
     # own, alternating.  Reported beside the headline, which keeps the
     # workload's partition.
     tuned = None
-    if not args.no_tune:
+    if not args.no_tune and pre_tuned is None:
         try:
             tuned = tune_partition(w, inp, ms_gemm_for_tuning=ms_gemm_local,
                                    partition=pipe.partition, steps=max(10, args.steps // 2))
@@ -812,6 +842,10 @@ def run_ours(args):
             "overlapped_step_kernels": kernels,
             "ms_overlapped_step_median": statistics.median(t_ov),
             "ms_overlapped_step_by_kernels": {k: statistics.mean(v) for k, v in t_var.items()},
+            "clocks_by_kernels": clk_var,
+            "sustained": sustained,
+            "partition_mode": args.partition,
+            "partition_tuned_before_timing": pre_tuned,
             "ms_serial_step_separate_kernels": statistics.mean(t_ser_sep),
             "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
             "gemm_frac_of_sustained": gemm_tflops / peak_sust,
@@ -1041,10 +1075,14 @@ def measure_e2e(ctx, b, args):
 
 def tune_partition(w, inp, ms_gemm_for_tuning, partition, steps):
     """The pages' predictive search (Algorithm 1) for this workload, with its
-    offline inputs measured here: the GEMM alone (this run) and the direct
-    consumer's in-kernel latency for first groups of sampled sizes.  Returns
-    the tuned partition, its prediction, and the measured overlapped steps
-    (median, L2 flushed) of the tuned and the workload's partitions."""
+    offline inputs measured here: the GEMM alone (this run), the direct
+    consumer's in-kernel latency for first groups of sampled sizes, and the
+    interference factors (the GEMM's slowdown beside the consumer and the
+    consumer's beside the GEMM, from traced steps with the workload's
+    partition).  Returns the tuned partitions with and without the
+    interference factors, their predictions, and the measured overlapped
+    steps (median, L2 flushed) of the tuned and the workload's partitions,
+    alternated."""
     from communication_overlap_gb300 import fo
     from communication_overlap_gb300.tuning import Tuner, sample_waves
     t = Tuner(w, inp, reps=10)
@@ -1052,20 +1090,36 @@ def tune_partition(w, inp, ms_gemm_for_tuning, partition, steps):
         gemm_us = ms_gemm_for_tuning * 1e3
         waves = sample_waves(t.pipe.waves)
         curve = t.curve(waves)
+        sigma, rho = t.interference(gemm_us, partition)
         parts, pred = fo.fo_tune_partition(t.desc(), gemm_us, curve)
+        parts_i, pred_i = fo.fo_tune_partition(t.desc(), gemm_us, curve, sigma, rho)
         t.reps = steps
-        meas = {"tuned": [], "workload": []}
-        for _ in range(2):      # alternate, to share drift between the two
-            meas["tuned"].append(t.step_us(parts))
-            meas["workload"].append(t.step_us(partition))
-        return {"partition": parts, "predicted_us": pred,
-                "predicted_us_workload_partition":
-                    fo.fo_predict_partition(t.desc(partition), gemm_us, curve),
-                "ms_step": statistics.median(meas["tuned"]) / 1e3,
-                "ms_step_workload_partition": statistics.median(meas["workload"]) / 1e3,
+        cands = {"tuned": parts, "tuned_interference": parts_i, "workload": partition}
+        meas = {k: [] for k in cands}
+        for _ in range(2):      # alternate, to share drift between them
+            for k, c in cands.items():
+                meas[k].append(t.step_us(c))
+        ms = {k: statistics.median(v) / 1e3 for k, v in meas.items()}
+        pw = fo.fo_predict_partition(t.desc(partition), gemm_us, curve)
+        pw_i = fo.fo_predict_partition(t.desc(partition), gemm_us, curve, sigma, rho)
+        return {"partition": parts, "predicted_us": pred, "ms_step": ms["tuned"],
+                "gemm_slowdown": sigma, "comm_slowdown": rho,
+                "partition_interference": parts_i, "predicted_interference_us": pred_i,
+                "ms_step_interference": ms["tuned_interference"],
+                "ms_step_workload_partition": ms["workload"],
+                "predicted_us_workload_partition": pw,
+                "predicted_interference_us_workload_partition": pw_i,
+                "prediction_error_workload_partition": pw / (ms["workload"] * 1e3) - 1.0,
+                "prediction_error_tuned": pred / (ms["tuned"] * 1e3) - 1.0,
+                "prediction_error_interference_tuned":
+                    pred_i / (ms["tuned_interference"] * 1e3) - 1.0,
+                "interference_fit": "comm_slowdown fitted on the workload partition's "
+                                    "measured step; the tuned partitions' steps are "
+                                    "predictions",
                 "curve_group_waves": waves,
-                "note": "Algorithm 1 with offline inputs measured in this run; the headline "
-                        "keeps the workload's partition"}
+                "note": "Algorithm 1 with offline inputs measured in this run, without and "
+                        "with the interference factors; the headline keeps the workload's "
+                        "partition unless --partition tuned"}
     finally:
         t.close()
 

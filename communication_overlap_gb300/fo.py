@@ -94,6 +94,13 @@ def lib():
             "fo_tune_partition": (ctypes.c_int, [ctypes.POINTER(fo_plan_desc), ctypes.c_double,
                                                  _dp, _dp, ctypes.c_int32, _i32p,
                                                  ctypes.c_int32, _i32p, _dp]),
+            "fo_predict_partition_ex": (ctypes.c_int, [ctypes.POINTER(fo_plan_desc),
+                                                       ctypes.c_double, _dp, _dp, ctypes.c_int32,
+                                                       ctypes.c_double, ctypes.c_double, _dp]),
+            "fo_tune_partition_ex": (ctypes.c_int, [ctypes.POINTER(fo_plan_desc), ctypes.c_double,
+                                                    _dp, _dp, ctypes.c_int32, ctypes.c_double,
+                                                    ctypes.c_double, _i32p, ctypes.c_int32,
+                                                    _i32p, _dp]),
             "fo_reorder_back_fused": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, _vpp,
                                                      _vpp, _vp, ctypes.c_int, _vp]),
             "fo_consume_reorder": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int, _vp, _vpp,
@@ -316,26 +323,57 @@ def _curve(curve):
     return b, t, len(pts)
 
 
-def fo_predict_partition(desc, gemm_us, curve):
-    """curve: [(bytes, us), ...]; desc carries the partition."""
+def _factor(x):
+    """An interference factor as passed to the library (None: 1)."""
+    return 1.0 if x is None else float(x)
+
+
+def fo_predict_partition(desc, gemm_us, curve, gemm_slowdown=None, comm_slowdown=None):
+    """curve: [(bytes, us), ...]; desc carries the partition.  With either
+    slowdown given, the interference model (fo_predict_partition_ex)."""
     b, t, n = _curve(curve)
     out = ctypes.c_double()
-    _check("fo_predict_partition",
-           lib().fo_predict_partition(ctypes.byref(desc), gemm_us, b, t, n, ctypes.byref(out)))
+    if gemm_slowdown is None and comm_slowdown is None:
+        _check("fo_predict_partition",
+               lib().fo_predict_partition(ctypes.byref(desc), gemm_us, b, t, n,
+                                          ctypes.byref(out)))
+    else:
+        _check("fo_predict_partition_ex",
+               lib().fo_predict_partition_ex(ctypes.byref(desc), gemm_us, b, t, n,
+                                             _factor(gemm_slowdown), _factor(comm_slowdown),
+                                             ctypes.byref(out)))
     return out.value
 
 
-def fo_tune_partition(desc, gemm_us, curve):
-    """Returns (waves per group, predicted us)."""
+def fo_tune_partition(desc, gemm_us, curve, gemm_slowdown=None, comm_slowdown=None):
+    """Returns (waves per group, predicted us).  With either slowdown given,
+    the interference model (fo_tune_partition_ex)."""
     b, t, n = _curve(curve)
     _, T = fo_wave_count(desc)
     parts = (ctypes.c_int32 * max(1, T))()
     ng = ctypes.c_int32()
     out = ctypes.c_double()
-    _check("fo_tune_partition",
-           lib().fo_tune_partition(ctypes.byref(desc), gemm_us, b, t, n, parts, T,
-                                   ctypes.byref(ng), ctypes.byref(out)))
+    if gemm_slowdown is None and comm_slowdown is None:
+        _check("fo_tune_partition",
+               lib().fo_tune_partition(ctypes.byref(desc), gemm_us, b, t, n, parts, T,
+                                       ctypes.byref(ng), ctypes.byref(out)))
+    else:
+        _check("fo_tune_partition_ex",
+               lib().fo_tune_partition_ex(ctypes.byref(desc), gemm_us, b, t, n,
+                                          _factor(gemm_slowdown), _factor(comm_slowdown), parts,
+                                          T, ctypes.byref(ng), ctypes.byref(out)))
     return list(parts)[:ng.value], out.value
+
+
+def fo_predict_partition_ex(desc, gemm_us, curve, gemm_slowdown, comm_slowdown):
+    """Algorithm 1's prediction with the interference factors."""
+    return fo_predict_partition(desc, gemm_us, curve, gemm_slowdown, comm_slowdown)
+
+
+def fo_tune_partition_ex(desc, gemm_us, curve, gemm_slowdown, comm_slowdown):
+    """The exact search with the interference factors: (waves per group,
+    predicted us)."""
+    return fo_tune_partition(desc, gemm_us, curve, gemm_slowdown, comm_slowdown)
 
 
 def partition_one_then_two(T):

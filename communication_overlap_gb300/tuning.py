@@ -15,8 +15,18 @@ Offline ([P1] "FlashOverlap: 信号驱动计算通信重叠论文详解", 四、
   * SM contention: W = the GEMM's persistent CTAs, fixed by the workload.
 Online: fo_tune_partition (exact over all 2^(T-1) candidates).
 
+Interference (one GPU: the GEMM and the consumer share memory and SMs and
+slow each other while both run), from the workload's own partition:
+  * gemm_slowdown: the GEMM's in-kernel duration in the overlapped step
+    over its duration alone (per-tile stamps);
+  * comm_slowdown: fitted so that the model reproduces that partition's
+    measured step (one calibration point; every other candidate is a
+    prediction).
+fo_tune_partition_ex / fo_predict_partition_ex take both.
+
 --validate runs the overlapped step for every candidate partition (T <= 8)
-and reports how the predicted best compares with the measured best.
+and reports how the predicted best compares with the measured best, with
+and without the interference factors.
 """
 import argparse
 import json
@@ -125,7 +135,60 @@ class Tuner:
                 spans.append(float(ran[:, 2].max() - ran[:, 1].min()) / 1e3)
             fo.fo_plan_set_trace(p.plan, 0, 0)
             pts.append((float(p.group_tiles[0] * self.tile_bytes), statistics.median(spans)))
+        self.last_curve = pts
         return pts
+
+    def interference(self, gemm_us, partition=None, reps=5):
+        """(gemm_slowdown, comm_slowdown) for the interference model, from
+        `partition` (default: the workload's one wave then groups of two):
+        gemm_slowdown is the GEMM's in-kernel duration inside the
+        overlapped step over its duration alone (per-tile stamps, median of
+        `reps`); comm_slowdown is then fitted (bisection) so that the
+        model, with this run's GEMM time `gemm_us` and latency curve (call
+        self.curve first), reproduces that partition's measured step."""
+        p = self.pipe
+        part = list(partition or fo.partition_one_then_two(p.waves))
+        p.replan(part)
+        kw = dict(fused=True, direct=True) if self.direct else {}
+        for _ in range(3):
+            p.step(overlap=True, **kw)
+        torch.cuda.synchronize()
+        W = p.desc_args["wave_width"]
+        trace = torch.zeros(p.tiles + 3 * W, dtype=torch.int64, device=p.device)
+        fo.fo_plan_set_trace(p.plan, trace.data_ptr())
+
+        def span():
+            st = trace.cpu()
+            return float(st[:p.tiles].max() - st[p.tiles:p.tiles + min(W, p.tiles)].min())
+        sig = []
+        for _ in range(reps):
+            self.flush()
+            p.gemm(p.s0, p.epoch)
+            torch.cuda.synchronize()
+            alone = span()
+            self.flush()
+            p.step(overlap=True, **kw)
+            torch.cuda.synchronize()
+            sig.append(span() / alone)
+        fo.fo_plan_set_trace(p.plan, 0)
+        sigma = statistics.median(sig)
+        measured = self.step_us(part)
+        desc = self.desc(part)
+
+        def pred(rho):
+            return fo.fo_predict_partition(desc, gemm_us, self.last_curve, sigma, rho)
+        lo, hi = 0.25, 8.0
+        if pred(lo) >= measured:
+            return sigma, lo
+        if pred(hi) <= measured:
+            return sigma, hi
+        for _ in range(50):
+            mid = 0.5 * (lo + hi)
+            if pred(mid) > measured:
+                hi = mid
+            else:
+                lo = mid
+        return sigma, 0.5 * (lo + hi)
 
     def step_us(self, partition):
         p = self.pipe
@@ -148,30 +211,50 @@ def run(name, validate=False, reps=20, kernels="direct"):
     try:
         gemm = t.gemm_us()
         curve = t.curve()
+        sigma, rho = t.interference(gemm)
         best, pred = fo.fo_tune_partition(t.desc(), gemm, curve)
+        best_i, pred_i = fo.fo_tune_partition(t.desc(), gemm, curve, sigma, rho)
         out = {"workload": name, "kernels": kernels, "waves": t.pipe.waves, "gemm_us": gemm,
-               "curve": curve, "tuned": best, "tuned_predicted_us": pred}
+               "curve": curve, "gemm_slowdown": sigma, "comm_slowdown": rho,
+               "tuned": best, "tuned_predicted_us": pred,
+               "tuned_interference": best_i, "tuned_interference_predicted_us": pred_i}
         base = fo.partition_one_then_two(t.pipe.waves)
         out["one_then_two_predicted_us"] = fo.fo_predict_partition(t.desc(base), gemm, curve)
+        out["one_then_two_predicted_interference_us"] = fo.fo_predict_partition(
+            t.desc(base), gemm, curve, sigma, rho)
         if validate:
             rows = []
             for cand in _design_space(t.pipe.waves):
                 rows.append({"partition": cand,
                              "predicted_us": fo.fo_predict_partition(t.desc(cand), gemm, curve),
+                             "predicted_interference_us": fo.fo_predict_partition(
+                                 t.desc(cand), gemm, curve, sigma, rho),
                              "measured_us": t.step_us(cand)})
             meas_best = min(rows, key=lambda r: r["measured_us"])
-            tuned_meas = next(r for r in rows if r["partition"] == best)["measured_us"]
-            finest = next(r for r in rows if r["partition"] == [1] * t.pipe.waves)
-            coarsest = next(r for r in rows if r["partition"] == [t.pipe.waves])
+            by_part = {tuple(r["partition"]): r for r in rows}
+            tuned_meas = by_part[tuple(best)]["measured_us"]
+            tuned_i_meas = by_part[tuple(best_i)]["measured_us"]
+            finest = by_part[tuple([1] * t.pipe.waves)]
+            coarsest = by_part[(t.pipe.waves,)]
+            ranked = sorted(r["measured_us"] for r in rows)
+
+            def err(key):
+                e = [abs(r[key] / r["measured_us"] - 1.0) for r in rows]
+                return {"mean": statistics.mean(e), "max": max(e)}
             out.update({
                 "candidates": len(rows),
                 "measured_best": meas_best,
                 "tuned_measured_us": tuned_meas,
                 "tuned_regret": tuned_meas / meas_best["measured_us"] - 1.0,
+                "rank_of_tuned": 1 + ranked.index(tuned_meas),
+                "tuned_interference_measured_us": tuned_i_meas,
+                "tuned_interference_regret": tuned_i_meas / meas_best["measured_us"] - 1.0,
+                "rank_of_tuned_interference": 1 + ranked.index(tuned_i_meas),
+                "prediction_error": err("predicted_us"),
+                "prediction_error_interference": err("predicted_interference_us"),
                 "finest_measured_us": finest["measured_us"],
                 "finest_loss": finest["measured_us"] / meas_best["measured_us"] - 1.0,
                 "coarsest_measured_us": coarsest["measured_us"],
-                "rank_of_tuned": 1 + sorted(r["measured_us"] for r in rows).index(tuned_meas),
                 "all": rows,
             })
         return out

@@ -456,6 +456,32 @@ fo_status fo_tune_partition(const fo_plan_desc* desc, double gemm_us,
                             int32_t n_points, int32_t* group_waves, int32_t capacity,
                             int32_t* n_groups, double* predicted_us);
 
+/* The same two calls with the interference of one GPU, where the GEMM and
+ * the consumer share memory and SMs and each slows the other while both run
+ * (the pages' model has them on separate hardware; this is a reading for
+ * one GPU, not the pages'):
+ *  gemm_slowdown (sigma > 0): while a communication runs, the GEMM advances
+ *      at 1 / sigma of its rate (gemm_us / T per wave alone);
+ *  comm_slowdown (rho > 0): while the GEMM runs, a communication advances at
+ *      1 / rho of the curve's rate.
+ * A group's communication starts once its waves are computed and the
+ * previous one has ended; the schedule is simulated event by event.
+ * sigma = rho = 1 gives fo_predict_partition / fo_tune_partition exactly.
+ * With other factors the search is exhaustive (all 2^(T-1) candidates, the
+ * first on ties) up to T = 20 waves; beyond it, a local search: single cuts
+ * toggled while the prediction falls, from the best of the exact plain
+ * optimum, the finest partition and one wave then groups of two.  Factors
+ * that are not finite and positive are FO_ERR_ARG. */
+fo_status fo_predict_partition_ex(const fo_plan_desc* desc, double gemm_us,
+                                  const double* curve_bytes, const double* curve_us,
+                                  int32_t n_points, double gemm_slowdown,
+                                  double comm_slowdown, double* predicted_us);
+fo_status fo_tune_partition_ex(const fo_plan_desc* desc, double gemm_us,
+                               const double* curve_bytes, const double* curve_us,
+                               int32_t n_points, double gemm_slowdown, double comm_slowdown,
+                               int32_t* group_waves, int32_t capacity, int32_t* n_groups,
+                               double* predicted_us);
+
 /* Element-wise epilogue fused into the post-communication pass ([P1] 五
  * "Epilogue 集成": ReLU, SiLU and bias addition usually run in the GEMM's
  * epilogue; FlashOverlap fuses the post-communication reorder with them).

@@ -25,6 +25,18 @@ Curve interpolation: piecewise linear in bytes between the samples (sorted
 by size); below the smallest sample its latency (a fixed floor); above the
 largest, the slope of the last two samples.  Candidates: all 2**(T-1)
 partitions, enumerated by ``plan.design_space``.
+
+Interference (not in the pages, whose compute and communication run on
+separate hardware): on one GPU the GEMM and the consumer share memory and
+SMs, so each slows the other while both run (reading R19).  Two measured
+factors: while a communication runs, the GEMM advances at 1 / sigma of its
+alone rate (gemm_slowdown); while the GEMM runs, a communication advances at
+1 / rho of the curve's rate (comm_slowdown).  A group's communication still
+starts once its own waves are computed and the previous group's
+communication has ended; everything else is the pages' loop.  The schedule
+is simulated event by event (wave completions and communication ends), with
+both rates constant between events.  With sigma = rho = 1 the events give
+back the pages' recurrence exactly.
 """
 from . import plan as P
 
@@ -53,26 +65,67 @@ def group_bytes(partition, wave_width, tiles, tile_bytes):
     return out
 
 
-def predict(partition, duration, curve, wave_width, tiles, tile_bytes):
-    """Predicted latency of one candidate, following Algorithm 1's loop."""
+def predict(partition, duration, curve, wave_width, tiles, tile_bytes,
+            gemm_slowdown=1.0, comm_slowdown=1.0):
+    """Predicted latency of one candidate: Algorithm 1's loop, with the
+    mutual slowdown of the module doc when a factor is not 1."""
     T = sum(partition)
     sizes = group_bytes(partition, wave_width, tiles, tile_bytes)
-    t_acc_p = 0.0
-    t_acc_m = 0.0
-    for g, nbytes in zip(partition, sizes):
-        t_p = duration / T * g
-        t_m = interp_latency(curve, nbytes)
-        t_acc_p = t_acc_p + t_p                  # this group's compute is done
-        t_acc_m = max(t_acc_p, t_acc_m) + t_m    # then its communication runs
-    return t_acc_m
+    if gemm_slowdown == 1.0 and comm_slowdown == 1.0:
+        t_acc_p = 0.0
+        t_acc_m = 0.0
+        for g, nbytes in zip(partition, sizes):
+            t_p = duration / T * g
+            t_m = interp_latency(curve, nbytes)
+            t_acc_p = t_acc_p + t_p                  # this group's compute is done
+            t_acc_m = max(t_acc_p, t_acc_m) + t_m    # then its communication runs
+        return t_acc_m
+    # event by event: GEMM work done (in alone microseconds), the running
+    # communication's remaining work (in curve microseconds)
+    ready = []                 # GEMM work at which each group is computed
+    w = 0
+    for g in partition:
+        w += g
+        ready.append(duration / T * w)
+    t, gemm_done = 0.0, 0.0
+    j, comm_left = 0, None
+    while True:
+        gemm_on = gemm_done < duration
+        if comm_left is None and j < len(partition) and gemm_done >= ready[j]:
+            comm_left = interp_latency(curve, sizes[j])
+        comm_on = comm_left is not None
+        if not gemm_on and not comm_on:
+            return t
+        gemm_rate = (1.0 / gemm_slowdown if comm_on else 1.0) if gemm_on else 0.0
+        comm_rate = (1.0 / comm_slowdown if gemm_on else 1.0) if comm_on else 0.0
+        dt = float("inf")
+        if gemm_on:            # the next group computed, or the GEMM's end
+            nxt = min([r for r in ready if r > gemm_done] + [duration])
+            dt = (nxt - gemm_done) / gemm_rate
+        if comm_on:
+            dt = min(dt, comm_left / comm_rate)
+        t += dt
+        if gemm_on:
+            gemm_done = min(duration, gemm_done + gemm_rate * dt)
+            # snap to a boundary reached within rounding
+            for r in ready + [duration]:
+                if abs(gemm_done - r) <= 1e-9 * max(1.0, duration):
+                    gemm_done = r
+        if comm_on:
+            comm_left -= comm_rate * dt
+            if comm_left <= 1e-9 * max(1.0, duration):
+                comm_left = None
+                j += 1
 
 
-def best_partition(T, duration, curve, wave_width, tiles, tile_bytes):
+def best_partition(T, duration, curve, wave_width, tiles, tile_bytes,
+                   gemm_slowdown=1.0, comm_slowdown=1.0):
     """Algorithm 1's online search: the candidate with the smallest
     prediction (the first one in enumeration order on ties)."""
     best, t_min = None, float("inf")
     for cand in P.design_space(T):
-        t = predict(cand, duration, curve, wave_width, tiles, tile_bytes)
+        t = predict(cand, duration, curve, wave_width, tiles, tile_bytes,
+                    gemm_slowdown, comm_slowdown)
         if t < t_min:
             best, t_min = cand, t
     return best, t_min

@@ -31,3 +31,23 @@ def test_tuner_small_allreduce(kernels):
         check_run(t.pipe, t.inp, res)
     finally:
         t.close()
+
+
+def test_interference_factors_and_tuned_partition():
+    """The measured interference factors are finite and at least 1; the
+    search with them returns a valid partition whose step is exact."""
+    w = W.scaled(W.WORKLOADS["allreduce"], M=1024, N=2048, K=256, wave_width=8)
+    t = Tuner(w, reps=3)
+    try:
+        gemm = t.gemm_us()
+        curve = t.curve()
+        sigma, rho = t.interference(gemm, reps=3)
+        assert 0.9 <= sigma < 10.0 and 0.25 <= rho <= 8.0
+        parts, pred = fo.fo_tune_partition(t.desc(), gemm, curve, sigma, rho)
+        plain = fo.fo_predict_partition(t.desc(parts), gemm, curve)
+        assert sum(parts) == t.pipe.waves and pred > 0
+        t.pipe.replan(parts)
+        t.pipe.step()
+        check_run(t.pipe, t.inp, t.pipe.results())
+    finally:
+        t.close()
