@@ -40,6 +40,9 @@ CASES = {
     # ReduceScatter: subtile k of every tile to rank k; the row-block reading
     "rs_subtile": ("reducescatter", dict(M=1024, N=512, K=192, wave_width=7), {}),
     "rs_subtile_pairs": ("reducescatter", dict(M=1024, N=512, K=256, wave_width=8), {}),
+    # other rank counts: 64-row subtiles (R = 2) and 16-row subtiles (R = 8)
+    "rs_subtile_r2": ("reducescatter", dict(M=1024, N=512, K=128, wave_width=5, n_dest=2), {}),
+    "rs_subtile_r8": ("reducescatter", dict(M=1024, N=768, K=128, wave_width=6, n_dest=8), {}),
     "rs_rowblock": ("reducescatter", dict(M=1024, N=512, K=192, wave_width=3,
                                           layout=W.LAYOUT_RS_ROWBLOCK), {}),
     # All-to-All sub-tokens: unpadded grids (odd W), padded grids as pairs
