@@ -615,10 +615,16 @@ class Bench:
         ms_mm = self.torch_mm()
         gemm_tf = self.flops / (ms_gemm * 1e-3) / 1e12
 
+        floor = ctx["event_floor_ms"]
+
         def bw(nbytes, ms):
             g = nbytes / (ms * 1e-3) / 1e9
-            return {"ms": ms, "gbs": g, "frac_of_measured": g / hbm,
-                    "frac_of_nominal": g / NOMINAL_HBM_GBS}
+            out = {"ms": ms, "gbs": g, "frac_of_measured": g / hbm,
+                   "frac_of_nominal": g / NOMINAL_HBM_GBS}
+            if ms > 2 * floor:   # the kernel's own time: the launch and event floor taken out
+                gk = nbytes / ((ms - floor) * 1e-3) / 1e9
+                out.update({"gbs_floor_removed": gk, "frac_of_measured_floor_removed": gk / hbm})
+            return out
         return {
             "config": workload_name(w),
             "partition": pipe.partition, "groups_tiles": pipe.group_tiles,
@@ -715,6 +721,19 @@ def run_ours(args):
     ctx = dict(torch=torch, fo=fo, dev=dev, local=local, hbm=hbm, peak_burst=peak_burst,
                sm_count=torch.cuda.get_device_properties(dev).multi_processor_count,
                flush=lambda: flush_buf.fill_(1))
+    # the launch and event floor: a one-element kernel timed like every leg
+    # (events on the stream around it, after the flush)
+    tiny = torch.zeros(1, device=dev)
+    s_tiny = torch.cuda.Stream(dev)
+    for _ in range(3):
+        with torch.cuda.stream(s_tiny):
+            tiny.add_(1)
+
+    def one_tiny():
+        with torch.cuda.stream(s_tiny):
+            tiny.add_(1)
+    ctx["event_floor_ms"] = statistics.median(timed(torch, s_tiny, one_tiny, args.steps,
+                                                    ctx["flush"]))
     w = workload(args, args.workload)
     b = Bench(ctx, w, args)
     pipe, s, flops, inp = b.pipe, b.s, b.flops, b.inp
@@ -850,6 +869,7 @@ def run_ours(args):
             "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
             "gemm_frac_of_sustained": gemm_tflops / peak_sust,
             "hbm_peak_gbs": hbm, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+            "event_floor_ms": ctx["event_floor_ms"],
             "nominal_bf16_tflops": NOMINAL_BF16_TFLOPS,
             "status_ok": status_ok,
             "tuned_partition": tuned,

@@ -6,22 +6,20 @@
 // Adaptable Overlapping ...", Figure 5 ("the tiles are reordered back when
 // communication finishes").
 //
-// A CTA moves half a tile (64 rows) at a time through two 32 KB buffers of
-// shared memory using the Tensor Memory Accelerator, so almost no thread
-// time goes into moving bytes, and the next half loads while the current
-// one is stored:
-//  * a half's rows are contiguous in the communication buffer (one run per
-//    destination part), so they arrive with one 1-D bulk copy per run (a
-//    per-row copy for the All-to-All layout, whose rows are spread over the
-//    receive buffers by rank);
-//  * a full half leaves with one 2-D tensor store of a 64 x tile_n box
-//    (min(h, 64)-row boxes per subtile piece for the ReduceScatter layout)
-//    into the row-major output; ragged halves and All-to-All rows leave as
-//    per-row bulk stores.
-// Three CTAs per SM keep ~192 KB per SM in flight; half tiles keep every
-// CTA busy to the end.  Items are handed out in launch order by a counter;
-// launched as the consumer's programmatic dependent, a CTA waits for its
-// item's group to be consumed.
+// A CTA moves one tile at a time through 64 KB of shared memory using the
+// Tensor Memory Accelerator, so almost no thread time goes into moving
+// bytes:
+//  * the tile's rows are contiguous in the communication buffer (one run
+//    per destination part), so they arrive with one 1-D bulk copy per run
+//    (a per-row copy for the All-to-All layout, whose rows are spread over
+//    the receive buffers by rank);
+//  * a full tile leaves with one 2-D tensor store of a 128 x tile_n box (a
+//    32-row box per subtile for the ReduceScatter layout) into the
+//    row-major output; ragged tiles and All-to-All rows leave as per-row
+//    512-byte bulk stores.
+// Three CTAs per SM keep ~192 KB per SM in flight.  Tiles are handed out in
+// launch order by a counter; launched as the consumer's programmatic
+// dependent, a CTA waits for its tile's group to be consumed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -36,9 +34,8 @@ namespace fo {
 namespace {
 
 constexpr int kRThreads = kTileM;                  // one thread per tile row
-constexpr int kRHalfRows = kTileM / 2;             // rows of a work item (half a tile)
-constexpr int kRHalfBytes = kRHalfRows * 256 * 2;  // a half 128 x 256 bf16 tile
-constexpr int kRSmem = 1024 + 2 * kRHalfBytes + 64;  // alignment slack, 2 buffers, barriers
+constexpr int kRTileBytes = kTileM * 256 * 2;      // a full 128 x 256 bf16 tile
+constexpr int kRSmem = 1024 + kRTileBytes + 64;    // alignment slack, tile, barrier
 constexpr uint64_t kRWaitLimitNs = 1000000000ull;  // 1 s per wait
 
 struct ReorderArgs {
@@ -49,8 +46,8 @@ struct ReorderArgs {
   int32_t* status;
   const uint16_t* bias;   // optional bf16[N] added before the activation
   int32_t act;            // fo_activation
-  int32_t unit_bytes, row_bytes, slot0, n_slots, box_rows;
-  int32_t* counters;         // [0] next item, [1] CTAs done (reset by the last CTA)
+  int32_t unit_bytes, row_bytes, slot0, n_slots;
+  int32_t* counters;         // [0] next tile, [1] CTAs done (reset by the last CTA)
   uint32_t* consumed;        // non-NULL: wait until consumed[group] == seq
   uint32_t seq;              // the preceding consume launch's number
   int32_t g0, g1;            // the groups this launch covers
@@ -76,239 +73,157 @@ __device__ __forceinline__ bool wait_consumed(const ReorderArgs& a, int32_t grou
   }
 }
 
-// One work item: half `hf` of the tile at slot s, rows [r0, r0 + n) of it.
-struct Item {
-  int32_t s, r0, n;
-  TileInfo ti;
-};
-
-__device__ __forceinline__ Item item_of(const ReorderArgs& a, int32_t t) {
-  Item it;
-  it.s = a.slot0 + (t >> 1);
-  it.ti = a.map.tile[it.s];
-  it.r0 = (t & 1) * kRHalfRows;
-  it.n = max(0, min(kRHalfRows, it.ti.rows - it.r0));
-  return it;
+__device__ __forceinline__ void reorder_row(const ReorderArgs& a, const TileInfo& ti, int32_t s,
+                                            int32_t r, int* k, int32_t* src_unit,
+                                            int32_t* dst_row) {
+  map_row(a.map, ti, s, r, k, src_unit, dst_row);
 }
 
-// Issue the loads of an item into buffer `sb` (completing on barrier
-// `bar`); returns the bytes expected there (0: nothing to move).  All
-// threads call it; the bytes are counted on the barrier by thread 0 before
-// any load is issued.
-__device__ __forceinline__ uint32_t load_item(const ReorderArgs& a, const Item& it, uint32_t sb,
-                                              uint32_t bar, uint64_t pol, int tid) {
-  const int32_t ub = a.unit_bytes;
-  const int lay = a.map.layout;
-  int rk = -1;
-  int32_t rsu = 0, rdr = 0;
-  if (lay == FO_LAYOUT_A2A_SUBTOKEN && tid < it.n)
-    map_row(a.map, it.ti, it.s, it.r0 + tid, &rk, &rsu, &rdr);
-  const int32_t in_rows =
-      lay == FO_LAYOUT_A2A_SUBTOKEN ? __syncthreads_count(rk >= 0) : it.n;
-  if (in_rows == 0) return 0;
-  if (tid == 0) mbar_expect_tx(bar, uint32_t(in_rows * ub));
-  __syncthreads();
-  if (lay == FO_LAYOUT_TILE || lay == FO_LAYOUT_RS_ROWBLOCK) {
-    if (tid == 0) {   // the half's rows are contiguous
-      int k;
-      int32_t su, dr;
-      map_row(a.map, it.ti, it.s, it.r0, &k, &su, &dr);
-      bulk_load_hint(sb, a.src[k] + int64_t(su) * ub, uint32_t(it.n * ub), bar, pol);
-    }
-  } else if (lay == FO_LAYOUT_RS_SUBTILE) {
-    // pieces of box_rows rows, each contiguous in one slice (a subtile or
-    // a half of one)
-    const int32_t br = a.box_rows;
-    if (tid < it.n / br) {
-      int k;
-      int32_t su, dr;
-      map_row(a.map, it.ti, it.s, it.r0 + tid * br, &k, &su, &dr);
-      bulk_load_hint(sb + tid * br * ub, a.src[k] + int64_t(su) * ub, uint32_t(br * ub), bar,
-                     pol);
-    }
-  } else if (rk >= 0) {   // All-to-All: row by row
-    bulk_load_hint(sb + tid * ub, a.src[rk] + int64_t(rsu) * ub, uint32_t(ub), bar, pol);
-  }
-  return uint32_t(in_rows * ub);
-}
-
-// Store an item from buffer `sb` to its final place (one bulk group per
-// issuing thread, committed).
-__device__ __forceinline__ void store_item(const ReorderArgs& a, const Item& it, uint32_t sb,
-                                           int tid) {
-  const int32_t ub = a.unit_bytes;
-  const int lay = a.map.layout;
-  if ((lay == FO_LAYOUT_TILE || lay == FO_LAYOUT_RS_ROWBLOCK) && it.n == kRHalfRows) {
-    if (tid == 0) {
-      int k;
-      int32_t su, dr;
-      map_row(a.map, it.ti, it.s, it.r0, &k, &su, &dr);
-      tensor_store_2d(&a.dst_map[k], sb, it.ti.col0, dr);
-      bulk_commit();
-    }
-  } else if (lay == FO_LAYOUT_RS_SUBTILE) {
-    const int32_t br = a.box_rows;
-    if (tid < it.n / br) {
-      int k;
-      int32_t su, dr;
-      map_row(a.map, it.ti, it.s, it.r0 + tid * br, &k, &su, &dr);
-      tensor_store_2d(&a.dst_map[k], sb + tid * br * ub, it.ti.col0, dr);
-      bulk_commit();
-    }
-  } else if (tid < it.n) {   // All-to-All rows and ragged halves: per row
-    int k;
-    int32_t su, dr;
-    map_row(a.map, it.ti, it.s, it.r0 + tid, &k, &su, &dr);
-    if (k >= 0) {
-      bulk_store(a.dst[k] + int64_t(dr) * a.row_bytes + int64_t(it.ti.col0) * 2,
-                 sb + tid * ub, uint32_t(ub));
-      bulk_commit();
-    }
-  }
-}
-
-// Work items are half tiles, handed out in launch order (a shared counter
-// when waiting on the consumer, else CTA b takes items b, b + grid, ...).
-// Two 32 KB buffers per CTA: the next item's loads are issued before the
-// current item is stored, so a load and a store are in flight together.
 __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constant__ ReorderArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* buf = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(buf + 2 * kRHalfBytes);   // [2]
-  __shared__ int s_ok[2];        // alternating words: no barrier lies between
-                                 // the last read of one and the next write
+  uint64_t* full = reinterpret_cast<uint64_t*>(buf + kRTileBytes);
+  __shared__ int s_ok, s_ready;   // separate words: no barrier lies between
+                                  // the last read of one and the next write
   __shared__ int32_t s_next[2];
   const int tid = threadIdx.x;
-  const uint32_t sbuf = smem_u32(buf);
-  const int32_t n_items = 2 * a.n_slots;
+  const uint32_t sbuf = smem_u32(buf), sfull = smem_u32(full);
+  // overlapped (waiting on the consumer): tiles come from a shared counter
+  // in launch order; otherwise CTA b takes tiles b, b + grid, ...
   const bool dyn = a.consumed != nullptr;
   if (tid == 0) {
-    mbar_init(smem_u32(&full[0]), 1);
-    mbar_init(smem_u32(&full[1]), 1);
+    mbar_init(sfull, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_next[0] = dyn ? atomicAdd(a.counters, 1) : int32_t(blockIdx.x);
   }
   __syncthreads();
+  const int32_t ub = a.unit_bytes;
   const uint64_t pol = l2_evict_first();   // the received data is read once
-  uint32_t phase[2] = {0, 0};
-  uint32_t expect[2] = {0, 0};   // bytes of the item loaded into each buffer (0: none)
-  bool pending[2] = {false, false};   // a load issued into the buffer, not yet waited for
-  int nb = 0;                    // which s_next word holds the current index
-  int b = 0;                     // buffer of the current item
-
-  // Waiting on the consumer, thread 0 waits for item t's group; the whole
-  // CTA sees the verdict (false: the wait ran out).
-  auto fetch = [&](int32_t t, int word) -> bool {
+  uint32_t phase = 0;
+  // thread 0 fetches the next index while the CTA works; with the shared
+  // counter, CTAs that start early -- beside a running GEMM and consumer --
+  // take the groups that finish first
+  for (int nb = 0;; nb ^= 1, phase ^= 1) {
+    const int32_t t = s_next[nb];
+    if (t >= a.n_slots) break;
+    const int32_t s = a.slot0 + t;
+    const TileInfo ti = a.map.tile[s];
     if (tid == 0) {
+      s_next[nb ^ 1] = dyn ? atomicAdd(a.counters, 1) : t + int32_t(gridDim.x);
       int ok = 1;
-      if (dyn && t < n_items) {
-        ok = wait_consumed(a, a.map.tile[a.slot0 + (t >> 1)].group) ? 1 : 0;
+      if (a.consumed != nullptr) {
+        ok = wait_consumed(a, ti.group) ? 1 : 0;
         // the consumer's generic stores are read next by the TMA engine
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
-      s_ok[word] = ok;
+      s_ready = ok;
     }
     __syncthreads();
-    return s_ok[word] != 0;
-  };
-
-  int32_t t = s_next[nb];
-  bool ok = t < n_items && fetch(t, 0);
-  Item cur{};
-  if (ok) {
-    cur = item_of(a, t);
-    expect[b] = load_item(a, cur, sbuf, smem_u32(&full[b]), pol, tid);
-    pending[b] = expect[b] != 0;
-  }
-  int word = 1;
-  while (ok) {
-    // the next item: its loads go into the other buffer once that buffer's
-    // last store has finished reading it
-    if (tid == 0) s_next[nb ^ 1] = dyn ? atomicAdd(a.counters, 1) : t + int32_t(gridDim.x);
+    if (!s_ready) break;
+    const bool whole = (a.map.layout == FO_LAYOUT_TILE || a.map.layout == FO_LAYOUT_RS_ROWBLOCK);
+    const bool a2a = a.map.layout == FO_LAYOUT_A2A_SUBTOKEN;
+    // All-to-All: this thread's row (k = -1: it holds no token, moves nowhere)
+    int rk = -1;
+    int32_t rsu = 0, rdr = 0;
+    if (a2a && tid < ti.rows) reorder_row(a, ti, s, tid, &rk, &rsu, &rdr);
+    const int32_t in_rows = a2a ? __syncthreads_count(rk >= 0) : ti.rows;
+    // the previous tile's stores have finished reading the buffer
+    bulk_wait_read_all();
     __syncthreads();
-    const int32_t tn = s_next[nb ^ 1];
-    bool have_next = tn < n_items;
-    Item nxt{};
-    if (have_next) {
-      have_next = fetch(tn, word);
-      word ^= 1;
-      if (!have_next) ok = false;   // a wait on the consumer ran out
-    }
-    if (have_next) {
-      bulk_wait_read_all();
-      __syncthreads();
-      nxt = item_of(a, tn);
-      expect[b ^ 1] = load_item(a, nxt, sbuf + (b ^ 1) * kRHalfBytes,
-                                smem_u32(&full[b ^ 1]), pol, tid);
-      pending[b ^ 1] = expect[b ^ 1] != 0;
-    }
-    // the current item lands (bounded wait), then leaves
-    if (expect[b] != 0) {
-      if (tid == 0) {
-        int landed = 1;
-        const uint32_t fb = smem_u32(&full[b]);
-        if (!mbar_try_wait(fb, phase[b])) {
-          const uint64_t t0 = globaltimer_ns();
-          while (!mbar_try_wait(fb, phase[b]))
-            if (globaltimer_ns() - t0 > kRWaitLimitNs) {
-              landed = 0;
-              atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
-              break;
-            }
-        }
-        s_ok[word] = landed;
+    if (tid == 0) mbar_expect_tx(sfull, uint32_t(in_rows * ub));
+    __syncthreads();
+    if (whole) {
+      if (tid == 0 && ti.rows > 0) {   // (a padding tile holds no rows)
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, 0, &k, &su, &dr);   // rows are contiguous from row 0
+        bulk_load_hint(sbuf, a.src[k] + int64_t(su) * ub, uint32_t(ti.rows * ub), sfull, pol);
       }
-      __syncthreads();
-      const bool landed = s_ok[word] != 0;
-      word ^= 1;
-      if (!landed) break;
-      pending[b] = false;
-      phase[b] ^= 1;
-      const uint32_t sb = sbuf + b * kRHalfBytes;
-      if (a.act != FO_ACT_NONE || a.bias != nullptr) {
-        // element-wise epilogue in place ([P1] 五: fused with the reorder):
-        // row r of the item is at r * unit_bytes in every layout
-        const int vpr = a.unit_bytes / 16;
-        uint8_t* base = buf + b * kRHalfBytes;
-        for (int v = tid; v < cur.n * vpr; v += kRThreads) {
-          const int r = v / vpr, cv = v - r * vpr;
-          uint4* pv = reinterpret_cast<uint4*>(base + r * a.unit_bytes + cv * 16);
-          *pv = epilogue8(*pv, a.bias, cur.ti.col0 + cv * 8, a.act);
-        }
-        // generic writes to shared memory, read next by the TMA engine
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
+    } else if (a.map.layout == FO_LAYOUT_RS_SUBTILE) {
+      if (tid < a.map.R) {   // subtile tid: rows tid*h .. +h, contiguous in slice tid
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, tid * a.map.h, &k, &su, &dr);
+        bulk_load_hint(sbuf + tid * a.map.h * ub, a.src[k] + int64_t(su) * ub,
+                       uint32_t(a.map.h * ub), sfull, pol);
       }
-      store_item(a, cur, sb, tid);
+    } else if (rk >= 0) {  // All-to-All: row by row
+      bulk_load_hint(sbuf + tid * ub, a.src[rk] + int64_t(rsu) * ub, uint32_t(ub), sfull, pol);
     }
-    if (!have_next) break;
-    cur = nxt;
-    t = tn;
-    nb ^= 1;
-    b ^= 1;
-  }
-  // every store has completed before the CTA (and its shared memory) ends;
-  // a load issued but not waited for (a wait ran out first) lands first
-  bulk_wait_all();
-  if (tid == 0)
-    for (int q = 0; q < 2; ++q)
-      if (pending[q] && !mbar_try_wait(smem_u32(&full[q]), phase[q])) {
+    // wait for the tile to land (bounded)
+    if (tid == 0) {
+      int ok = 1;
+      if (!mbar_try_wait(sfull, phase)) {
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(&full[q]), phase[q]))
-          if (globaltimer_ns() - t0 > kRWaitLimitNs) break;
+        while (!mbar_try_wait(sfull, phase))
+          if (globaltimer_ns() - t0 > kRWaitLimitNs) {
+            ok = 0;
+            atomicCAS(a.status, 0, int32_t(FO_ERR_TIMEOUT));
+            break;
+          }
       }
-  __syncthreads();
+      s_ok = ok;
+    }
+    __syncthreads();
+    if (!s_ok) break;
+    if (a.act != FO_ACT_NONE || a.bias != nullptr) {
+      // element-wise epilogue in place ([P1] 五: fused with the reorder):
+      // row r of the tile is at r * ub in every layout
+      const int vpr = ub / 16;
+      for (int v = tid; v < ti.rows * vpr; v += kRThreads) {
+        const int r = v / vpr, cv = v - r * vpr;
+        uint4* pv = reinterpret_cast<uint4*>(buf + r * ub + cv * 16);
+        *pv = epilogue8(*pv, a.bias, ti.col0 + cv * 8, a.act);
+      }
+      // generic writes to shared memory, read next by the TMA engine
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+    }
+    if (whole && ti.rows == kTileM) {
+      if (tid == 0) {
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, 0, &k, &su, &dr);
+        tensor_store_2d(&a.dst_map[k], sbuf, ti.col0, dr);
+        bulk_commit();
+      }
+    } else if (a.map.layout == FO_LAYOUT_RS_SUBTILE) {
+      if (tid < a.map.R) {
+        int k;
+        int32_t su, dr;
+        reorder_row(a, ti, s, tid * a.map.h, &k, &su, &dr);
+        tensor_store_2d(&a.dst_map[k], sbuf + tid * a.map.h * ub, ti.col0, dr);
+        bulk_commit();
+      }
+    } else if (a2a) {  // All-to-All rows: per row
+      if (rk >= 0) {
+        bulk_store(a.dst[rk] + int64_t(rdr) * a.row_bytes + int64_t(ti.col0) * 2,
+                   sbuf + tid * ub, uint32_t(ub));
+        bulk_commit();
+      }
+    } else if (tid < ti.rows) {  // ragged tiles: per row
+      int k;
+      int32_t su, dr;
+      reorder_row(a, ti, s, tid, &k, &su, &dr);
+      bulk_store(a.dst[k] + int64_t(dr) * a.row_bytes + int64_t(ti.col0) * 2, sbuf + tid * ub,
+                 uint32_t(ub));
+      bulk_commit();
+    }
+  }
+  // every store has completed before the CTA (and its shared memory) ends
+  bulk_wait_all();
   // Launched as the consumer's programmatic dependent, this grid completes
   // only after the consumer has: a later launch on the stream (a consume of
   // the next group) then never meets the consumer still running.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the last CTA resets the item counter for the next launch
+  // the last CTA resets the tile counter for the next launch
   if (!dyn) return;
+  __syncthreads();
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.counters + 1, 1) == int32_t(gridDim.x) - 1) {
-      // every item is done: clear the groups' consumed flags too, so a
+      // every tile is done: clear the groups' consumed flags too, so a
       // launch that carries the same sequence number (a replayed graph)
       // waits for its own consumer
       for (int32_t j = a.g0; j < a.g1; ++j) atomicExch(a.consumed + j, 0u);
@@ -319,17 +234,6 @@ __global__ void __launch_bounds__(kRThreads) reorder_kernel(const __grid_constan
 }
 
 }  // namespace
-
-// Rows of the output boxes the reorder stores with one tensor copy: a half
-// tile (64 rows); for ReduceScatter subtiles of h = 128 / R rows, min(h, 64)
-// (a piece of a half that lies in one slice).
-int box_rows_of(const fo_plan* p) {
-  if (p->layout == FO_LAYOUT_RS_SUBTILE) {
-    const int h = kTileM / p->R;
-    return h < kRHalfRows ? h : kRHalfRows;
-  }
-  return kRHalfRows;
-}
 
 fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
                               const void* const* src, void* const* dst, const void* bias,
@@ -351,7 +255,7 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
     a.src[k] = static_cast<const uint8_t*>(src[k]);
     a.dst[k] = static_cast<uint8_t*>(dst[k]);
     if (p->layout != FO_LAYOUT_A2A_SUBTOKEN) {
-      const int box_rows = box_rows_of(p);
+      const int box_rows = p->layout == FO_LAYOUT_RS_SUBTILE ? kTileM / p->R : kTileM;
       if (!encode_tensor_map_2d(&a.dst_map[k], dst[k], uint64_t(p->N),
                                 uint64_t(p->final_rows[k]), uint32_t(p->tile_n),
                                 uint32_t(box_rows), false))
@@ -366,12 +270,11 @@ fo_status launch_reorder_back(const fo_plan* p, int32_t g0, int32_t g1,
   a.row_bytes = p->N * 2;
   a.slot0 = p->group_slot_begin[g0];
   a.n_slots = p->group_slot_begin[g1] - a.slot0;
-  a.box_rows = box_rows_of(p);
   a.counters = p->dev.rtile;
   a.g0 = g0;
   a.g1 = g1;
   int ctas = p->reorder_ctas > 0 ? p->reorder_ctas : 3 * p->sm_count;
-  if (ctas > 2 * a.n_slots) ctas = 2 * a.n_slots;
+  if (ctas > a.n_slots) ctas = a.n_slots;
   // With overlap on, the reorder is a programmatic dependent of the
   // consumer launched just before it on the stream: its CTAs start once all
   // the consumer's CTAs are resident (on SMs the GEMM leaves room on) and
