@@ -1110,9 +1110,10 @@ def tune_partition(w, inp, ms_gemm_for_tuning, partition, steps):
         gemm_us = ms_gemm_for_tuning * 1e3
         waves = sample_waves(t.pipe.waves)
         curve = t.curve(waves)
+        curve_l = t.curve_in_launch(waves)
         sigma, rho = t.interference(gemm_us, partition)
         parts, pred = fo.fo_tune_partition(t.desc(), gemm_us, curve)
-        parts_i, pred_i = fo.fo_tune_partition(t.desc(), gemm_us, curve, sigma, rho)
+        parts_i, pred_i = fo.fo_tune_partition(t.desc(), gemm_us, curve_l, sigma, rho)
         t.reps = steps
         cands = {"tuned": parts, "tuned_interference": parts_i, "workload": partition}
         meas = {k: [] for k in cands}
@@ -1121,7 +1122,7 @@ def tune_partition(w, inp, ms_gemm_for_tuning, partition, steps):
                 meas[k].append(t.step_us(c))
         ms = {k: statistics.median(v) / 1e3 for k, v in meas.items()}
         pw = fo.fo_predict_partition(t.desc(partition), gemm_us, curve)
-        pw_i = fo.fo_predict_partition(t.desc(partition), gemm_us, curve, sigma, rho)
+        pw_i = fo.fo_predict_partition(t.desc(partition), gemm_us, curve_l, sigma, rho)
         return {"partition": parts, "predicted_us": pred, "ms_step": ms["tuned"],
                 "gemm_slowdown": sigma, "comm_slowdown": rho,
                 "partition_interference": parts_i, "predicted_interference_us": pred_i,

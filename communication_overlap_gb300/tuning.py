@@ -22,6 +22,9 @@ slow each other while both run), from the workload's own partition:
   * comm_slowdown: fitted so that the model reproduces that partition's
     measured step (one calibration point; every other candidate is a
     prediction).
+The interference model takes the consumer's latency per group inside one
+persistent launch (curve_in_launch: no launch or ramp-up per group, as in
+the step), the pages' model the latency of a launch per group (curve).
 fo_tune_partition_ex / fo_predict_partition_ex take both.
 
 --validate runs the overlapped step for every candidate partition (T <= 8)
@@ -138,6 +141,48 @@ class Tuner:
         self.last_curve = pts
         return pts
 
+    def curve_in_launch(self, waves=None):
+        """[(bytes, us)]: the consumer's latency per group inside one
+        persistent launch, as the overlapped step runs it.  For group size
+        k: plan the waves as groups of k (the remainder last), raise every
+        flag with a step, then run the consumer over all groups alone;
+        each full group after the first takes the time between its last
+        chunk and the previous group's (consumer stamps), no launch or
+        ramp-up in it; median over groups and repetitions.  Sizes with
+        fewer than two full groups are skipped (the predictor extrapolates
+        from the last two samples)."""
+        p = self.pipe
+        T = p.waves
+        sm = torch.cuda.get_device_properties(p.device).multi_processor_count
+        pts = []
+        for k in (waves or range(1, T + 1)):
+            if T // k < 2:
+                continue
+            part = [k] * (T // k) + ([T % k] if T % k else [])
+            p.replan(part)
+            p.step(overlap=False)
+            torch.cuda.synchronize()
+            p.set_overlap(False)
+            trace = torch.zeros(2 * p.P + 16 * sm, dtype=torch.int64, device=p.device)
+            fo.fo_plan_set_trace(p.plan, 0, trace.data_ptr())
+            lat = []
+            for _ in range(self.reps):
+                self.flush()
+                trace.zero_()
+                if self.direct:
+                    p.consume_reorder(p.s0, p.epoch, direct=True)
+                else:
+                    p.consume(p.s0, p.epoch)
+                torch.cuda.synchronize()
+                done = trace[:p.P].cpu().tolist()
+                lat += [(done[j] - done[j - 1]) / 1e3 for j in range(1, T // k)]
+            fo.fo_plan_set_trace(p.plan, 0, 0)
+            pts.append((float(p.group_tiles[1] * self.tile_bytes), statistics.median(lat)))
+        if len(pts) < 2:   # too few waves: the stand-alone curve
+            return self.curve(waves)
+        self.last_curve = pts
+        return pts
+
     def interference(self, gemm_us, partition=None, reps=5):
         """(gemm_slowdown, comm_slowdown) for the interference model, from
         `partition` (default: the workload's one wave then groups of two):
@@ -210,25 +255,27 @@ def run(name, validate=False, reps=20, kernels="direct"):
     t = Tuner(w, reps=reps, kernels=kernels)
     try:
         gemm = t.gemm_us()
-        curve = t.curve()
+        curve = t.curve()                  # the pages' model: one launch per group
+        curve_l = t.curve_in_launch()      # the interference model: groups in one launch
         sigma, rho = t.interference(gemm)
         best, pred = fo.fo_tune_partition(t.desc(), gemm, curve)
-        best_i, pred_i = fo.fo_tune_partition(t.desc(), gemm, curve, sigma, rho)
+        best_i, pred_i = fo.fo_tune_partition(t.desc(), gemm, curve_l, sigma, rho)
         out = {"workload": name, "kernels": kernels, "waves": t.pipe.waves, "gemm_us": gemm,
-               "curve": curve, "gemm_slowdown": sigma, "comm_slowdown": rho,
+               "curve": curve, "curve_in_launch": curve_l,
+               "gemm_slowdown": sigma, "comm_slowdown": rho,
                "tuned": best, "tuned_predicted_us": pred,
                "tuned_interference": best_i, "tuned_interference_predicted_us": pred_i}
         base = fo.partition_one_then_two(t.pipe.waves)
         out["one_then_two_predicted_us"] = fo.fo_predict_partition(t.desc(base), gemm, curve)
         out["one_then_two_predicted_interference_us"] = fo.fo_predict_partition(
-            t.desc(base), gemm, curve, sigma, rho)
+            t.desc(base), gemm, curve_l, sigma, rho)
         if validate:
             rows = []
             for cand in _design_space(t.pipe.waves):
                 rows.append({"partition": cand,
                              "predicted_us": fo.fo_predict_partition(t.desc(cand), gemm, curve),
                              "predicted_interference_us": fo.fo_predict_partition(
-                                 t.desc(cand), gemm, curve, sigma, rho),
+                                 t.desc(cand), gemm, curve_l, sigma, rho),
                              "measured_us": t.step_us(cand)})
             meas_best = min(rows, key=lambda r: r["measured_us"])
             by_part = {tuple(r["partition"]): r for r in rows}

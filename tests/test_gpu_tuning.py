@@ -51,3 +51,20 @@ def test_interference_factors_and_tuned_partition():
         check_run(t.pipe, t.inp, t.pipe.results())
     finally:
         t.close()
+
+
+def test_curve_in_one_launch():
+    """The latency curve measured inside one persistent consumer launch:
+    positive, growing with the group size, and below the curve of one
+    launch per group (no launch or ramp-up per group)."""
+    w = W.scaled(W.WORKLOADS["allreduce"], M=2048, N=2048, K=256, wave_width=4)
+    t = Tuner(w, reps=3)
+    try:
+        alone = dict(t.curve())
+        inl = t.curve_in_launch()
+        assert len(inl) >= 2 and all(us > 0 for _, us in inl)
+        assert inl[-1][1] > inl[0][1]
+        b0, us0 = inl[0]
+        assert us0 < alone[b0]
+    finally:
+        t.close()
