@@ -93,8 +93,12 @@ def parse():
                          "tuned in this run before the timed steps")
     ap.add_argument("--ncu-gemm", action="store_true",
                     help="only GEMM launches (warm-up + --steps), for ncu captures")
+    ap.add_argument("--ncu-matmul", action="store_true",
+                    help="only torch.matmul (cuBLAS) on the workload's operands (warm-up + "
+                         "--steps calls), the library reference point for ncu captures")
     ap.add_argument("--experts", type=int, default=0,
-                    help="with --ncu-gemm: the grouped workload cut to its first experts")
+                    help="with --ncu-gemm / --ncu-matmul: the grouped workload cut to its "
+                         "first experts")
     return ap.parse_args()
 
 
@@ -674,12 +678,10 @@ def measure_compact(ctx, w, args):
         torch.cuda.empty_cache()
 
 
-def run_ncu_gemm(args):
-    """Only GEMM launches of the workload (optionally its first --experts
-    experts): the small case for ncu captures of the GEMM."""
-    import torch
+def ncu_case(args):
+    """The workload of an ncu capture and its inputs, the grouped workload
+    optionally cut to its first --experts experts."""
     from communication_overlap_gb300 import workloads as W
-    from communication_overlap_gb300.pipeline import Pipeline
     w = workload(args, args.workload)
     inp = W.make_inputs(w)
     if w.grouped and args.experts:
@@ -690,6 +692,15 @@ def run_ncu_gemm(args):
         inp.A, inp.B = inp.A[:rows], inp.B[:e]
         inp.expert_rows = inp.expert_rows[:e]
         inp.row_token, inp.row_slot = inp.row_token[:rows], inp.row_slot[:rows]
+    return w, inp
+
+
+def run_ncu_gemm(args):
+    """Only GEMM launches of the workload (optionally its first --experts
+    experts): the small case for ncu captures of the GEMM."""
+    import torch
+    from communication_overlap_gb300.pipeline import Pipeline
+    w, inp = ncu_case(args)
     pipe = Pipeline(w, inp)
     for _ in range(args.warmup):
         pipe.gemm(pipe.s0, 1)
@@ -703,6 +714,23 @@ def run_ncu_gemm(args):
                       "count_ok": ok}))
     pipe.close()
     return 0 if ok else 1
+
+
+def run_ncu_matmul(args):
+    """torch.matmul (cuBLAS) on the workload's operands, one call per
+    expert: the library reference point of an ncu capture."""
+    import torch
+    w, inp = ncu_case(args)
+    A = torch.from_numpy(inp.A.view(np.int16)).cuda().view(torch.bfloat16)
+    B = [torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16) for b in inp.B]
+    rows = np.cumsum([0] + list(inp.expert_rows))
+    for _ in range(args.warmup + args.steps):
+        for e, Bm in enumerate(B):
+            torch.matmul(A[rows[e]:rows[e + 1]], Bm)
+    torch.cuda.synchronize()
+    print(json.dumps({"ncu_matmul": w.name, "M": w.M, "experts": len(B),
+                      "calls": (args.warmup + args.steps) * len(B)}))
+    return 0
 
 
 def run_ours(args):
@@ -1190,6 +1218,8 @@ def main():
         return run_reference(args)
     if args.ncu_gemm:
         return run_ncu_gemm(args)
+    if args.ncu_matmul:
+        return run_ncu_matmul(args)
     return run_ours(args)
 
 
