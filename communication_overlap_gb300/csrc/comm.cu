@@ -532,9 +532,11 @@ fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int devi
   return cudaGetLastError() == cudaSuccess ? FO_OK : FO_ERR_CUDA;
 }
 
+// deep: at most one CTA per SM, so each thread may keep twice the copy
+// vectors in flight (the same bytes in flight per SM as two CTAs of 4)
 template <int VPU, bool DIRECT>
 fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int dv,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool deep) {
   switch (kind) {
     case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kFusedUnroll<FO_CONS_COPY>, VPU, DIRECT>(a, ctas, ov, dv, st);
     // the direct sum of at most 4 partials keeps two vectors per source in
@@ -549,7 +551,15 @@ fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int 
         if (a.c.n_partials <= kPartialsInFlight<2>)
           return launch_fused_kind<FO_CONS_RS, 2, VPU, true>(a, ctas, ov, dv, st);
       return launch_fused_kind<FO_CONS_RS, kFusedUnroll<FO_CONS_RS>, VPU, DIRECT>(a, ctas, ov, dv, st);
-    case FO_CONS_A2A: return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU, DIRECT>(a, ctas, ov, dv, st);
+    // the direct bucket runs at one CTA per SM beside the GEMM; there it
+    // keeps 8 vectors per thread in flight (72 registers, no spills;
+    // measured: alone at that grid 731 -> 568 us on the All-to-All layer, the
+    // step no slower).  At 4 CTAs per SM that was slower (0.75 -> 0.64 of the
+    // copy bandwidth), so larger grids keep 4.
+    case FO_CONS_A2A:
+      if constexpr (DIRECT)
+        if (deep) return launch_fused_kind<FO_CONS_A2A, 8, VPU, true>(a, ctas, ov, dv, st);
+      return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU, DIRECT>(a, ctas, ov, dv, st);
   }
   return FO_ERR_ARG;
 }
@@ -724,11 +734,12 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
                ? p->consumer_pace : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool ov = p->overlap != 0;
+  const bool deep = ctas <= p->sm_count;
   if (a.direct)
-    return p->tile_n == 256 ? launch_fused_vpu<32, true>(kind, a, ctas, ov, p->device, st)
-                            : launch_fused_vpu<16, true>(kind, a, ctas, ov, p->device, st);
-  return p->tile_n == 256 ? launch_fused_vpu<32, false>(kind, a, ctas, ov, p->device, st)
-                          : launch_fused_vpu<16, false>(kind, a, ctas, ov, p->device, st);
+    return p->tile_n == 256 ? launch_fused_vpu<32, true>(kind, a, ctas, ov, p->device, st, deep)
+                            : launch_fused_vpu<16, true>(kind, a, ctas, ov, p->device, st, deep);
+  return p->tile_n == 256 ? launch_fused_vpu<32, false>(kind, a, ctas, ov, p->device, st, deep)
+                          : launch_fused_vpu<16, false>(kind, a, ctas, ov, p->device, st, deep);
 }
 
 }  // namespace fo

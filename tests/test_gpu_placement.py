@@ -145,3 +145,22 @@ def test_exact_placement_full_size(name):
         check_exact_run(pipe, inp, pipe.results(), direct=True)
     finally:
         pipe.close()
+
+
+@pytest.mark.parametrize("per_sm", [0, 1, 4])
+def test_exact_placement_direct_bucket_grids(per_sm):
+    """The direct All-to-All bucket at its default grid (one CTA per SM, 8
+    vectors per thread in flight), at an explicit one per SM and at four per
+    SM (4 vectors per thread): the same bytes, bit for bit."""
+    w = W.scaled(W.WORKLOADS["alltoall"], M=2 * 700, N=768, K=256, n_tokens=700, n_experts=5,
+                 wave_width=8, pad_expert_tile_rows=True)
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    inp = exact_inputs(w)
+    pipe = Pipeline(w, inp, consumer_ctas=per_sm * sm)
+    try:
+        fill_comm_sentinel(pipe)
+        for _ in range(2):
+            pipe.step(fused=True, direct=True)
+        check_exact_run(pipe, inp, pipe.results(), direct=True)
+    finally:
+        pipe.close()
