@@ -93,6 +93,10 @@ def parse():
                          "tuned in this run before the timed steps")
     ap.add_argument("--ncu-gemm", action="store_true",
                     help="only GEMM launches (warm-up + --steps), for ncu captures")
+    ap.add_argument("--ncu-step", action="store_true",
+                    help="only overlapped steps of the workload (warm-up + --steps), the "
+                         "grouped one optionally cut to --experts experts: the small case for "
+                         "ncu captures of the consumer")
     ap.add_argument("--ncu-matmul", action="store_true",
                     help="only torch.matmul (cuBLAS) on the workload's operands (warm-up + "
                          "--steps calls), the library reference point for ncu captures")
@@ -717,6 +721,25 @@ def run_ncu_gemm(args):
     return 0 if ok else 1
 
 
+def run_ncu_step(args):
+    """Only overlapped steps (the benchmark's step kernels) of the workload,
+    optionally cut to its first --experts experts."""
+    import torch
+    from communication_overlap_gb300.pipeline import Pipeline
+    w, inp = ncu_case(args)
+    pipe = Pipeline(w, inp)
+    kernels = "direct" if args.step_kernels == "auto" else args.step_kernels
+    kw = dict(fused=kernels in ("fused", "direct"), direct=kernels == "direct")
+    for _ in range(args.warmup + args.steps):
+        pipe.step(overlap=True, **kw)
+    torch.cuda.synchronize()
+    ok = int(pipe.buf.status.item()) == 0 and pipe.buf.count.cpu().tolist() == pipe.group_tiles
+    print(json.dumps({"ncu_step": w.name, "M": w.M, "experts": w.n_experts,
+                      "steps": args.warmup + args.steps, "step_kernels": kernels, "ok": ok}))
+    pipe.close()
+    return 0 if ok else 1
+
+
 def run_ncu_matmul(args):
     """torch.matmul (cuBLAS) on the workload's operands, one call per
     expert: the library reference point of an ncu capture."""
@@ -830,6 +853,28 @@ def run_ours(args):
                          "steps (no flush between them); the headline is timed after the "
                          "warm-up"}
 
+    # reading of the wave: W = the GEMM's persistent CTAs; the workloads fix
+    # W = 148, and where the device has another SM count the same path with
+    # W = that count is timed beside it
+    w_sm = None
+    if sm_count != w.wave_width and world == 1:
+        from communication_overlap_gb300 import workloads as W_
+        b_sm = Bench(ctx, W_.scaled(w, wave_width=sm_count), args)
+        try:
+            b_sm.warm()
+            t_gemm_sm = b_sm.timed(lambda: b_sm.pipe.gemm(b_sm.s, b_sm.pipe.epoch))
+            t_step_sm = b_sm.timed(b_sm.ovl)
+            w_sm = {"wave_width": sm_count, "waves": b_sm.pipe.waves,
+                    "gemm_pairs": bool(b_sm.pipe.pairable),
+                    "ms_gemm_alone": statistics.mean(t_gemm_sm),
+                    "ms_overlapped_step": statistics.mean(t_step_sm),
+                    "value_tflops": flops / (statistics.mean(t_step_sm) * 1e-3) / 1e12,
+                    "status_ok": int(b_sm.pipe.buf.status.item()) == 0}
+        finally:
+            b_sm.close()
+            del b_sm
+            torch.cuda.empty_cache()
+
     if args.trace_out:
         write_trace(ctx, b, args.trace_out)
 
@@ -893,6 +938,7 @@ def run_ours(args):
             "clocks_by_kernels": clk_var,
             "sustained": sustained,
             "partition_mode": args.partition,
+            "w_sm_count": w_sm,
             "partition_tuned_before_timing": pre_tuned,
             "ms_serial_step_separate_kernels": statistics.mean(t_ser_sep),
             "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
@@ -1221,6 +1267,8 @@ def main():
         return run_ncu_gemm(args)
     if args.ncu_matmul:
         return run_ncu_matmul(args)
+    if args.ncu_step:
+        return run_ncu_step(args)
     return run_ours(args)
 
 
