@@ -239,26 +239,36 @@ def timed(torch, stream, fn, steps, flush=None):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def traffic_from_profile(workload, kernel_src):
-    """Per-launch DRAM bytes of the GEMM on `workload` from the committed ncu
-    summary (profiles/signaled_gemm_<workload>_ncu.md), if it was taken on
-    the current source of the kernel (else None)."""
-    path = os.path.join(ROOT, "profiles", f"signaled_gemm_{workload}_ncu.md")
+def launch_order_key(w):
+    """The plan inputs that fix the GEMM's launch order, as the committed ncu
+    summaries record them."""
+    return (f"swizzle={w.swizzle} serpentine={int(w.serpentine)} "
+            f"pad={int(w.pad_expert_tile_rows)}")
+
+
+def traffic_from_profile(w, kernel_src):
+    """Per-launch DRAM bytes of the GEMM on workload `w` from the committed
+    ncu summary (profiles/signaled_gemm_<workload>_ncu.md), if it was taken
+    on the current source of the kernel and the workload's launch order
+    (else None)."""
+    path = os.path.join(ROOT, "profiles", f"signaled_gemm_{w.name}_ncu.md")
     try:
         txt = open(path).read()
     except OSError:
         return None
     h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
-    src, traffic = None, None
+    src, order, traffic = None, None, None
     for line in txt.splitlines():
         if line.startswith("source_sha256_16:"):
             src = line.split(":", 1)[1].strip()
+        if line.startswith("launch_order:"):
+            order = line.split(":", 1)[1].strip()
         if line.startswith("traffic_bytes_per_launch:"):
             try:
                 traffic = float(line.split(":", 1)[1].strip())
             except ValueError:
                 traffic = None
-    return traffic if src == h else None
+    return traffic if src == h and order == launch_order_key(w) else None
 
 
 # ----------------------------------------------------------------- CPU oracle leg
@@ -648,6 +658,10 @@ class Bench:
             "torch_matmul_tflops": self.flops / (ms_mm * 1e-3) / 1e12,
             "gemm_in_kernel_ms_alone": span_alone, "gemm_in_kernel_ms_in_step": span_step,
             "gemm_slowdown": span_step / span_alone,
+            # DRAM bytes per GEMM launch from the committed ncu summary taken
+            # on this kernel source and launch order (None if there is none)
+            "gemm_traffic_bytes": traffic_from_profile(
+                w, os.path.join(ROOT, "communication_overlap_gb300", "csrc", "gemm.cu")),
             "consumer_bytes": cb,
             "direct_alone_step_grid": bw(cb, alone["direct"]),
             "direct_alone_full_grid": bw(cb, alone["direct_full"]),
@@ -920,7 +934,7 @@ def run_ours(args):
     ms_e2e_serial = rmax(e2e["ms_one_step_at_a_time"])
 
     gemm_tflops = flops / (ms_gemm * 1e-3) / 1e12
-    traffic = traffic_from_profile(w.name, os.path.join(ROOT, "communication_overlap_gb300",
+    traffic = traffic_from_profile(w, os.path.join(ROOT, "communication_overlap_gb300",
                                                          "csrc", "gemm.cu"))
     out = None
     if rank == 0:
