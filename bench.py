@@ -87,6 +87,10 @@ def parse():
                     choices=["workload", "forward", "serpentine"],
                     help="column order inside the launch order's bands (default: each "
                          "workload's own)")
+    ap.add_argument("--swizzle", type=int, default=0,
+                    help="band height of the launch order in tile rows (default: each "
+                         "workload's own; e.g. 8 for the bands every workload used before "
+                         "the taller ones)")
     ap.add_argument("--partition", default="workload", choices=["workload", "tuned"],
                     help="the headline's wave-group partition: the workload's own (one wave, "
                          "then groups of two) or Algorithm 1's with the interference factors, "
@@ -107,11 +111,14 @@ def parse():
 
 
 def workload(args, name):
-    """The named workload, with the launch order's band order if given."""
+    """The named workload, with the launch order's band order and band
+    height if given."""
     from communication_overlap_gb300 import workloads as W
     w = W.WORKLOADS[name]
     if args.band_order != "workload":
         w = W.scaled(w, serpentine=args.band_order == "serpentine")
+    if getattr(args, "swizzle", 0) > 0:
+        w = W.scaled(w, swizzle=args.swizzle)
     return w
 
 
@@ -605,6 +612,19 @@ class Bench:
         r["consumer_full"] = self.timed(lambda: pipe.consume(s, pipe.epoch))
         fo.fo_plan_set_launch(pipe.plan, self.args.consumer_ctas, self.args.reorder_ctas, False)
         pipe.set_overlap(True)
+        # The reorder's bytes moved by a plain device-to-device copy
+        # (torch.Tensor.copy_), timed the same way: the event-timed ceiling
+        # of a move of this size, launch ramp and tail included.
+        n = moved_rows(self.w, self.inp) * self.w.N * 2
+        src = torch.empty(n, dtype=torch.uint8, device=self.ctx["dev"])
+        dst = torch.empty_like(src)
+
+        def plain_copy():
+            with torch.cuda.stream(s):
+                dst.copy_(src)
+        plain_copy()
+        r["plain_copy"] = self.timed(plain_copy)
+        del src, dst
         return {k: statistics.mean(v) for k, v in r.items()}
 
     def torch_mm(self):
@@ -669,6 +689,8 @@ class Bench:
             "consumer_alone_step_grid": bw(cb, alone["consumer"]),
             "consumer_alone_full_grid": bw(cb, alone["consumer_full"]),
             "reorder_alone": bw(reo_bytes, alone["reorder"]),
+            "plain_copy_same_bytes": bw(reo_bytes, alone["plain_copy"]),
+            "reorder_frac_of_plain_copy": alone["plain_copy"] / alone["reorder"],
             "clocks": clk,
             "status_ok": int(pipe.buf.status.item()) == 0,
         }
@@ -1018,8 +1040,9 @@ def compact_view(rec):
             "gemm_tflops_alone", "gemm_frac_of_measured_peak", "gemm_frac_of_nominal_peak",
             "ms_torch_matmul", "gemm_slowdown", "gemm_in_kernel_ms_alone",
             "gemm_in_kernel_ms_in_step", "consumer_bytes", "direct_alone_step_grid",
-            "direct_alone_full_grid", "consumer_in_step", "reorder_alone", "clocks",
-            "status_ok", "step_kernels")
+            "direct_alone_full_grid", "consumer_in_step", "reorder_alone",
+            "plain_copy_same_bytes", "reorder_frac_of_plain_copy", "gemm_traffic_bytes",
+            "clocks", "status_ok", "step_kernels")
     out = {k: rec[k] for k in keep if k in rec}
     if isinstance(out.get("consumer_in_step"), dict):
         out["consumer_in_step"] = {k: v for k, v in out["consumer_in_step"].items()
