@@ -91,6 +91,12 @@ def parse():
                     help="band height of the launch order in tile rows (default: each "
                          "workload's own; e.g. 8 for the bands every workload used before "
                          "the taller ones)")
+    ap.add_argument("--wave-width", type=int, default=0,
+                    help="W, the GEMM's persistent CTAs and the wave width (default: each "
+                         "workload's own, 148)")
+    ap.add_argument("--consumer-sms", default="shared", choices=["shared", "reserved"],
+                    help="the consumer's CTAs beside the GEMM's (shared) or only on the SMs "
+                         "the GEMM leaves free (reserved: [P1] 四's communication SMs)")
     ap.add_argument("--partition", default="workload", choices=["workload", "tuned"],
                     help="the headline's wave-group partition: the workload's own (one wave, "
                          "then groups of two) or Algorithm 1's with the interference factors, "
@@ -119,6 +125,8 @@ def workload(args, name):
         w = W.scaled(w, serpentine=args.band_order == "serpentine")
     if getattr(args, "swizzle", 0) > 0:
         w = W.scaled(w, swizzle=args.swizzle)
+    if getattr(args, "wave_width", 0) > 0:
+        w = W.scaled(w, wave_width=args.wave_width)
     return w
 
 
@@ -448,7 +456,9 @@ class Bench:
         torch, dev = ctx["torch"], ctx["dev"]
         self.inp = W.make_inputs(w)
         self.pipe = Pipeline(w, self.inp, device=dev, consumer_ctas=args.consumer_ctas,
-                             reorder_ctas=args.reorder_ctas)
+                             reorder_ctas=args.reorder_ctas,
+                             reserved_consumer_sms=getattr(args, "consumer_sms",
+                                                           "shared") == "reserved")
         self.s = self.pipe.s0
         # FLOPs of the rows that hold a token: with fixed expert capacities
         # the empty rows are not work (the GEMM skips tiles that have none)
@@ -893,7 +903,8 @@ def run_ours(args):
     # W = 148, and where the device has another SM count the same path with
     # W = that count is timed beside it
     w_sm = None
-    if sm_count != w.wave_width and world == 1:
+    # (with the reserved placement W = the SM count leaves the consumer no SM)
+    if sm_count != w.wave_width and world == 1 and args.consumer_sms == "shared":
         from communication_overlap_gb300 import workloads as W_
         b_sm = Bench(ctx, W_.scaled(w, wave_width=sm_count), args)
         try:
@@ -1000,6 +1011,7 @@ def run_ours(args):
                        "groups_tiles": group_tiles, "consumer": consumer_name(w),
                        "l2": "flushed before every timed step (256 MiB write)",
                        "consumer_ctas": args.consumer_ctas or "library default",
+                       "consumer_sms": args.consumer_sms,
                        "step_kernels": STEP_KERNELS[kernels],
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_burst,

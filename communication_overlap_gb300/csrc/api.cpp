@@ -107,6 +107,30 @@ fo_status fo_plan_set_pacing(fo_plan* p, int32_t ctas_during_gemm) {
   return FO_OK;
 }
 
+fo_status fo_plan_set_consumer_placement(fo_plan* p, fo_consumer_placement placement) {
+  if (!p) return FO_ERR_ARG;
+  if (placement == FO_CONSUMER_SHARED) {
+    p->consumer_smem = 0;
+    return FO_OK;
+  }
+  if (placement != FO_CONSUMER_RESERVED) return FO_ERR_ARG;
+  if (fo::reserved_sms(p) <= 0) return FO_ERR_UNSUPPORTED;
+  int cap = 0, per_block = 0;
+  if (cudaDeviceGetAttribute(&cap, cudaDevAttrMaxSharedMemoryPerMultiprocessor, p->device) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&per_block, cudaDevAttrReservedSharedMemoryPerBlock, p->device) !=
+          cudaSuccess)
+    return FO_ERR_CUDA;
+  // more than an SM holding a GEMM CTA has left, counting the system's
+  // reservation of each of the two CTAs; rounded up to 4 KB
+  int need = cap - fo::gemm_smem_bytes() - 2 * per_block + 1;
+  if (need < 1) need = 1;
+  need = (need + 4095) / 4096 * 4096;
+  if (need > 48 * 1024) return FO_ERR_UNSUPPORTED;   // above the default dynamic limit
+  p->consumer_smem = need;
+  return FO_OK;
+}
+
 fo_status fo_plan_set_gemm(fo_plan* p, fo_gemm_variant variant, int32_t* pairable,
                            int32_t* pair_capacity) {
   if (!p) return FO_ERR_ARG;

@@ -31,6 +31,22 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// Reserved placement with the default grid: default_ctas returns minus the
+// number of SMs the GEMM leaves free, and the launch turns that into as many
+// CTAs as those SMs hold at once (the kernel's own occupancy: threads,
+// registers and the requested shared memory), so that no CTA waits for an
+// SM and then lands on one a finished GEMM CTA left.
+template <typename Kernel>
+int resolve_grid(Kernel kernel, int ctas, int smem) {
+  if (ctas > 0) return ctas;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, size_t(smem)) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  return per_sm * (-ctas > 0 ? -ctas : 1);
+}
+
 // 16-byte vectors each lane keeps in flight per source (per iteration): the
 // sums keep one per source, all sources at once (sum_partials).
 template <int KIND>
@@ -508,7 +524,7 @@ __global__ void __maxnreg__(72) consume_reorder_kernel(const __grid_constant__ F
 
 template <int KIND, int U, int VPU, bool DIRECT>
 fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int device,
-                            cudaStream_t st) {
+                            cudaStream_t st, int smem) {
   static std::once_flag once[64];
   static cudaError_t err[64];
   const int d = device < 64 ? device : 63;
@@ -519,8 +535,9 @@ fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int devi
   });
   if (err[d] != cudaSuccess) return FO_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(ctas);
+  cfg.gridDim = dim3(resolve_grid(consume_reorder_kernel<KIND, U, VPU, DIRECT>, ctas, smem));
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = size_t(smem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -536,21 +553,21 @@ fo_status launch_fused_kind(const FusedArgs& a, int ctas, bool overlap, int devi
 // vectors in flight (the same bytes in flight per SM as two CTAs of 4)
 template <int VPU, bool DIRECT>
 fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int dv,
-                           cudaStream_t st, bool deep) {
+                           cudaStream_t st, bool deep, int smem) {
   switch (kind) {
-    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kFusedUnroll<FO_CONS_COPY>, VPU, DIRECT>(a, ctas, ov, dv, st);
+    case FO_CONS_COPY: return launch_fused_kind<FO_CONS_COPY, kFusedUnroll<FO_CONS_COPY>, VPU, DIRECT>(a, ctas, ov, dv, st, smem);
     // the direct sum of at most 4 partials keeps two vectors per source in
     // flight (measured: reducescatter's sum alone 3% faster; the step even)
     case FO_CONS_SUM:
       if constexpr (DIRECT)
         if (a.c.n_partials <= kPartialsInFlight<2>)
-          return launch_fused_kind<FO_CONS_SUM, 2, VPU, true>(a, ctas, ov, dv, st);
-      return launch_fused_kind<FO_CONS_SUM, kFusedUnroll<FO_CONS_SUM>, VPU, DIRECT>(a, ctas, ov, dv, st);
+          return launch_fused_kind<FO_CONS_SUM, 2, VPU, true>(a, ctas, ov, dv, st, smem);
+      return launch_fused_kind<FO_CONS_SUM, kFusedUnroll<FO_CONS_SUM>, VPU, DIRECT>(a, ctas, ov, dv, st, smem);
     case FO_CONS_RS:
       if constexpr (DIRECT)
         if (a.c.n_partials <= kPartialsInFlight<2>)
-          return launch_fused_kind<FO_CONS_RS, 2, VPU, true>(a, ctas, ov, dv, st);
-      return launch_fused_kind<FO_CONS_RS, kFusedUnroll<FO_CONS_RS>, VPU, DIRECT>(a, ctas, ov, dv, st);
+          return launch_fused_kind<FO_CONS_RS, 2, VPU, true>(a, ctas, ov, dv, st, smem);
+      return launch_fused_kind<FO_CONS_RS, kFusedUnroll<FO_CONS_RS>, VPU, DIRECT>(a, ctas, ov, dv, st, smem);
     // the direct bucket runs at one CTA per SM beside the GEMM; there it
     // keeps 8 vectors per thread in flight (72 registers, no spills;
     // measured: alone at that grid 731 -> 568 us on the All-to-All layer, the
@@ -558,8 +575,8 @@ fo_status launch_fused_vpu(int kind, const FusedArgs& a, int ctas, bool ov, int 
     // copy bandwidth), so larger grids keep 4.
     case FO_CONS_A2A:
       if constexpr (DIRECT)
-        if (deep) return launch_fused_kind<FO_CONS_A2A, 8, VPU, true>(a, ctas, ov, dv, st);
-      return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU, DIRECT>(a, ctas, ov, dv, st);
+        if (deep) return launch_fused_kind<FO_CONS_A2A, 8, VPU, true>(a, ctas, ov, dv, st, smem);
+      return launch_fused_kind<FO_CONS_A2A, kFusedUnroll<FO_CONS_A2A>, VPU, DIRECT>(a, ctas, ov, dv, st, smem);
   }
   return FO_ERR_ARG;
 }
@@ -610,6 +627,8 @@ int log2_exact(int v) {
 // GEMM dominates the step and 1 CTA per SM slows it least.
 int default_ctas(const fo_plan* p, int requested, int kind, bool fused, bool direct) {
   if (requested > 0) return requested;
+  // reserved placement: resolved at launch (resolve_grid)
+  if (p->consumer_smem > 0) return -reserved_sms(p);
   if (fused) return (direct && kind == FO_CONS_A2A ? 1 : 3) * p->sm_count;
   return (kind == FO_CONS_SUM || kind == FO_CONS_RS) ? 4 * p->sm_count : p->sm_count;
 }
@@ -620,7 +639,7 @@ int default_ctas(const fo_plan* p, int requested, int kind, bool fused, bool dir
 // GEMM's so its CTAs can share SMs with GEMM CTAs.
 template <int KIND, int U>
 fo_status launch_consume_kind(const ConsumeArgs& a, int ctas, bool overlap, int device,
-                              cudaStream_t st) {
+                              cudaStream_t st, int smem) {
   static std::once_flag once[64];
   static cudaError_t err[64];
   const int d = device < 64 ? device : 63;
@@ -631,9 +650,9 @@ fo_status launch_consume_kind(const ConsumeArgs& a, int ctas, bool overlap, int 
   });
   if (err[d] != cudaSuccess) return FO_ERR_CUDA;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(ctas);
+  cfg.gridDim = dim3(resolve_grid(consume_kernel<KIND, U>, ctas, smem));
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = size_t(smem);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -678,11 +697,12 @@ fo_status launch_consume(const fo_plan* p, int32_t g0, int32_t g1, int kind,
   const int ctas = default_ctas(p, p->consumer_ctas, kind, false, false);
   const bool ov = p->overlap != 0;
   const int dv = p->device;
+  const int smem = p->consumer_smem;
   switch (kind) {
-    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, dv, st);
-    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, dv, st);
-    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>>(a, ctas, ov, dv, st);
-    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, dv, st);
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, dv, st, smem);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, dv, st, smem);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>>(a, ctas, ov, dv, st, smem);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, dv, st, smem);
   }
   return FO_ERR_ARG;
 }
@@ -734,12 +754,12 @@ fo_status launch_consume_reorder(const fo_plan* p, int32_t g0, int32_t g1, int k
                ? p->consumer_pace : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool ov = p->overlap != 0;
-  const bool deep = ctas <= p->sm_count;
+  const bool deep = ctas > 0 && ctas <= p->sm_count;   // (reserved default: several per SM)
   if (a.direct)
-    return p->tile_n == 256 ? launch_fused_vpu<32, true>(kind, a, ctas, ov, p->device, st, deep)
-                            : launch_fused_vpu<16, true>(kind, a, ctas, ov, p->device, st, deep);
-  return p->tile_n == 256 ? launch_fused_vpu<32, false>(kind, a, ctas, ov, p->device, st, deep)
-                          : launch_fused_vpu<16, false>(kind, a, ctas, ov, p->device, st, deep);
+    return p->tile_n == 256 ? launch_fused_vpu<32, true>(kind, a, ctas, ov, p->device, st, deep, p->consumer_smem)
+                            : launch_fused_vpu<16, true>(kind, a, ctas, ov, p->device, st, deep, p->consumer_smem);
+  return p->tile_n == 256 ? launch_fused_vpu<32, false>(kind, a, ctas, ov, p->device, st, deep, p->consumer_smem)
+                          : launch_fused_vpu<16, false>(kind, a, ctas, ov, p->device, st, deep, p->consumer_smem);
 }
 
 }  // namespace fo
@@ -896,10 +916,10 @@ extern "C" fo_status fo_consume_group_noalloc(const fo_plan* p, int32_t group,
   // earlier on this stream may still be running (see g_noalloc_pending)
   const bool ov = p->overlap != 0 && !noalloc_take_pending(device, cs);
   switch (kind) {
-    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, device, cs);
-    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, device, cs);
-    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>>(a, ctas, ov, device, cs);
-    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, device, cs);
+    case FO_CONS_COPY: return launch_consume_kind<FO_CONS_COPY, kUnroll<FO_CONS_COPY>>(a, ctas, ov, device, cs, p->consumer_smem);
+    case FO_CONS_SUM: return launch_consume_kind<FO_CONS_SUM, kUnroll<FO_CONS_SUM>>(a, ctas, ov, device, cs, p->consumer_smem);
+    case FO_CONS_RS: return launch_consume_kind<FO_CONS_RS, kUnroll<FO_CONS_RS>>(a, ctas, ov, device, cs, p->consumer_smem);
+    case FO_CONS_A2A: return launch_consume_kind<FO_CONS_A2A, kUnroll<FO_CONS_A2A>>(a, ctas, ov, device, cs, p->consumer_smem);
   }
   return FO_ERR_ARG;
 }

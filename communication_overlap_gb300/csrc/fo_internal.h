@@ -101,6 +101,10 @@ struct fo_plan {
   // least this many wait for the last group's flag before taking work
   // (0: every CTA works from the first flag on)
   int consumer_pace = 0;
+  // FO_CONSUMER_RESERVED: the consumers launch with this much (unused)
+  // dynamic shared memory, more than an SM holding a GEMM CTA has left, so
+  // their CTAs run on the SMs the GEMM leaves free (0: shared placement)
+  int consumer_smem = 0;
   int gemm_variant = 0;   // fo_gemm_variant
   // last-wave split: when the last wave holds split_n <= W / 2 tiles, each
   // is computed by two CTAs over halves of K (0: no split possible)
@@ -132,6 +136,12 @@ int32_t place_of(const fo_plan* p, int32_t slot, int32_t r);
 constexpr int kPlaceShift = 28;
 // The data kernels move 16-byte vectors: buffers must start on 16 bytes.
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// SMs without a CTA of the plan's signaled GEMM while it runs (its grid is
+// min(W, tiles) CTAs, one per SM).
+inline int reserved_sms(const fo_plan* p) {
+  return p->sm_count - (p->W < p->tiles ? p->W : p->tiles);
+}
 // Counters, flags and status words are 32-bit atomics, stamps 64-bit.
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; }
@@ -144,6 +154,7 @@ fo_status launch_plan_route(const fo_plan* p, const int32_t* row_token, const in
 
 // gemm.cu
 int gemm_pair_capacity(const fo_plan* p);
+int gemm_smem_bytes();
 fo_status launch_signaled_gemm(const fo_plan* p, const void* A,
                                const void* const* B, void* C_r,
                                int32_t* count, uint32_t* flags, uint32_t epoch,

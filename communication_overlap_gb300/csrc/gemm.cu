@@ -916,6 +916,16 @@ int gemm_pair_capacity(const fo_plan* p) {
   return p->tile_n == 256 ? pair_capacity_bn<256>(p->device) : pair_capacity_bn<128>(p->device);
 }
 
+// Dynamic shared memory of a GEMM CTA: the smallest over the kernel's
+// variants (the ring is 192 KB in every variant, so they are all equal).
+int gemm_smem_bytes() {
+  int m = Cfg<256, true>::kSmemBytes;
+  m = Cfg<256, false>::kSmemBytes < m ? Cfg<256, false>::kSmemBytes : m;
+  m = Cfg<128, true>::kSmemBytes < m ? Cfg<128, true>::kSmemBytes : m;
+  m = Cfg<128, false>::kSmemBytes < m ? Cfg<128, false>::kSmemBytes : m;
+  return m;
+}
+
 fo_status launch_signaled_gemm(const fo_plan* p, const void* A, const void* const* B,
                                void* C_r, int32_t* count, uint32_t* flags, uint32_t epoch,
                                void* stream) {

@@ -19,6 +19,7 @@ FO_CONS_COPY, FO_CONS_SUM, FO_CONS_RS, FO_CONS_A2A = range(4)
 FO_GEMM_AUTO, FO_GEMM_SINGLE, FO_GEMM_PAIRS = range(3)
 FO_ACT_NONE, FO_ACT_RELU, FO_ACT_SILU = range(3)
 FO_BAND_FORWARD, FO_BAND_SERPENTINE = range(2)
+FO_CONSUMER_SHARED, FO_CONSUMER_RESERVED = range(2)
 (FO_TAB_SLOT_TILE, FO_TAB_TILE_SLOT, FO_TAB_SLOT_GROUP, FO_TAB_GROUP_TILES, FO_TAB_UNIT,
  FO_TAB_PART_START, FO_TAB_PART_LEN, FO_TAB_PART_DST, FO_TAB_DEST_UNITS,
  FO_TAB_FINAL_ROWS, FO_TAB_DEST_CAPACITY, FO_TAB_SLOT_LIVE, FO_TAB_UNIT_PLACE) = range(13)
@@ -72,6 +73,7 @@ def lib():
                                                   ctypes.c_int32]),
             "fo_plan_set_trace": (ctypes.c_int, [_vp, _vp, _vp]),
             "fo_plan_set_pacing": (ctypes.c_int, [_vp, ctypes.c_int32]),
+            "fo_plan_set_consumer_placement": (ctypes.c_int, [_vp, ctypes.c_int]),
             "fo_plan_set_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _i32p, _i32p]),
             "fo_plan_set_split": (ctypes.c_int, [_vp, ctypes.c_int32, _i32p]),
             "fo_plan_device_status": (ctypes.c_int, [_vp, _i32p, ctypes.c_int32]),
@@ -216,6 +218,13 @@ def fo_plan_set_launch(plan, consumer_ctas=0, reorder_ctas=0, overlap=True):
 def fo_plan_set_pacing(plan, ctas_during_gemm=0):
     """Consumer CTAs that take work while the GEMM runs (0: all)."""
     _check("fo_plan_set_pacing", lib().fo_plan_set_pacing(plan, int(ctas_during_gemm)))
+
+
+def fo_plan_set_consumer_placement(plan, placement=FO_CONSUMER_SHARED):
+    """Consumer CTAs beside the GEMM's (shared) or only on the SMs the GEMM
+    leaves free (reserved)."""
+    _check("fo_plan_set_consumer_placement",
+           lib().fo_plan_set_consumer_placement(plan, int(placement)))
 
 
 def fo_plan_set_gemm(plan, variant=FO_GEMM_AUTO):

@@ -52,7 +52,7 @@ class Pipeline:
 
     def __init__(self, w: Workload, inp: Inputs, device="cuda", partition=None,
                  wave_width=None, consumer_ctas=0, reorder_ctas=0, upload=True,
-                 gemm_variant=None):
+                 gemm_variant=None, reserved_consumer_sms=False):
         self.w = w
         self.device = torch.device(device)
         W = w.wave_width if wave_width is None else wave_width
@@ -70,6 +70,10 @@ class Pipeline:
         self.plan = fo.fo_plan_groups(self.desc)
         self.gemm_variant = fo.FO_GEMM_AUTO if gemm_variant is None else gemm_variant
         self.pairable, self.pair_capacity = fo.fo_plan_set_gemm(self.plan, self.gemm_variant)
+        # consumer CTAs only on the SMs the GEMM leaves free (see fo.h)
+        self.reserved_consumer_sms = reserved_consumer_sms
+        if reserved_consumer_sms:
+            fo.fo_plan_set_consumer_placement(self.plan, fo.FO_CONSUMER_RESERVED)
         self.consumer_ctas, self.reorder_ctas = consumer_ctas, reorder_ctas
         self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
@@ -119,6 +123,8 @@ class Pipeline:
         self.desc = fo.make_desc(**self.desc_args, group_waves=self.partition)
         self.plan = fo.fo_plan_groups(self.desc)
         fo.fo_plan_set_gemm(self.plan, self.gemm_variant)
+        if self.reserved_consumer_sms:
+            fo.fo_plan_set_consumer_placement(self.plan, fo.FO_CONSUMER_RESERVED)
         self._overlap = None
         _, _, self.group_tiles, _ = fo.fo_plan_info(self.plan)
         self.P = len(self.partition)

@@ -217,6 +217,29 @@ fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
  * first flag on.  The results do not depend on it. */
 fo_status fo_plan_set_pacing(fo_plan* plan, int32_t ctas_during_gemm);
 
+/* Where the consumer's CTAs run beside the GEMM.  [P1] 四、实时调优, offline
+ * stage: the communication kernel occupies some SMs, and the GEMM's wave
+ * count is taken over the SMs left to it (tiles / (SMs - communication
+ * SMs)); here the plan's wave width W plays that role.
+ *  FO_CONSUMER_SHARED (default): consumer CTAs may share an SM with a CTA
+ *      of the signaled GEMM.
+ *  FO_CONSUMER_RESERVED: fo_consume_group, fo_consume_reorder and
+ *      fo_consume_group_noalloc request (unused) dynamic shared memory that
+ *      does not fit beside a GEMM CTA, so while the GEMM runs their CTAs
+ *      run only on the SMs it leaves free: the device's SM count minus
+ *      min(W, tiles).  Their default grid is then as many CTAs as those
+ *      SMs hold at once (the kernel's occupancy with that shared memory), so
+ *      none waits for an SM; a grid set with fo_plan_set_launch still wins.
+ * The results do not depend on the placement.  FO_ERR_ARG for an unknown
+ * value; FO_ERR_UNSUPPORTED for FO_CONSUMER_RESERVED when the GEMM leaves
+ * no SM free, or when the shared memory needed is above the default
+ * dynamic limit (48 KB); FO_ERR_CUDA when the device cannot be queried. */
+typedef enum {
+  FO_CONSUMER_SHARED = 0,
+  FO_CONSUMER_RESERVED = 1
+} fo_consumer_placement;
+fo_status fo_plan_set_consumer_placement(fo_plan* plan, fo_consumer_placement placement);
+
 /* How fo_signaled_gemm maps tiles onto CTAs.  Either way W CTAs take the
  * launch slots c, c + W, ... (wave = slot / W) and every tile gets the same
  * epilogue; only the MMA differs.
