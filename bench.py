@@ -449,12 +449,14 @@ class Bench:
     """One workload planned and resident, with the step and the timing legs
     the headline and the per-workload records share."""
 
-    def __init__(self, ctx, w, args):
+    def __init__(self, ctx, w, args, inp=None, routes=None):
         from communication_overlap_gb300 import workloads as W
         from communication_overlap_gb300.pipeline import Pipeline
         self.ctx, self.w, self.args = ctx, w, args
         torch, dev = ctx["torch"], ctx["dev"]
-        self.inp = W.make_inputs(w)
+        # (inputs and routings of another Bench of the same workload may be
+        # passed in: they do not depend on the launch order)
+        self.inp = W.make_inputs(w) if inp is None else inp
         self.pipe = Pipeline(w, self.inp, device=dev, consumer_ctas=args.consumer_ctas,
                              reorder_ctas=args.reorder_ctas,
                              reserved_consumer_sms=getattr(args, "consumer_sms",
@@ -471,8 +473,8 @@ class Bench:
         # dispatch gather, outside the path), and rebuilds the routing tables
         # on the device (fo_plan_route) before its GEMM.
         self.dyn = w.capacity > 0
-        self.routes = []
-        if self.dyn:
+        self.routes = list(routes) if routes else []
+        if self.dyn and not self.routes:
             X = W.token_matrix(w)
             for k in range(1, 5):
                 _, tok, sl = W.routing(w, k)
@@ -706,6 +708,52 @@ class Bench:
         }
 
 
+def band8_leg(ctx, b, args, reps=3):
+    """The workload on the same inputs with bands of 8 tile rows (swizzle
+    8, the per-configuration launch order every workload used before the
+    taller bands), timed alternately with its own launch order: the GEMM
+    alone and the overlapped step, medians over 2 * `reps` runs of --steps
+    steps each, the order reversed every other time.  None for a workload whose bands are already 8
+    high."""
+    from communication_overlap_gb300 import workloads as W_
+    if b.w.swizzle == 8:
+        return None
+    torch = ctx["torch"]
+    b8 = Bench(ctx, W_.scaled(b.w, swizzle=8), args, inp=b.inp, routes=b.routes)
+    try:
+        b8.warm()
+        g8, g, st8, st = [], [], [], []
+
+        def legs(x, out_step, out_gemm):
+            out_step.append(statistics.mean(x.timed(x.ovl)))
+            out_gemm.append(statistics.mean(x.timed(lambda: x.pipe.gemm(x.s, x.pipe.epoch))))
+        with Clocks(ctx["local"]) as clk:
+            # the order alternates, so that a clock that drifts (the power
+            # cap) favours neither launch order
+            for r in range(2 * reps):
+                if r % 2 == 0:
+                    legs(b8, st8, g8)
+                    legs(b, st, g)
+                else:
+                    legs(b, st, g)
+                    legs(b8, st8, g8)
+        torch.cuda.synchronize()
+        return {"swizzle": 8, "workload_swizzle": b.w.swizzle,
+                "ms_overlapped_step": statistics.median(st8),
+                "ms_overlapped_step_workload_swizzle": statistics.median(st),
+                "value_tflops": b.flops / (statistics.median(st8) * 1e-3) / 1e12,
+                "ms_gemm_alone": statistics.median(g8),
+                "ms_gemm_alone_workload_swizzle": statistics.median(g),
+                "clocks": clk.summary(),
+                "status_ok": int(b8.pipe.buf.status.item()) == 0,
+                "note": "the same inputs, GEMM and consumer; only the launch order's band "
+                        "height differs; timed alternately in one loop"}
+    finally:
+        b8.close()
+        del b8
+        torch.cuda.empty_cache()
+
+
 def measure_compact(ctx, w, args):
     """A workload other than the headline: the overlapped and serial steps,
     the GEMM alone, the GEMM's slowdown, the consumer's bandwidth (alone and
@@ -722,6 +770,7 @@ def measure_compact(ctx, w, args):
         rec = b.record(statistics.mean(t_ov), statistics.mean(t_ser), statistics.mean(t_gemm),
                        clk.summary())
         rec["step_kernels"] = b.kernels
+        rec["swizzle_8"] = band8_leg(ctx, b, args)
         return rec
     finally:
         b.close()
@@ -922,6 +971,10 @@ def run_ours(args):
             del b_sm
             torch.cuda.empty_cache()
 
+    # the launch order every workload used before the taller bands, on the
+    # same inputs, alternated with the workload's own
+    band8 = band8_leg(ctx, b, args) if world == 1 else None
+
     if args.trace_out:
         write_trace(ctx, b, args.trace_out)
 
@@ -986,6 +1039,7 @@ def run_ours(args):
             "sustained": sustained,
             "partition_mode": args.partition,
             "w_sm_count": w_sm,
+            "swizzle_8": band8,
             "partition_tuned_before_timing": pre_tuned,
             "ms_serial_step_separate_kernels": statistics.mean(t_ser_sep),
             "ms_gemm_alone_no_signal": statistics.mean(t_gemm_nosig),
@@ -1054,7 +1108,7 @@ def compact_view(rec):
             "gemm_in_kernel_ms_in_step", "consumer_bytes", "direct_alone_step_grid",
             "direct_alone_full_grid", "consumer_in_step", "reorder_alone",
             "plain_copy_same_bytes", "reorder_frac_of_plain_copy", "gemm_traffic_bytes",
-            "clocks", "status_ok", "step_kernels")
+            "swizzle_8", "clocks", "status_ok", "step_kernels")
     out = {k: rec[k] for k in keep if k in rec}
     if isinstance(out.get("consumer_in_step"), dict):
         out["consumer_in_step"] = {k: v for k, v in out["consumer_in_step"].items()
