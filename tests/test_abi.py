@@ -130,3 +130,23 @@ def test_a2a_plan_without_routing_starts_empty():
         assert e.value.status == fo.FO_ERR_ARG
     finally:
         fo.fo_plan_destroy(plan)
+
+
+def test_consumer_placement_arguments():
+    """fo_plan_set_consumer_placement: a null plan or an unknown placement is
+    an argument error; a host-only plan (no device, so no SM is known to be
+    free) cannot reserve SMs; the shared placement is always accepted."""
+    assert fo.lib().fo_plan_set_consumer_placement(None, fo.FO_CONSUMER_SHARED) == fo.FO_ERR_ARG
+    d = fo.make_desc(M=256, N=512, K=256, tile_n=128, swizzle=2, wave_width=2,
+                     group_waves=(1, 2, 1), host_only=True)
+    plan = fo.fo_plan_groups(d)
+    try:
+        with pytest.raises(fo.FoError) as e:
+            fo.fo_plan_set_consumer_placement(plan, 7)
+        assert e.value.status == fo.FO_ERR_ARG
+        with pytest.raises(fo.FoError) as e:
+            fo.fo_plan_set_consumer_placement(plan, fo.FO_CONSUMER_RESERVED)
+        assert e.value.status == fo.FO_ERR_UNSUPPORTED
+        fo.fo_plan_set_consumer_placement(plan, fo.FO_CONSUMER_SHARED)
+    finally:
+        fo.fo_plan_destroy(plan)
