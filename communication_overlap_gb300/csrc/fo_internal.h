@@ -136,15 +136,16 @@ int32_t place_of(const fo_plan* p, int32_t slot, int32_t r);
 constexpr int kPlaceShift = 28;
 // The data kernels move 16-byte vectors: buffers must start on 16 bytes.
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// Counters, flags and status words are 32-bit atomics, stamps 64-bit.
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; }
 
 // SMs without a CTA of the plan's signaled GEMM while it runs (its grid is
 // min(W, tiles) CTAs, one per SM).
 inline int reserved_sms(const fo_plan* p) {
   return p->sm_count - (p->W < p->tiles ? p->W : p->tiles);
 }
-// Counters, flags and status words are 32-bit atomics, stamps 64-bit.
-inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
-inline bool aligned8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7) == 0; }
+
 void set_a2a_outputs(fo_plan* p, int32_t n_tokens, int32_t top_k);
 fo_status refresh_routing(fo_plan* p);
 

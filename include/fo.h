@@ -214,7 +214,8 @@ fo_status fo_plan_set_launch(fo_plan* plan, int32_t consumer_ctas,
  * group on.  A consumer that moves less data while the GEMM runs competes
  * less with it for HBM and SM time, and catches up once it has finished.
  * 0 (default) or a value of at least the grid: every CTA works from the
- * first flag on.  The results do not depend on it. */
+ * first flag on.  With FO_CONSUMER_RESERVED and its default grid (below)
+ * pacing is off.  The results do not depend on it. */
 fo_status fo_plan_set_pacing(fo_plan* plan, int32_t ctas_during_gemm);
 
 /* Where the consumer's CTAs run beside the GEMM.  [P1] 四、实时调优, offline
