@@ -52,6 +52,13 @@ def test_status_strings():
     dict(layout=fo.FO_LAYOUT_A2A_SUBTOKEN, n_dest=2,  # (token 0, slot 0) twice: rank
          row_token=[0, 0] + [-1] * 254, row_slot=[0] * 256),  # 0 outgrows its buffer
     dict(wave_width=0),                # host-only plan needs an explicit W
+    dict(M=0), dict(N=0), dict(K=0),   # empty operands
+    dict(M=-128), dict(K=-64),
+    dict(swizzle=-1), dict(wave_width=-3),
+    dict(group_waves=(-1, 5)),         # a negative group
+    dict(band_order=5),                # unknown band order
+    dict(pad_expert_tile_rows=True),   # padding is an All-to-All option
+    dict(tile_m=64),                   # unsupported tile height
 ])
 def test_bad_descriptions_are_rejected(bad):
     args = dict(M=256, N=512, K=256, tile_n=128, swizzle=2, wave_width=2,
@@ -150,3 +157,19 @@ def test_consumer_placement_arguments():
         fo.fo_plan_set_consumer_placement(plan, fo.FO_CONSUMER_SHARED)
     finally:
         fo.fo_plan_destroy(plan)
+
+
+def test_smallest_plans():
+    """One row (a ragged tile row of 1) and a single group covering every
+    wave are valid plans."""
+    for args, tiles, waves in ((dict(M=1, group_waves=(1, 1)), 4, 2),
+                               (dict(M=256, group_waves=(4,)), 8, 4)):
+        a = dict(M=256, N=512, K=256, tile_n=128, swizzle=2, wave_width=2, host_only=True)
+        a.update(args)
+        plan = fo.fo_plan_groups(fo.make_desc(**a))
+        try:
+            t, w, g, _ = fo.fo_plan_info(plan)
+            assert (t, w) == (tiles, waves)
+            assert sum(g) == tiles
+        finally:
+            fo.fo_plan_destroy(plan)
