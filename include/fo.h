@@ -145,7 +145,8 @@ fo_status fo_wave_count(const fo_plan_desc* desc, int32_t* tiles, int32_t* waves
  * (unless host_only).  On success *out owns them. */
 fo_status fo_plan_groups(const fo_plan_desc* desc, fo_plan** out);
 
-/* Sizes of a plan.  Any output pointer may be NULL.  group_tiles: [P];
+/* Sizes of a plan ([P1] 一: tiles, waves and |G_j|, the tiles of each
+ * group).  Any output pointer may be NULL.  group_tiles: [P];
  * tile_to_slot: [tiles], row-major tile id -> launch slot. */
 fo_status fo_plan_info(const fo_plan* plan, int32_t* tiles, int32_t* waves,
                        int32_t* n_groups, int32_t* group_tiles,
@@ -189,7 +190,9 @@ typedef enum {
 fo_status fo_plan_table(const fo_plan* plan, int32_t which, int32_t* out,
                         int64_t capacity, int64_t* length);
 
-/* Launch settings of the consumer and reorder kernels.
+/* Launch settings of the consumer and reorder kernels ([P1] 五: the
+ * communication side runs beside the GEMM and moves each group once it is
+ * signalled).
  *  consumer_ctas, reorder_ctas: grid sizes (<= 0: the defaults, measured
  *      beside the GEMM: consumer 4 CTAs per SM for SUM / RS, 1 per SM for
  *      COPY / A2A, 3 per SM for fo_consume_reorder (its direct variant: 1
