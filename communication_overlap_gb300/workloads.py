@@ -89,9 +89,13 @@ class Workload:
 # layer one band per expert (64 is above any expert's tile rows).  Measured
 # against swizzle 8, interleaved: the AllReduce step 190.6 -> 185.8 us, the
 # All-to-All step 2493 -> 2333 us.  The dynamic layer's experts hold 40 tile
-# rows of capacity, of which the last ~7 are empty and skipped: bands of 32
-# keep those in a short band of their own, so whole waves skip together
-# (its step 2785 us at 8, 2683 us at 64, 2594 us at 32, interleaved).
+# rows of capacity, and a routing fills at most 34 of them (4096 +- ~60
+# tokens per expert, 34 x 128 = 4352): bands of 34 hold every row a routing
+# can fill, and the short band of the 6 rows none reaches is skipped in whole
+# waves.  Every CTA then gets the same number of live tiles (its busiest CTA
+# 0.3 % above the mean, against 5 % in bands of 32, whose short band leaves
+# its live tiles to every fourth CTA).  Interleaved: the step 2785 us in bands
+# of 8, 2683 us in one band, 2610 us in bands of 32, 2519 us in bands of 34.
 # ReduceScatter's B (22.5 MB) stays in L2 at any band height (106.2 us at 8,
 # 107.4 us at 32), so it keeps 8.
 WORKLOADS = {
@@ -107,7 +111,7 @@ WORKLOADS = {
                          layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
                          n_tokens=16384, n_experts=8, top_k=2, pad_expert_tile_rows=True,
                          serpentine=True),
-    "alltoall_dynamic": Workload("alltoall_dynamic", 6, 8 * 5120, 14336, 4096, swizzle=32,
+    "alltoall_dynamic": Workload("alltoall_dynamic", 6, 8 * 5120, 14336, 4096, swizzle=34,
                                  layout=LAYOUT_A2A, consumer=CONS_A2A, n_dest=8,
                                  n_tokens=16384, n_experts=8, top_k=2, capacity=5120,
                                  serpentine=True),
