@@ -127,7 +127,7 @@ def test_exact_placement_device_routing(mode, pad, serp):
         pipe.close()
 
 
-FULL = ["wave_pattern", "allreduce", "reducescatter", "alltoall"]
+FULL = ["wave_pattern", "allreduce", "reducescatter", "alltoall", "alltoall_dynamic"]
 
 
 @pytest.mark.parametrize("name", FULL)
