@@ -20,7 +20,7 @@ import numpy as np
 import torch
 
 from . import fo
-from .workloads import Workload, Inputs, LAYOUT_TILE
+from .workloads import Workload, Inputs
 
 _CONSUMER_OF = {0: fo.FO_CONS_COPY, 1: fo.FO_CONS_SUM, 2: fo.FO_CONS_RS, 3: fo.FO_CONS_A2A}
 
